@@ -1,0 +1,405 @@
+"""Benchmark of the DSA lightning-indexer decode step on GB300.
+
+One step = the whole hot path over one batch of seeded synthetic inputs:
+quantize_query -> insert_key -> decode_layout -> score_paged (+ fused top-k).
+The default workload is ``fp8_decode`` (64 requests x 1 row, 4096..8192 keys,
+FP8 keys with FP32 scales at 132 B/token, top-2048).
+
+Prints one JSON line.  ``value`` is scored keys per second (sum of the row
+bounds over the timed steps / device time), inputs resident in HBM, L2
+flushed between steps.  ``--impl reference`` times the CPU oracle instead.
+
+Multi-GPU (``torchrun``): every rank runs its own replica of the workload
+(the step has no exchange); the timing is the max over ranks and ``value``
+sums the keys of all ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
+
+import numpy as np  # noqa: E402
+
+METRIC = "indexer scored keys/sec and cache GB/s (score+top-k) vs roofline, 1 GB300"
+UNIT = "keys/s"
+L2_FLUSH_BYTES = 512 << 20
+STEP_KERNELS = 6   # quantize_query, insert_key, decode_layout, plan, score, select
+
+
+def workload_desc(wl) -> str:
+    kind = {"fp8": "FP8 E4M3 keys, FP32 scales (132 B/token)",
+            "fp8_mx": "FP8 E4M3 keys, UE8M0 scales (132 B/token)",
+            "mxfp4": "MXFP4 keys (68 B/token)"}[wl.fmt]
+    return (f"{wl.name}: {wl.R} requests, {int(wl.query_lens.sum())} rows (+{wl.num_rows - int(wl.query_lens.sum())}"
+            f" padding), seq {int(wl.seq_lens.min())}..{int(wl.seq_lens.max())}, {kind}, top-{wl.topk}")
+
+
+def algorithmic_bytes(wl, row_ends) -> dict:
+    """Bytes the step must move at least: unique cache bytes of the scored keys
+    (each request's keys once), the quantised query rows and head weights, the
+    block-table entries read, and the top-k indices written."""
+    per_token = 68 if wl.fmt == "mxfp4" else 132
+    starts = np.concatenate([[0], np.cumsum(wl.query_lens)])
+    keys_unique = 0
+    pages = 0
+    for q in range(wl.R):
+        e = row_ends[starts[q]:starts[q + 1]]
+        m = int(e.max()) if e.size else 0
+        keys_unique += m
+        pages += (m + 63) // 64
+    q_bytes = 2176 if wl.fmt == "mxfp4" else 4096
+    cache = keys_unique * per_token
+    other = wl.num_rows * (q_bytes + 64 + 4) + pages * 4
+    topk = wl.num_rows * wl.topk * 4
+    return dict(cache=cache, score_kernel=cache + other, step=cache + other + topk,
+                keys_unique=keys_unique, scored=int(row_ends.sum()))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        import datetime
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10 or not parts[2].isdigit():
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if self.t0 is not None and not (self.t0 - 0.05 <= ts <= (self.t1 or ts) + 0.05):
+                    continue
+                rows.append(parts[1:])
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed region"], "samples": 0}
+        sm = [int(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def score_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("score.cu", "common.cuh", "scan.cuh"):
+        h.update(open(os.path.join(ROOT, "sparse_attention_indexer_score_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, units_per_launch: int):
+    """DRAM bytes per launch of the scoring kernel from the committed ncu
+    summary, scaled to this launch, or None when absent or stale."""
+    path = os.path.join(ROOT, "profiles", "score_kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    e = d.get(workload)
+    if not e or e.get("source_hash") != score_source_hash():
+        return None
+    return float(e["dram_bytes"]) * units_per_launch / float(e["units"])
+
+
+# ----------------------------------------------------------------- CPU oracle
+def _request_problem(wl, q):
+    """The oracle's inputs for request q alone: its quantised rows, their bounds,
+    a compact cache holding its pages (built by the oracle's own insert)."""
+    from oracle import indexer as O
+    from synth import bf16_bits_to_f32
+    rows = [r for r in range(wl.num_rows) if wl.row_request[r] == q]
+    q_rows, w = O.quantize_query(wl.fmt, bf16_bits_to_f32(wl.q_bits[rows]), bf16_bits_to_f32(wl.wv_bits[rows]))
+    _, row_ends = O.decode_layout(wl.seq_lens, wl.query_lens, wl.num_rows)
+    stride = O.page_bytes(wl.fmt)
+    n = (int(wl.seq_lens[q]) + 63) // 64
+    remap = {int(p): i for i, p in enumerate(wl.block_table[q, :n])}
+    cache = np.zeros(max(1, n) * stride, np.uint8)
+    kb, sl = wl.prefill(q)
+    sl2 = np.array([remap[int(s // 64)] * 64 + int(s % 64) for s in sl], dtype=np.int64)
+    O.insert_key(wl.fmt, cache, stride, n, bf16_bits_to_f32(kb), wl.gamma, wl.beta, wl.eps, sl2)
+    srows = [r for r in rows if wl.step_slots[r] >= 0]
+    if srows:
+        ss = wl.step_slots[srows]
+        sl3 = np.array([remap[int(s // 64)] * 64 + int(s % 64) for s in ss], dtype=np.int64)
+        O.insert_key(wl.fmt, cache, stride, n, bf16_bits_to_f32(wl.step_key_bits[srows]), wl.gamma, wl.beta,
+                     wl.eps, sl3)
+    return dict(q_rows=q_rows, w=w, starts=np.array([0, len(rows)], np.int32),
+                row_ends=row_ends[rows], cache=cache, bt=np.arange(n, dtype=np.int32)[None, :], stride=stride)
+
+
+def oracle_sample(wl, budget_s: float, rng_seed: int = 0):
+    """Times the oracle's score + top-k, request by request in a seeded random
+    order, until about ``budget_s`` seconds; returns (scored keys, seconds, desc).
+    Building each request's cache is set-up and is not timed."""
+    from oracle import indexer as O
+    order = np.random.default_rng(rng_seed).permutation(wl.R)
+    keys, secs, used = 0, 0.0, 0
+    for q in order:
+        if wl.query_lens[q] == 0:
+            continue
+        o = _request_problem(wl, int(q))
+        t = time.perf_counter()
+        s = O.score_paged(wl.fmt, o["q_rows"], o["w"], o["cache"], o["stride"], o["bt"], o["starts"], o["row_ends"])
+        O.topk(s, o["row_ends"], wl.topk)
+        secs += time.perf_counter() - t
+        keys += int(o["row_ends"].sum())
+        used += 1
+        if secs >= budget_s:
+            break
+    return keys, secs, f"{used} of {wl.R} requests of {wl.name} (score + top-k of their rows)"
+
+
+def run_reference(args, wl):
+    """The oracle on the host cores: each step a bounded sample of the workload."""
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    per_step = max(0.5, min(8.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(wl, per_step / 4)
+    keys = 0
+    secs = 0.0
+    desc = ""
+    for i in range(args.steps):
+        k, s, desc = oracle_sample(wl, per_step, rng_seed=i)
+        keys += k
+        secs += s
+    value = keys / secs if secs > 0 else 0.0
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step about {per_step:.1f} s of oracle work: {desc}"},
+    }
+    print(json.dumps(line))
+
+
+# ----------------------------------------------------------------- GPU
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from sparse_attention_indexer_score_gb300 import build as _b
+    _b.build()
+    from sparse_attention_indexer_score_gb300 import dsa
+    from sparse_attention_indexer_score_gb300.step import DecodeIndexer
+    from dsa_case import bf16_tensor
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    ix = DecodeIndexer(wl.fmt, wl.num_pages, torch.from_numpy(wl.block_table), torch.from_numpy(wl.gamma),
+                       torch.from_numpy(wl.beta), wl.eps, wl.num_rows, wl.topk, dev)
+    kb, sl = wl.prefill_all()
+    chunk = 1 << 20
+    for i in range(0, kb.shape[0], chunk):
+        ix.insert(bf16_tensor(kb[i:i + chunk], dev), torch.from_numpy(sl[i:i + chunk]).to(dev))
+    del kb, sl
+    host = dict(q=bf16_tensor(wl.q_bits, "cpu"), wv=bf16_tensor(wl.wv_bits, "cpu"),
+                keys=bf16_tensor(wl.step_key_bits, "cpu"), slots=torch.from_numpy(wl.step_slots),
+                seq=torch.from_numpy(wl.seq_lens), qlen=torch.from_numpy(wl.query_lens))
+    d = {k: v.to(dev) for k, v in host.items()}
+    max_q = int(wl.query_lens.max(initial=0))
+    topk_out = torch.empty((wl.num_rows, wl.topk), dtype=torch.int32, device=dev)
+    q_out = torch.zeros((wl.num_rows, 4096), dtype=torch.uint8, device=dev)
+    w_out = torch.empty((wl.num_rows, 32), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(inp):
+        return ix.step(inp["q"], inp["wv"], inp["keys"], inp["slots"], inp["seq"], inp["qlen"], max_q,
+                       topk_out=topk_out, q_out=q_out, w_out=w_out)
+
+    out = step(d)
+    torch.cuda.synchronize()
+    row_ends = out.row_ends.cpu().numpy()
+    ab = algorithmic_bytes(wl, row_ends)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(d)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    # headline: K steps, device time of each step (flush excluded)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        clocks.mark_start()
+        for a, b in evs:
+            flush.zero_()
+            a.record()
+            step(d)
+            b.record()
+        torch.cuda.synchronize()
+        clocks.mark_end()
+        if world > 1:
+            dist.barrier()
+    clk = clocks.summary()
+    step_ms = sum(a.elapsed_time(b) for a, b in evs)
+
+    # the scoring kernel alone (events recorded by the library around it)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in kev:
+        flush.zero_()
+        dsa.set_score_timing(a, b)
+        step(d)
+    dsa.set_score_timing(None, None)
+    torch.cuda.synchronize()
+    kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+
+    # end to end through the public API from pinned host buffers
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    h_top = torch.empty((wl.num_rows, wl.topk), dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = h_top.numel() * 4
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in eev:
+        flush.zero_()
+        a.record()
+        for k in d:
+            d[k].copy_(pinned[k], non_blocking=True)
+        step(d)
+        h_top.copy_(topk_out, non_blocking=True)
+        b.record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
+
+    times = torch.tensor([step_ms, e2e_ms, kernel_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    step_ms, e2e_ms, kernel_ms = times.tolist()
+    if rank != 0:
+        return
+    keys_total = ab["scored"] * args.steps * world
+    value = keys_total / (step_ms / 1e3)
+    peaks = measured_peaks()
+    achieved = ab["score_kernel"] / (kernel_ms / 1e3) / 1e9
+    traffic = ncu_traffic(wl.name, ab["score_kernel"])
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {"fp8": "fp8_e4m3", "fp8_mx": "fp8_e4m3", "mxfp4": "fp4_e2m1"}[wl.fmt],
+        "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "rows": wl.num_rows, "requests": wl.R,
+                   "scored_keys_per_step": ab["scored"], "unique_keys_per_step": ab["keys_unique"],
+                   "cache_bytes_per_step": ab["cache"], "l2": "flushed before every step (512 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "cache_gbs": ab["cache"] * args.steps * world / (step_ms / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "score_kernel", "kernel_us": kernel_ms * 1e3,
+                     "peak_source": f"{peaks['source']} HBM copy bandwidth",
+                     "step_frac": (ab["step"] / (step_ms / args.steps / 1e3) / 1e9) / peaks["hbm_gbs"]},
+        "e2e": {"value": keys_total / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": STEP_KERNELS * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        keys, secs, desc = oracle_sample(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": keys / secs if secs else None, "unit": UNIT,
+                                "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", 1)), "kind": "oracle",
+                                "sample": f"{desc}; {secs:.1f} s"}
+    print(json.dumps(line))
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="fp8_decode")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    from synth import make_workload
+    wl = make_workload(args.config)
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, wl, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

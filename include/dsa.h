@@ -1,0 +1,246 @@
+/*
+ * dsa.h - C ABI of the GB300 DSA lightning-indexer decode step.
+ *
+ * One decode step of the DeepSeek-style sparse-attention indexer, as the
+ * indexer pages state it:
+ *   1. dsa_quantize_query  per-head FP8 (power-of-two scale folded into the
+ *                          head weights) or MXFP4 query rows;
+ *   2. dsa_insert_key      LayerNorm (FP32) + quantise + paged insert of the
+ *                          shared 128-column indexer key;
+ *   3. dsa_decode_layout   request grouping and causal key bounds of the
+ *                          (speculative-verify) query rows;
+ *   4. dsa_score_paged     paged MQA logits score[t] = sum_h w_h * ReLU(q_h . k_t),
+ *                          with the top-k selection fused behind it;
+ *   5. dsa_topk            top-k of an existing logits matrix.
+ *
+ * Conventions for every call:
+ *   - Every pointer argument except `stream` is a DEVICE pointer owned by the
+ *     caller.  The library allocates no device memory; scratch comes from a
+ *     caller workspace sized by dsa_workspace_size / dsa_topk_workspace_size.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     only enqueues work and returns; nothing waits for the GPU.
+ *   - Return value: DSA_OK, or a negative DSA_ERR_* code.  Argument checks
+ *     happen on the host before anything is enqueued, so an error return
+ *     means no work was queued (except DSA_ERR_CUDA, which reports a failed
+ *     launch).
+ *   - Invalid *device data* (a page id outside the pool, a slot past the
+ *     cache, row bounds past the block table, inconsistent request starts) is
+ *     never trapped on: the offending access is skipped (or clamped) and a bit
+ *     is OR-ed into the optional caller-provided int32 `status` word.
+ *   - Empty inputs (zero rows, zero keys) return DSA_OK and launch nothing.
+ *
+ * Constants: 32 heads x 128 columns per query row, 128-column keys, 64-token
+ * cache pages (page "cutedsl.dsa.index", module docstring and DsaIndex).
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_HEADS 32
+#define DSA_DIM 128
+#define DSA_PAGE_TOKENS 64
+#define DSA_Q_ROW_BYTES 4096          /* one quantised query row: 32 x 128 B */
+#define DSA_FP4_SCALES 2048           /* byte offset of the MXFP4 query scales in a row */
+#define DSA_FP8_PAGE_BYTES 8448       /* 64 x (128 B E4M3 + 4 B scale) */
+#define DSA_FP4_PAGE_BYTES 4352       /* 64 x (64 B E2M1 + 4 B UE8M0) */
+
+/* Key / query formats.  Page "cutedsl.dsa.index", module docstring:
+ *  DSA_FMT_FP8     E4M3 keys, one power-of-two FP32 scale per token (132 B/token);
+ *                  E4M3 queries with the per-head scale folded into the weights.
+ *  DSA_FMT_FP8_MX  as DSA_FMT_FP8, but the key scale is stored as its exponent
+ *                  in four equal UE8M0 bytes (the "mx" scales).  The scorer treats
+ *                  byte b as the scale of columns 32b..32b+31, which for the
+ *                  four equal bytes the writer stores is the token's one scale.
+ *  DSA_FMT_MXFP4   E2M1 keys and queries, one UE8M0 scale per 32 columns
+ *                  (68 B/token); the head weights carry only the 1/64 factor. */
+typedef enum {
+    DSA_FMT_FP8 = 0,
+    DSA_FMT_FP8_MX = 1,
+    DSA_FMT_MXFP4 = 2
+} dsa_format;
+
+/* Return codes. */
+#define DSA_OK 0
+#define DSA_ERR_INVALID (-1)      /* bad shape, stride, alignment, null pointer, count */
+#define DSA_ERR_UNSUPPORTED (-2)  /* unknown format or a size the kernels do not handle */
+#define DSA_ERR_CUDA (-3)         /* a kernel launch or a driver call failed */
+
+/* Bits of the device status word (OR-ed in by the kernels). */
+#define DSA_STATUS_BAD_SLOT 1       /* a slot >= num_pages * 64 was skipped */
+#define DSA_STATUS_BAD_PAGE 2       /* a block-table entry outside [0, num_pages) was read as zeros */
+#define DSA_STATUS_BAD_GEOMETRY 4   /* starts / row bounds out of range were clamped */
+#define DSA_STATUS_TIMEOUT 8        /* an internal pipeline wait gave up (about 1 s); results invalid */
+
+/*
+ * dsa_quantize_query - quantise indexer query rows and fold the head weights.
+ *
+ * Page "cutedsl.dsa.index": DsaIndex.kernel, DsaIndex.fp8_query,
+ * quantize_fp4_query, fp4_query_views.
+ *
+ *   q       BF16, row r head h column c at q[r * q_row_stride + h * 128 + c];
+ *           q_row_stride >= 4096 elements, a multiple of 8; q 16-byte aligned.
+ *   wv      BF16 head-weight logits, wv[r * wv_row_stride + h].
+ *   rows    number of query rows (>= 0).
+ *   q_out   uint8 [rows][4096], 16-byte aligned.
+ *           FP8 formats: head h's 128 E4M3 codes at h * 128, codes of v / 2^e where
+ *             2^e is the smallest power of two with 448 * 2^e >= max(1e-10, amax_h).
+ *           DSA_FMT_MXFP4: head h's 64 bytes of E2M1 pairs at h * 64 (column 2j in the
+ *             low nibble of byte j), its four UE8M0 bytes (column block b at byte b)
+ *             at 2048 + h * 4; bytes 2176..4095 are not written.
+ *   w_out   BF16 [rows][32]: FP8: BF16(wv * 2^e / 64); MXFP4: BF16(wv / 64).
+ */
+int dsa_quantize_query(int fmt, const void* q, int64_t q_row_stride,
+                       const void* wv, int64_t wv_row_stride, int64_t rows,
+                       void* q_out, void* w_out, void* stream);
+
+/*
+ * dsa_insert_key - LayerNorm (FP32) + BF16 + quantise + insert of indexer keys.
+ *
+ * Page "cutedsl.dsa.index": insert_key, insert_fp4_key, module docstring;
+ * page "amd.ops.fp4_indexer": store_keys (negative slots are padding).
+ *
+ *   k            BF16 wk projections, key i column c at k[i * k_row_stride + c];
+ *                k_row_stride >= 128 and a multiple of 8; k 16-byte aligned.
+ *   gamma, beta  FP32 [128] LayerNorm weight and bias; eps the LayerNorm epsilon.
+ *   slots        int64 [n]: slot = page * 64 + offset; < 0 = padding (no write);
+ *                >= num_pages * 64 is skipped and flagged DSA_STATUS_BAD_SLOT.
+ *   cache        uint8, page p at cache + p * page_stride (16-byte aligned,
+ *                page_stride a multiple of 16 and >= 8448 (FP8) or 4352 (MXFP4)).
+ *                FP8 page: 64 x 128 B E4M3 codes at offset * 128, then 64 x 4 B
+ *                scales at 8192 + offset * 4 (FP32 2^e, or the byte e + 127 four
+ *                times for DSA_FMT_FP8_MX).  MXFP4 page: 64 x 64 B E2M1 at
+ *                offset * 64, then 64 x 4 UE8M0 at 4096 + offset * 4.
+ *   status       optional int32 device word (may be NULL).
+ *
+ * The LayerNorm is computed in a fixed order: per 8-column group a sequential
+ * FP32 sum, the 16 group sums combined by an xor butterfly (8, 4, 2, 1),
+ * correctly rounded division, square root and reciprocal, no fused
+ * multiply-add.  Keys with the same slot in one call race (last writer wins).
+ */
+int dsa_insert_key(int fmt, const void* k, int64_t k_row_stride,
+                   const float* gamma, const float* beta, float eps,
+                   const int64_t* slots, int64_t n,
+                   void* cache, int64_t page_stride, int64_t num_pages,
+                   int32_t* status, void* stream);
+
+/*
+ * dsa_decode_layout - group verify rows by request and bound their keys.
+ *
+ * Page "amd.ops.fp4_indexer": decode_layout (without its DCP branch).
+ *
+ *   seq_lens     int32 [num_seq] global sequence lengths (num_seq >= num_requests;
+ *                entries past num_requests are ignored).
+ *   query_lens   int32 [num_requests] rows per request (>= 0).
+ *   num_rows     rows to bound (>= 0); rows past the last request are padding.
+ *   starts       int32 [num_requests + 1] out: [0, cumsum(query_lens)].
+ *   row_ends     int32 [num_rows] out: for row r of request q,
+ *                max(0, seq_len[q] - query_len[q] + (r - starts[q]) + 1); 0 for padding.
+ * Errors (DSA_ERR_INVALID): num_rows < 0, num_requests < 0, num_seq < num_requests.
+ */
+int dsa_decode_layout(const int32_t* seq_lens, int64_t num_seq,
+                      const int32_t* query_lens, int64_t num_requests,
+                      int64_t num_rows, int32_t* starts, int32_t* row_ends,
+                      void* stream);
+
+/*
+ * dsa_workspace_size - bytes of scratch dsa_score_paged needs for these sizes
+ * (rows query rows, num_requests requests, max_pages block-table columns, top-k k).
+ * The workspace must be zero-filled before its first use; every call that
+ * completes leaves it zero-filled again, so it can be reused without clearing.
+ */
+size_t dsa_workspace_size(int fmt, int64_t rows, int64_t num_requests,
+                          int64_t max_pages, int64_t k);
+
+/*
+ * dsa_score_paged - paged MQA logits of grouped query rows, fused with top-k.
+ *
+ * Page "cutedsl.dsa.index" (module docstring: the MQA logits take the FP8 /
+ * MXFP4 query and the paged indexer cache); page "amd.ops.fp4_indexer":
+ * score_paged (block table, query_starts, row_ends, logits width
+ * max_pages * 64); page "cutedsl.dsa.overlap" (scoring and top-k).
+ *
+ *   q_rows        uint8 [rows][4096] from dsa_quantize_query (16-byte aligned;
+ *                 32-byte aligned for MXFP4).
+ *   w             BF16 [rows][32] head weights from dsa_quantize_query.
+ *   cache         paged cache written by dsa_insert_key (same layout rules;
+ *                 for MXFP4 the base must be 32-byte aligned and page_stride a
+ *                 multiple of 32).
+ *   block_table   int32, request q's page j at block_table[q * bt_stride + j],
+ *                 max_pages columns.
+ *   starts        int32 [num_requests + 1]: rows starts[q] .. starts[q+1]-1 form
+ *                 request q and share its keys.
+ *   row_ends      int32 [rows]: row r scores positions t < row_ends[r]
+ *                 (bounded by max_pages * 64).  Rows outside every request score
+ *                 nothing.
+ *   max_query_len the largest starts[q+1] - starts[q] (>= 0; informational).
+ *   logits        optional FP32 [rows][logits_ld] out (logits_ld >= max_pages * 64):
+ *                 score[r][t] for t < row_ends[r], -inf for the rest of the
+ *                 max_pages * 64 columns.  NULL keeps the logits in the workspace.
+ *   k, topk       optional top-k (k > 0 and topk != NULL): int32 [rows][k] of
+ *                 positions t (logical key indices of the request) of the k
+ *                 largest scores of each row, in no particular order; rows with
+ *                 at most k keys list 0..row_end-1 in order, then -1.
+ *   workspace     scratch of at least dsa_workspace_size(...) bytes, 256-byte
+ *                 aligned, zero-filled before first use.
+ *   status        optional int32 device word.
+ *
+ * score[r][t] = sum_h w[r][h] * ReLU(q_h . k_t), q and k dequantised (FP8 keys
+ * times their scale; MXFP4 values times their block scales), accumulated in
+ * FP32 on the tensor cores.  Keys come from page block_table[q][t / 64], token
+ * t % 64.
+ */
+int dsa_score_paged(int fmt, const void* q_rows, const void* w,
+                    const void* cache, int64_t page_stride, int64_t num_pages,
+                    const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                    const int32_t* starts, const int32_t* row_ends,
+                    int64_t num_requests, int64_t rows, int64_t max_query_len,
+                    float* logits, int64_t logits_ld,
+                    int64_t k, int32_t* topk,
+                    void* workspace, size_t workspace_bytes,
+                    int32_t* status, void* stream);
+
+/*
+ * dsa_topk_workspace_size - bytes of scratch dsa_topk needs (zero-filled before
+ * first use, left zero-filled by every completed call).
+ */
+size_t dsa_topk_workspace_size(int64_t rows, int64_t k);
+
+/*
+ * dsa_topk - top-k positions of each row of an FP32 logits matrix.
+ *
+ * Page "cutedsl.dsa.overlap" (the indexer path ends in "scoring and top-k");
+ * page "amd.ops.fp4_indexer": decode_tile_size (per-row selection scratch).
+ *
+ *   logits    FP32 [rows][ld], row r valid for t < min(row_ends[r], width).
+ *   row_ends  int32 [rows].
+ *   out       int32 [rows][k]: positions of the k largest values (any order);
+ *             rows with at most k valid entries list them in order, then -1.
+ * Equal values at the k-th place are broken arbitrarily.
+ */
+int dsa_topk(const float* logits, int64_t ld, const int32_t* row_ends,
+             int64_t rows, int64_t width, int64_t k, int32_t* out,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_set_score_timing - profiling hook: when both events are non-NULL,
+ * dsa_score_paged records `before` just ahead of its scoring kernel and
+ * `after` just behind it on the call's stream, so the scoring kernel alone can
+ * be timed.  Pass NULLs to switch it off.  Not thread-safe; events are
+ * cudaEvent_t handles owned by the caller.
+ */
+void dsa_set_score_timing(void* before, void* after);
+
+/* dsa_version - library version string. */
+const char* dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

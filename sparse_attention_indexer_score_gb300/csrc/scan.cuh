@@ -1,0 +1,39 @@
+// Block-wide prefix sums for the single-CTA bookkeeping kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace dsa {
+
+// Inclusive scan of one int per thread over a block of up to 1024 threads.
+// `warp_tmp` is shared scratch of 32 ints.  Returns the inclusive prefix; the
+// block total is written to *total (all threads read it after the call).
+__device__ __forceinline__ int block_inclusive_scan(int v, int* warp_tmp, int* total) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, v, d);
+        if (lane >= d) v += o;
+    }
+    if (lane == 31) warp_tmp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int s = (lane < nwarps) ? warp_tmp[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, s, d);
+            if (lane >= d) s += o;
+        }
+        warp_tmp[lane] = s;   // inclusive prefix over warps
+        if (lane == 31) *total = s;
+    }
+    __syncthreads();
+    const int before = (warp > 0) ? warp_tmp[warp - 1] : 0;
+    const int result = v + before;
+    __syncthreads();   // warp_tmp may be reused by the caller's next scan
+    return result;
+}
+
+}  // namespace dsa

@@ -1,0 +1,586 @@
+// Paged MQA logits of grouped query rows on the Blackwell tensor cores,
+// fused with the first pass of the top-k selection.
+//
+// score[r][t] = sum_h w[r][h] * ReLU(q_h . k_t)   (page "cutedsl.dsa.index",
+// module docstring; page "amd.ops.fp4_indexer", score_paged).
+//
+// Work unit: a tile of 128 keys (two 64-token cache pages from the block table)
+// against a segment of up to 4 query rows of one request (N = 32 * rows MMA
+// columns), so the keys a request's rows share are read from HBM once.
+// Keys sit on the MMA's M dimension, heads x rows on N:
+//   D[128 keys][32 * rows] = K[128 x 128] . Q[32 * rows x 128]^T   (FP32 in TMEM)
+//
+// Warp roles of the persistent CTA (one per SM):
+//   warp 0     TMA producer: block-table gather of key pages (+ their scales)
+//              into an 8-stage shared-memory ring; query rows per segment.
+//   warp 1     tcgen05 issuer: scale factors into TMEM, 4 MMAs (K = 32 each)
+//              per tile into one of two TMEM accumulators.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = key),
+//              ReLU-weighted head sum, FP32 key scale, logits store, and a
+//              shared-memory histogram of the scores for the top-k pass.
+//
+// Formats: FP8 uses kind::f8f6f4 (E4M3 x E4M3) and multiplies the FP32 key
+// scale in the epilogue.  FP8-MX and MXFP4 use kind::mxf8f6f4 with UE8M0 block
+// scales in TMEM (one per 32 columns); MXFP4 keys and queries are unpacked by
+// TMA into the 16-byte-aligned E2M1 layout the MMA reads.
+#include "host.h"
+#include "scan.cuh"
+
+namespace dsa {
+
+constexpr int kStages = 8;
+constexpr int kTileRows = 128;
+constexpr int kTileBytes = kTileRows * 128;   // codes of 128 keys in shared memory
+constexpr int kPageSmem = 64 * 128;           // one page's codes in shared memory
+constexpr int kSegRows = 4;                   // query rows per segment
+constexpr int kQBufBytes = kSegRows * kQRowBytes;
+constexpr int kScoreThreads = 192;
+
+constexpr int OFF_TILES = 0;
+constexpr int OFF_QBUF = OFF_TILES + kStages * kTileBytes;
+constexpr int OFF_RAWSC = OFF_QBUF + 2 * kQBufBytes;
+constexpr int OFF_SFA = OFF_RAWSC + kStages * 512;
+constexpr int OFF_QSF = OFF_SFA + kStages * 512;
+constexpr int OFF_SFB = OFF_QSF + 2 * 512;
+constexpr int OFF_KS = OFF_SFB + 2 * 512;
+constexpr int OFF_HIST = OFF_KS + 2 * 128 * 4;
+constexpr int OFF_W = OFF_HIST + kSegRows * kHistBins * 4;
+constexpr int OFF_ROWINFO = OFF_W + kSegRows * kHeads * 4;
+constexpr int OFF_BAR = OFF_ROWINFO + 64;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1;
+constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
+constexpr int kScoreSmem = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
+
+// TMEM columns: two accumulators of up to 128 columns, then scale factors.
+constexpr uint32_t TM_ACC = 0;
+constexpr uint32_t TM_SFA = 256;                  // kStages x 4 columns
+constexpr uint32_t TM_SFB = TM_SFA + 4 * kStages; // 2 x 4 columns
+constexpr uint32_t TM_COLS = 512;
+
+struct ScoreArgs {
+    int fmt;
+    int num_pages;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    const uint8_t* q_rows;
+    const __nv_bfloat16* w;
+    const int* info;
+    const int4* segs;
+    const int* seg_prefix;
+    const int* eff_end;
+    float* logits;
+    int64_t ld;
+    int hist_k;          // rows whose bound exceeds hist_k get a histogram; -1: none
+    unsigned* hist;
+    int32_t* status;
+};
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier over the 128 epilogue threads returning the OR of `pred`.
+__device__ __forceinline__ bool epi_sync_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
+
+// Segment s with prefix[s] <= t < prefix[s + 1] (prefix[S] > t).
+__device__ __forceinline__ int find_segment(const int* prefix, int S, int t) {
+    int lo = 0, hi = S;   // answer in [0, S)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// ----------------------------------------------------------------- plan
+// One CTA: validates request starts and row bounds, splits requests into
+// segments of up to 4 rows and lays their 128-key tiles out in one index space.
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ starts,
+                                                    const int32_t* __restrict__ row_ends, int R, int rows,
+                                                    int max_keys, int* __restrict__ info, int4* __restrict__ segs,
+                                                    int* __restrict__ seg_prefix, int* __restrict__ eff_end,
+                                                    int32_t* status) {
+    pdl_launch_dependents();
+    __shared__ int warp_tmp[32];
+    __shared__ int chunk_total;
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) eff_end[r] = 0;
+    __syncthreads();
+    int carry = 0;
+    bool bad = false;
+    for (int base = 0; base < R; base += blockDim.x) {
+        const int q = base + threadIdx.x;
+        int s0 = 0, s1 = 0;
+        if (q < R) {
+            const int a = starts[q], b = starts[q + 1];
+            if (a < 0 || b < a || b > rows) bad = true;
+            s0 = min(max(a, 0), rows);
+            s1 = min(max(b, s0), rows);
+        }
+        const int nseg = (s1 - s0 + kSegRows - 1) / kSegRows;
+        const int inc = block_inclusive_scan(nseg, warp_tmp, &chunk_total);
+        const int sbase = carry + inc - nseg;
+        for (int i = 0; i < nseg; ++i) {
+            if (sbase + i > rows) { bad = true; break; }   // overlapping requests: capacity is rows + 1
+            const int row0 = s0 + i * kSegRows;
+            const int nr = min(kSegRows, s1 - row0);
+            int maxend = 0;
+            for (int r = row0; r < row0 + nr; ++r) {
+                int e = row_ends[r];
+                if (e > max_keys) { bad = true; e = max_keys; }
+                e = max(e, 0);
+                eff_end[r] = e;
+                maxend = max(maxend, e);
+            }
+            segs[sbase + i] = make_int4(q, row0, nr, maxend);
+        }
+        carry += chunk_total;
+        __syncthreads();
+    }
+    if (bad && status) atomicOr(status, DSA_STATUS_BAD_GEOMETRY);
+    const int S = min(carry, rows + 1);
+    __syncthreads();
+    carry = 0;
+    for (int base = 0; base < S; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const int tiles = (i < S) ? (segs[i].w + kTileRows - 1) / kTileRows : 0;
+        const int inc = block_inclusive_scan(tiles, warp_tmp, &chunk_total);
+        if (i < S) seg_prefix[i] = carry + inc - tiles;
+        carry += chunk_total;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        seg_prefix[S] = carry;
+        info[0] = S;
+        info[1] = carry;
+    }
+}
+
+// ----------------------------------------------------------------- roles
+__device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUtensorMap* smap,
+                                              const CUtensorMap* qmap, const ScoreArgs& p, uint8_t* smem,
+                                              uint64_t* full, uint64_t* empty, uint64_t* qfull, uint64_t* qempty,
+                                              volatile int* abort, int t0, int t1, int seg) {
+    const bool fp4 = (p.fmt == DSA_FMT_MXFP4);
+    int cur = -1, i_seg = 0, it = 0;
+    int4 si = make_int4(0, 0, 0, 0);
+    for (int t = t0; t < t1; ++t, ++it) {
+        while (t >= p.seg_prefix[seg + 1]) ++seg;
+        if (seg != cur) {
+            cur = seg;
+            si = p.segs[seg];
+            const int qb = i_seg & 1;
+            if (!mbar_wait(qempty + qb, ((i_seg >> 1) & 1) ^ 1, abort, p.status)) break;
+            const uint32_t bytes = si.z * (kQRowBytes + (fp4 ? 128u : 0u));
+            mbar_arrive_expect_tx(qfull + qb, bytes);
+            uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
+            for (int r = 0; r < si.z; ++r) {
+                tma_load_3d(qdst + r * kQRowBytes, qmap, 0, 0, si.y + r, qfull + qb);
+                if (fp4)
+                    bulk_load(smem + OFF_QSF + qb * 512 + r * 128,
+                              p.q_rows + static_cast<int64_t>(si.y + r) * kQRowBytes + kFp4Scales, 128, qfull + qb);
+            }
+            ++i_seg;
+        }
+        const int j = t - p.seg_prefix[seg];
+        const int s = it % kStages;
+        if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status)) break;
+        const int npages = (si.w + kPage - 1) / kPage;
+        int pid[2];
+        uint32_t bytes = 0;
+        for (int h = 0; h < 2; ++h) {
+            const int pg = 2 * j + h;
+            pid[h] = -1;
+            if (pg < npages) {
+                const int v = p.block_table[static_cast<int64_t>(si.x) * p.bt_stride + pg];
+                if (v >= 0 && v < p.num_pages) {
+                    pid[h] = v;
+                    bytes += kPageSmem + 256;
+                } else if (p.status) {
+                    atomicOr(p.status, DSA_STATUS_BAD_PAGE);
+                }
+            }
+        }
+        if (bytes == 0) {
+            mbar_arrive(full + s);   // nothing valid to load; scores of these keys are unspecified
+        } else {
+            mbar_arrive_expect_tx(full + s, bytes);
+            uint8_t* dst = smem + OFF_TILES + s * kTileBytes;
+            for (int h = 0; h < 2; ++h) {
+                if (pid[h] < 0) continue;
+                tma_load_3d(dst + h * kPageSmem, kmap, 0, 0, pid[h], full + s);
+                tma_load_2d(smem + OFF_RAWSC + s * 512 + h * 256, smap, 0, pid[h], full + s);
+            }
+        }
+    }
+    // Drain: every copy issued must have landed before the CTA exits.
+    for (int i = max(0, it - kStages); i < it; ++i) mbar_drain(full + (i % kStages), (i / kStages) & 1);
+    for (int i = max(0, i_seg - 2); i < i_seg; ++i) mbar_drain(qfull + (i & 1), (i >> 1) & 1);
+}
+
+__device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* full,
+                                         uint64_t* empty, uint64_t* qfull, uint64_t* qempty, uint64_t* tfull,
+                                         uint64_t* tempty, uint64_t* done_bar, volatile int* abort, int t0, int t1,
+                                         int seg) {
+    const int lane = threadIdx.x & 31;
+    const bool f32scale = (p.fmt == DSA_FMT_FP8);
+    const bool fp4 = (p.fmt == DSA_FMT_MXFP4);
+    if (p.fmt == DSA_FMT_FP8_MX) {
+        // FP8 queries carry no block scales (their scale is folded into w): 2^0 everywhere.
+        reinterpret_cast<uint4*>(smem + OFF_SFB)[lane] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc_cp_32x128b_warpx4(tmem + TM_SFB, desc_rows16(smem_u32(smem + OFF_SFB)));
+        __syncwarp();
+    }
+    int cur = -1, qb = 0, i_seg = 0, it = 0, nrows = 0;
+    for (int t = t0; t < t1; ++t, ++it) {
+        while (t >= p.seg_prefix[seg + 1]) ++seg;
+        if (seg != cur) {
+            if (cur >= 0 && lane == 0) tc_commit(qempty + qb);
+            cur = seg;
+            nrows = p.segs[seg].z;
+            qb = i_seg & 1;
+            const bool ok = mbar_wait(qfull + qb, (i_seg >> 1) & 1, abort, p.status);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            if (fp4) {
+                // Query block scales: line L of the atom holds the words of MMA
+                // rows L, 32 + L, 64 + L, 96 + L (row r * 32 + h = head h of query row r).
+                const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + OFF_QSF + qb * 512);
+                uint4 line;
+                line.x = raw[lane];
+                line.y = nrows > 1 ? raw[32 + lane] : 0x7F7F7F7Fu;
+                line.z = nrows > 2 ? raw[64 + lane] : 0x7F7F7F7Fu;
+                line.w = nrows > 3 ? raw[96 + lane] : 0x7F7F7F7Fu;
+                reinterpret_cast<uint4*>(smem + OFF_SFB + qb * 512)[lane] = line;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    tc_cp_32x128b_warpx4(tmem + TM_SFB + qb * 4, desc_rows16(smem_u32(smem + OFF_SFB + qb * 512)));
+            }
+            ++i_seg;
+        }
+        const int s = it % kStages;
+        const int a = it & 1;
+        bool ok = mbar_wait(full + s, (it / kStages) & 1, abort, p.status);
+        ok = ok && mbar_wait(tempty + a, ((it >> 1) & 1) ^ 1, abort, p.status);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        tc_fence_after();
+        const uint32_t* rs = reinterpret_cast<const uint32_t*>(smem + OFF_RAWSC + s * 512);
+        const uint32_t w0 = rs[lane], w1 = rs[32 + lane], w2 = rs[64 + lane], w3 = rs[96 + lane];
+        if (f32scale) {
+            float* ks = reinterpret_cast<float*>(smem + OFF_KS + a * 512);
+            ks[lane] = __uint_as_float(w0);
+            ks[32 + lane] = __uint_as_float(w1);
+            ks[64 + lane] = __uint_as_float(w2);
+            ks[96 + lane] = __uint_as_float(w3);
+        } else {
+            reinterpret_cast<uint4*>(smem + OFF_SFA + s * 512)[lane] = make_uint4(w0, w1, w2, w3);
+            fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t d = tmem + TM_ACC + a * 128;
+            const uint64_t ad = desc_sw128(smem_u32(smem + OFF_TILES + s * kTileBytes));
+            const uint64_t bd = desc_sw128(smem_u32(smem + OFF_QBUF + qb * kQBufBytes));
+            const uint32_t n = 32u * nrows;
+            if (f32scale) {
+                const uint32_t id = idesc_f8f6f4(kMmaE4M3, kMmaE4M3, 128, n);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc_mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, id, kk > 0);
+            } else {
+                const uint32_t sfa = tmem + TM_SFA + s * 4;
+                tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
+                const uint32_t fm = fp4 ? kMmaE2M1 : kMmaE4M3;
+                const uint32_t sfb = tmem + TM_SFB + (fp4 ? qb * 4 : 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc_mx(fm, fm, 128, n, kk, kk), sfa, sfb, kk > 0);
+            }
+            tc_commit(empty + s);
+            tc_commit(tfull + a);
+            mbar_arrive(tfull + a);   // releases the key scales written above
+        }
+        __syncwarp();
+    }
+    if (lane == 0) {
+        tc_commit(done_bar);
+        mbar_drain(done_bar, 0);
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ void flush_hist(const ScoreArgs& p, unsigned* hs, const int* rinfo, int row0, int nrows,
+                                           int e) {
+    epi_sync();
+    for (int b = e; b < kHistBins; b += 128) {
+        for (int r = 0; r < nrows; ++r) {
+            if (!rinfo[4 + r]) continue;
+            const unsigned c = hs[r * kHistBins + b];
+            if (c) {
+                atomicAdd(p.hist + static_cast<int64_t>(row0 + r) * kHistBins + b, c);
+                hs[r * kHistBins + b] = 0;
+            }
+        }
+    }
+    epi_sync();
+}
+
+__device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* tfull,
+                                              uint64_t* tempty, volatile int* abort, int t0, int t1, int seg) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = threadIdx.x - 64;
+    const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int m = quarter * 32 + lane;       // key of the tile this thread owns
+    float* wsm = reinterpret_cast<float*>(smem + OFF_W);
+    int* rinfo = reinterpret_cast<int*>(smem + OFF_ROWINFO);   // [0,4): bounds, [4,8): histogram on
+    unsigned* hs = reinterpret_cast<unsigned*>(smem + OFF_HIST);
+    const bool f32scale = (p.fmt == DSA_FMT_FP8);
+    int cur = -1, row0 = 0, nrows = 0, it = 0;
+    bool aborted = false;
+    for (int t = t0; t < t1; ++t, ++it) {
+        while (t >= p.seg_prefix[seg + 1]) ++seg;
+        if (seg != cur) {
+            if (cur >= 0) flush_hist(p, hs, rinfo, row0, nrows, e);
+            cur = seg;
+            const int4 si = p.segs[seg];
+            row0 = si.y;
+            nrows = si.z;
+            if (e < nrows * kHeads)
+                wsm[e] = __bfloat162float(p.w[static_cast<int64_t>(row0 + e / kHeads) * kHeads + e % kHeads]);
+            if (e < nrows) {
+                const int end = p.eff_end[row0 + e];
+                rinfo[e] = end;
+                rinfo[4 + e] = (p.hist_k >= 0 && end > p.hist_k) ? 1 : 0;
+            }
+            epi_sync();
+        }
+        const int j = t - p.seg_prefix[seg];
+        const int a = it & 1;
+        const bool ok = mbar_wait(tfull + a, (it >> 1) & 1, abort, p.status);
+        if (epi_sync_any(!ok)) { aborted = true; break; }
+        tc_fence_after();
+        const float ksm = f32scale ? reinterpret_cast<const float*>(smem + OFF_KS + a * 512)[m] : 1.0f;
+        const int tpos = j * kTileRows + m;
+        for (int r = 0; r < nrows; ++r) {
+            uint32_t v[32];
+            tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC + a * 128 + r * 32, v);
+            tc_wait_ld();
+            const float* wr = wsm + r * kHeads;
+            float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+            for (int h = 0; h < 32; h += 2) {
+                s0 = fmaf(wr[h], fmaxf(__uint_as_float(v[h]), 0.0f), s0);
+                s1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(v[h + 1]), 0.0f), s1);
+            }
+            const float sc = (s0 + s1) * ksm;
+            if (tpos < rinfo[r]) {
+                p.logits[static_cast<int64_t>(row0 + r) * p.ld + tpos] = sc;
+                if (rinfo[4 + r]) atomicAdd(hs + r * kHistBins + hist_bin(sc), 1u);
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(tempty + a);
+    }
+    if (cur >= 0 && !aborted) flush_hist(p, hs, rinfo, row0, nrows, e);
+}
+
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    score_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap smap,
+                 const __grid_constant__ CUtensorMap qmap, const ScoreArgs args) {
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kStages;
+    uint64_t* qfull = bars + 2 * kStages;
+    uint64_t* qempty = qfull + 2;
+    uint64_t* tfull = qempty + 2;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done_bar = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    const int warp = threadIdx.x >> 5;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(qfull + b, 1);
+            mbar_init(qempty + b, 1);
+            mbar_init(tfull + b, 2);
+            mbar_init(tempty + b, 128);
+        }
+        mbar_init(done_bar, 1);
+        *abort = 0;
+        mbar_fence_init();
+        tma_prefetch(&kmap);
+        tma_prefetch(&smap);
+        tma_prefetch(&qmap);
+    }
+    if (warp == 1) tc_alloc(tmem_slot, TM_COLS);
+    unsigned* hs = reinterpret_cast<unsigned*>(smem + OFF_HIST);
+    for (int i = threadIdx.x; i < kSegRows * kHistBins; i += blockDim.x) hs[i] = 0;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    pdl_launch_dependents();
+    pdl_wait();   // the plan kernel's segments and tile prefix
+
+    const int S = args.info[0];
+    const int T = args.info[1];
+    const int64_t G = gridDim.x;
+    const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * T / G);
+    const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * T / G);
+    if (t0 < t1) {
+        const int seg = find_segment(args.seg_prefix, S, t0);
+        if (warp == 0) {
+            if ((threadIdx.x & 31) == 0)
+                producer_role(&kmap, &smap, &qmap, args, smem, full, empty, qfull, qempty, abort, t0, t1, seg);
+        } else if (warp == 1) {
+            mma_role(args, smem, tmem, full, empty, qfull, qempty, tfull, tempty, done_bar, abort, t0, t1, seg);
+        } else {
+            epilogue_role(args, smem, tmem, tfull, tempty, abort, t0, t1, seg);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tc_dealloc(tmem, TM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------- host
+static void* g_time_before = nullptr;
+static void* g_time_after = nullptr;
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" void dsa_set_score_timing(void* before, void* after) {
+    g_time_before = before;
+    g_time_after = after;
+}
+
+extern "C" size_t dsa_workspace_size(int fmt, int64_t rows, int64_t num_requests, int64_t max_pages, int64_t k) {
+    (void)fmt;
+    (void)num_requests;
+    (void)k;
+    if (rows < 0 || max_pages < 0) return 0;
+    return workspace_layout(rows, max_pages * kPage, true, true).total;
+}
+
+extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const void* cache, int64_t page_stride,
+                               int64_t num_pages, const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                               const int32_t* starts, const int32_t* row_ends, int64_t num_requests, int64_t rows,
+                               int64_t max_query_len, float* logits, int64_t logits_ld, int64_t k, int32_t* topk,
+                               void* workspace, size_t workspace_bytes, int32_t* status, void* stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4) return DSA_ERR_UNSUPPORTED;
+    if (rows < 0 || num_requests < 0 || max_pages < 0 || num_pages < 0 || k < 0 || max_query_len < 0)
+        return DSA_ERR_INVALID;
+    if (rows == 0) return DSA_OK;
+    const bool fp4 = (fmt == DSA_FMT_MXFP4);
+    const int64_t width = max_pages * kPage;
+    if (rows > (1 << 30) || num_requests > (1 << 30) || width > (int64_t(1) << 30) || num_pages > 0x7FFFFFFF)
+        return DSA_ERR_UNSUPPORTED;
+    if (!q_rows || !w || !starts || !row_ends || !workspace) return DSA_ERR_INVALID;
+    if (num_pages > 0 && !cache) return DSA_ERR_INVALID;
+    if (max_pages > 0 && num_requests > 0 && (!block_table || bt_stride < max_pages)) return DSA_ERR_INVALID;
+    const int64_t min_stride = fp4 ? DSA_FP4_PAGE_BYTES : DSA_FP8_PAGE_BYTES;
+    if (page_stride < min_stride || page_stride % (fp4 ? 32 : 16)) return DSA_ERR_INVALID;
+    if (!aligned(cache, fp4 ? 32 : 16) || !aligned(q_rows, fp4 ? 32 : 16) || !aligned(workspace, 256) ||
+        !aligned(w, 2))
+        return DSA_ERR_INVALID;
+    if (logits && (logits_ld < width || !aligned(logits, 4))) return DSA_ERR_INVALID;
+    const bool want_topk = (k > 0 && topk != nullptr);
+    if (k > (int64_t(1) << 30)) return DSA_ERR_UNSUPPORTED;
+    const WsLayout L = workspace_layout(rows, width, true, logits == nullptr);
+    if (workspace_bytes < L.total) return DSA_ERR_INVALID;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* out_logits = logits ? logits : reinterpret_cast<float*>(ws + L.logits);
+    const int64_t ld = logits ? logits_ld : width;
+
+    // Tensor maps: key pages, key scales, query rows.
+    CUtensorMap kmap, smap, qmap;
+    const cuuint64_t np = static_cast<cuuint64_t>(num_pages > 0 ? num_pages : 1);
+    uint8_t* cache_b = static_cast<uint8_t*>(const_cast<void*>(cache));
+    void* cache_addr = cache_b ? static_cast<void*>(cache_b) : workspace;   // unused when there are no pages
+    {
+        const cuuint64_t dims[3] = {128, 64, np};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(fp4 ? 64 : 128), static_cast<cuuint64_t>(page_stride)};
+        const cuuint32_t box[3] = {128, 64, 1};
+        if (encode_tiled(&kmap, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                         cache_addr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return DSA_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[2] = {64, np};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(page_stride)};
+        const cuuint32_t box[2] = {64, 1};
+        uint8_t* sbase = cache_b ? cache_b + (fp4 ? kFp4KeyBytes : kFp8KeyBytes) : static_cast<uint8_t*>(workspace);
+        if (encode_tiled(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sbase, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+            return DSA_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[3] = {128, 32, static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(fp4 ? 64 : 128), kQRowBytes};
+        const cuuint32_t box[3] = {128, 32, 1};
+        if (encode_tiled(&qmap, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                         const_cast<void*>(q_rows), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return DSA_ERR_CUDA;
+    }
+
+    int* info = reinterpret_cast<int*>(ws + L.info);
+    int4* segs = reinterpret_cast<int4*>(ws + L.segs);
+    int* seg_prefix = reinterpret_cast<int*>(ws + L.seg_prefix);
+    int* eff_end = reinterpret_cast<int*>(ws + L.eff_end);
+    plan_kernel<<<1, 1024, 0, stream>>>(starts, row_ends, static_cast<int>(num_requests), static_cast<int>(rows),
+                                        static_cast<int>(width), info, segs, seg_prefix, eff_end, status);
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        attr_set = true;
+    }
+    ScoreArgs a;
+    a.fmt = fmt;
+    a.num_pages = static_cast<int>(num_pages);
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.q_rows = static_cast<const uint8_t*>(q_rows);
+    a.w = static_cast<const __nv_bfloat16*>(w);
+    a.info = info;
+    a.segs = segs;
+    a.seg_prefix = seg_prefix;
+    a.eff_end = eff_end;
+    a.logits = out_logits;
+    a.ld = ld;
+    a.hist_k = want_topk ? static_cast<int>(k) : -1;
+    a.hist = reinterpret_cast<unsigned*>(ws + L.hist);
+    a.status = status;
+    if (g_time_before && g_time_after) cudaEventRecord(static_cast<cudaEvent_t>(g_time_before), stream);
+    if (launch_pdl(score_kernel, dim3(device_sm_count()), dim3(kScoreThreads), kScoreSmem, stream, kmap, smap, qmap,
+                   a) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    if (g_time_before && g_time_after) cudaEventRecord(static_cast<cudaEvent_t>(g_time_after), stream);
+    if (!want_topk && !logits) return DSA_OK;
+    return launch_select(out_logits, logits, ld, width, eff_end, rows, want_topk ? k : 0, want_topk ? topk : nullptr,
+                         ws, L, stream, true);
+}

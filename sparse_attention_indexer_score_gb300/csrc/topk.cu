@@ -1,0 +1,364 @@
+// Top-k selection over per-row scores (radix select on order-preserving bits).
+//
+// Page "cutedsl.dsa.overlap": the indexer path is "wq_b -> DsaIndex -> scoring
+// and top-k"; page "amd.ops.fp4_indexer", decode_tile_size, budgets per-row
+// selection scratch next to the logits.
+//
+// Pass 1 (fused into the scoring epilogue, or hist_kernel here): a 2048-bin
+// histogram of the top 11 bits of each row's order-preserving score keys.
+// Pass 2 (select_kernel, several CTAs per row): every CTA finds the boundary
+// bin B where the count from the top reaches k, emits positions in bins above
+// B, and appends bin-B candidates to a per-row buffer.  The last CTA of a row
+// (a done counter, no waiting) resolves the boundary bin with two more radix
+// levels (11 + 10 bits) over the candidates, and clears the row's histogram
+// and counters so the workspace is zero again for the next call.
+#include <mutex>
+
+#include "host.h"
+#include "scan.cuh"
+
+namespace dsa {
+
+constexpr int kSelThreads = 256;
+constexpr int kChunk = 4096;   // positions per select CTA
+
+struct SelectArgs {
+    const float* logits;
+    float* fill;         // when non-null: write -inf at [end, width) of each row
+    int64_t ld;
+    int64_t width;
+    const int32_t* ends;
+    int k;               // 0: fill only
+    int32_t* out;
+    unsigned* hist;
+    int* counters;
+    uint2* cand;
+};
+
+__device__ __forceinline__ int clamp_end(const int32_t* ends, int row, int64_t width) {
+    const int64_t e = ends[row];
+    return static_cast<int>(e < 0 ? 0 : (e > width ? width : e));
+}
+
+// Warp-aggregated atomic increment: returns this lane's slot when pred holds.
+__device__ __forceinline__ int aggregated_inc(int* ctr, bool pred) {
+    const unsigned act = __activemask();
+    const unsigned m = __ballot_sync(act, pred);
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    if (m) {
+        const int leader = __ffs(m) - 1;
+        if (lane == leader) base = atomicAdd(ctr, __popc(m));
+        base = __shfl_sync(act, base, leader);
+    }
+    return base + __popc(m & ((1u << lane) - 1u));
+}
+
+// Finds, over `bins` counts in shared memory, the bin B where the count from
+// the top first reaches `need`; stores B and the count strictly above it.
+__device__ void find_boundary(const unsigned* h, int bins, int need, int* out_bin, int* out_above, int* tmp) {
+    const int per = bins / kSelThreads;   // bins per thread (8 or 4)
+    const int first = bins - (threadIdx.x + 1) * per;   // thread 0 owns the top bins
+    int local = 0;
+    for (int i = 0; i < per; ++i) local += static_cast<int>(h[first + i]);
+    int total;
+    const int inc = block_inclusive_scan(local, tmp, &total);
+    int cum = inc - local;   // count in bins above this thread's range
+    for (int b = first + per - 1; b >= first; --b) {
+        const int c = static_cast<int>(h[b]);
+        if (cum < need && cum + c >= need) {
+            *out_bin = b;
+            *out_above = cum;
+        }
+        cum += c;
+    }
+}
+
+__global__ void __launch_bounds__(kSelThreads) hist_kernel(const float* __restrict__ logits, int64_t ld,
+                                                           int64_t width, const int32_t* __restrict__ ends, int k,
+                                                           unsigned* __restrict__ hist) {
+    __shared__ unsigned h[kHistBins];
+    const int row = blockIdx.x;
+    const int n = clamp_end(ends, row, width);
+    if (n <= k) return;
+    const int64_t lo = static_cast<int64_t>(blockIdx.y) * kChunk;
+    if (lo >= n) return;
+    const int64_t hi = min(static_cast<int64_t>(n), lo + kChunk);
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = 0;
+    __syncthreads();
+    const float* src = logits + static_cast<int64_t>(row) * ld;
+    for (int64_t t = lo + threadIdx.x; t < hi; t += kSelThreads) atomicAdd(&h[hist_bin(src[t])], 1u);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
+        if (h[i]) atomicAdd(hist + static_cast<int64_t>(row) * kHistBins + i, h[i]);
+}
+
+// Streams the boundary-bin candidates of a row: from the candidate buffer when
+// it did not overflow, else by re-reading the row and keeping bin == B.
+struct CandSource {
+    const uint2* buf;
+    int count;
+    bool from_row;
+    const float* row;
+    int n;
+    uint32_t bin;
+    template <typename F>
+    __device__ __forceinline__ void for_each(F&& f) const {
+        if (!from_row) {
+            for (int i = threadIdx.x; i < count; i += kSelThreads) {
+                const uint2 c = buf[i];
+                f(c.x, static_cast<int>(c.y));
+            }
+        } else {
+            for (int t = threadIdx.x; t < n; t += kSelThreads) {
+                const uint32_t key = order_key(row[t]);
+                if ((key >> (32 - kHistBits)) == bin) f(key, t);
+            }
+        }
+    }
+};
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a, int pdl) {
+    __shared__ unsigned h[kHistBins];
+    __shared__ int tmp[32];
+    __shared__ int s_bin, s_above, s_last, s_emit;
+    if (pdl) pdl_wait();
+    const int row = blockIdx.x;
+    const int64_t lo = static_cast<int64_t>(blockIdx.y) * kChunk;
+    const int n = clamp_end(a.ends, row, a.width);
+    if (a.fill) {
+        float* dst = a.fill + static_cast<int64_t>(row) * a.ld;
+        const int64_t hi = min(a.width, lo + kChunk);
+        for (int64_t t = max(lo, static_cast<int64_t>(n)) + threadIdx.x; t < hi; t += kSelThreads)
+            dst[t] = -__int_as_float(0x7F800000);
+    }
+    const int k = a.k;
+    if (k <= 0) return;
+    int32_t* out = a.out + static_cast<int64_t>(row) * k;
+    if (n <= k) {
+        const int64_t hi = min(static_cast<int64_t>(k), lo + kChunk);
+        for (int64_t pos = lo + threadIdx.x; pos < hi; pos += kSelThreads) out[pos] = pos < n ? static_cast<int>(pos) : -1;
+        return;
+    }
+    const int nch = (n + kChunk - 1) / kChunk;
+    if (blockIdx.y >= nch) return;
+    unsigned* ghist = a.hist + static_cast<int64_t>(row) * kHistBins;
+    int* ctr = a.counters + static_cast<int64_t>(row) * 4;
+    uint2* cand = a.cand + static_cast<int64_t>(row) * kCandCap;
+    const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
+
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = ghist[i];
+    if (threadIdx.x == 0) {
+        s_bin = 0;
+        s_above = 0;
+    }
+    __syncthreads();
+    find_boundary(h, kHistBins, k, &s_bin, &s_above, tmp);
+    __syncthreads();
+    const uint32_t B = static_cast<uint32_t>(s_bin);
+    const int64_t hi = min(static_cast<int64_t>(n), lo + kChunk);
+    for (int64_t t0 = lo; t0 < hi; t0 += kSelThreads) {
+        const int64_t t = t0 + threadIdx.x;
+        uint32_t key = 0;
+        if (t < hi) key = order_key(src[t]);
+        const uint32_t b = key >> (32 - kHistBits);
+        const bool win = (t < hi) && b > B;
+        const bool bnd = (t < hi) && b == B;
+        const int pw = aggregated_inc(ctr + 0, win);
+        if (win && pw < k) out[pw] = static_cast<int>(t);
+        const int pc = aggregated_inc(ctr + 1, bnd);
+        if (bnd && pc < kCandCap) cand[pc] = make_uint2(key, static_cast<uint32_t>(t));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = (atomicAdd(ctr + 2, 1) == nch - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // Last CTA of the row: resolve the boundary bin.
+    const int above = s_above;
+    int need = k - above;
+    const int ncand = *reinterpret_cast<volatile int*>(ctr + 1);
+    CandSource srcs{cand, min(ncand, kCandCap), ncand > kCandCap, src, n, B};
+    if (threadIdx.x == 0) s_emit = 0;
+    // level 2: bits [20:10]
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = 0;
+    __syncthreads();
+    srcs.for_each([&](uint32_t key, int) { atomicAdd(&h[(key >> 10) & 0x7FF], 1u); });
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        s_bin = 0;
+        s_above = 0;
+    }
+    __syncthreads();
+    find_boundary(h, kHistBins, need, &s_bin, &s_above, tmp);
+    __syncthreads();
+    const uint32_t B2 = static_cast<uint32_t>(s_bin);
+    const int above2 = s_above;
+    srcs.for_each([&](uint32_t key, int t) {
+        if (((key >> 10) & 0x7FF) > B2) {
+            const int e = atomicAdd(&s_emit, 1);
+            if (e < need) out[above + e] = t;
+        }
+    });
+    // level 3: bits [9:0] among level-2 bin B2
+    for (int i = threadIdx.x; i < 1024; i += kSelThreads) h[i] = 0;
+    __syncthreads();
+    srcs.for_each([&](uint32_t key, int) {
+        if (((key >> 10) & 0x7FF) == B2) atomicAdd(&h[key & 0x3FF], 1u);
+    });
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        s_bin = 0;
+        s_above = 0;
+    }
+    __syncthreads();
+    const int need2 = need - above2;
+    find_boundary(h, 1024, need2, &s_bin, &s_above, tmp);
+    __syncthreads();
+    const uint32_t B3 = static_cast<uint32_t>(s_bin);
+    const uint32_t kB = (B << (32 - kHistBits)) | (B2 << 10) | B3;
+    srcs.for_each([&](uint32_t key, int t) {
+        if (((key >> 10) & 0x7FF) == B2 && (key & 0x3FF) > B3) {
+            const int e = atomicAdd(&s_emit, 1);
+            if (e < need) out[above + e] = t;
+        }
+    });
+    __syncthreads();
+    srcs.for_each([&](uint32_t key, int t) {
+        if (key == kB) {
+            const int e = atomicAdd(&s_emit, 1);
+            if (e < need) out[above + e] = t;
+        }
+    });
+    __syncthreads();
+    // Short only when the histogram disagreed with the scores (an aborted scoring pass).
+    for (int e = s_emit + threadIdx.x; e < need; e += kSelThreads) out[above + e] = -1;
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) ghist[i] = 0;
+    if (threadIdx.x < 4) ctr[threadIdx.x] = 0;
+}
+
+// ----------------------------------------------------------------- host utilities
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout workspace_layout(int64_t rows, int64_t width, bool with_plan, bool with_logits) {
+    WsLayout L{};
+    size_t off = 0;
+    const size_t r = static_cast<size_t>(rows);
+    L.info = off;
+    off = align256(off + (with_plan ? 8 * sizeof(int) : 0));
+    L.segs = off;
+    off = align256(off + (with_plan ? (r + 1) * sizeof(int4) : 0));
+    L.seg_prefix = off;
+    off = align256(off + (with_plan ? (r + 2) * sizeof(int) : 0));
+    L.eff_end = off;
+    off = align256(off + (with_plan ? r * sizeof(int) : 0));
+    L.hist = off;
+    off = align256(off + r * kHistBins * sizeof(unsigned));
+    L.counters = off;
+    off = align256(off + r * 4 * sizeof(int));
+    L.cand = off;
+    off = align256(off + r * kCandCap * sizeof(uint2));
+    L.logits = off;
+    off = align256(off + (with_logits ? r * static_cast<size_t>(width) * sizeof(float) : 0));
+    L.total = off;
+    return L;
+}
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (!cache[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* addr,
+                      const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                      CUtensorMapSwizzle swizzle) {
+    using Fn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                            const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                            CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static Fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<Fn>(p);
+    });
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, type, rank, addr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int launch_select(const float* logits, float* logits_fill, int64_t ld, int64_t width, const int32_t* ends,
+                  int64_t rows, int64_t k, int32_t* out, uint8_t* ws, const WsLayout& L, cudaStream_t stream,
+                  bool pdl) {
+    SelectArgs a;
+    a.logits = logits;
+    a.fill = logits_fill;
+    a.ld = ld;
+    a.width = width;
+    a.ends = ends;
+    a.k = static_cast<int>(k);
+    a.out = out;
+    a.hist = reinterpret_cast<unsigned*>(ws + L.hist);
+    a.counters = reinterpret_cast<int*>(ws + L.counters);
+    a.cand = reinterpret_cast<uint2*>(ws + L.cand);
+    const int64_t span = (k > width) ? k : width;
+    const int64_t chunks = (span + kChunk - 1) / kChunk;
+    if (chunks == 0 || rows == 0) return DSA_OK;
+    if (chunks > 65535 || rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(chunks));
+    cudaError_t err;
+    if (pdl) err = launch_pdl(select_kernel, grid, dim3(kSelThreads), 0, stream, a, 1);
+    else {
+        select_kernel<<<grid, kSelThreads, 0, stream>>>(a, 0);
+        err = cudaGetLastError();
+    }
+    return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" size_t dsa_topk_workspace_size(int64_t rows, int64_t k) {
+    (void)k;
+    if (rows < 0) return 0;
+    return workspace_layout(rows, 0, false, false).total;
+}
+
+extern "C" int dsa_topk(const float* logits, int64_t ld, const int32_t* row_ends, int64_t rows, int64_t width,
+                        int64_t k, int32_t* out, void* workspace, size_t workspace_bytes, void* stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (rows < 0 || width < 0 || k < 0 || ld < width) return DSA_ERR_INVALID;
+    if (rows == 0 || k == 0) return DSA_OK;
+    if (!row_ends || !out || !workspace || (width > 0 && !logits)) return DSA_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return DSA_ERR_INVALID;
+    if (k > (int64_t(1) << 30) || width > (int64_t(1) << 30)) return DSA_ERR_UNSUPPORTED;
+    const WsLayout L = workspace_layout(rows, 0, false, false);
+    if (workspace_bytes < L.total) return DSA_ERR_INVALID;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int64_t chunks = (width + kChunk - 1) / kChunk;
+    if (chunks > 65535 || rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    if (chunks > 0) {
+        hist_kernel<<<dim3(static_cast<unsigned>(rows), static_cast<unsigned>(chunks)), kSelThreads, 0, stream>>>(
+            logits, ld, width, row_ends, static_cast<int>(k), reinterpret_cast<unsigned*>(ws + L.hist));
+        if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    }
+    return launch_select(logits, nullptr, ld, width, row_ends, rows, k, out, ws, L, stream, false);
+}
+
+extern "C" const char* dsa_version(void) { return "dsa-gb300 0.1.0"; }

@@ -1,0 +1,209 @@
+"""Python binding of ``libdsa.so`` (C ABI declared in ``include/dsa.h``).
+
+Argument marshalling only: tensors become device pointers, sizes and strides
+become integers, the current CUDA stream is passed through, and a negative
+return code raises.  Every step of the decode step runs in the library's CUDA
+kernels; there is no fallback path.  The library is loaded on first use and a
+missing library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdsa.so")
+
+FORMATS = {"fp8": 0, "fp8_mx": 1, "mxfp4": 2}
+ERRORS = {-1: "invalid argument", -2: "unsupported", -3: "CUDA launch or driver error"}
+STATUS_BITS = {1: "bad slot", 2: "bad page", 4: "bad geometry", 8: "timeout"}
+Q_ROW_BYTES = 4096
+PAGE_BYTES = {"fp8": 8448, "fp8_mx": 8448, "mxfp4": 4352}
+
+_lib = None
+
+_c = ctypes
+_P = _c.c_void_p
+_I64 = _c.c_int64
+_SIGS = {
+    "dsa_quantize_query": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P]),
+    "dsa_insert_key": (_c.c_int, [_c.c_int, _P, _I64, _P, _P, _c.c_float, _P, _I64, _P, _I64, _I64, _P, _P]),
+    "dsa_decode_layout": (_c.c_int, [_P, _I64, _P, _I64, _I64, _P, _P, _P]),
+    "dsa_workspace_size": (_c.c_size_t, [_c.c_int, _I64, _I64, _I64, _I64]),
+    "dsa_score_paged": (_c.c_int, [_c.c_int, _P, _P, _P, _I64, _I64, _P, _I64, _I64, _P, _P, _I64, _I64, _I64,
+                                   _P, _I64, _I64, _P, _P, _c.c_size_t, _P, _P]),
+    "dsa_topk_workspace_size": (_c.c_size_t, [_I64, _I64]),
+    "dsa_topk": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _P, _P, _c.c_size_t, _P]),
+    "dsa_set_score_timing": (None, [_P, _P]),
+    "dsa_version": (_c.c_char_p, []),
+}
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise RuntimeError(f"{what}: {ERRORS.get(rc, rc)}")
+
+
+def _fmt(fmt: str) -> int:
+    if fmt not in FORMATS:
+        raise ValueError(f"unknown format {fmt!r}; expected one of {sorted(FORMATS)}")
+    return FORMATS[fmt]
+
+
+def quantize_query(fmt: str, q: torch.Tensor, wv: torch.Tensor,
+                   q_out: Optional[torch.Tensor] = None,
+                   w_out: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """q: BF16 [rows, 32, 128] (row stride >= 4096); wv: BF16 [rows, 32].
+    Returns (uint8 [rows, 4096] quantised rows, BF16 [rows, 32] head weights)."""
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or tuple(q.shape[1:]) != (32, 128) or q.stride(2) != 1 \
+            or q.stride(1) != 128:
+        raise ValueError("q must be BF16 [rows, 32, 128] with contiguous heads")
+    if wv.dtype != torch.bfloat16 or wv.dim() != 2 or wv.shape[1] != 32 or wv.stride(1) != 1:
+        raise ValueError("wv must be BF16 [rows, 32]")
+    rows = q.shape[0]
+    if q_out is None:
+        q_out = torch.zeros((rows, Q_ROW_BYTES), dtype=torch.uint8, device=q.device)
+    if w_out is None:
+        w_out = torch.empty((rows, 32), dtype=torch.bfloat16, device=q.device)
+    rc = lib().dsa_quantize_query(_fmt(fmt), _ptr(q), q.stride(0), _ptr(wv), wv.stride(0), rows,
+                                  _ptr(q_out), _ptr(w_out), _stream(q.device))
+    _check(rc, "dsa_quantize_query")
+    return q_out, w_out
+
+
+def insert_key(fmt: str, k: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,
+               slots: torch.Tensor, cache: torch.Tensor, page_stride: int, num_pages: int,
+               status: Optional[torch.Tensor] = None) -> None:
+    """k: BF16 [n, 128]; gamma, beta: FP32 [128]; slots: int64 [n]; cache: uint8 buffer."""
+    if k.dtype != torch.bfloat16 or k.dim() != 2 or k.shape[1] != 128 or k.stride(1) != 1:
+        raise ValueError("k must be BF16 [n, 128] with contiguous rows")
+    if slots.dtype != torch.int64 or slots.dim() != 1 or slots.numel() != k.shape[0] or \
+            (slots.numel() and slots.stride(0) != 1):
+        raise ValueError("slots must be int64 [n], one per key")
+    if gamma.dtype != torch.float32 or beta.dtype != torch.float32 or gamma.numel() != 128 or beta.numel() != 128:
+        raise ValueError("gamma and beta must be FP32 [128]")
+    rc = lib().dsa_insert_key(_fmt(fmt), _ptr(k), k.stride(0), _ptr(gamma), _ptr(beta), float(eps),
+                              _ptr(slots), k.shape[0], _ptr(cache), int(page_stride), int(num_pages),
+                              _ptr(status), _stream(k.device))
+    _check(rc, "dsa_insert_key")
+
+
+def decode_layout(seq_lens: torch.Tensor, query_lens: torch.Tensor, num_rows: int,
+                  starts: Optional[torch.Tensor] = None,
+                  row_ends: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """int32 seq_lens [>= R], query_lens [R] -> (starts int32 [R + 1], row_ends int32 [num_rows])."""
+    if seq_lens.dim() != 1 or query_lens.dim() != 1:
+        raise ValueError("Sequence and query lengths must be one-dimensional")
+    if seq_lens.dtype != torch.int32 or query_lens.dtype != torch.int32:
+        raise ValueError("lengths must be int32")
+    R = query_lens.numel()
+    dev = query_lens.device
+    if starts is None:
+        starts = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    if row_ends is None:
+        row_ends = torch.empty(max(num_rows, 0), dtype=torch.int32, device=dev)
+    rc = lib().dsa_decode_layout(_ptr(seq_lens), seq_lens.numel(), _ptr(query_lens), R, int(num_rows),
+                                 _ptr(starts), _ptr(row_ends), _stream(dev))
+    _check(rc, "dsa_decode_layout")
+    return starts, row_ends
+
+
+def workspace_size(fmt: str, rows: int, num_requests: int, max_pages: int, k: int) -> int:
+    return int(lib().dsa_workspace_size(_fmt(fmt), rows, num_requests, max_pages, k))
+
+
+def topk_workspace_size(rows: int, k: int) -> int:
+    return int(lib().dsa_topk_workspace_size(rows, k))
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled workspace (the library leaves it zero-filled after each call)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def score_paged(fmt: str, q_rows: torch.Tensor, w: torch.Tensor, cache: torch.Tensor, page_stride: int,
+                num_pages: int, block_table: torch.Tensor, starts: torch.Tensor, row_ends: torch.Tensor,
+                max_query_len: int, k: int = 0, want_logits: bool = False,
+                workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                logits: Optional[torch.Tensor] = None, topk_out: Optional[torch.Tensor] = None):
+    """Paged logits (+ top-k).  Returns (logits FP32 [rows, max_pages*64] or None,
+    top-k int32 [rows, k] or None)."""
+    rows = row_ends.numel()
+    R = starts.numel() - 1
+    max_pages = block_table.shape[1] if block_table.dim() == 2 else 0
+    width = max_pages * 64
+    dev = q_rows.device
+    if block_table.dtype != torch.int32 or starts.dtype != torch.int32 or row_ends.dtype != torch.int32:
+        raise ValueError("block_table, starts and row_ends must be int32")
+    if block_table.dim() == 2 and block_table.numel() and block_table.stride(1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    if want_logits and logits is None:
+        logits = torch.empty((rows, width), dtype=torch.float32, device=dev)
+    if k > 0 and topk_out is None:
+        topk_out = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(workspace_size(fmt, rows, R, max_pages, k), dev)
+    rc = lib().dsa_score_paged(
+        _fmt(fmt), _ptr(q_rows), _ptr(w), _ptr(cache), int(page_stride), int(num_pages),
+        _ptr(block_table), block_table.stride(0) if block_table.dim() == 2 else 0, max_pages,
+        _ptr(starts), _ptr(row_ends), R, rows, int(max_query_len),
+        _ptr(logits), logits.stride(0) if logits is not None else 0,
+        int(k), _ptr(topk_out), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+    _check(rc, "dsa_score_paged")
+    return logits, topk_out
+
+
+def topk(logits: torch.Tensor, row_ends: torch.Tensor, k: int, width: Optional[int] = None,
+         workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Top-k positions of each row of FP32 logits [rows, >= width] (valid below row_ends)."""
+    if logits.dtype != torch.float32 or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be FP32 [rows, width] with contiguous rows")
+    rows = logits.shape[0]
+    width = logits.shape[1] if width is None else int(width)
+    if out is None:
+        out = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
+    if workspace is None:
+        workspace = new_workspace(topk_workspace_size(rows, k), logits.device)
+    rc = lib().dsa_topk(_ptr(logits), logits.stride(0), _ptr(row_ends), rows, width, int(k), _ptr(out),
+                        _ptr(workspace), workspace.numel(), _stream(logits.device))
+    _check(rc, "dsa_topk")
+    return out
+
+
+def set_score_timing(before: Optional[torch.cuda.Event], after: Optional[torch.cuda.Event]) -> None:
+    """Record `before`/`after` around the scoring kernel of later score_paged calls."""
+    if before is None or after is None:
+        lib().dsa_set_score_timing(None, None)
+    else:
+        lib().dsa_set_score_timing(before.cuda_event, after.cuda_event)
+
+
+def version() -> str:
+    return lib().dsa_version().decode()

@@ -1,0 +1,67 @@
+"""One decode step of the indexer on the GPU, end to end through the C ABI.
+
+``DecodeIndexer`` owns the device state a serving loop keeps between steps
+(the paged key cache, the block table, a zero-filled workspace) and runs the
+step's five calls on the current stream:
+quantize_query -> insert_key -> decode_layout -> score_paged (+ fused top-k).
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import dsa
+
+
+@dataclass
+class StepOutput:
+    q_rows: torch.Tensor        # uint8 [rows, 4096]
+    w: torch.Tensor             # bf16 [rows, 32]
+    starts: torch.Tensor        # int32 [R + 1]
+    row_ends: torch.Tensor      # int32 [rows]
+    topk: Optional[torch.Tensor]
+    logits: Optional[torch.Tensor]
+
+
+class DecodeIndexer:
+    def __init__(self, fmt: str, num_pages: int, block_table: torch.Tensor, gamma: torch.Tensor,
+                 beta: torch.Tensor, eps: float, max_rows: int, topk: int, device="cuda",
+                 page_stride: Optional[int] = None):
+        self.fmt = fmt
+        self.device = torch.device(device)
+        self.page_stride = int(page_stride or dsa.PAGE_BYTES[fmt])
+        self.num_pages = int(num_pages)
+        self.cache = torch.zeros(max(1, self.num_pages) * self.page_stride, dtype=torch.uint8, device=self.device)
+        self.block_table = block_table.to(self.device, torch.int32).contiguous()
+        self.gamma = gamma.to(self.device, torch.float32).contiguous()
+        self.beta = beta.to(self.device, torch.float32).contiguous()
+        self.eps = float(eps)
+        self.k = int(topk)
+        R = self.block_table.shape[0]
+        max_pages = self.block_table.shape[1]
+        self.workspace = dsa.new_workspace(dsa.workspace_size(fmt, max_rows, R, max_pages, self.k), self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def insert(self, keys: torch.Tensor, slots: torch.Tensor) -> None:
+        dsa.insert_key(self.fmt, keys, self.gamma, self.beta, self.eps, slots, self.cache, self.page_stride,
+                       self.num_pages, self.status)
+
+    def step(self, q: torch.Tensor, wv: torch.Tensor, keys: torch.Tensor, slots: torch.Tensor,
+             seq_lens: torch.Tensor, query_lens: torch.Tensor, max_query_len: int,
+             want_logits: bool = False, topk_out: Optional[torch.Tensor] = None,
+             q_out: Optional[torch.Tensor] = None, w_out: Optional[torch.Tensor] = None) -> StepOutput:
+        rows = q.shape[0]
+        q_rows, w = dsa.quantize_query(self.fmt, q, wv, q_out, w_out)
+        self.insert(keys, slots)
+        starts, row_ends = dsa.decode_layout(seq_lens, query_lens, rows)
+        logits, top = dsa.score_paged(self.fmt, q_rows, w, self.cache, self.page_stride, self.num_pages,
+                                      self.block_table, starts, row_ends, max_query_len, k=self.k,
+                                      want_logits=want_logits, workspace=self.workspace, status=self.status,
+                                      topk_out=topk_out)
+        return StepOutput(q_rows, w, starts, row_ends, top, logits)
+
+    def status_bits(self) -> int:
+        return int(self.status.item())

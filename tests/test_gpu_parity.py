@@ -1,0 +1,213 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on GB300."""
+
+import numpy as np
+import pytest
+
+from dsa_case import bf16_tensor, check_logits, check_topk, gpu_run, oracle_run
+from oracle import indexer as O
+from synth import bf16_bits_to_f32, make_workload
+
+pytestmark = pytest.mark.gpu
+FMTS = ["fp8", "fp8_mx", "mxfp4"]
+
+
+def _special_queries(rng, rows):
+    q = rng.standard_normal((rows, 32, 128)).astype(np.float32)
+    q[0, 0] = 0.0                                   # all-zero head: amax floor
+    q[0, 1] = 1e-12                                 # below the FP8 amax floor
+    q[0, 2] *= 1e30                                 # huge
+    q[0, 3, ::7] *= 40.0                            # outliers
+    q[0, 4] = -0.0
+    q[0, 5, :32] = 0.0                              # one all-zero MXFP4 block
+    q[0, 6] = np.float32(448.0) * np.sign(q[0, 6])  # on the FP8 saturation point
+    q[0, 7, :] = np.float32(6.0)
+    q[1] *= np.float32(2.0 ** -100)                 # tiny but normal
+    u = q.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_quantize_query_bit_exact(cuda_lib, fmt):
+    import torch
+    rng = np.random.default_rng(1)
+    rows = 37
+    qb = _special_queries(rng, rows)
+    wvb = ((rng.standard_normal((rows, 32)).astype(np.float32).view(np.uint32) >> 16)).astype(np.uint16)
+    q_rows, w = cuda_lib.quantize_query(fmt, bf16_tensor(qb, "cuda"), bf16_tensor(wvb, "cuda"))
+    want_rows, want_w = O.quantize_query(fmt, bf16_bits_to_f32(qb), bf16_bits_to_f32(wvb))
+    used = 4096 if fmt != "mxfp4" else 2176
+    got = q_rows.cpu().numpy()
+    assert np.array_equal(got[:, :used], want_rows[:, :used])
+    assert not got[:, used:].any()
+    assert np.array_equal(w.float().cpu().numpy(), want_w)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_insert_key_bit_exact(cuda_lib, fmt):
+    import torch
+    rng = np.random.default_rng(2)
+    n, num_pages = 300, 6
+    x = (rng.standard_normal((n, 128)) * 2.0).astype(np.float32)
+    x[0] = 3.25                                   # zero variance
+    x[1, ::2] = 1e20                              # huge spread
+    x[2] = 0.0
+    x[3, :32] *= 1e-30
+    kb = ((x.view(np.uint32).astype(np.uint64) + 0x7FFF + ((x.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+    gamma = bf16_bits_to_f32(((1 + 0.1 * rng.standard_normal(128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16))
+    beta = bf16_bits_to_f32(((0.1 * rng.standard_normal(128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16))
+    slots = rng.permutation(num_pages * 64)[:n].astype(np.int64)
+    slots[5] = -1
+    slots[6] = num_pages * 64 + 3                 # past the pool
+    stride = O.page_bytes(fmt) + 64               # physical stride above the section size
+    cache = torch.zeros(num_pages * stride, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.insert_key(fmt, bf16_tensor(kb, "cuda"), torch.from_numpy(gamma).cuda(), torch.from_numpy(beta).cuda(),
+                        1e-6, torch.from_numpy(slots).cuda(), cache, stride, num_pages, status)
+    want = np.zeros(num_pages * stride, np.uint8)
+    bad = O.insert_key(fmt, want, stride, num_pages, bf16_bits_to_f32(kb), gamma, beta, 1e-6, slots)
+    assert bad == 1
+    got = cache.cpu().numpy()
+    diff = np.nonzero(got != want)[0]
+    assert diff.size == 0, (diff[:10], got[diff[:10]], want[diff[:10]])
+    assert int(status.item()) & 1
+
+
+def test_decode_layout_parity(cuda_lib):
+    import json, os, torch
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "decode_layout.json")))
+    cases = [(np.array(c["seq_lens"], np.int32), np.array(c["query_lens"], np.int32), c["num_rows"])
+             for c in g["cases"]]
+    rng = np.random.default_rng(4)
+    for _ in range(40):
+        R = int(rng.integers(0, 3000))
+        qlen = rng.integers(0, 6, R).astype(np.int32)
+        seq = rng.integers(0, 70000, R + int(rng.integers(0, 3))).astype(np.int32)
+        cases.append((seq, qlen, int(qlen.sum()) + int(rng.integers(0, 5))))
+    for seq, qlen, num_rows in cases:
+        st, en = cuda_lib.decode_layout(torch.from_numpy(seq).cuda(), torch.from_numpy(qlen).cuda(), num_rows)
+        ws, we = O.decode_layout(seq, qlen, num_rows)
+        assert np.array_equal(st.cpu().numpy(), ws) and np.array_equal(en.cpu().numpy(), we)
+
+
+SMALL = [
+    dict(R=2, seq=(256, 256), qlen=(1, 1)),
+    dict(R=5, seq=(100, 700), qlen=(1, 1)),
+    dict(R=7, seq=(60, 400), qlen=(1, 6), pad_rows=3),      # segments of more than 4 rows
+    dict(R=4, seq=(127, 130), qlen=(2, 4), pad_rows=1),     # ragged tails around one tile
+    dict(R=3, seq=(1, 3), qlen=(1, 3)),                      # bounds of 0..3 keys
+    dict(R=9, seq=(2000, 5000), qlen=(1, 4), pad_rows=2),
+]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_score_topk_parity_small(cuda_lib, fmt, case):
+    spec = dict(SMALL[case])
+    wl = make_workload("tiny_fp8", fmt=fmt, seed=100 + case, topk=[16, 64, 100, 5, 2, 512][case], **spec)
+    g = gpu_run(wl)
+    o = oracle_run(wl)
+    assert g["status"] == 0
+    assert np.array_equal(g["starts"], o["starts"]) and np.array_equal(g["row_ends"], o["row_ends"])
+    used = 4096 if fmt != "mxfp4" else 2176
+    assert np.array_equal(g["q_rows"][:, :used], o["q_rows"][:, :used])
+    rows = range(wl.num_rows)
+    check_logits(g["logits"], o["scores"], o["row_ends"], rows)
+    check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, rows)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_score_cache_bytes_match_oracle(cuda_lib, fmt):
+    """The GPU cache after prefill + step equals the oracle's, page by page."""
+    wl = make_workload("tiny_fp8", fmt=fmt, seed=7, R=3, seq=(100, 300), qlen=(1, 2), topk=8)
+    g = gpu_run(wl)
+    o = oracle_run(wl)
+    cache = g["cache"].cpu().numpy()
+    stride = g["page_stride"]
+    for p_gpu, p_or in o["remap"].items():
+        assert np.array_equal(cache[p_gpu * stride:p_gpu * stride + O.page_bytes(fmt)],
+                              o["cache"][p_or * stride:p_or * stride + O.page_bytes(fmt)]), p_gpu
+
+
+def test_topk_standalone_exact(cuda_lib):
+    import torch
+    rng = np.random.default_rng(5)
+    rows, width = 23, 20000
+    logits = np.round(rng.standard_normal((rows, width)), 2).astype(np.float32)   # heavy ties
+    logits[3] = 1.0                                                               # all equal
+    logits[4, :5000] = -np.inf
+    ends = rng.integers(0, width + 1, rows).astype(np.int32)
+    ends[0], ends[1], ends[2], ends[3] = width, 0, 10, width
+    for k in (1, 7, 64, 2048, 19999):
+        got = cuda_lib.topk(torch.from_numpy(logits).cuda(), torch.from_numpy(ends).cuda(), k).cpu().numpy()
+        want = O.topk(logits, ends, k)
+        for r in range(rows):
+            n = int(ends[r])
+            if n <= k:
+                assert list(got[r]) == list(want[r]), (k, r)
+                continue
+            assert len(set(got[r].tolist())) == k and np.all((got[r] >= 0) & (got[r] < n))
+            kth = logits[r, want[r, k - 1]]
+            g_vals = logits[r, got[r]]
+            assert np.all(g_vals >= kth), (k, r)
+            # the multiset of selected values is unique
+            assert np.array_equal(np.sort(g_vals), np.sort(logits[r, want[r]])), (k, r)
+
+
+def test_workspace_reuse_and_status(cuda_lib):
+    """A second call on the same workspace gives the same answer (the workspace
+    is left zero-filled), and a bad block-table entry sets the status bit."""
+    import torch
+    from dsa_case import bf16_tensor
+    wl = make_workload("tiny_fp8", fmt="fp8", seed=11, R=4, seq=(3000, 6000), qlen=(1, 3), topk=256)
+    g1 = gpu_run(wl)
+    g2 = gpu_run(wl)
+    for r in range(wl.num_rows):
+        assert set(g1["topk"][r].tolist()) == set(g2["topk"][r].tolist())
+    q_rows = torch.from_numpy(g1["q_rows"]).cuda()
+    w = torch.from_numpy(g1["w"]).to(torch.bfloat16).cuda()
+    bt = torch.from_numpy(wl.block_table).cuda()
+    bt[0, 0] = wl.num_pages + 5
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache = torch.zeros(wl.num_pages * 8448, dtype=torch.uint8, device="cuda")
+    cuda_lib.score_paged("fp8", q_rows, w, cache, 8448, wl.num_pages, bt, torch.from_numpy(g1["starts"]).cuda(),
+                         torch.from_numpy(g1["row_ends"]).cuda(), 3, k=16, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 2
+
+
+def test_empty_and_degenerate(cuda_lib):
+    import torch
+    e = torch.zeros(0, dtype=torch.int32, device="cuda")
+    st, en = cuda_lib.decode_layout(e, e, 4)
+    assert st.cpu().tolist() == [0] and en.cpu().tolist() == [0, 0, 0, 0]
+    q = torch.zeros((0, 32, 128), dtype=torch.bfloat16, device="cuda")
+    wv = torch.zeros((0, 32), dtype=torch.bfloat16, device="cuda")
+    r, w = cuda_lib.quantize_query("fp8", q, wv)
+    assert r.shape == (0, 4096)
+    # rows outside every request score nothing: logits -inf, top-k -1
+    wl = make_workload("tiny_fp8", fmt="fp8", seed=3, R=1, seq=(300, 300), qlen=(1, 1), pad_rows=2, topk=8)
+    g = gpu_run(wl)
+    assert np.all(np.isneginf(g["logits"][1:])) and np.all(g["topk"][1:] == -1)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp8", "fp8_decode", "mxfp4_decode", "spec_verify", "long_mxfp4"])
+def test_full_size_sampled_rows(cuda_lib, name):
+    """The named decode-step workloads at full size, in the launch configuration
+    the bench times; the oracle checks a sample of rows (all for the tiny one)."""
+    wl = make_workload(name)
+    g = gpu_run(wl, want_logits=True)
+    assert g["status"] == 0
+    rng = np.random.default_rng(0)
+    real = [r for r in range(wl.num_rows) if wl.row_request[r] >= 0]
+    if name == "tiny_fp8":
+        rows = list(range(wl.num_rows))
+    else:
+        rows = sorted(set(rng.choice(real, size=min(3, len(real)), replace=False).tolist() + [real[-1]]))
+        if name == "spec_verify":
+            rows += [wl.num_rows - 1]     # a padding row
+    o = oracle_run(wl, rows=rows)
+    assert np.array_equal(g["row_ends"], o["row_ends"])
+    used = 4096 if wl.fmt != "mxfp4" else 2176
+    assert np.array_equal(g["q_rows"][:, :used], o["q_rows"][:, :used])
+    check_logits(g["logits"], o["scores"], o["row_ends"], rows)
+    check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, rows)
