@@ -32,6 +32,11 @@ constexpr int kStages = 8;
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * 128;   // codes of 128 keys in shared memory
 constexpr int kPageSmem = 64 * 128;           // one page's codes in shared memory
+// Transaction bytes of one TMA copy count the packed source: a 64-key MXFP4
+// page (16U4_ALIGN16B, unpacked to 8192 bytes of shared memory) counts 4096,
+// an MXFP4 query row 2048.
+constexpr uint32_t kFp8PageTx = 64 * 128, kFp4PageTx = 64 * 64;
+constexpr uint32_t kFp8QRowTx = kQRowBytes, kFp4QRowTx = kQRowBytes / 2;
 constexpr int kSegRows = 4;                   // query rows per segment
 constexpr int kQBufBytes = kSegRows * kQRowBytes;
 constexpr int kScoreThreads = 192;
@@ -176,7 +181,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
             si = p.segs[seg];
             const int qb = i_seg & 1;
             if (!mbar_wait(qempty + qb, ((i_seg >> 1) & 1) ^ 1, abort, p.status)) break;
-            const uint32_t bytes = si.z * (kQRowBytes + (fp4 ? 128u : 0u));
+            const uint32_t bytes = si.z * (fp4 ? kFp4QRowTx + 128u : kFp8QRowTx);
             mbar_arrive_expect_tx(qfull + qb, bytes);
             uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
             for (int r = 0; r < si.z; ++r) {
@@ -200,7 +205,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
                 const int v = p.block_table[static_cast<int64_t>(si.x) * p.bt_stride + pg];
                 if (v >= 0 && v < p.num_pages) {
                     pid[h] = v;
-                    bytes += kPageSmem + 256;
+                    bytes += (fp4 ? kFp4PageTx : kFp8PageTx) + 256;
                 } else if (p.status) {
                     atomicOr(p.status, DSA_STATUS_BAD_PAGE);
                 }
