@@ -73,7 +73,7 @@ typedef enum {
 
 /* Bits of the device status word (OR-ed in by the kernels). */
 #define DSA_STATUS_BAD_SLOT 1       /* a slot >= num_pages * 64 was skipped */
-#define DSA_STATUS_BAD_PAGE 2       /* a block-table entry outside [0, num_pages) was read as zeros */
+#define DSA_STATUS_BAD_PAGE 2       /* a block-table entry outside [0, num_pages) was not loaded; scores of its keys are unspecified */
 #define DSA_STATUS_BAD_GEOMETRY 4   /* starts / row bounds out of range were clamped */
 #define DSA_STATUS_TIMEOUT 8        /* an internal pipeline wait gave up (about 1 s); results invalid */
 
@@ -231,10 +231,18 @@ int dsa_topk(const float* logits, int64_t ld, const int32_t* row_ends,
  * dsa_set_score_timing - profiling hook: when both events are non-NULL,
  * dsa_score_paged records `before` just ahead of its scoring kernel and
  * `after` just behind it on the call's stream, so the scoring kernel alone can
- * be timed.  Pass NULLs to switch it off.  Not thread-safe; events are
- * cudaEvent_t handles owned by the caller.
+ * be timed.  Pass NULLs to switch it off.  Not thread-safe.  The events must
+ * come from dsa_timing_event_create (the library's own CUDA runtime).
  */
 void dsa_set_score_timing(void* before, void* after);
+
+/* dsa_timing_event_create / _destroy / _elapsed_ms - CUDA events of the
+ * library's runtime for dsa_set_score_timing.  _elapsed_ms waits for `end`
+ * and writes the milliseconds between the two records.  Return DSA_OK or
+ * DSA_ERR_CUDA. */
+int dsa_timing_event_create(void** event);
+int dsa_timing_event_destroy(void* event);
+int dsa_timing_elapsed_ms(void* start, void* end, float* ms);
 
 /* dsa_version - library version string. */
 const char* dsa_version(void);

@@ -480,6 +480,26 @@ extern "C" void dsa_set_score_timing(void* before, void* after) {
     g_time_after = after;
 }
 
+extern "C" int dsa_timing_event_create(void** event) {
+    if (!event) return DSA_ERR_INVALID;
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return DSA_ERR_CUDA;
+    *event = static_cast<void*>(e);
+    return DSA_OK;
+}
+
+extern "C" int dsa_timing_event_destroy(void* event) {
+    return cudaEventDestroy(static_cast<cudaEvent_t>(event)) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+extern "C" int dsa_timing_elapsed_ms(void* start, void* end, float* ms) {
+    if (!start || !end || !ms) return DSA_ERR_INVALID;
+    if (cudaEventSynchronize(static_cast<cudaEvent_t>(end)) != cudaSuccess) return DSA_ERR_CUDA;
+    return cudaEventElapsedTime(ms, static_cast<cudaEvent_t>(start), static_cast<cudaEvent_t>(end)) == cudaSuccess
+               ? DSA_OK
+               : DSA_ERR_CUDA;
+}
+
 extern "C" size_t dsa_workspace_size(int fmt, int64_t rows, int64_t num_requests, int64_t max_pages, int64_t k) {
     (void)fmt;
     (void)num_requests;

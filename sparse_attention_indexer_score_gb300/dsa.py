@@ -39,6 +39,9 @@ _SIGS = {
     "dsa_topk_workspace_size": (_c.c_size_t, [_I64, _I64]),
     "dsa_topk": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _P, _P, _c.c_size_t, _P]),
     "dsa_set_score_timing": (None, [_P, _P]),
+    "dsa_timing_event_create": (_c.c_int, [_c.POINTER(_P)]),
+    "dsa_timing_event_destroy": (_c.c_int, [_P]),
+    "dsa_timing_elapsed_ms": (_c.c_int, [_P, _P, _c.POINTER(_c.c_float)]),
     "dsa_version": (_c.c_char_p, []),
 }
 
@@ -197,12 +200,31 @@ def topk(logits: torch.Tensor, row_ends: torch.Tensor, k: int, width: Optional[i
     return out
 
 
-def set_score_timing(before: Optional[torch.cuda.Event], after: Optional[torch.cuda.Event]) -> None:
+class TimingEvent:
+    """A CUDA event of the library's own runtime (for ``set_score_timing``)."""
+
+    def __init__(self):
+        h = _P()
+        _check(lib().dsa_timing_event_create(ctypes.byref(h)), "dsa_timing_event_create")
+        self.handle = h.value
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.dsa_timing_event_destroy(self.handle)
+            self.handle = None
+
+    def elapsed_ms(self, end: "TimingEvent") -> float:
+        ms = _c.c_float()
+        _check(lib().dsa_timing_elapsed_ms(self.handle, end.handle, ctypes.byref(ms)), "dsa_timing_elapsed_ms")
+        return float(ms.value)
+
+
+def set_score_timing(before: Optional[TimingEvent], after: Optional[TimingEvent]) -> None:
     """Record `before`/`after` around the scoring kernel of later score_paged calls."""
     if before is None or after is None:
         lib().dsa_set_score_timing(None, None)
     else:
-        lib().dsa_set_score_timing(before.cuda_event, after.cuda_event)
+        lib().dsa_set_score_timing(before.handle, after.handle)
 
 
 def version() -> str:
