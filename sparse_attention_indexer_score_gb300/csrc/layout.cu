@@ -5,6 +5,7 @@
 // R - 1, and scores keys t < max(0, seq_len - query_len + (r - start) + 1);
 // rows at or past starts[R] are padding with bound 0.  No device-to-host
 // reads: one CTA scans the query lengths, then bounds every row.
+#include "host.h"
 #include "scan.cuh"
 
 namespace dsa {
@@ -15,6 +16,8 @@ __global__ void __launch_bounds__(1024) decode_layout_kernel(const int32_t* __re
                                                              int32_t* __restrict__ row_ends) {
     __shared__ int warp_tmp[32];
     __shared__ int chunk_total;
+    pdl_launch_dependents();
+    pdl_wait();
     int carry = 0;
     if (threadIdx.x == 0) starts[0] = 0;
     for (int base = 0; base < num_req; base += blockDim.x) {
@@ -55,7 +58,8 @@ extern "C" int dsa_decode_layout(const int32_t* seq_lens, int64_t num_seq, const
     if (num_requests > 0x7FFFFFFF - 1 || num_rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
     if (!starts || (num_rows > 0 && !row_ends) || (num_requests > 0 && (!seq_lens || !query_lens)))
         return DSA_ERR_INVALID;
-    decode_layout_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
-        seq_lens, query_lens, static_cast<int>(num_requests), num_rows, starts, row_ends);
-    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    const cudaError_t err = launch_pdl(decode_layout_kernel, dim3(1), dim3(1024), 0, static_cast<cudaStream_t>(stream),
+                                       seq_lens, query_lens, static_cast<int>(num_requests), num_rows, starts,
+                                       row_ends);
+    return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

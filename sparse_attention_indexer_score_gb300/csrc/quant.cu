@@ -3,6 +3,7 @@
 //
 // Page "cutedsl.dsa.index": DsaIndex.fp8_query, quantize_fp4_query,
 // insert_key, insert_fp4_key, mxfp4_scale (definition only), e2m1x2.
+#include "host.h"
 #include "common.cuh"
 
 namespace dsa {
@@ -52,6 +53,8 @@ __global__ void __launch_bounds__(256) quantize_query_kernel(int fmt, const uint
                                                              int64_t wv_stride, int64_t rows,
                                                              uint8_t* __restrict__ q_out,
                                                              __nv_bfloat16* __restrict__ w_out) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (gw >= rows * kHeads) return;
@@ -104,6 +107,8 @@ __global__ void __launch_bounds__(256) insert_key_kernel(int fmt, const uint16_t
                                                          const int64_t* __restrict__ slots, int64_t n,
                                                          uint8_t* __restrict__ cache, int64_t page_stride,
                                                          int64_t num_pages, int32_t* status) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t key = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
     const int j = threadIdx.x & 15;
     const unsigned hmask = (threadIdx.x & 16) ? 0xFFFF0000u : 0x0000FFFFu;
@@ -210,10 +215,11 @@ extern "C" int dsa_quantize_query(int fmt, const void* q, int64_t q_row_stride, 
     const int64_t warps = rows * kHeads;
     const int64_t blocks = (warps * 32 + 255) / 256;
     if (blocks > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
-    quantize_query_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        fmt, static_cast<const uint16_t*>(q), q_row_stride, static_cast<const uint16_t*>(wv), wv_row_stride, rows,
-        static_cast<uint8_t*>(q_out), static_cast<__nv_bfloat16*>(w_out));
-    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    const cudaError_t err = launch_pdl(quantize_query_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                       static_cast<cudaStream_t>(stream), fmt, static_cast<const uint16_t*>(q),
+                                       q_row_stride, static_cast<const uint16_t*>(wv), wv_row_stride, rows,
+                                       static_cast<uint8_t*>(q_out), static_cast<__nv_bfloat16*>(w_out));
+    return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 extern "C" int dsa_insert_key(int fmt, const void* k, int64_t k_row_stride, const float* gamma, const float* beta,
@@ -230,8 +236,9 @@ extern "C" int dsa_insert_key(int fmt, const void* k, int64_t k_row_stride, cons
         return DSA_ERR_INVALID;
     const int64_t blocks = (n * 16 + 255) / 256;
     if (blocks > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
-    insert_key_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        fmt, static_cast<const uint16_t*>(k), k_row_stride, gamma, beta, eps, slots, n,
-        static_cast<uint8_t*>(cache), page_stride, num_pages, status);
-    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    const cudaError_t err = launch_pdl(insert_key_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                       static_cast<cudaStream_t>(stream), fmt, static_cast<const uint16_t*>(k),
+                                       k_row_stride, gamma, beta, eps, slots, n, static_cast<uint8_t*>(cache),
+                                       page_stride, num_pages, status);
+    return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
                                                     int* __restrict__ seg_prefix, int* __restrict__ eff_end,
                                                     int32_t* status) {
     pdl_launch_dependents();
+    pdl_wait();
     __shared__ int warp_tmp[32];
     __shared__ int chunk_total;
     for (int r = threadIdx.x; r < rows; r += blockDim.x) eff_end[r] = 0;
@@ -167,65 +168,117 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 }
 
 // ----------------------------------------------------------------- roles
+// Per-tile load plan resolved by one lane of the producer warp.
+struct TilePlan {
+    int seg;   // segment of the tile
+    int pid0;  // physical page of keys 0..63 (-1: none)
+    int pid1;  // physical page of keys 64..127 (-1: none)
+};
+
+__device__ __forceinline__ TilePlan plan_tile(const ScoreArgs& p, int t, int t1, int seg, int S) {
+    TilePlan tp{-1, -1, -1};
+    if (t >= t1) return tp;
+    if (t >= p.seg_prefix[seg + 1]) {
+        // binary search in (seg, S): the tile lies past the starting segment
+        int lo = seg + 1, hi = S;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.seg_prefix[mid] <= t) lo = mid; else hi = mid;
+        }
+        seg = lo;
+    }
+    tp.seg = seg;
+    const int4 si = p.segs[seg];
+    const int j = t - p.seg_prefix[seg];
+    const int npages = (si.w + kPage - 1) / kPage;
+    const int32_t* row = p.block_table + static_cast<int64_t>(si.x) * p.bt_stride;
+    bool bad = false;
+    if (2 * j < npages) {
+        const int v = row[2 * j];
+        if (v >= 0 && v < p.num_pages) tp.pid0 = v; else bad = true;
+    }
+    if (2 * j + 1 < npages) {
+        const int v = row[2 * j + 1];
+        if (v >= 0 && v < p.num_pages) tp.pid1 = v; else bad = true;
+    }
+    if (bad && p.status) atomicOr(p.status, DSA_STATUS_BAD_PAGE);
+    return tp;
+}
+
+// Warp 0.  Its 32 lanes resolve the segments and block-table entries of 32
+// tiles at once (the next batch's loads are in flight while lane 0 issues the
+// current batch's TMA copies), so block-table latency is paid once per batch.
 __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUtensorMap* smap,
                                               const CUtensorMap* qmap, const ScoreArgs& p, uint8_t* smem,
                                               uint64_t* full, uint64_t* empty, uint64_t* qfull, uint64_t* qempty,
                                               volatile int* abort, int t0, int t1, int seg) {
+    const int lane = threadIdx.x & 31;
     const bool fp4 = (p.fmt == DSA_FMT_MXFP4);
     int cur = -1, i_seg = 0, it = 0;
-    int4 si = make_int4(0, 0, 0, 0);
-    for (int t = t0; t < t1; ++t, ++it) {
-        while (t >= p.seg_prefix[seg + 1]) ++seg;
-        if (seg != cur) {
-            cur = seg;
-            si = p.segs[seg];
-            const int qb = i_seg & 1;
-            if (!mbar_wait(qempty + qb, ((i_seg >> 1) & 1) ^ 1, abort, p.status)) break;
-            const uint32_t bytes = si.z * (fp4 ? kFp4QRowTx + 128u : kFp8QRowTx);
-            mbar_arrive_expect_tx(qfull + qb, bytes);
-            uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
-            for (int r = 0; r < si.z; ++r) {
-                tma_load_3d(qdst + r * kQRowBytes, qmap, 0, 0, si.y + r, qfull + qb);
-                if (fp4)
-                    bulk_load(smem + OFF_QSF + qb * 512 + r * 128,
-                              p.q_rows + static_cast<int64_t>(si.y + r) * kQRowBytes + kFp4Scales, 128, qfull + qb);
-            }
-            ++i_seg;
-        }
-        const int j = t - p.seg_prefix[seg];
-        const int s = it % kStages;
-        if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status)) break;
-        const int npages = (si.w + kPage - 1) / kPage;
-        int pid[2];
-        uint32_t bytes = 0;
-        for (int h = 0; h < 2; ++h) {
-            const int pg = 2 * j + h;
-            pid[h] = -1;
-            if (pg < npages) {
-                const int v = p.block_table[static_cast<int64_t>(si.x) * p.bt_stride + pg];
-                if (v >= 0 && v < p.num_pages) {
-                    pid[h] = v;
-                    bytes += (fp4 ? kFp4PageTx : kFp8PageTx) + 256;
-                } else if (p.status) {
-                    atomicOr(p.status, DSA_STATUS_BAD_PAGE);
+    bool ok = true;
+    const int S = p.info[0];
+    TilePlan nxt = plan_tile(p, t0 + lane, t1, seg, S);
+    for (int base = t0; base < t1 && ok; base += 32) {
+        const TilePlan mine = nxt;
+        const int last = min(31, t1 - 1 - base);
+        const int seg_end = __shfl_sync(0xFFFFFFFFu, mine.seg, last);
+        if (base + 32 < t1) nxt = plan_tile(p, base + 32 + lane, t1, seg_end, S);
+        for (int i = 0; i <= last; ++i) {
+            const int sg = __shfl_sync(0xFFFFFFFFu, mine.seg, i);
+            const int p0 = __shfl_sync(0xFFFFFFFFu, mine.pid0, i);
+            const int p1 = __shfl_sync(0xFFFFFFFFu, mine.pid1, i);
+            if (lane == 0) {
+                if (sg != cur) {
+                    cur = sg;
+                    const int4 si = p.segs[sg];
+                    const int qb = i_seg & 1;
+                    ok = mbar_wait(qempty + qb, ((i_seg >> 1) & 1) ^ 1, abort, p.status);
+                    if (ok) {
+                        const uint32_t bytes = si.z * (fp4 ? kFp4QRowTx + 128u : kFp8QRowTx);
+                        mbar_arrive_expect_tx(qfull + qb, bytes);
+                        uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
+                        for (int r = 0; r < si.z; ++r) {
+                            tma_load_3d(qdst + r * kQRowBytes, qmap, 0, 0, si.y + r, qfull + qb);
+                            if (fp4)
+                                bulk_load(smem + OFF_QSF + qb * 512 + r * 128,
+                                          p.q_rows + static_cast<int64_t>(si.y + r) * kQRowBytes + kFp4Scales, 128,
+                                          qfull + qb);
+                        }
+                        ++i_seg;
+                    }
+                }
+                const int s = it % kStages;
+                ok = ok && mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status);
+                if (ok) {
+                    const uint32_t page_tx = (fp4 ? kFp4PageTx : kFp8PageTx) + 256;
+                    const uint32_t bytes = (p0 >= 0 ? page_tx : 0u) + (p1 >= 0 ? page_tx : 0u);
+                    if (bytes == 0) {
+                        mbar_arrive(full + s);   // no valid page: scores of these keys are unspecified
+                    } else {
+                        mbar_arrive_expect_tx(full + s, bytes);
+                        uint8_t* dst = smem + OFF_TILES + s * kTileBytes;
+                        if (p0 >= 0) {
+                            tma_load_3d(dst, kmap, 0, 0, p0, full + s);
+                            tma_load_2d(smem + OFF_RAWSC + s * 512, smap, 0, p0, full + s);
+                        }
+                        if (p1 >= 0) {
+                            tma_load_3d(dst + kPageSmem, kmap, 0, 0, p1, full + s);
+                            tma_load_2d(smem + OFF_RAWSC + s * 512 + 256, smap, 0, p1, full + s);
+                        }
+                    }
+                    ++it;
                 }
             }
-        }
-        if (bytes == 0) {
-            mbar_arrive(full + s);   // nothing valid to load; scores of these keys are unspecified
-        } else {
-            mbar_arrive_expect_tx(full + s, bytes);
-            uint8_t* dst = smem + OFF_TILES + s * kTileBytes;
-            for (int h = 0; h < 2; ++h) {
-                if (pid[h] < 0) continue;
-                tma_load_3d(dst + h * kPageSmem, kmap, 0, 0, pid[h], full + s);
-                tma_load_2d(smem + OFF_RAWSC + s * 512 + h * 256, smap, 0, pid[h], full + s);
-            }
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
         }
     }
-    // Drain: every copy issued must have landed before the CTA exits.
-    for (int i = max(0, it - kStages); i < it; ++i) mbar_drain(full + (i % kStages), (i / kStages) & 1);
-    for (int i = max(0, i_seg - 2); i < i_seg; ++i) mbar_drain(qfull + (i & 1), (i >> 1) & 1);
+    if (lane == 0) {
+        // Drain: every copy issued must have landed before the CTA exits.
+        for (int i = max(0, it - kStages); i < it; ++i) mbar_drain(full + (i % kStages), (i / kStages) & 1);
+        for (int i = max(0, i_seg - 2); i < i_seg; ++i) mbar_drain(qfull + (i & 1), (i >> 1) & 1);
+    }
+    __syncwarp();
 }
 
 __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* full,
@@ -384,9 +437,14 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
                 s1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(v[h + 1]), 0.0f), s1);
             }
             const float sc = (s0 + s1) * ksm;
-            if (tpos < rinfo[r]) {
-                p.logits[static_cast<int64_t>(row0 + r) * p.ld + tpos] = sc;
-                if (rinfo[4 + r]) atomicAdd(hs + r * kHistBins + hist_bin(sc), 1u);
+            const bool valid = tpos < rinfo[r];
+            if (valid) p.logits[static_cast<int64_t>(row0 + r) * p.ld + tpos] = sc;
+            const unsigned counted = __ballot_sync(0xFFFFFFFFu, valid && rinfo[4 + r]);
+            if (valid && rinfo[4 + r]) {
+                // one shared-memory add per distinct bin of the warp
+                const uint32_t bin = hist_bin(sc);
+                const unsigned peers = __match_any_sync(counted, bin);
+                if (lane == __ffs(peers) - 1) atomicAdd(hs + r * kHistBins + bin, static_cast<unsigned>(__popc(peers)));
             }
         }
         tc_fence_before();
@@ -449,8 +507,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (t0 < t1) {
         const int seg = find_segment(args.seg_prefix, S, t0);
         if (warp == 0) {
-            if ((threadIdx.x & 31) == 0)
-                producer_role(&kmap, &smap, &qmap, args, smem, full, empty, qfull, qempty, abort, t0, t1, seg);
+            producer_role(&kmap, &smap, &qmap, args, smem, full, empty, qfull, qempty, abort, t0, t1, seg);
         } else if (warp == 1) {
             mma_role(args, smem, tmem, full, empty, qfull, qempty, tfull, tempty, done_bar, abort, t0, t1, seg);
         } else {
@@ -574,9 +631,10 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     int4* segs = reinterpret_cast<int4*>(ws + L.segs);
     int* seg_prefix = reinterpret_cast<int*>(ws + L.seg_prefix);
     int* eff_end = reinterpret_cast<int*>(ws + L.eff_end);
-    plan_kernel<<<1, 1024, 0, stream>>>(starts, row_ends, static_cast<int>(num_requests), static_cast<int>(rows),
-                                        static_cast<int>(width), info, segs, seg_prefix, eff_end, status);
-    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, starts, row_ends, static_cast<int>(num_requests),
+                   static_cast<int>(rows), static_cast<int>(width), info, segs, seg_prefix, eff_end,
+                   status) != cudaSuccess)
+        return DSA_ERR_CUDA;
 
     static bool attr_set = false;
     if (!attr_set) {

@@ -21,6 +21,8 @@ namespace dsa {
 
 constexpr int kSelThreads = 256;
 constexpr int kChunk = 4096;   // positions per select CTA
+constexpr int kPerThread = kChunk / kSelThreads;
+constexpr int kRefineCap = 4096;   // boundary candidates the last CTA keeps in shared memory
 
 struct SelectArgs {
     const float* logits;
@@ -78,6 +80,8 @@ __global__ void __launch_bounds__(kSelThreads) hist_kernel(const float* __restri
                                                            int64_t width, const int32_t* __restrict__ ends, int k,
                                                            unsigned* __restrict__ hist) {
     __shared__ unsigned h[kHistBins];
+    pdl_launch_dependents();
+    pdl_wait();
     const int row = blockIdx.x;
     const int n = clamp_end(ends, row, width);
     if (n <= k) return;
@@ -87,24 +91,33 @@ __global__ void __launch_bounds__(kSelThreads) hist_kernel(const float* __restri
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = 0;
     __syncthreads();
     const float* src = logits + static_cast<int64_t>(row) * ld;
-    for (int64_t t = lo + threadIdx.x; t < hi; t += kSelThreads) atomicAdd(&h[hist_bin(src[t])], 1u);
+    float v[kPerThread];
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t t = lo + i * kSelThreads + threadIdx.x;
+        v[i] = t < hi ? src[t] : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i)
+        if (lo + i * kSelThreads + threadIdx.x < hi) atomicAdd(&h[hist_bin(v[i])], 1u);
     __syncthreads();
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
         if (h[i]) atomicAdd(hist + static_cast<int64_t>(row) * kHistBins + i, h[i]);
 }
 
-// Streams the boundary-bin candidates of a row: from the candidate buffer when
-// it did not overflow, else by re-reading the row and keeping bin == B.
+// Streams the boundary-bin candidates of a row: from shared memory when they
+// fit, else from the candidate buffer when it did not overflow, else by
+// re-reading the row and keeping bin == B.
 struct CandSource {
     const uint2* buf;
     int count;
-    bool from_row;
+    int mode;   // 0: shared-memory copy, 1: global buffer, 2: re-read the row
     const float* row;
     int n;
     uint32_t bin;
     template <typename F>
     __device__ __forceinline__ void for_each(F&& f) const {
-        if (!from_row) {
+        if (mode != 2) {
             for (int i = threadIdx.x; i < count; i += kSelThreads) {
                 const uint2 c = buf[i];
                 f(c.x, static_cast<int>(c.y));
@@ -122,6 +135,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     __shared__ unsigned h[kHistBins];
     __shared__ int tmp[32];
     __shared__ int s_bin, s_above, s_last, s_emit;
+    __shared__ uint2 cbuf[kRefineCap];
     if (pdl) pdl_wait();
     const int row = blockIdx.x;
     const int64_t lo = static_cast<int64_t>(blockIdx.y) * kChunk;
@@ -146,7 +160,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     int* ctr = a.counters + static_cast<int64_t>(row) * 4;
     uint2* cand = a.cand + static_cast<int64_t>(row) * kCandCap;
     const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
-
+    const int64_t hi = min(static_cast<int64_t>(n), lo + kChunk);
+    float v[kPerThread];   // this CTA's scores, loaded while the histogram is read
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t t = lo + i * kSelThreads + threadIdx.x;
+        v[i] = t < hi ? src[t] : 0.0f;
+    }
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = ghist[i];
     if (threadIdx.x == 0) {
         s_bin = 0;
@@ -156,11 +176,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     find_boundary(h, kHistBins, k, &s_bin, &s_above, tmp);
     __syncthreads();
     const uint32_t B = static_cast<uint32_t>(s_bin);
-    const int64_t hi = min(static_cast<int64_t>(n), lo + kChunk);
-    for (int64_t t0 = lo; t0 < hi; t0 += kSelThreads) {
-        const int64_t t = t0 + threadIdx.x;
-        uint32_t key = 0;
-        if (t < hi) key = order_key(src[t]);
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t t = lo + i * kSelThreads + threadIdx.x;
+        const uint32_t key = order_key(v[i]);
         const uint32_t b = key >> (32 - kHistBits);
         const bool win = (t < hi) && b > B;
         const bool bnd = (t < hi) && b == B;
@@ -182,7 +201,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     const int above = s_above;
     int need = k - above;
     const int ncand = *reinterpret_cast<volatile int*>(ctr + 1);
-    CandSource srcs{cand, min(ncand, kCandCap), ncand > kCandCap, src, n, B};
+    CandSource srcs{cand, min(ncand, kCandCap), ncand > kCandCap ? 2 : 1, src, n, B};
+    if (ncand <= kRefineCap) {
+        for (int i = threadIdx.x; i < ncand; i += kSelThreads) cbuf[i] = cand[i];
+        srcs.buf = cbuf;
+        srcs.mode = 0;
+    }
     if (threadIdx.x == 0) s_emit = 0;
     // level 2: bits [20:10]
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = 0;
@@ -354,11 +378,12 @@ extern "C" int dsa_topk(const float* logits, int64_t ld, const int32_t* row_ends
     const int64_t chunks = (width + kChunk - 1) / kChunk;
     if (chunks > 65535 || rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
     if (chunks > 0) {
-        hist_kernel<<<dim3(static_cast<unsigned>(rows), static_cast<unsigned>(chunks)), kSelThreads, 0, stream>>>(
-            logits, ld, width, row_ends, static_cast<int>(k), reinterpret_cast<unsigned*>(ws + L.hist));
-        if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+        if (launch_pdl(hist_kernel, dim3(static_cast<unsigned>(rows), static_cast<unsigned>(chunks)),
+                       dim3(kSelThreads), 0, stream, logits, ld, width, row_ends, static_cast<int>(k),
+                       reinterpret_cast<unsigned*>(ws + L.hist)) != cudaSuccess)
+            return DSA_ERR_CUDA;
     }
-    return launch_select(logits, nullptr, ld, width, row_ends, rows, k, out, ws, L, stream, false);
+    return launch_select(logits, nullptr, ld, width, row_ends, rows, k, out, ws, L, stream, true);
 }
 
 extern "C" const char* dsa_version(void) { return "dsa-gb300 0.1.0"; }
