@@ -59,7 +59,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
         objs = list(pool.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    # Shared CUDA runtime: in a process that imported torch, the loader reuses
+    # torch's libcudart.so.13, so the library and torch share one runtime
+    # (current device, streams, events).  The rpath is the fallback for C callers.
+    libdir = os.path.join(os.path.dirname(os.path.dirname(cc)), "lib64")
+    cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, f"-Xlinker=-rpath,{libdir}"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
