@@ -228,6 +228,32 @@ int dsa_topk(const float* logits, int64_t ld, const int32_t* row_ends,
              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dsa_topk_noalloc - dsa_topk for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot obtain scratch memory when they call the library: a serving engine
+ * that reserved nearly all HBM for its KV cache up front and forbids further
+ * cudaMalloc, or a plugin host that passes a kernel its inputs and outputs but
+ * no allocator.  It computes what dsa_topk computes, with the same arguments
+ * minus the workspace.  Its scratch is a file-scope device array of
+ * DSA_TOPK_NOALLOC_MAX_ROWS rows (about 4.7 MB), held by every GPU that loads
+ * the library until the process exits.
+ *
+ *   - rows > DSA_TOPK_NOALLOC_MAX_ROWS returns DSA_ERR_UNSUPPORTED (split the rows
+ *     over several calls).
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array: it clears the parts that must start at
+ *     zero on its stream, but calls that overlap on the GPU (other streams or
+ *     other threads) race and must be serialised by the caller.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define DSA_TOPK_NOALLOC_MAX_ROWS 64
+int dsa_topk_noalloc(const float* logits, int64_t ld, const int32_t* row_ends,
+                     int64_t rows, int64_t width, int64_t k, int32_t* out, void* stream);
+
+/*
  * dsa_set_score_timing - profiling hook: when both events are non-NULL,
  * dsa_score_paged records `before` just ahead of its scoring kernel and
  * `after` just behind it on the call's stream, so the scoring kernel alone can

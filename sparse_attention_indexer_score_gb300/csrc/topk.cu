@@ -387,3 +387,64 @@ extern "C" int dsa_topk(const float* logits, int64_t ld, const int32_t* row_ends
 }
 
 extern "C" const char* dsa_version(void) { return "dsa-gb300 0.1.0"; }
+
+// ----------------------------------------------------------------- top-k without allocation
+// Some callers cannot allocate device memory when they call the library: a
+// serving engine that reserved nearly all HBM for its KV cache up front and
+// forbids further cudaMalloc, or a plugin host that hands a kernel its inputs
+// and outputs but no allocator.  dsa_topk_noalloc serves them with scratch that
+// lives in this file-scope array instead of a caller workspace.  Every GPU that
+// loads the library holds the array until the process exits.
+namespace dsa {
+
+constexpr size_t noalloc_align(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t kNoAllocBytes = noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kHistBins * sizeof(unsigned)) +
+                                 noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * 4 * sizeof(int)) +
+                                 noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kCandCap * sizeof(uint2));
+
+static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocBytes];
+
+// Device address of g_topk_scratch on the current device, looked up once per
+// device (in host code the array's name is only a stand-in, not an address).
+static int noalloc_scratch(uint8_t** ptr) {
+    static std::mutex mu;
+    static uint8_t* addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || !p) return DSA_ERR_CUDA;
+        addr[dev] = static_cast<uint8_t*>(p);
+    }
+    *ptr = addr[dev];
+    return DSA_OK;
+}
+
+}  // namespace dsa
+
+extern "C" int dsa_topk_noalloc(const float* logits, int64_t ld, const int32_t* row_ends, int64_t rows,
+                                int64_t width, int64_t k, int32_t* out, void* stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (rows < 0 || width < 0 || k < 0 || ld < width) return DSA_ERR_INVALID;
+    if (rows > DSA_TOPK_NOALLOC_MAX_ROWS) return DSA_ERR_UNSUPPORTED;   // past the static scratch
+    if (rows == 0 || k == 0) return DSA_OK;
+    if (!row_ends || !out || (width > 0 && !logits)) return DSA_ERR_INVALID;
+    if (k > (int64_t(1) << 30) || width > (int64_t(1) << 30)) return DSA_ERR_UNSUPPORTED;
+    const int64_t chunks = (width + kChunk - 1) / kChunk;
+    if (chunks > 65535) return DSA_ERR_UNSUPPORTED;
+    uint8_t* ws = nullptr;
+    const int rc = noalloc_scratch(&ws);
+    if (rc != DSA_OK) return rc;
+    const WsLayout L = workspace_layout(rows, 0, false, false);
+    if (L.total > kNoAllocBytes) return DSA_ERR_UNSUPPORTED;
+    // The array keeps the last call's contents: clear the histograms and counters.
+    if (cudaMemsetAsync(ws + L.hist, 0, L.cand - L.hist, stream) != cudaSuccess) return DSA_ERR_CUDA;
+    if (chunks > 0) {
+        if (launch_pdl(hist_kernel, dim3(static_cast<unsigned>(rows), static_cast<unsigned>(chunks)),
+                       dim3(kSelThreads), 0, stream, logits, ld, width, row_ends, static_cast<int>(k),
+                       reinterpret_cast<unsigned*>(ws + L.hist)) != cudaSuccess)
+            return DSA_ERR_CUDA;
+    }
+    return launch_select(logits, nullptr, ld, width, row_ends, rows, k, out, ws, L, stream, true);
+}

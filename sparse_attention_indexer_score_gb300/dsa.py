@@ -38,6 +38,7 @@ _SIGS = {
                                    _P, _I64, _I64, _P, _P, _c.c_size_t, _P, _P]),
     "dsa_topk_workspace_size": (_c.c_size_t, [_I64, _I64]),
     "dsa_topk": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _P, _P, _c.c_size_t, _P]),
+    "dsa_topk_noalloc": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _P, _P]),
     "dsa_set_score_timing": (None, [_P, _P]),
     "dsa_timing_event_create": (_c.c_int, [_c.POINTER(_P)]),
     "dsa_timing_event_destroy": (_c.c_int, [_P]),
@@ -217,6 +218,28 @@ class TimingEvent:
         ms = _c.c_float()
         _check(lib().dsa_timing_elapsed_ms(self.handle, end.handle, ctypes.byref(ms)), "dsa_timing_elapsed_ms")
         return float(ms.value)
+
+
+TOPK_NOALLOC_MAX_ROWS = 64
+
+
+def topk_noalloc(logits: torch.Tensor, row_ends: torch.Tensor, k: int, width: Optional[int] = None,
+                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """``topk`` without a workspace, for callers that cannot allocate device
+    memory: the library's own static scratch (at most 64 rows) is used instead.
+    Pass ``out`` to avoid the one allocation this wrapper would make."""
+    if logits.dtype != torch.float32 or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be FP32 [rows, width] with contiguous rows")
+    rows = logits.shape[0]
+    if rows > TOPK_NOALLOC_MAX_ROWS:
+        raise ValueError(f"topk_noalloc handles at most {TOPK_NOALLOC_MAX_ROWS} rows per call, got {rows}")
+    width = logits.shape[1] if width is None else int(width)
+    if out is None:
+        out = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
+    rc = lib().dsa_topk_noalloc(_ptr(logits), logits.stride(0), _ptr(row_ends), rows, width, int(k), _ptr(out),
+                                _stream(logits.device))
+    _check(rc, "dsa_topk_noalloc")
+    return out
 
 
 def set_score_timing(before: Optional[TimingEvent], after: Optional[TimingEvent]) -> None:
