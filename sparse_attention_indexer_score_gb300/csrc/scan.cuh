@@ -7,7 +7,8 @@ namespace dsa {
 
 // Inclusive scan of one int per thread over a block of up to 1024 threads.
 // `warp_tmp` is shared scratch of 32 ints.  Returns the inclusive prefix; the
-// block total is written to *total (all threads read it after the call).
+// block total is written to *total, which must be shared memory (all threads
+// read it after the call; one thread writes it).
 __device__ __forceinline__ int block_inclusive_scan(int v, int* warp_tmp, int* total) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;

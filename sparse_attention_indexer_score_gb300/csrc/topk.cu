@@ -42,20 +42,6 @@ __device__ __forceinline__ int clamp_end(const int32_t* ends, int row, int64_t w
     return static_cast<int>(e < 0 ? 0 : (e > width ? width : e));
 }
 
-// Warp-aggregated atomic increment: returns this lane's slot when pred holds.
-__device__ __forceinline__ int aggregated_inc(int* ctr, bool pred) {
-    const unsigned act = __activemask();
-    const unsigned m = __ballot_sync(act, pred);
-    const int lane = threadIdx.x & 31;
-    int base = 0;
-    if (m) {
-        const int leader = __ffs(m) - 1;
-        if (lane == leader) base = atomicAdd(ctr, __popc(m));
-        base = __shfl_sync(act, base, leader);
-    }
-    return base + __popc(m & ((1u << lane) - 1u));
-}
-
 // Finds, over `bins` counts in shared memory, the bin B where the count from
 // the top first reaches `need`; stores B and the count strictly above it.
 __device__ void find_boundary(const unsigned* h, int bins, int need, int* out_bin, int* out_above, int* tmp) {
@@ -134,7 +120,7 @@ struct CandSource {
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a, int pdl) {
     __shared__ unsigned h[kHistBins];
     __shared__ int tmp[32];
-    __shared__ int s_bin, s_above, s_last, s_emit;
+    __shared__ int s_bin, s_above, s_last, s_emit, s_wbase, s_cbase, s_tot;
     __shared__ uint2 cbuf[kRefineCap];
     if (pdl) pdl_wait();
     const int row = blockIdx.x;
@@ -176,17 +162,39 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     find_boundary(h, kHistBins, k, &s_bin, &s_above, tmp);
     __syncthreads();
     const uint32_t B = static_cast<uint32_t>(s_bin);
+    // Count this thread's winners and boundary candidates, place them with two
+    // block scans and one global add per counter for the whole CTA.
+    int nwin = 0, nbnd = 0;
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t t = lo + i * kSelThreads + threadIdx.x;
+        const uint32_t b = order_key(v[i]) >> (32 - kHistBits);
+        nwin += (t < hi && b > B) ? 1 : 0;
+        nbnd += (t < hi && b == B) ? 1 : 0;
+    }
+    int pw = block_inclusive_scan(nwin, tmp, &s_tot) - nwin;
+    const int tot_w = s_tot;
+    int pc = block_inclusive_scan(nbnd, tmp, &s_tot) - nbnd;
+    const int tot_b = s_tot;
+    if (threadIdx.x == 0) {
+        s_wbase = tot_w ? atomicAdd(ctr + 0, tot_w) : 0;
+        s_cbase = tot_b ? atomicAdd(ctr + 1, tot_b) : 0;
+    }
+    __syncthreads();
+    pw += s_wbase;
+    pc += s_cbase;
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
         const int64_t t = lo + i * kSelThreads + threadIdx.x;
         const uint32_t key = order_key(v[i]);
         const uint32_t b = key >> (32 - kHistBits);
-        const bool win = (t < hi) && b > B;
-        const bool bnd = (t < hi) && b == B;
-        const int pw = aggregated_inc(ctr + 0, win);
-        if (win && pw < k) out[pw] = static_cast<int>(t);
-        const int pc = aggregated_inc(ctr + 1, bnd);
-        if (bnd && pc < kCandCap) cand[pc] = make_uint2(key, static_cast<uint32_t>(t));
+        if (t < hi && b > B) {
+            if (pw < k) out[pw] = static_cast<int>(t);
+            ++pw;
+        } else if (t < hi && b == B) {
+            if (pc < kCandCap) cand[pc] = make_uint2(key, static_cast<uint32_t>(t));
+            ++pc;
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
