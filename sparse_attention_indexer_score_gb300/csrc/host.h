@@ -12,11 +12,14 @@ namespace dsa {
 // Byte offsets of the regions of a dsa_score_paged / dsa_topk workspace.
 // Every region starts on a 256-byte boundary.  `hist` and `counters` must be
 // zero on entry and are zero again when a call completes.
+constexpr int kMaxScoreCtas = 1024;   // largest scoring grid the plan table holds
+
 struct WsLayout {
     size_t info;        // int[8]: segment count, tile count
     size_t segs;        // int4[rows + 1]: request, first row, rows, largest bound
     size_t seg_prefix;  // int[rows + 2]: exclusive prefix of tiles per segment
     size_t eff_end;     // int[rows]: row bounds after validation (0 outside every request)
+    size_t cta;         // int4[kMaxScoreCtas]: per scoring CTA {first tile, end tile, first segment, segments}
     size_t hist;        // uint32[rows][2048]: histogram of the top 11 order-preserving score bits
     size_t counters;    // int[rows][4]: winners emitted, candidates kept, chunks done, spare
     size_t cand;        // uint2[rows][kCandCap]: boundary-bin candidates (key, position)

@@ -14,7 +14,7 @@
 //   warp 0     TMA producer: block-table gather of key pages (+ their scales)
 //              into an 8-stage shared-memory ring; query rows per segment.
 //   warp 1     tcgen05 issuer: scale factors into TMEM, 4 MMAs (K = 32 each)
-//              per tile into one of two TMEM accumulators.
+//              per tile into one of three TMEM accumulators.
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = key),
 //              ReLU-weighted head sum, FP32 key scale, logits store, and a
 //              shared-memory histogram of the scores for the top-k pass.
@@ -40,6 +40,8 @@ constexpr uint32_t kFp8QRowTx = kQRowBytes, kFp4QRowTx = kQRowBytes / 2;
 constexpr int kSegRows = 4;                   // query rows per segment
 constexpr int kQBufBytes = kSegRows * kQRowBytes;
 constexpr int kScoreThreads = 192;
+constexpr int kAcc = 3;                       // TMEM accumulators in flight (MMA latency is hidden behind 2)
+constexpr int kPlanSmemSegs = 4096;           // segments whose tile prefix the plan keeps on chip
 
 constexpr int OFF_TILES = 0;
 constexpr int OFF_QBUF = OFF_TILES + kStages * kTileBytes;
@@ -48,17 +50,17 @@ constexpr int OFF_SFA = OFF_RAWSC + kStages * 512;
 constexpr int OFF_QSF = OFF_SFA + kStages * 512;
 constexpr int OFF_SFB = OFF_QSF + 2 * 512;
 constexpr int OFF_KS = OFF_SFB + 2 * 512;
-constexpr int OFF_HIST = OFF_KS + 2 * 128 * 4;
+constexpr int OFF_HIST = OFF_KS + kAcc * 128 * 4;
 constexpr int OFF_W = OFF_HIST + kSegRows * kHistBins * 4;
 constexpr int OFF_ROWINFO = OFF_W + kSegRows * kHeads * 4;
 constexpr int OFF_BAR = OFF_ROWINFO + 64;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 * kAcc + 1;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kScoreSmem = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
 
-// TMEM columns: two accumulators of up to 128 columns, then scale factors.
+// TMEM columns: kAcc accumulators of up to 128 columns, then scale factors.
 constexpr uint32_t TM_ACC = 0;
-constexpr uint32_t TM_SFA = 256;                  // kStages x 4 columns
+constexpr uint32_t TM_SFA = kAcc * 128;           // kStages x 4 columns
 constexpr uint32_t TM_SFB = TM_SFA + 4 * kStages; // 2 x 4 columns
 constexpr uint32_t TM_COLS = 512;
 
@@ -73,6 +75,7 @@ struct ScoreArgs {
     const int4* segs;
     const int* seg_prefix;
     const int* eff_end;
+    const int4* cta;
     float* logits;
     int64_t ld;
     int hist_k;          // rows whose bound exceeds hist_k get a histogram; -1: none
@@ -110,11 +113,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
                                                     const int32_t* __restrict__ row_ends, int R, int rows,
                                                     int max_keys, int* __restrict__ info, int4* __restrict__ segs,
                                                     int* __restrict__ seg_prefix, int* __restrict__ eff_end,
-                                                    int32_t* status) {
+                                                    int4* __restrict__ cta, int G, int32_t* status) {
     pdl_launch_dependents();
     pdl_wait();
     __shared__ int warp_tmp[32];
     __shared__ int chunk_total;
+    __shared__ int sp[kPlanSmemSegs + 1];   // tile prefix, when the segments fit
     for (int r = threadIdx.x; r < rows; r += blockDim.x) eff_end[r] = 0;
     __syncthreads();
     int carry = 0;
@@ -156,14 +160,36 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         const int i = base + threadIdx.x;
         const int tiles = (i < S) ? (segs[i].w + kTileRows - 1) / kTileRows : 0;
         const int inc = block_inclusive_scan(tiles, warp_tmp, &chunk_total);
-        if (i < S) seg_prefix[i] = carry + inc - tiles;
+        if (i < S) {
+            seg_prefix[i] = carry + inc - tiles;
+            if (i < kPlanSmemSegs) sp[i] = carry + inc - tiles;
+        }
         carry += chunk_total;
         __syncthreads();
     }
+    const int T = carry;
     if (threadIdx.x == 0) {
-        seg_prefix[S] = carry;
+        seg_prefix[S] = T;
+        if (S <= kPlanSmemSegs) sp[S] = T;
         info[0] = S;
-        info[1] = carry;
+        info[1] = T;
+    }
+    __syncthreads();
+    // Tile range and first segment of every scoring CTA, so that a CTA starts
+    // from one load instead of a search through global memory.
+    for (int c = threadIdx.x; c < G; c += blockDim.x) {
+        const int t0 = static_cast<int>(static_cast<int64_t>(c) * T / G);
+        const int t1 = static_cast<int>(static_cast<int64_t>(c + 1) * T / G);
+        int seg = -1;
+        if (S <= kPlanSmemSegs && S > 0) {
+            int lo = 0, hi = S;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (sp[mid] <= t0) lo = mid; else hi = mid;
+            }
+            seg = lo;
+        }
+        cta[c] = make_int4(t0, t1, seg, S);
     }
 }
 
@@ -211,12 +237,11 @@ __device__ __forceinline__ TilePlan plan_tile(const ScoreArgs& p, int t, int t1,
 __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUtensorMap* smap,
                                               const CUtensorMap* qmap, const ScoreArgs& p, uint8_t* smem,
                                               uint64_t* full, uint64_t* empty, uint64_t* qfull, uint64_t* qempty,
-                                              volatile int* abort, int t0, int t1, int seg) {
+                                              volatile int* abort, int t0, int t1, int seg, int S) {
     const int lane = threadIdx.x & 31;
     const bool fp4 = (p.fmt == DSA_FMT_MXFP4);
     int cur = -1, i_seg = 0, it = 0;
     bool ok = true;
-    const int S = p.info[0];
     TilePlan nxt = plan_tile(p, t0 + lane, t1, seg, S);
     for (int base = t0; base < t1 && ok; base += 32) {
         const TilePlan mine = nxt;
@@ -324,9 +349,9 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             ++i_seg;
         }
         const int s = it % kStages;
-        const int a = it & 1;
+        const int a = it % kAcc;
         bool ok = mbar_wait(full + s, (it / kStages) & 1, abort, p.status);
-        ok = ok && mbar_wait(tempty + a, ((it >> 1) & 1) ^ 1, abort, p.status);
+        ok = ok && mbar_wait(tempty + a, ((it / kAcc) & 1) ^ 1, abort, p.status);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
         const uint32_t* rs = reinterpret_cast<const uint32_t*>(smem + OFF_RAWSC + s * 512);
@@ -419,9 +444,15 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
             epi_sync();
         }
         const int j = t - p.seg_prefix[seg];
-        const int a = it & 1;
-        const bool ok = mbar_wait(tfull + a, (it >> 1) & 1, abort, p.status);
-        if (epi_sync_any(!ok)) { aborted = true; break; }
+        const int a = it % kAcc;
+        // Warps proceed independently; a warp that gave up keeps walking the
+        // loop without waiting, so the segment barriers above stay uniform.
+        if (aborted) continue;
+        const bool ok = mbar_wait(tfull + a, (it / kAcc) & 1, abort, p.status);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+            aborted = true;
+            continue;
+        }
         tc_fence_after();
         const float ksm = f32scale ? reinterpret_cast<const float*>(smem + OFF_KS + a * 512)[m] : 1.0f;
         const int tpos = j * kTileRows + m;
@@ -429,12 +460,15 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
             uint32_t v[32];
             tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC + a * 128 + r * 32, v);
             tc_wait_ld();
-            const float* wr = wsm + r * kHeads;
+            const float4* wr = reinterpret_cast<const float4*>(wsm + r * kHeads);
             float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-            for (int h = 0; h < 32; h += 2) {
-                s0 = fmaf(wr[h], fmaxf(__uint_as_float(v[h]), 0.0f), s0);
-                s1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(v[h + 1]), 0.0f), s1);
+            for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 w4 = wr[h4];
+                s0 = fmaf(w4.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.0f), s0);
+                s1 = fmaf(w4.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f), s1);
+                s0 = fmaf(w4.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f), s0);
+                s1 = fmaf(w4.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.0f), s1);
             }
             const float sc = (s0 + s1) * ksm;
             const bool valid = tpos < rinfo[r];
@@ -450,7 +484,8 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
         tc_fence_before();
         mbar_arrive(tempty + a);
     }
-    if (cur >= 0 && !aborted) flush_hist(p, hs, rinfo, row0, nrows, e);
+    const bool any_aborted = epi_sync_any(aborted);   // uniform over the four warps
+    if (cur >= 0 && !any_aborted) flush_hist(p, hs, rinfo, row0, nrows, e);
 }
 
 __global__ void __launch_bounds__(kScoreThreads, 1)
@@ -464,8 +499,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     uint64_t* qfull = bars + 2 * kStages;
     uint64_t* qempty = qfull + 2;
     uint64_t* tfull = qempty + 2;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* done_bar = tempty + 2;
+    uint64_t* tempty = tfull + kAcc;
+    uint64_t* done_bar = tempty + kAcc;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     const int warp = threadIdx.x >> 5;
@@ -478,6 +513,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(qfull + b, 1);
             mbar_init(qempty + b, 1);
+        }
+        for (int b = 0; b < kAcc; ++b) {
             mbar_init(tfull + b, 2);
             mbar_init(tempty + b, 128);
         }
@@ -499,15 +536,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     pdl_launch_dependents();
     pdl_wait();   // the plan kernel's segments and tile prefix
 
-    const int S = args.info[0];
-    const int T = args.info[1];
-    const int64_t G = gridDim.x;
-    const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * T / G);
-    const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * T / G);
+    const int4 range = args.cta[blockIdx.x];   // {first tile, end tile, first segment, segments}
+    const int t0 = range.x, t1 = range.y, S = range.w;
     if (t0 < t1) {
-        const int seg = find_segment(args.seg_prefix, S, t0);
+        const int seg = range.z >= 0 ? range.z : find_segment(args.seg_prefix, S, t0);
         if (warp == 0) {
-            producer_role(&kmap, &smap, &qmap, args, smem, full, empty, qfull, qempty, abort, t0, t1, seg);
+            producer_role(&kmap, &smap, &qmap, args, smem, full, empty, qfull, qempty, abort, t0, t1, seg, S);
         } else if (warp == 1) {
             mma_role(args, smem, tmem, full, empty, qfull, qempty, tfull, tempty, done_bar, abort, t0, t1, seg);
         } else {
@@ -631,8 +665,10 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     int4* segs = reinterpret_cast<int4*>(ws + L.segs);
     int* seg_prefix = reinterpret_cast<int*>(ws + L.seg_prefix);
     int* eff_end = reinterpret_cast<int*>(ws + L.eff_end);
+    int4* cta = reinterpret_cast<int4*>(ws + L.cta);
+    const int grid = device_sm_count() < kMaxScoreCtas ? device_sm_count() : kMaxScoreCtas;
     if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, starts, row_ends, static_cast<int>(num_requests),
-                   static_cast<int>(rows), static_cast<int>(width), info, segs, seg_prefix, eff_end,
+                   static_cast<int>(rows), static_cast<int>(width), info, segs, seg_prefix, eff_end, cta, grid,
                    status) != cudaSuccess)
         return DSA_ERR_CUDA;
 
@@ -653,13 +689,14 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     a.segs = segs;
     a.seg_prefix = seg_prefix;
     a.eff_end = eff_end;
+    a.cta = cta;
     a.logits = out_logits;
     a.ld = ld;
     a.hist_k = want_topk ? static_cast<int>(k) : -1;
     a.hist = reinterpret_cast<unsigned*>(ws + L.hist);
     a.status = status;
     if (g_time_before && g_time_after) cudaEventRecord(static_cast<cudaEvent_t>(g_time_before), stream);
-    if (launch_pdl(score_kernel, dim3(device_sm_count()), dim3(kScoreThreads), kScoreSmem, stream, kmap, smap, qmap,
+    if (launch_pdl(score_kernel, dim3(grid), dim3(kScoreThreads), kScoreSmem, stream, kmap, smap, qmap,
                    a) != cudaSuccess)
         return DSA_ERR_CUDA;
     if (g_time_before && g_time_after) cudaEventRecord(static_cast<cudaEvent_t>(g_time_after), stream);

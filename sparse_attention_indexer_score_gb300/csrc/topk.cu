@@ -288,6 +288,8 @@ WsLayout workspace_layout(int64_t rows, int64_t width, bool with_plan, bool with
     off = align256(off + (with_plan ? (r + 2) * sizeof(int) : 0));
     L.eff_end = off;
     off = align256(off + (with_plan ? r * sizeof(int) : 0));
+    L.cta = off;
+    off = align256(off + (with_plan ? kMaxScoreCtas * sizeof(int4) : 0));
     L.hist = off;
     off = align256(off + r * kHistBins * sizeof(unsigned));
     L.counters = off;
