@@ -6,12 +6,15 @@
 //
 // Pass 1 (fused into the scoring epilogue, or hist_kernel here): a 2048-bin
 // histogram of the top 11 bits of each row's order-preserving score keys.
-// Pass 2 (select_kernel, several CTAs per row): every CTA finds the boundary
-// bin B where the count from the top reaches k, emits positions in bins above
-// B, and appends bin-B candidates to a per-row buffer.  The last CTA of a row
-// (a done counter, no waiting) resolves the boundary bin with two more radix
-// levels (11 + 10 bits) over the candidates, and clears the row's histogram
-// and counters so the workspace is zero again for the next call.
+// Pass 2 (select_kernel): the boundary bin B is where the count from the top
+// reaches k; positions in bins above B are winners, bin B holds the
+// candidates, resolved by two more radix levels (bits 20..10, then 9..0).
+// Rows of at most 8192 positions take one CTA that holds the row in
+// registers and its candidates in shared memory.  Longer rows take one CTA
+// per 4096 positions; each appends its candidates to a per-row buffer, and
+// the last CTA of the row (a done counter, no waiting) resolves them.  Every
+// placement uses block scans, not contended atomics.  The row's histogram and
+// counters are cleared at the end, so the workspace is zero for the next call.
 #include <mutex>
 
 #include "host.h"
@@ -117,10 +120,83 @@ struct CandSource {
     }
 };
 
+// Writes the positions of the candidates matching `pred` to out[base ..),
+// at most `limit` of them, placed by a block scan (no shared atomics).
+// Returns how many candidates matched (every thread gets the same value).
+template <typename Pred>
+__device__ int emit_matching(const CandSource& src, Pred pred, int32_t* out, int base, int limit, int* tmp,
+                             int* s_tot) {
+    int mine = 0;
+    src.for_each([&](uint32_t key, int) { mine += pred(key) ? 1 : 0; });
+    int pos = block_inclusive_scan(mine, tmp, s_tot) - mine;
+    const int total = *s_tot;
+    if (mine) {
+        src.for_each([&](uint32_t key, int t) {
+            if (pred(key)) {
+                if (pos < limit) out[base + pos] = t;
+                ++pos;
+            }
+        });
+    }
+    __syncthreads();
+    return total;
+}
+
+// Resolves the boundary bin of a row: `need` more positions come from the
+// candidates (keys whose top 11 bits equal the bin B), chosen by two more
+// radix levels (bits 20..10, then 9..0); positions go to out[above ..).
+__device__ void refine_boundary(const CandSource& src, uint32_t B, int32_t* out, int above, int need,
+                                unsigned* h, int* tmp, int* s_bin, int* s_above, int* s_tot) {
+    // level 2: bits [20:10]
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = 0;
+    if (threadIdx.x == 0) {
+        *s_bin = 0;
+        *s_above = 0;
+    }
+    __syncthreads();
+    src.for_each([&](uint32_t key, int) { atomicAdd(&h[(key >> 10) & 0x7FF], 1u); });
+    __syncthreads();
+    find_boundary(h, kHistBins, need, s_bin, s_above, tmp);
+    __syncthreads();
+    const uint32_t B2 = static_cast<uint32_t>(*s_bin);
+    const int n2 = emit_matching(src, [&](uint32_t key) { return ((key >> 10) & 0x7FF) > B2; }, out, above, need,
+                                 tmp, s_tot);
+    // level 3: bits [9:0] within level-2 bin B2
+    for (int i = threadIdx.x; i < 1024; i += kSelThreads) h[i] = 0;
+    if (threadIdx.x == 0) {
+        *s_bin = 0;
+        *s_above = 0;
+    }
+    __syncthreads();
+    src.for_each([&](uint32_t key, int) {
+        if (((key >> 10) & 0x7FF) == B2) atomicAdd(&h[key & 0x3FF], 1u);
+    });
+    __syncthreads();
+    const int need2 = need - n2;
+    find_boundary(h, 1024, need2, s_bin, s_above, tmp);
+    __syncthreads();
+    const uint32_t B3 = static_cast<uint32_t>(*s_bin);
+    const int n3 = emit_matching(
+        src, [&](uint32_t key) { return ((key >> 10) & 0x7FF) == B2 && (key & 0x3FF) > B3; }, out, above + n2,
+        need2, tmp, s_tot);
+    // equal keys at the boundary: the first ones in candidate order
+    const uint32_t kB = (B << (32 - kHistBits)) | (B2 << 10) | B3;
+    const int left = need2 - n3;
+    const int n4 = emit_matching(src, [&](uint32_t key) { return key == kB; }, out, above + n2 + n3, left, tmp,
+                                 s_tot);
+    // Short only when the histogram disagreed with the scores (an aborted scoring pass).
+    for (int e = n2 + n3 + min(n4, left) + threadIdx.x; e < need; e += kSelThreads) out[above + e] = -1;
+}
+
+// Rows of at most kSingleRow positions are selected by one CTA holding the
+// whole row in registers; longer rows are split into kChunk-position CTAs.
+constexpr int kSingleRow = 8192;
+constexpr int kSinglePer = kSingleRow / kSelThreads;
+
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a, int pdl) {
     __shared__ unsigned h[kHistBins];
     __shared__ int tmp[32];
-    __shared__ int s_bin, s_above, s_last, s_emit, s_wbase, s_cbase, s_tot;
+    __shared__ int s_bin, s_above, s_last, s_wbase, s_cbase, s_tot;
     __shared__ uint2 cbuf[kRefineCap];
     if (pdl) pdl_wait();
     const int row = blockIdx.x;
@@ -140,12 +216,65 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
         for (int64_t pos = lo + threadIdx.x; pos < hi; pos += kSelThreads) out[pos] = pos < n ? static_cast<int>(pos) : -1;
         return;
     }
+    unsigned* ghist = a.hist + static_cast<int64_t>(row) * kHistBins;
+    const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
+
+    if (n <= kSingleRow) {
+        // ---- one CTA per row: scores in registers, candidates in shared memory
+        if (blockIdx.y != 0) return;
+        float v[kSinglePer];
+#pragma unroll
+        for (int i = 0; i < kSinglePer; ++i) {
+            const int t = i * kSelThreads + threadIdx.x;
+            v[i] = t < n ? src[t] : 0.0f;
+        }
+        for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = ghist[i];
+        if (threadIdx.x == 0) {
+            s_bin = 0;
+            s_above = 0;
+        }
+        __syncthreads();
+        find_boundary(h, kHistBins, k, &s_bin, &s_above, tmp);
+        __syncthreads();
+        const uint32_t B = static_cast<uint32_t>(s_bin);
+        const int above = s_above;
+        int nwin = 0, nbnd = 0;
+#pragma unroll
+        for (int i = 0; i < kSinglePer; ++i) {
+            const int t = i * kSelThreads + threadIdx.x;
+            const uint32_t b = order_key(v[i]) >> (32 - kHistBits);
+            nwin += (t < n && b > B) ? 1 : 0;
+            nbnd += (t < n && b == B) ? 1 : 0;
+        }
+        int pw = block_inclusive_scan(nwin, tmp, &s_tot) - nwin;
+        int pc = block_inclusive_scan(nbnd, tmp, &s_tot) - nbnd;
+        const int ncand = s_tot;
+#pragma unroll
+        for (int i = 0; i < kSinglePer; ++i) {
+            const int t = i * kSelThreads + threadIdx.x;
+            const uint32_t key = order_key(v[i]);
+            const uint32_t b = key >> (32 - kHistBits);
+            if (t < n && b > B) {
+                if (pw < k) out[pw] = t;
+                ++pw;
+            } else if (t < n && b == B) {
+                if (pc < kRefineCap) cbuf[pc] = make_uint2(key, static_cast<uint32_t>(t));
+                ++pc;
+            }
+        }
+        __syncthreads();
+        const CandSource srcs{cbuf, min(ncand, kRefineCap), ncand <= kRefineCap ? 0 : 2, src, n, B};
+        refine_boundary(srcs, B, out, above, k - above, h, tmp, &s_bin, &s_above, &s_tot);
+        __syncthreads();
+        for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) ghist[i] = 0;
+        return;
+    }
+
+    // ---- several CTAs per row
     const int nch = (n + kChunk - 1) / kChunk;
     if (blockIdx.y >= nch) return;
-    unsigned* ghist = a.hist + static_cast<int64_t>(row) * kHistBins;
     int* ctr = a.counters + static_cast<int64_t>(row) * 4;
     uint2* cand = a.cand + static_cast<int64_t>(row) * kCandCap;
-    const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
     const int64_t hi = min(static_cast<int64_t>(n), lo + kChunk);
     float v[kPerThread];   // this CTA's scores, loaded while the histogram is read
 #pragma unroll
@@ -207,7 +336,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
 
     // Last CTA of the row: resolve the boundary bin.
     const int above = s_above;
-    int need = k - above;
     const int ncand = *reinterpret_cast<volatile int*>(ctr + 1);
     CandSource srcs{cand, min(ncand, kCandCap), ncand > kCandCap ? 2 : 1, src, n, B};
     if (ncand <= kRefineCap) {
@@ -215,60 +343,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
         srcs.buf = cbuf;
         srcs.mode = 0;
     }
-    if (threadIdx.x == 0) s_emit = 0;
-    // level 2: bits [20:10]
-    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = 0;
     __syncthreads();
-    srcs.for_each([&](uint32_t key, int) { atomicAdd(&h[(key >> 10) & 0x7FF], 1u); });
+    refine_boundary(srcs, B, out, above, k - above, h, tmp, &s_bin, &s_above, &s_tot);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        s_bin = 0;
-        s_above = 0;
-    }
-    __syncthreads();
-    find_boundary(h, kHistBins, need, &s_bin, &s_above, tmp);
-    __syncthreads();
-    const uint32_t B2 = static_cast<uint32_t>(s_bin);
-    const int above2 = s_above;
-    srcs.for_each([&](uint32_t key, int t) {
-        if (((key >> 10) & 0x7FF) > B2) {
-            const int e = atomicAdd(&s_emit, 1);
-            if (e < need) out[above + e] = t;
-        }
-    });
-    // level 3: bits [9:0] among level-2 bin B2
-    for (int i = threadIdx.x; i < 1024; i += kSelThreads) h[i] = 0;
-    __syncthreads();
-    srcs.for_each([&](uint32_t key, int) {
-        if (((key >> 10) & 0x7FF) == B2) atomicAdd(&h[key & 0x3FF], 1u);
-    });
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        s_bin = 0;
-        s_above = 0;
-    }
-    __syncthreads();
-    const int need2 = need - above2;
-    find_boundary(h, 1024, need2, &s_bin, &s_above, tmp);
-    __syncthreads();
-    const uint32_t B3 = static_cast<uint32_t>(s_bin);
-    const uint32_t kB = (B << (32 - kHistBits)) | (B2 << 10) | B3;
-    srcs.for_each([&](uint32_t key, int t) {
-        if (((key >> 10) & 0x7FF) == B2 && (key & 0x3FF) > B3) {
-            const int e = atomicAdd(&s_emit, 1);
-            if (e < need) out[above + e] = t;
-        }
-    });
-    __syncthreads();
-    srcs.for_each([&](uint32_t key, int t) {
-        if (key == kB) {
-            const int e = atomicAdd(&s_emit, 1);
-            if (e < need) out[above + e] = t;
-        }
-    });
-    __syncthreads();
-    // Short only when the histogram disagreed with the scores (an aborted scoring pass).
-    for (int e = s_emit + threadIdx.x; e < need; e += kSelThreads) out[above + e] = -1;
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) ghist[i] = 0;
     if (threadIdx.x < 4) ctr[threadIdx.x] = 0;
 }

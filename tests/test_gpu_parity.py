@@ -135,8 +135,9 @@ def test_topk_standalone_exact(cuda_lib):
     logits = np.round(rng.standard_normal((rows, width)), 2).astype(np.float32)   # heavy ties
     logits[3] = 1.0                                                               # all equal
     logits[4, :5000] = -np.inf
+    logits[5] = -2.5                                                              # all equal, short row
     ends = rng.integers(0, width + 1, rows).astype(np.int32)
-    ends[0], ends[1], ends[2], ends[3] = width, 0, 10, width
+    ends[0], ends[1], ends[2], ends[3], ends[5], ends[6] = width, 0, 10, width, 6000, 8192
     for k in (1, 7, 64, 2048, 19999):
         got = cuda_lib.topk(torch.from_numpy(logits).cuda(), torch.from_numpy(ends).cuda(), k).cpu().numpy()
         want = O.topk(logits, ends, k)
