@@ -142,6 +142,31 @@ __device__ int emit_matching(const CandSource& src, Pred pred, int32_t* out, int
     return total;
 }
 
+// Top `need` of at most kRankMax candidates held in shared memory, by rank
+// counting: rank(c) = candidates with a larger key, plus equal keys earlier in
+// the list.  Ranks are distinct, so exactly min(need, ncand) positions are
+// written.  One candidate per thread; the keys are read four at a time from
+// `keys` (a copy padded with zeros, which never outrank a real key).
+constexpr int kRankMax = kSelThreads;
+__device__ void rank_select(const uint2* c, uint32_t* keys, int ncand, int32_t* out, int above, int need) {
+    const int i = threadIdx.x;
+    if (i < ncand) keys[i] = c[i].x;
+    else if (i < ((ncand + 3) & ~3)) keys[i] = 0u;
+    __syncthreads();
+    if (i < ncand) {
+        const uint2 me = c[i];
+        int rank = 0;
+        for (int j = 0; j < ncand; j += 4) {
+            const uint4 k4 = *reinterpret_cast<const uint4*>(keys + j);   // a broadcast read
+            rank += (k4.x > me.x || (k4.x == me.x && j + 0 < i)) ? 1 : 0;
+            rank += (k4.y > me.x || (k4.y == me.x && j + 1 < i)) ? 1 : 0;
+            rank += (k4.z > me.x || (k4.z == me.x && j + 2 < i)) ? 1 : 0;
+            rank += (k4.w > me.x || (k4.w == me.x && j + 3 < i)) ? 1 : 0;
+        }
+        if (rank < need) out[above + rank] = static_cast<int>(me.y);
+    }
+}
+
 // Resolves the boundary bin of a row: `need` more positions come from the
 // candidates (keys whose top 11 bits equal the bin B), chosen by two more
 // radix levels (bits 20..10, then 9..0); positions go to out[above ..).
@@ -194,7 +219,7 @@ constexpr int kSingleRow = 8192;
 constexpr int kSinglePer = kSingleRow / kSelThreads;
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a, int pdl) {
-    __shared__ unsigned h[kHistBins];
+    __shared__ __align__(16) unsigned h[kHistBins];   // histogram, then rank_select's key copy
     __shared__ int tmp[32];
     __shared__ int s_bin, s_above, s_last, s_wbase, s_cbase, s_tot;
     __shared__ uint2 cbuf[kRefineCap];
@@ -246,9 +271,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
             nwin += (t < n && b > B) ? 1 : 0;
             nbnd += (t < n && b == B) ? 1 : 0;
         }
-        int pw = block_inclusive_scan(nwin, tmp, &s_tot) - nwin;
-        int pc = block_inclusive_scan(nbnd, tmp, &s_tot) - nbnd;
-        const int ncand = s_tot;
+        // one scan of both counts (each at most 8192) packed in 16-bit halves
+        const int packed = nwin | (nbnd << 16);
+        const int ex = block_inclusive_scan(packed, tmp, &s_tot) - packed;
+        int pw = ex & 0xFFFF;
+        int pc = ex >> 16;
+        const int ncand = s_tot >> 16;
 #pragma unroll
         for (int i = 0; i < kSinglePer; ++i) {
             const int t = i * kSelThreads + threadIdx.x;
@@ -263,8 +291,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
             }
         }
         __syncthreads();
-        const CandSource srcs{cbuf, min(ncand, kRefineCap), ncand <= kRefineCap ? 0 : 2, src, n, B};
-        refine_boundary(srcs, B, out, above, k - above, h, tmp, &s_bin, &s_above, &s_tot);
+        if (ncand <= kRankMax) {
+            rank_select(cbuf, h, ncand, out, above, k - above);
+        } else {
+            const CandSource srcs{cbuf, min(ncand, kRefineCap), ncand <= kRefineCap ? 0 : 2, src, n, B};
+            refine_boundary(srcs, B, out, above, k - above, h, tmp, &s_bin, &s_above, &s_tot);
+        }
         __syncthreads();
         for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) ghist[i] = 0;
         return;
@@ -301,10 +333,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
         nwin += (t < hi && b > B) ? 1 : 0;
         nbnd += (t < hi && b == B) ? 1 : 0;
     }
-    int pw = block_inclusive_scan(nwin, tmp, &s_tot) - nwin;
-    const int tot_w = s_tot;
-    int pc = block_inclusive_scan(nbnd, tmp, &s_tot) - nbnd;
-    const int tot_b = s_tot;
+    const int packed = nwin | (nbnd << 16);   // each count is at most kChunk
+    const int ex = block_inclusive_scan(packed, tmp, &s_tot) - packed;
+    int pw = ex & 0xFFFF;
+    int pc = ex >> 16;
+    const int tot_w = s_tot & 0xFFFF;
+    const int tot_b = s_tot >> 16;
     if (threadIdx.x == 0) {
         s_wbase = tot_w ? atomicAdd(ctr + 0, tot_w) : 0;
         s_cbase = tot_b ? atomicAdd(ctr + 1, tot_b) : 0;
@@ -344,7 +378,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
         srcs.mode = 0;
     }
     __syncthreads();
-    refine_boundary(srcs, B, out, above, k - above, h, tmp, &s_bin, &s_above, &s_tot);
+    if (srcs.mode == 0 && ncand <= kRankMax)
+        rank_select(cbuf, h, ncand, out, above, k - above);
+    else
+        refine_boundary(srcs, B, out, above, k - above, h, tmp, &s_bin, &s_above, &s_tot);
     __syncthreads();
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) ghist[i] = 0;
     if (threadIdx.x < 4) ctr[threadIdx.x] = 0;
