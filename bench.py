@@ -6,8 +6,11 @@ The default workload is ``fp8_decode`` (64 requests x 1 row, 4096..8192 keys,
 FP8 keys with FP32 scales at 132 B/token, top-2048).
 
 Prints one JSON line.  ``value`` is scored keys per second (sum of the row
-bounds over the timed steps / device time), inputs resident in HBM, L2
-flushed between steps.  ``--impl reference`` times the CPU oracle instead.
+bounds over the timed steps / device time) with inputs resident in HBM.  Each
+step is a CUDA-graph replay of the five calls; the key cache is replicated
+until the replicas exceed three times the L2 size and the steps use them in
+turn, so every step reads its keys from HBM.  ``--impl reference`` times the
+CPU oracle instead.
 
 Multi-GPU (``torchrun``): every rank runs its own replica of the workload
 (the step has no exchange); the timing is the max over ranks and ``value``
@@ -36,7 +39,6 @@ import numpy as np  # noqa: E402
 
 METRIC = "indexer scored keys/sec and cache GB/s (score+top-k) vs roofline, 1 GB300"
 UNIT = "keys/s"
-L2_FLUSH_BYTES = 512 << 20
 STEP_KERNELS = 6   # quantize_query, insert_key, decode_layout, plan, score, select
 
 
@@ -257,6 +259,12 @@ def run_ours(args, wl, rank, world, local_rank):
     for i in range(0, kb.shape[0], chunk):
         ix.insert(bf16_tensor(kb[i:i + chunk], dev), torch.from_numpy(sl[i:i + chunk]).to(dev))
     del kb, sl
+    # Inputs larger than L2: replicas of the key cache, one per step in turn, so
+    # that every step reads its keys from HBM (no flush kernel between steps).
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20) or (126 << 20)
+    cache_bytes = ix.cache.numel()
+    n_rep = max(2, min(64, -(-3 * l2 // cache_bytes)))
+    caches = [ix.cache] + [ix.cache.clone() for _ in range(n_rep - 1)]
     host = dict(q=bf16_tensor(wl.q_bits, "cpu"), wv=bf16_tensor(wl.wv_bits, "cpu"),
                 keys=bf16_tensor(wl.step_key_bits, "cpu"), slots=torch.from_numpy(wl.step_slots),
                 seq=torch.from_numpy(wl.seq_lens), qlen=torch.from_numpy(wl.query_lens))
@@ -265,34 +273,51 @@ def run_ours(args, wl, rank, world, local_rank):
     topk_out = torch.empty((wl.num_rows, wl.topk), dtype=torch.int32, device=dev)
     q_out = torch.zeros((wl.num_rows, 4096), dtype=torch.uint8, device=dev)
     w_out = torch.empty((wl.num_rows, 32), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def step(inp):
+    def step(inp, r):
+        ix.cache = caches[r]
         return ix.step(inp["q"], inp["wv"], inp["keys"], inp["slots"], inp["seq"], inp["qlen"], max_q,
                        topk_out=topk_out, q_out=q_out, w_out=w_out)
 
-    out = step(d)
+    out = None
+    for r in range(n_rep):          # eager warm-up: lazy driver state, kernel attributes
+        out = step(d, r)
     torch.cuda.synchronize()
     row_ends = out.row_ends.cpu().numpy()
     ab = algorithmic_bytes(wl, row_ends)
-    for _ in range(args.warmup):
-        flush.zero_()
-        step(d)
+
+    # One CUDA graph per replica for the timed steps; a second set with the
+    # library's events around the scoring kernel for the roofline timing.
+    graphs, kgraphs, kev = [], [], []
+    for r in range(n_rep):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(d, r)
+        graphs.append(g)
+        a, b = dsa.TimingEvent(), dsa.TimingEvent()
+        kg = torch.cuda.CUDAGraph()
+        dsa.set_score_timing(a, b)
+        with torch.cuda.graph(kg):
+            step(d, r)
+        dsa.set_score_timing(None, None)
+        kgraphs.append(kg)
+        kev.append((a, b))
+    for i in range(args.warmup * n_rep):
+        graphs[i % n_rep].replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
 
-    # headline: K steps, device time of each step (flush excluded)
+    # headline: K steps (graph replays), device time of each step
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clocks:
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         clocks.mark_start()
-        for a, b in evs:
-            flush.zero_()
+        for i, (a, b) in enumerate(evs):
             a.record()
-            step(d)
+            graphs[i % n_rep].replay()
             b.record()
         torch.cuda.synchronize()
         clocks.mark_end()
@@ -301,32 +326,31 @@ def run_ours(args, wl, rank, world, local_rank):
     clk = clocks.summary()
     step_ms = sum(a.elapsed_time(b) for a, b in evs)
 
-    # the scoring kernel alone (events recorded by the library around it)
-    kev = [(dsa.TimingEvent(), dsa.TimingEvent()) for _ in range(args.steps)]
-    for a, b in kev:
-        flush.zero_()
-        dsa.set_score_timing(a, b)
-        step(d)
-    dsa.set_score_timing(None, None)
-    torch.cuda.synchronize()
-    kernel_ms = sum(a.elapsed_ms(b) for a, b in kev) / args.steps
+    # the scoring kernel alone
+    kernel_ms = 0.0
+    for i in range(args.steps):
+        kgraphs[i % n_rep].replay()
+        a, b = kev[i % n_rep]
+        kernel_ms += a.elapsed_ms(b)
+    kernel_ms /= args.steps
 
-    # end to end through the public API from pinned host buffers
+    # end to end through the public API (eager calls) from pinned host buffers
     pinned = {k: v.pin_memory() for k, v in host.items()}
     h_top = torch.empty((wl.num_rows, wl.topk), dtype=torch.int32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = h_top.numel() * 4
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for a, b in eev:
-        flush.zero_()
+    e2e_steps = min(args.steps, 200)
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(eev):
         a.record()
         for k in d:
             d[k].copy_(pinned[k], non_blocking=True)
-        step(d)
+        step(d, i % n_rep)
         h_top.copy_(topk_out, non_blocking=True)
         b.record()
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) * args.steps / e2e_steps
 
     times = torch.tensor([step_ms, e2e_ms, kernel_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -346,7 +370,10 @@ def run_ours(args, wl, rank, world, local_rank):
         "data": "synthetic",
         "config": {"workload": workload_desc(wl), "rows": wl.num_rows, "requests": wl.R,
                    "scored_keys_per_step": ab["scored"], "unique_keys_per_step": ab["keys_unique"],
-                   "cache_bytes_per_step": ab["cache"], "l2": "flushed before every step (512 MiB write)",
+                   "cache_bytes_per_step": ab["cache"],
+                   "l2": (f"inputs larger than L2: {n_rep} replicas of the key cache "
+                          f"({n_rep * cache_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB) used in turn, no flush"),
+                   "launch": "one CUDA graph per replica, replayed per step (PDL edges kept)",
                    "parallelism": f"replicas x{world}"},
         "cache_gbs": ab["cache"] * args.steps * world / (step_ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -355,7 +382,7 @@ def run_ours(args, wl, rank, world, local_rank):
                      "peak_source": f"{peaks['source']} HBM copy bandwidth",
                      "step_frac": (ab["step"] / (step_ms / args.steps / 1e3) / 1e9) / peaks["hbm_gbs"]},
         "e2e": {"value": keys_total / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "how": "eager public-API calls, host copies in the timed region"},
         "gpu_launches": STEP_KERNELS * args.steps,
         "clocks": clk,
     }

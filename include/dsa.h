@@ -257,8 +257,9 @@ int dsa_topk_noalloc(const float* logits, int64_t ld, const int32_t* row_ends,
  * dsa_set_score_timing - profiling hook: when both events are non-NULL,
  * dsa_score_paged records `before` just ahead of its scoring kernel and
  * `after` just behind it on the call's stream, so the scoring kernel alone can
- * be timed.  Pass NULLs to switch it off.  Not thread-safe.  The events must
- * come from dsa_timing_event_create (the library's own CUDA runtime).
+ * be timed.  Pass NULLs to switch it off.  Not thread-safe.  The records are
+ * "external", so a call captured into a CUDA graph records them on every
+ * replay.
  */
 void dsa_set_score_timing(void* before, void* after);
 

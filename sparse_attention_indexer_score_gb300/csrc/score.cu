@@ -695,11 +695,13 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     a.hist_k = want_topk ? static_cast<int>(k) : -1;
     a.hist = reinterpret_cast<unsigned*>(ws + L.hist);
     a.status = status;
-    if (g_time_before && g_time_after) cudaEventRecord(static_cast<cudaEvent_t>(g_time_before), stream);
+    if (g_time_before && g_time_after)   // external: kept as a record node under stream capture
+        cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_time_before), stream, cudaEventRecordExternal);
     if (launch_pdl(score_kernel, dim3(grid), dim3(kScoreThreads), kScoreSmem, stream, kmap, smap, qmap,
                    a) != cudaSuccess)
         return DSA_ERR_CUDA;
-    if (g_time_before && g_time_after) cudaEventRecord(static_cast<cudaEvent_t>(g_time_after), stream);
+    if (g_time_before && g_time_after)
+        cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_time_after), stream, cudaEventRecordExternal);
     if (!want_topk && !logits) return DSA_OK;
     return launch_select(out_logits, logits, ld, width, eff_end, rows, want_topk ? k : 0, want_topk ? topk : nullptr,
                          ws, L, stream, true);
