@@ -45,6 +45,15 @@ __device__ __forceinline__ int clamp_end(const int32_t* ends, int row, int64_t w
     return static_cast<int>(e < 0 ? 0 : (e > width ? width : e));
 }
 
+// Copies a row's 2048-bin histogram to shared memory, all loads in flight.
+__device__ __forceinline__ void load_hist(unsigned* h, const unsigned* ghist) {
+    unsigned r[kHistBins / kSelThreads];
+#pragma unroll
+    for (int i = 0; i < kHistBins / kSelThreads; ++i) r[i] = ghist[i * kSelThreads + threadIdx.x];
+#pragma unroll
+    for (int i = 0; i < kHistBins / kSelThreads; ++i) h[i * kSelThreads + threadIdx.x] = r[i];
+}
+
 // Finds, over `bins` counts in shared memory, the bin B where the count from
 // the top first reaches `need`; stores B and the count strictly above it.
 __device__ void find_boundary(const unsigned* h, int bins, int need, int* out_bin, int* out_above, int* tmp) {
@@ -216,12 +225,14 @@ __device__ void refine_boundary(const CandSource& src, uint32_t B, int32_t* out,
 // Rows of at most kSingleRow positions are selected by one CTA holding the
 // whole row in registers; longer rows are split into kChunk-position CTAs.
 constexpr int kSingleRow = 8192;
-constexpr int kSinglePer = kSingleRow / kSelThreads;
+constexpr int kSelDynSmem = kSingleRow * sizeof(float);   // the staged row
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a, int pdl) {
     __shared__ __align__(16) unsigned h[kHistBins];   // histogram, then rank_select's key copy
     __shared__ int tmp[32];
     __shared__ int s_bin, s_above, s_last, s_wbase, s_cbase, s_tot;
+    __shared__ uint64_t s_bar;
+    __shared__ int s_ww[kSelThreads / 32], s_wb[kSelThreads / 32];
     __shared__ uint2 cbuf[kRefineCap];
     if (pdl) pdl_wait();
     const int row = blockIdx.x;
@@ -245,50 +256,70 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
 
     if (n <= kSingleRow) {
-        // ---- one CTA per row: scores in registers, candidates in shared memory
+        // ---- one CTA per row: the row staged in shared memory by one bulk
+        // copy (while the histogram is read), then compact loops over it.
         if (blockIdx.y != 0) return;
-        float v[kSinglePer];
-#pragma unroll
-        for (int i = 0; i < kSinglePer; ++i) {
-            const int t = i * kSelThreads + threadIdx.x;
-            v[i] = t < n ? src[t] : 0.0f;
-        }
-        for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = ghist[i];
+        extern __shared__ __align__(16) float srow[];
+        const int n4 = (n + 3) & ~3;
+        const bool bulk = (reinterpret_cast<uintptr_t>(src) % 16) == 0 && n4 <= a.ld;
         if (threadIdx.x == 0) {
             s_bin = 0;
             s_above = 0;
+            if (bulk) {
+                mbar_init(&s_bar, 1);
+                mbar_fence_init();
+                mbar_arrive_expect_tx(&s_bar, static_cast<uint32_t>(n4) * 4u);
+                bulk_load(srow, src, static_cast<uint32_t>(n4) * 4u, &s_bar);
+            }
         }
+        if (!bulk)
+            for (int t = threadIdx.x; t < n; t += kSelThreads) srow[t] = src[t];
+        load_hist(h, ghist);
         __syncthreads();
         find_boundary(h, kHistBins, k, &s_bin, &s_above, tmp);
+        if (bulk) mbar_drain(&s_bar, 0);   // bounded wait for the row
         __syncthreads();
         const uint32_t B = static_cast<uint32_t>(s_bin);
         const int above = s_above;
-        int nwin = 0, nbnd = 0;
-#pragma unroll
-        for (int i = 0; i < kSinglePer; ++i) {
-            const int t = i * kSelThreads + threadIdx.x;
-            const uint32_t b = order_key(v[i]) >> (32 - kHistBits);
-            nwin += (t < n && b > B) ? 1 : 0;
-            nbnd += (t < n && b == B) ? 1 : 0;
+        // Place winners (bin > B) and candidates (bin == B) with warp ballots:
+        // each warp writes one contiguous run per iteration, so stores coalesce.
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const unsigned lt = (1u << lane) - 1u;
+        int wwin = 0, wbnd = 0;
+        for (int t0 = 0; t0 < n; t0 += kSelThreads) {
+            const int t = t0 + threadIdx.x;
+            const uint32_t b = t < n ? order_key(srow[t]) >> (32 - kHistBits) : 0u;
+            wwin += __popc(__ballot_sync(0xFFFFFFFFu, t < n && b > B));
+            wbnd += __popc(__ballot_sync(0xFFFFFFFFu, t < n && b == B));
         }
-        // one scan of both counts (each at most 8192) packed in 16-bit halves
-        const int packed = nwin | (nbnd << 16);
-        const int ex = block_inclusive_scan(packed, tmp, &s_tot) - packed;
-        int pw = ex & 0xFFFF;
-        int pc = ex >> 16;
-        const int ncand = s_tot >> 16;
-#pragma unroll
-        for (int i = 0; i < kSinglePer; ++i) {
-            const int t = i * kSelThreads + threadIdx.x;
-            const uint32_t key = order_key(v[i]);
-            const uint32_t b = key >> (32 - kHistBits);
-            if (t < n && b > B) {
-                if (pw < k) out[pw] = t;
-                ++pw;
-            } else if (t < n && b == B) {
-                if (pc < kRefineCap) cbuf[pc] = make_uint2(key, static_cast<uint32_t>(t));
-                ++pc;
+        if (lane == 0) {
+            s_ww[warp] = wwin;
+            s_wb[warp] = wbnd;
+        }
+        __syncthreads();
+        int pw = 0, pc = 0, ncand = 0;
+        for (int i = 0; i < kSelThreads / 32; ++i) {
+            if (i < warp) {
+                pw += s_ww[i];
+                pc += s_wb[i];
             }
+            ncand += s_wb[i];
+        }
+        for (int t0 = 0; t0 < n; t0 += kSelThreads) {
+            const int t = t0 + threadIdx.x;
+            const uint32_t key = t < n ? order_key(srow[t]) : 0u;
+            const uint32_t b = key >> (32 - kHistBits);
+            const unsigned mw = __ballot_sync(0xFFFFFFFFu, t < n && b > B);
+            const unsigned mb = __ballot_sync(0xFFFFFFFFu, t < n && b == B);
+            if (t < n && b > B) {
+                const int pos = pw + __popc(mw & lt);
+                if (pos < k) out[pos] = t;
+            } else if (t < n && b == B) {
+                const int pos = pc + __popc(mb & lt);
+                if (pos < kRefineCap) cbuf[pos] = make_uint2(key, static_cast<uint32_t>(t));
+            }
+            pw += __popc(mw);
+            pc += __popc(mb);
         }
         __syncthreads();
         if (ncand <= kRankMax) {
@@ -314,7 +345,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
         const int64_t t = lo + i * kSelThreads + threadIdx.x;
         v[i] = t < hi ? src[t] : 0.0f;
     }
-    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = ghist[i];
+    load_hist(h, ghist);
     if (threadIdx.x == 0) {
         s_bin = 0;
         s_above = 0;
@@ -323,22 +354,32 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     find_boundary(h, kHistBins, k, &s_bin, &s_above, tmp);
     __syncthreads();
     const uint32_t B = static_cast<uint32_t>(s_bin);
-    // Count this thread's winners and boundary candidates, place them with two
-    // block scans and one global add per counter for the whole CTA.
-    int nwin = 0, nbnd = 0;
+    // Place winners and candidates with warp ballots (coalesced runs per warp
+    // and iteration); the CTA's bases come from one global add per counter.
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    int wwin = 0, wbnd = 0;
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
         const int64_t t = lo + i * kSelThreads + threadIdx.x;
         const uint32_t b = order_key(v[i]) >> (32 - kHistBits);
-        nwin += (t < hi && b > B) ? 1 : 0;
-        nbnd += (t < hi && b == B) ? 1 : 0;
+        wwin += __popc(__ballot_sync(0xFFFFFFFFu, t < hi && b > B));
+        wbnd += __popc(__ballot_sync(0xFFFFFFFFu, t < hi && b == B));
     }
-    const int packed = nwin | (nbnd << 16);   // each count is at most kChunk
-    const int ex = block_inclusive_scan(packed, tmp, &s_tot) - packed;
-    int pw = ex & 0xFFFF;
-    int pc = ex >> 16;
-    const int tot_w = s_tot & 0xFFFF;
-    const int tot_b = s_tot >> 16;
+    if (lane == 0) {
+        s_ww[warp] = wwin;
+        s_wb[warp] = wbnd;
+    }
+    __syncthreads();
+    int pw = 0, pc = 0, tot_w = 0, tot_b = 0;
+    for (int i = 0; i < kSelThreads / 32; ++i) {
+        if (i < warp) {
+            pw += s_ww[i];
+            pc += s_wb[i];
+        }
+        tot_w += s_ww[i];
+        tot_b += s_wb[i];
+    }
     if (threadIdx.x == 0) {
         s_wbase = tot_w ? atomicAdd(ctr + 0, tot_w) : 0;
         s_cbase = tot_b ? atomicAdd(ctr + 1, tot_b) : 0;
@@ -351,13 +392,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
         const int64_t t = lo + i * kSelThreads + threadIdx.x;
         const uint32_t key = order_key(v[i]);
         const uint32_t b = key >> (32 - kHistBits);
+        const unsigned mw = __ballot_sync(0xFFFFFFFFu, t < hi && b > B);
+        const unsigned mb = __ballot_sync(0xFFFFFFFFu, t < hi && b == B);
         if (t < hi && b > B) {
-            if (pw < k) out[pw] = static_cast<int>(t);
-            ++pw;
+            const int pos = pw + __popc(mw & lt);
+            if (pos < k) out[pos] = static_cast<int>(t);
         } else if (t < hi && b == B) {
-            if (pc < kCandCap) cand[pc] = make_uint2(key, static_cast<uint32_t>(t));
-            ++pc;
+            const int pos = pc + __popc(mb & lt);
+            if (pos < kCandCap) cand[pos] = make_uint2(key, static_cast<uint32_t>(t));
         }
+        pw += __popc(mw);
+        pc += __popc(mb);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -470,9 +515,18 @@ int launch_select(const float* logits, float* logits_fill, int64_t ld, int64_t w
     if (chunks > 65535 || rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
     const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(chunks));
     cudaError_t err;
-    if (pdl) err = launch_pdl(select_kernel, grid, dim3(kSelThreads), 0, stream, a, 1);
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelDynSmem) !=
+            cudaSuccess)
+            return DSA_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    if (pdl) err = launch_pdl(select_kernel, grid, dim3(kSelThreads), kSelDynSmem, stream, a, 1);
     else {
-        select_kernel<<<grid, kSelThreads, 0, stream>>>(a, 0);
+        select_kernel<<<grid, kSelThreads, kSelDynSmem, stream>>>(a, 0);
         err = cudaGetLastError();
     }
     return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
