@@ -22,7 +22,7 @@
 
 namespace dsa {
 
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 1024;
 constexpr int kChunk = 4096;   // positions per select CTA
 constexpr int kPerThread = kChunk / kSelThreads;
 constexpr int kRefineCap = 4096;   // boundary candidates the last CTA keeps in shared memory
@@ -154,26 +154,32 @@ __device__ int emit_matching(const CandSource& src, Pred pred, int32_t* out, int
 // Top `need` of at most kRankMax candidates held in shared memory, by rank
 // counting: rank(c) = candidates with a larger key, plus equal keys earlier in
 // the list.  Ranks are distinct, so exactly min(need, ncand) positions are
-// written.  One candidate per thread; the keys are read four at a time from
-// `keys` (a copy padded with zeros, which never outrank a real key).
-constexpr int kRankMax = kSelThreads;
+// written.  Four threads share a candidate, each scanning every fourth group
+// of four keys of `keys` (a copy padded with zeros, which never outrank a real
+// key); two shuffles add their counts.
+constexpr int kRankMax = kSelThreads / 4;
 __device__ void rank_select(const uint2* c, uint32_t* keys, int ncand, int32_t* out, int above, int need) {
     const int i = threadIdx.x;
+    const int padded = (ncand + 15) & ~15;
     if (i < ncand) keys[i] = c[i].x;
-    else if (i < ((ncand + 3) & ~3)) keys[i] = 0u;
+    else if (i < padded) keys[i] = 0u;
     __syncthreads();
-    if (i < ncand) {
-        const uint2 me = c[i];
-        int rank = 0;
-        for (int j = 0; j < ncand; j += 4) {
-            const uint4 k4 = *reinterpret_cast<const uint4*>(keys + j);   // a broadcast read
-            rank += (k4.x > me.x || (k4.x == me.x && j + 0 < i)) ? 1 : 0;
-            rank += (k4.y > me.x || (k4.y == me.x && j + 1 < i)) ? 1 : 0;
-            rank += (k4.z > me.x || (k4.z == me.x && j + 2 < i)) ? 1 : 0;
-            rank += (k4.w > me.x || (k4.w == me.x && j + 3 < i)) ? 1 : 0;
+    const int cand = i >> 2, part = i & 3;
+    uint2 me = make_uint2(0u, 0u);
+    int rank = 0;
+    if (cand < ncand) {
+        me = c[cand];
+        for (int j = part * 4; j < ncand; j += 16) {
+            const uint4 k4 = *reinterpret_cast<const uint4*>(keys + j);
+            rank += (k4.x > me.x || (k4.x == me.x && j + 0 < cand)) ? 1 : 0;
+            rank += (k4.y > me.x || (k4.y == me.x && j + 1 < cand)) ? 1 : 0;
+            rank += (k4.z > me.x || (k4.z == me.x && j + 2 < cand)) ? 1 : 0;
+            rank += (k4.w > me.x || (k4.w == me.x && j + 3 < cand)) ? 1 : 0;
         }
-        if (rank < need) out[above + rank] = static_cast<int>(me.y);
     }
+    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 1);
+    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 2);
+    if (cand < ncand && part == 0 && rank < need) out[above + rank] = static_cast<int>(me.y);
 }
 
 // Resolves the boundary bin of a row: `need` more positions come from the
