@@ -39,9 +39,19 @@ constexpr uint32_t kFp8PageTx = 64 * 128, kFp4PageTx = 64 * 64;
 constexpr uint32_t kFp8QRowTx = kQRowBytes, kFp4QRowTx = kQRowBytes / 2;
 constexpr int kSegRows = 4;                   // query rows per segment
 constexpr int kQBufBytes = kSegRows * kQRowBytes;
-constexpr int kScoreThreads = 192;
+// Two epilogue groups of four warps (one per TMEM lane quarter) drain
+// alternate tiles, so two accumulators are read out at once.
+constexpr int kEpiGroups = 2;
+constexpr int kEpiWarps = 4 * kEpiGroups;
+constexpr int kScoreThreads = 64 + 32 * kEpiWarps;
 constexpr int kAcc = 3;                       // TMEM accumulators in flight (MMA latency is hidden behind 2)
 constexpr int kPlanSmemSegs = 4096;           // segments whose tile prefix the plan keeps on chip
+// Tile assignment: every CTA owns an equal contiguous range of the first
+// three quarters of the tiles (segment locality); the last quarter is a pool
+// claimed in chunks of kChunkTiles by whichever CTA runs out of work first,
+// which absorbs the speed differences between SMs.
+constexpr int kPoolDiv = 4;
+constexpr int kChunkTiles = 4;
 
 constexpr int OFF_TILES = 0;
 constexpr int OFF_QBUF = OFF_TILES + kStages * kTileBytes;
@@ -50,13 +60,14 @@ constexpr int OFF_SFA = OFF_RAWSC + kStages * 512;
 constexpr int OFF_QSF = OFF_SFA + kStages * 512;
 constexpr int OFF_SFB = OFF_QSF + 2 * 512;
 constexpr int OFF_KS = OFF_SFB + 2 * 512;
-constexpr int OFF_HIST = OFF_KS + kAcc * 128 * 4;
-constexpr int OFF_W = OFF_HIST + kSegRows * kHistBins * 4;
-constexpr int OFF_ROWINFO = OFF_W + kSegRows * kHeads * 4;
-constexpr int OFF_BAR = OFF_ROWINFO + 64;
+constexpr int OFF_W = OFF_KS + kAcc * 128 * 4;            // float[kEpiWarps][4 rows][32 heads]: w per warp
+constexpr int OFF_SINFO = OFF_W + kEpiWarps * kSegRows * kHeads * 4;   // int2[kStages]: {tile in segment, segment}
+constexpr int OFF_AINFO = OFF_SINFO + kStages * 8;        // int2[kAcc]: the same per accumulator
+constexpr int OFF_BAR = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 * kAcc + 1;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kScoreSmem = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
+static_assert(kScoreSmem <= 227 * 1024, "scoring CTA exceeds the shared memory of an SM");
 
 // TMEM columns: kAcc accumulators of up to 128 columns, then scale factors.
 constexpr uint32_t TM_ACC = 0;
@@ -71,7 +82,7 @@ struct ScoreArgs {
     int64_t bt_stride;
     const uint8_t* q_rows;
     const __nv_bfloat16* w;
-    const int* info;
+    int* claim;          // chunk counter of the shared tail pool (zeroed by the plan)
     const int4* segs;
     const int* seg_prefix;
     const int* eff_end;
@@ -82,19 +93,6 @@ struct ScoreArgs {
     unsigned* hist;
     int32_t* status;
 };
-
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-// Barrier over the 128 epilogue threads returning the OR of `pred`.
-__device__ __forceinline__ bool epi_sync_any(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred))
-        : "memory");
-    return r != 0;
-}
 
 // Segment s with prefix[s] <= t < prefix[s + 1] (prefix[S] > t).
 __device__ __forceinline__ int find_segment(const int* prefix, int S, int t) {
@@ -168,18 +166,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         __syncthreads();
     }
     const int T = carry;
+    const int Ts = T - (T / kPoolDiv) / kChunkTiles * kChunkTiles;   // tiles of the static ranges
     if (threadIdx.x == 0) {
         seg_prefix[S] = T;
         if (S <= kPlanSmemSegs) sp[S] = T;
         info[0] = S;
         info[1] = T;
+        info[2] = 0;   // pool chunks claimed
+        info[3] = Ts;
     }
     __syncthreads();
-    // Tile range and first segment of every scoring CTA, so that a CTA starts
-    // from one load instead of a search through global memory.
+    // Static tile range and first segment of every scoring CTA, so that a CTA
+    // starts from one load instead of a search through global memory.
     for (int c = threadIdx.x; c < G; c += blockDim.x) {
-        const int t0 = static_cast<int>(static_cast<int64_t>(c) * T / G);
-        const int t1 = static_cast<int>(static_cast<int64_t>(c + 1) * T / G);
+        const int t0 = static_cast<int>(static_cast<int64_t>(c) * Ts / G);
+        const int t1 = static_cast<int>(static_cast<int64_t>(c + 1) * Ts / G);
         int seg = -1;
         if (S <= kPlanSmemSegs && S > 0) {
             int lo = 0, hi = S;
@@ -197,12 +198,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 // Per-tile load plan resolved by one lane of the producer warp.
 struct TilePlan {
     int seg;   // segment of the tile
+    int j;     // tile index within the segment
     int pid0;  // physical page of keys 0..63 (-1: none)
     int pid1;  // physical page of keys 64..127 (-1: none)
 };
 
 __device__ __forceinline__ TilePlan plan_tile(const ScoreArgs& p, int t, int t1, int seg, int S) {
-    TilePlan tp{-1, -1, -1};
+    TilePlan tp{-1, 0, -1, -1};
     if (t >= t1) return tp;
     if (t >= p.seg_prefix[seg + 1]) {
         // binary search in (seg, S): the tile lies past the starting segment
@@ -216,6 +218,7 @@ __device__ __forceinline__ TilePlan plan_tile(const ScoreArgs& p, int t, int t1,
     tp.seg = seg;
     const int4 si = p.segs[seg];
     const int j = t - p.seg_prefix[seg];
+    tp.j = j;
     const int npages = (si.w + kPage - 1) / kPage;
     const int32_t* row = p.block_table + static_cast<int64_t>(si.x) * p.bt_stride;
     bool bad = false;
@@ -231,88 +234,151 @@ __device__ __forceinline__ TilePlan plan_tile(const ScoreArgs& p, int t, int t1,
     return tp;
 }
 
+// Segment of tile t (the last s with prefix[s] <= t) by a 32-way search of
+// the whole warp: each round keeps one of 32 sub-ranges of [lo, hi).
+__device__ __forceinline__ int warp_find_segment(const int* prefix, int S, int t) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = S;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) >> 5;
+        const int i = lo + lane * step;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, i < hi && prefix[i] <= t);   // lanes 0..L (prefix sorted)
+        lo += (31 - __clz(m)) * step;
+        hi = min(hi, lo + step);
+    }
+    return lo;
+}
+
+// Issues the loads of one tile (lane 0 of the producer warp): the segment's
+// query rows when the segment changes, then the key pages and scales into the
+// next ring stage, tagged with {tile in segment, segment}.
+struct Producer {
+    const CUtensorMap* kmap;
+    const CUtensorMap* smap;
+    const CUtensorMap* qmap;
+    uint8_t* smem;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* qfull;
+    uint64_t* qempty;
+    volatile int* abort;
+    bool fp4;
+    int cur = -1, i_seg = 0, it = 0;
+
+    __device__ __forceinline__ bool issue(const ScoreArgs& p, int sg, int j, int p0, int p1) {
+        if (sg != cur) {
+            cur = sg;
+            const int4 si = p.segs[sg];
+            const int qb = i_seg & 1;
+            if (!mbar_wait(qempty + qb, ((i_seg >> 1) & 1) ^ 1, abort, p.status)) return false;
+            const uint32_t bytes = si.z * (fp4 ? kFp4QRowTx + 128u : kFp8QRowTx);
+            mbar_arrive_expect_tx(qfull + qb, bytes);
+            uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
+            for (int r = 0; r < si.z; ++r) {
+                tma_load_3d(qdst + r * kQRowBytes, qmap, 0, 0, si.y + r, qfull + qb);
+                if (fp4)
+                    bulk_load(smem + OFF_QSF + qb * 512 + r * 128,
+                              p.q_rows + static_cast<int64_t>(si.y + r) * kQRowBytes + kFp4Scales, 128, qfull + qb);
+            }
+            ++i_seg;
+        }
+        const int s = it % kStages;
+        if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status)) return false;
+        reinterpret_cast<int2*>(smem + OFF_SINFO)[s] = make_int2(j, sg);
+        const uint32_t page_tx = (fp4 ? kFp4PageTx : kFp8PageTx) + 256;
+        const uint32_t bytes = (p0 >= 0 ? page_tx : 0u) + (p1 >= 0 ? page_tx : 0u);
+        if (bytes == 0) {
+            mbar_arrive(full + s);   // no valid page: scores of these keys are unspecified
+        } else {
+            mbar_arrive_expect_tx(full + s, bytes);
+            uint8_t* dst = smem + OFF_TILES + s * kTileBytes;
+            if (p0 >= 0) {
+                tma_load_3d(dst, kmap, 0, 0, p0, full + s);
+                tma_load_2d(smem + OFF_RAWSC + s * 512, smap, 0, p0, full + s);
+            }
+            if (p1 >= 0) {
+                tma_load_3d(dst + kPageSmem, kmap, 0, 0, p1, full + s);
+                tma_load_2d(smem + OFF_RAWSC + s * 512 + 256, smap, 0, p1, full + s);
+            }
+        }
+        ++it;
+        return true;
+    }
+
+    // End of this CTA's sequence: a stage tagged -1 with no copies.
+    __device__ __forceinline__ bool finish(const ScoreArgs& p) {
+        const int s = it % kStages;
+        if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status)) return false;
+        reinterpret_cast<int2*>(smem + OFF_SINFO)[s] = make_int2(-1, -1);
+        mbar_arrive(full + s);
+        ++it;
+        return true;
+    }
+};
+
 // Warp 0.  Its 32 lanes resolve the segments and block-table entries of 32
 // tiles at once (the next batch's loads are in flight while lane 0 issues the
 // current batch's TMA copies), so block-table latency is paid once per batch.
-__device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUtensorMap* smap,
-                                              const CUtensorMap* qmap, const ScoreArgs& p, uint8_t* smem,
-                                              uint64_t* full, uint64_t* empty, uint64_t* qfull, uint64_t* qempty,
-                                              volatile int* abort, int t0, int t1, int seg, int S) {
+// After its own range the warp claims chunks of the pool until none is left.
+__device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, int t0, int t1, int seg, int S,
+                                              int Ts, int T) {
     const int lane = threadIdx.x & 31;
-    const bool fp4 = (p.fmt == DSA_FMT_MXFP4);
-    int cur = -1, i_seg = 0, it = 0;
     bool ok = true;
-    TilePlan nxt = plan_tile(p, t0 + lane, t1, seg, S);
-    for (int base = t0; base < t1 && ok; base += 32) {
-        const TilePlan mine = nxt;
-        const int last = min(31, t1 - 1 - base);
-        const int seg_end = __shfl_sync(0xFFFFFFFFu, mine.seg, last);
-        if (base + 32 < t1) nxt = plan_tile(p, base + 32 + lane, t1, seg_end, S);
-        for (int i = 0; i <= last; ++i) {
+    if (t0 < t1) {
+        TilePlan nxt = plan_tile(p, t0 + lane, t1, seg, S);
+        for (int base = t0; base < t1 && ok; base += 32) {
+            const TilePlan mine = nxt;
+            const int last = min(31, t1 - 1 - base);
+            const int seg_end = __shfl_sync(0xFFFFFFFFu, mine.seg, last);
+            if (base + 32 < t1) nxt = plan_tile(p, base + 32 + lane, t1, seg_end, S);
+            for (int i = 0; i <= last && ok; ++i) {
+                const int sg = __shfl_sync(0xFFFFFFFFu, mine.seg, i);
+                const int j = __shfl_sync(0xFFFFFFFFu, mine.j, i);
+                const int p0 = __shfl_sync(0xFFFFFFFFu, mine.pid0, i);
+                const int p1 = __shfl_sync(0xFFFFFFFFu, mine.pid1, i);
+                if (lane == 0) ok = pr.issue(p, sg, j, p0, p1);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            }
+        }
+    }
+    while (ok && Ts < T) {
+        int id = 0;
+        if (lane == 0) id = atomicAdd(p.claim, 1);
+        id = __shfl_sync(0xFFFFFFFFu, id, 0);
+        const int64_t base = Ts + static_cast<int64_t>(id) * kChunkTiles;
+        if (base >= T) break;
+        const int b = static_cast<int>(base);
+        const int end = min(T, b + kChunkTiles);
+        const TilePlan mine = plan_tile(p, b + lane, end, warp_find_segment(p.seg_prefix, S, b), S);
+        for (int i = 0; i < end - b && ok; ++i) {
             const int sg = __shfl_sync(0xFFFFFFFFu, mine.seg, i);
+            const int j = __shfl_sync(0xFFFFFFFFu, mine.j, i);
             const int p0 = __shfl_sync(0xFFFFFFFFu, mine.pid0, i);
             const int p1 = __shfl_sync(0xFFFFFFFFu, mine.pid1, i);
-            if (lane == 0) {
-                if (sg != cur) {
-                    cur = sg;
-                    const int4 si = p.segs[sg];
-                    const int qb = i_seg & 1;
-                    ok = mbar_wait(qempty + qb, ((i_seg >> 1) & 1) ^ 1, abort, p.status);
-                    if (ok) {
-                        const uint32_t bytes = si.z * (fp4 ? kFp4QRowTx + 128u : kFp8QRowTx);
-                        mbar_arrive_expect_tx(qfull + qb, bytes);
-                        uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
-                        for (int r = 0; r < si.z; ++r) {
-                            tma_load_3d(qdst + r * kQRowBytes, qmap, 0, 0, si.y + r, qfull + qb);
-                            if (fp4)
-                                bulk_load(smem + OFF_QSF + qb * 512 + r * 128,
-                                          p.q_rows + static_cast<int64_t>(si.y + r) * kQRowBytes + kFp4Scales, 128,
-                                          qfull + qb);
-                        }
-                        ++i_seg;
-                    }
-                }
-                const int s = it % kStages;
-                ok = ok && mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status);
-                if (ok) {
-                    const uint32_t page_tx = (fp4 ? kFp4PageTx : kFp8PageTx) + 256;
-                    const uint32_t bytes = (p0 >= 0 ? page_tx : 0u) + (p1 >= 0 ? page_tx : 0u);
-                    if (bytes == 0) {
-                        mbar_arrive(full + s);   // no valid page: scores of these keys are unspecified
-                    } else {
-                        mbar_arrive_expect_tx(full + s, bytes);
-                        uint8_t* dst = smem + OFF_TILES + s * kTileBytes;
-                        if (p0 >= 0) {
-                            tma_load_3d(dst, kmap, 0, 0, p0, full + s);
-                            tma_load_2d(smem + OFF_RAWSC + s * 512, smap, 0, p0, full + s);
-                        }
-                        if (p1 >= 0) {
-                            tma_load_3d(dst + kPageSmem, kmap, 0, 0, p1, full + s);
-                            tma_load_2d(smem + OFF_RAWSC + s * 512 + 256, smap, 0, p1, full + s);
-                        }
-                    }
-                    ++it;
-                }
-            }
+            if (lane == 0) ok = pr.issue(p, sg, j, p0, p1);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            if (!ok) break;
         }
     }
     if (lane == 0) {
+        if (ok) pr.finish(p);
         // Drain: every copy issued must have landed before the CTA exits.
-        for (int i = max(0, it - kStages); i < it; ++i) mbar_drain(full + (i % kStages), (i / kStages) & 1);
-        for (int i = max(0, i_seg - 2); i < i_seg; ++i) mbar_drain(qfull + (i & 1), (i >> 1) & 1);
+        const int it = pr.it, i_seg = pr.i_seg;
+        for (int i = max(0, it - kStages); i < it; ++i) mbar_drain(pr.full + (i % kStages), (i / kStages) & 1);
+        for (int i = max(0, i_seg - 2); i < i_seg; ++i) mbar_drain(pr.qfull + (i & 1), (i >> 1) & 1);
     }
     __syncwarp();
 }
 
+// Warp 1.  Follows the producer's stage tags; hands each accumulator's tag
+// to the epilogue (and the end-of-sequence tag as the last one).
 __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* full,
                                          uint64_t* empty, uint64_t* qfull, uint64_t* qempty, uint64_t* tfull,
-                                         uint64_t* tempty, uint64_t* done_bar, volatile int* abort, int t0, int t1,
-                                         int seg) {
+                                         uint64_t* tempty, uint64_t* done_bar, volatile int* abort) {
     const int lane = threadIdx.x & 31;
     const bool f32scale = (p.fmt == DSA_FMT_FP8);
     const bool fp4 = (p.fmt == DSA_FMT_MXFP4);
+    const int2* sinfo = reinterpret_cast<const int2*>(smem + OFF_SINFO);
+    int2* ainfo = reinterpret_cast<int2*>(smem + OFF_AINFO);
     if (p.fmt == DSA_FMT_FP8_MX) {
         // FP8 queries carry no block scales (their scale is folded into w): 2^0 everywhere.
         reinterpret_cast<uint4*>(smem + OFF_SFB)[lane] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
@@ -321,16 +387,34 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
         if (lane == 0) tc_cp_32x128b_warpx4(tmem + TM_SFB, desc_rows16(smem_u32(smem + OFF_SFB)));
         __syncwarp();
     }
-    int cur = -1, qb = 0, i_seg = 0, it = 0, nrows = 0;
-    for (int t = t0; t < t1; ++t, ++it) {
-        while (t >= p.seg_prefix[seg + 1]) ++seg;
+    int cur = -1, qb = 0, i_seg = 0, nrows = 0;
+    for (int it = 0;; ++it) {
+        const int s = it % kStages;
+        const int a = it % kAcc;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full + s, (it / kStages) & 1, abort, p.status))) break;
+        const int2 tag = sinfo[s];
+        if (tag.y < 0) {
+            // one end tag for each epilogue group (they take alternate accumulators)
+            for (int q = 0; q < kEpiGroups; ++q) {
+                const int aq = (it + q) % kAcc;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty + aq, (((it + q) / kAcc) & 1) ^ 1, abort, p.status)))
+                    break;
+                if (lane == 0) {
+                    ainfo[aq] = tag;
+                    mbar_arrive(tfull + aq);
+                    mbar_arrive(tfull + aq);
+                }
+                __syncwarp();
+            }
+            break;
+        }
+        const int seg = tag.y;
         if (seg != cur) {
             if (cur >= 0 && lane == 0) tc_commit(qempty + qb);
             cur = seg;
             nrows = p.segs[seg].z;
             qb = i_seg & 1;
-            const bool ok = mbar_wait(qfull + qb, (i_seg >> 1) & 1, abort, p.status);
-            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(qfull + qb, (i_seg >> 1) & 1, abort, p.status))) break;
             if (fp4) {
                 // Query block scales: line L of the atom holds the words of MMA
                 // rows L, 32 + L, 64 + L, 96 + L (row r * 32 + h = head h of query row r).
@@ -348,11 +432,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             }
             ++i_seg;
         }
-        const int s = it % kStages;
-        const int a = it % kAcc;
-        bool ok = mbar_wait(full + s, (it / kStages) & 1, abort, p.status);
-        ok = ok && mbar_wait(tempty + a, ((it / kAcc) & 1) ^ 1, abort, p.status);
-        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty + a, ((it / kAcc) & 1) ^ 1, abort, p.status))) break;
         tc_fence_after();
         const uint32_t* rs = reinterpret_cast<const uint32_t*>(smem + OFF_RAWSC + s * 512);
         const uint32_t w0 = rs[lane], w1 = rs[32 + lane], w2 = rs[64 + lane], w3 = rs[96 + lane];
@@ -385,9 +465,10 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc_mx(fm, fm, 128, n, kk, kk), sfa, sfb, kk > 0);
             }
+            ainfo[a] = tag;
             tc_commit(empty + s);
             tc_commit(tfull + a);
-            mbar_arrive(tfull + a);   // releases the key scales written above
+            mbar_arrive(tfull + a);   // releases the key scales and the tag written above
         }
         __syncwarp();
     }
@@ -398,94 +479,95 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
     __syncwarp();
 }
 
-__device__ __forceinline__ void flush_hist(const ScoreArgs& p, unsigned* hs, const int* rinfo, int row0, int nrows,
-                                           int e) {
-    epi_sync();
-    for (int b = e; b < kHistBins; b += 128) {
-        for (int r = 0; r < nrows; ++r) {
-            if (!rinfo[4 + r]) continue;
-            const unsigned c = hs[r * kHistBins + b];
-            if (c) {
-                atomicAdd(p.hist + static_cast<int64_t>(row0 + r) * kHistBins + b, c);
-                hs[r * kHistBins + b] = 0;
-            }
-        }
+// Scores of one query row for the 32 keys of this warp (one per lane) from
+// the 32 head columns v of its accumulator.
+__device__ __forceinline__ float head_sum(const uint32_t* v, const float* wr, float ksm) {
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int h4 = 0; h4 < 8; ++h4) {
+        const float4 w4 = reinterpret_cast<const float4*>(wr)[h4];
+        s[0] = fmaf(w4.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.0f), s[0]);
+        s[1] = fmaf(w4.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f), s[1]);
+        s[2] = fmaf(w4.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f), s[2]);
+        s[3] = fmaf(w4.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.0f), s[3]);
     }
-    epi_sync();
+    return ((s[0] + s[1]) + (s[2] + s[3])) * ksm;
 }
 
+// Logit store and histogram count of one row's 32 scores (one per lane);
+// the warp adds one count per distinct bin to the row's histogram in global
+// memory.
+__device__ __forceinline__ void emit_row(const ScoreArgs& p, int row, int tpos, float sc, int end, bool hist_on,
+                                         int lane) {
+    const bool valid = tpos < end;
+    if (valid) p.logits[static_cast<int64_t>(row) * p.ld + tpos] = sc;
+    const unsigned counted = __ballot_sync(0xFFFFFFFFu, valid && hist_on);
+    if (valid && hist_on) {
+        const uint32_t bin = hist_bin(sc);
+        const unsigned peers = __match_any_sync(counted, bin);
+        if (lane == __ffs(peers) - 1)
+            atomicAdd(p.hist + static_cast<int64_t>(row) * kHistBins + bin, static_cast<unsigned>(__popc(peers)));
+    }
+}
+
+// Warps 2 .. 2 + kEpiWarps.  Group g = (warp - 2) / 4 drains the accumulators
+// of sequence positions g, g + kEpiGroups, ...; every warp works on its own
+// (per-warp head weights, row bounds in registers, one arrival per tile).
 __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* tfull,
-                                              uint64_t* tempty, volatile int* abort, int t0, int t1, int seg) {
+                                              uint64_t* tempty, volatile int* abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = threadIdx.x - 64;
+    const int group = (warp - 2) >> 2;
     const int quarter = warp & 3;            // TMEM lanes this warp may access
     const int m = quarter * 32 + lane;       // key of the tile this thread owns
-    float* wsm = reinterpret_cast<float*>(smem + OFF_W);
-    int* rinfo = reinterpret_cast<int*>(smem + OFF_ROWINFO);   // [0,4): bounds, [4,8): histogram on
-    unsigned* hs = reinterpret_cast<unsigned*>(smem + OFF_HIST);
+    float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - 2) * (kSegRows * kHeads);
+    const int2* ainfo = reinterpret_cast<const int2*>(smem + OFF_AINFO);
     const bool f32scale = (p.fmt == DSA_FMT_FP8);
-    int cur = -1, row0 = 0, nrows = 0, it = 0;
-    bool aborted = false;
-    for (int t = t0; t < t1; ++t, ++it) {
-        while (t >= p.seg_prefix[seg + 1]) ++seg;
-        if (seg != cur) {
-            if (cur >= 0) flush_hist(p, hs, rinfo, row0, nrows, e);
-            cur = seg;
-            const int4 si = p.segs[seg];
+    const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC;
+    int cur = -1, row0 = 0, nrows = 0;
+    int end_l = 0;        // lane r < nrows: bound of row row0 + r
+    unsigned hist_m = 0;  // bit r: row r gets a histogram
+    for (int it = group;; it += kEpiGroups) {
+        const int a = it % kAcc;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull + a, (it / kAcc) & 1, abort, p.status))) break;
+        tc_fence_after();
+        const int2 tag = ainfo[a];   // {tile in segment, segment}; segment -1 ends the sequence
+        if (tag.y < 0) break;
+        if (tag.y != cur) {
+            cur = tag.y;
+            const int4 si = p.segs[cur];
             row0 = si.y;
             nrows = si.z;
-            if (e < nrows * kHeads)
-                wsm[e] = __bfloat162float(p.w[static_cast<int64_t>(row0 + e / kHeads) * kHeads + e % kHeads]);
-            if (e < nrows) {
-                const int end = p.eff_end[row0 + e];
-                rinfo[e] = end;
-                rinfo[4 + e] = (p.hist_k >= 0 && end > p.hist_k) ? 1 : 0;
-            }
-            epi_sync();
+            for (int r = 0; r < nrows; ++r)
+                wsm[r * kHeads + lane] = __bfloat162float(p.w[static_cast<int64_t>(row0 + r) * kHeads + lane]);
+            end_l = lane < nrows ? p.eff_end[row0 + lane] : 0;
+            hist_m = __ballot_sync(0xFFFFFFFFu, lane < nrows && p.hist_k >= 0 && end_l > p.hist_k);
+            __syncwarp();
         }
-        const int j = t - p.seg_prefix[seg];
-        const int a = it % kAcc;
-        // Warps proceed independently; a warp that gave up keeps walking the
-        // loop without waiting, so the segment barriers above stay uniform.
-        if (aborted) continue;
-        const bool ok = mbar_wait(tfull + a, (it / kAcc) & 1, abort, p.status);
-        if (!__all_sync(0xFFFFFFFFu, ok)) {
-            aborted = true;
-            continue;
-        }
-        tc_fence_after();
         const float ksm = f32scale ? reinterpret_cast<const float*>(smem + OFF_KS + a * 512)[m] : 1.0f;
-        const int tpos = j * kTileRows + m;
-        for (int r = 0; r < nrows; ++r) {
+        const int tpos = tag.x * kTileRows + m;
+        const uint32_t acc = tbase + a * 128;
+        int r = 0;
+        for (; r + 2 <= nrows; r += 2) {
+            uint32_t v[64];
+            tc_ld_32x32b_x64(acc + r * 32, v);
+            tc_wait_ld_regs<64>(v);
+            const float s0 = head_sum(v, wsm + r * kHeads, ksm);
+            const float s1 = head_sum(v + 32, wsm + (r + 1) * kHeads, ksm);
+            emit_row(p, row0 + r, tpos, s0, __shfl_sync(0xFFFFFFFFu, end_l, r), (hist_m >> r) & 1, lane);
+            emit_row(p, row0 + r + 1, tpos, s1, __shfl_sync(0xFFFFFFFFu, end_l, r + 1), (hist_m >> (r + 1)) & 1,
+                     lane);
+        }
+        if (r < nrows) {
             uint32_t v[32];
-            tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC + a * 128 + r * 32, v);
-            tc_wait_ld();
-            const float4* wr = reinterpret_cast<const float4*>(wsm + r * kHeads);
-            float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-            for (int h4 = 0; h4 < 8; ++h4) {
-                const float4 w4 = wr[h4];
-                s0 = fmaf(w4.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.0f), s0);
-                s1 = fmaf(w4.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f), s1);
-                s0 = fmaf(w4.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f), s0);
-                s1 = fmaf(w4.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.0f), s1);
-            }
-            const float sc = (s0 + s1) * ksm;
-            const bool valid = tpos < rinfo[r];
-            if (valid) p.logits[static_cast<int64_t>(row0 + r) * p.ld + tpos] = sc;
-            const unsigned counted = __ballot_sync(0xFFFFFFFFu, valid && rinfo[4 + r]);
-            if (valid && rinfo[4 + r]) {
-                // one shared-memory add per distinct bin of the warp
-                const uint32_t bin = hist_bin(sc);
-                const unsigned peers = __match_any_sync(counted, bin);
-                if (lane == __ffs(peers) - 1) atomicAdd(hs + r * kHistBins + bin, static_cast<unsigned>(__popc(peers)));
-            }
+            tc_ld_32x32b_x32(acc + r * 32, v);
+            tc_wait_ld_regs<32>(v);
+            const float s0 = head_sum(v, wsm + r * kHeads, ksm);
+            emit_row(p, row0 + r, tpos, s0, __shfl_sync(0xFFFFFFFFu, end_l, r), (hist_m >> r) & 1, lane);
         }
         tc_fence_before();
-        mbar_arrive(tempty + a);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty + a);
     }
-    const bool any_aborted = epi_sync_any(aborted);   // uniform over the four warps
-    if (cur >= 0 && !any_aborted) flush_hist(p, hs, rinfo, row0, nrows, e);
 }
 
 __global__ void __launch_bounds__(kScoreThreads, 1)
@@ -516,7 +598,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         for (int b = 0; b < kAcc; ++b) {
             mbar_init(tfull + b, 2);
-            mbar_init(tempty + b, 128);
+            mbar_init(tempty + b, 4);
         }
         mbar_init(done_bar, 1);
         *abort = 0;
@@ -526,8 +608,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         tma_prefetch(&qmap);
     }
     if (warp == 1) tc_alloc(tmem_slot, TM_COLS);
-    unsigned* hs = reinterpret_cast<unsigned*>(smem + OFF_HIST);
-    for (int i = threadIdx.x; i < kSegRows * kHistBins; i += blockDim.x) hs[i] = 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -536,17 +616,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     pdl_launch_dependents();
     pdl_wait();   // the plan kernel's segments and tile prefix
 
-    const int4 range = args.cta[blockIdx.x];   // {first tile, end tile, first segment, segments}
-    const int t0 = range.x, t1 = range.y, S = range.w;
-    if (t0 < t1) {
-        const int seg = range.z >= 0 ? range.z : find_segment(args.seg_prefix, S, t0);
-        if (warp == 0) {
-            producer_role(&kmap, &smap, &qmap, args, smem, full, empty, qfull, qempty, abort, t0, t1, seg, S);
-        } else if (warp == 1) {
-            mma_role(args, smem, tmem, full, empty, qfull, qempty, tfull, tempty, done_bar, abort, t0, t1, seg);
-        } else {
-            epilogue_role(args, smem, tmem, tfull, tempty, abort, t0, t1, seg);
-        }
+    if (warp == 0) {
+        const int4 range = args.cta[blockIdx.x];   // {first tile, end tile, first segment, segments}
+        const int T = args.claim[-1], Ts = args.claim[1];
+        const int t0 = range.x, t1 = range.y, S = range.w;
+        const int seg = (t0 < t1 && range.z < 0) ? find_segment(args.seg_prefix, S, t0) : range.z;
+        Producer pr{&kmap, &smap, &qmap, smem, full, empty, qfull, qempty, abort, args.fmt == DSA_FMT_MXFP4};
+        producer_role(pr, args, t0, t1, seg, S, Ts, T);
+    } else if (warp == 1) {
+        mma_role(args, smem, tmem, full, empty, qfull, qempty, tfull, tempty, done_bar, abort);
+    } else {
+        epilogue_role(args, smem, tmem, tfull, tempty, abort);
     }
     tc_fence_before();
     __syncthreads();
@@ -685,7 +765,7 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     a.bt_stride = bt_stride;
     a.q_rows = static_cast<const uint8_t*>(q_rows);
     a.w = static_cast<const __nv_bfloat16*>(w);
-    a.info = info;
+    a.claim = info + 2;   // info: {segments, tiles, pool chunks claimed, static tiles}
     a.segs = segs;
     a.seg_prefix = seg_prefix;
     a.eff_end = eff_end;
