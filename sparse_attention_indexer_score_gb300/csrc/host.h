@@ -21,6 +21,7 @@ struct WsLayout {
     size_t eff_end;     // int[rows]: row bounds after validation (0 outside every request)
     size_t cta;         // int4[kMaxScoreCtas]: per scoring CTA {first tile, end tile, first segment, segments}
     size_t hist;        // uint32[rows][2048]: histogram of the top 11 order-preserving score bits
+    size_t hist2;       // uint32[rows][2048]: level-2 histogram (bits 20..10) of rows longer than one select CTA
     size_t counters;    // int[rows][4]: winners emitted, candidates kept, chunks done, spare
     size_t cand;        // uint2[rows][kCandCap]: boundary-bin candidates (key, position)
     size_t logits;      // float[rows][width] when the caller keeps no logits

@@ -4,17 +4,20 @@
 // and top-k"; page "amd.ops.fp4_indexer", decode_tile_size, budgets per-row
 // selection scratch next to the logits.
 //
-// Pass 1 (fused into the scoring epilogue, or hist_kernel here): a 2048-bin
+// Level 1 (fused into the scoring epilogue, or hist_kernel here): a 2048-bin
 // histogram of the top 11 bits of each row's order-preserving score keys.
-// Pass 2 (select_kernel): the boundary bin B is where the count from the top
-// reaches k; positions in bins above B are winners, bin B holds the
-// candidates, resolved by two more radix levels (bits 20..10, then 9..0).
-// Rows of at most 8192 positions take one CTA that holds the row in
-// registers and its candidates in shared memory.  Longer rows take one CTA
-// per 4096 positions; each appends its candidates to a per-row buffer, and
-// the last CTA of the row (a done counter, no waiting) resolves them.  Every
-// placement uses block scans, not contended atomics.  The row's histogram and
-// counters are cleared at the end, so the workspace is zero for the next call.
+// select_kernel takes a row in chunks of 8192 positions, one 1024-thread CTA
+// per chunk, the chunk's scores in registers.  Every CTA finds the level-1
+// boundary bin B1 (where the count from the top reaches k); positions above
+// it are winners, placed at once; positions in B1 are candidates, kept in a
+// buffer and counted in a level-2 histogram (key bits 20..10).  The one CTA of
+// a short row, or the last CTA of a longer row (a done counter, no waiting),
+// then makes one pass over the candidates: level-2 winners are placed, the
+// candidates of the level-2 boundary bin are kept in shared memory with a
+// level-3 histogram (bits 9..0), and those settle the rest, equal keys last.
+// Positions within the top k come out in no particular order.  The row's
+// histograms and counters are cleared at the end, so the workspace is zero
+// for the next call.
 #include <mutex>
 
 #include "host.h"
@@ -23,9 +26,11 @@
 namespace dsa {
 
 constexpr int kSelThreads = 1024;
-constexpr int kChunk = 4096;   // positions per select CTA
-constexpr int kPerThread = kChunk / kSelThreads;
-constexpr int kRefineCap = 4096;   // boundary candidates the last CTA keeps in shared memory
+constexpr int kPerThread = 8;
+constexpr int kChunk = kSelThreads * kPerThread;   // positions per select CTA
+constexpr int kRefineCap = 4096;   // level-1 candidates of a one-chunk row kept in shared memory
+constexpr int kLevel3Cap = 2048;   // level-3 candidates kept in shared memory
+constexpr int kSelDynSmem = kRefineCap * sizeof(uint2) + kLevel3Cap * sizeof(uint2);
 
 struct SelectArgs {
     const float* logits;
@@ -35,9 +40,10 @@ struct SelectArgs {
     const int32_t* ends;
     int k;               // 0: fill only
     int32_t* out;
-    unsigned* hist;
-    int* counters;
-    uint2* cand;
+    unsigned* hist;      // level-1 histograms, [rows][2048]
+    unsigned* hist2;     // level-2 histograms of rows longer than one chunk, [rows][2048]
+    int* counters;       // [rows][4]: winners placed, candidates kept, chunks done, spare
+    uint2* cand;         // [rows][kCandCap]: level-1 candidates (key, position)
 };
 
 __device__ __forceinline__ int clamp_end(const int32_t* ends, int row, int64_t width) {
@@ -56,8 +62,9 @@ __device__ __forceinline__ void load_hist(unsigned* h, const unsigned* ghist) {
 
 // Finds, over `bins` counts in shared memory, the bin B where the count from
 // the top first reaches `need`; stores B and the count strictly above it.
+// Leaves both untouched when the counts never reach `need`.
 __device__ void find_boundary(const unsigned* h, int bins, int need, int* out_bin, int* out_above, int* tmp) {
-    const int per = bins / kSelThreads;   // bins per thread (8 or 4)
+    const int per = bins / kSelThreads;   // bins per thread (2 or 1)
     const int first = bins - (threadIdx.x + 1) * per;   // thread 0 owns the top bins
     int local = 0;
     for (int i = 0; i < per; ++i) local += static_cast<int>(h[first + i]);
@@ -72,6 +79,20 @@ __device__ void find_boundary(const unsigned* h, int bins, int need, int* out_bi
         }
         cum += c;
     }
+}
+
+// Position for this lane among the lanes of its warp where `pred` holds, the
+// warp's run taken from `counter` with one atomic; -1 where `pred` is false.
+// Every lane of the warp must call it.
+__device__ __forceinline__ int warp_slot(bool pred, int* counter) {
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, pred);
+    if (m == 0) return -1;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(m) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(counter, __popc(m));
+    base = __shfl_sync(0xFFFFFFFFu, base, leader);
+    return pred ? base + __popc(m & ((1u << lane) - 1u)) : -1;
 }
 
 __global__ void __launch_bounds__(kSelThreads) hist_kernel(const float* __restrict__ logits, int64_t ld,
@@ -103,143 +124,62 @@ __global__ void __launch_bounds__(kSelThreads) hist_kernel(const float* __restri
         if (h[i]) atomicAdd(hist + static_cast<int64_t>(row) * kHistBins + i, h[i]);
 }
 
-// Streams the boundary-bin candidates of a row: from shared memory when they
-// fit, else from the candidate buffer when it did not overflow, else by
-// re-reading the row and keeping bin == B.
+// The level-1 candidates of a row (keys in bin B1): a buffer of `count`
+// (key, position) pairs in shared or global memory, or, when the buffer
+// overflowed, the row itself filtered by bin.  for_each calls f(valid, key,
+// position) with the same trip count on every lane of a warp.
 struct CandSource {
-    const uint2* buf;
+    const uint2* buf;   // nullptr: re-read the row
     int count;
-    int mode;   // 0: shared-memory copy, 1: global buffer, 2: re-read the row
     const float* row;
     int n;
-    uint32_t bin;
+    uint32_t b1;
     template <typename F>
     __device__ __forceinline__ void for_each(F&& f) const {
-        if (mode != 2) {
-            for (int i = threadIdx.x; i < count; i += kSelThreads) {
-                const uint2 c = buf[i];
-                f(c.x, static_cast<int>(c.y));
+        const int lane = threadIdx.x & 31;
+        const int w0 = threadIdx.x - lane;
+        if (buf) {
+            constexpr int U = 4;
+            for (int base = w0; base < count; base += kSelThreads * U) {
+                uint2 c[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = base + u * kSelThreads + lane;
+                    c[u] = i < count ? buf[i] : make_uint2(0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    f(base + u * kSelThreads + lane < count, c[u].x, static_cast<int>(c[u].y));
             }
         } else {
-            for (int t = threadIdx.x; t < n; t += kSelThreads) {
-                const uint32_t key = order_key(row[t]);
-                if ((key >> (32 - kHistBits)) == bin) f(key, t);
+            constexpr int U = 8;
+            for (int base = w0; base < n; base += kSelThreads * U) {
+                float x[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int t = base + u * kSelThreads + lane;
+                    x[u] = t < n ? row[t] : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int t = base + u * kSelThreads + lane;
+                    const uint32_t key = order_key(x[u]);
+                    f(t < n && (key >> (32 - kHistBits)) == b1, key, t);
+                }
             }
         }
     }
 };
 
-// Writes the positions of the candidates matching `pred` to out[base ..),
-// at most `limit` of them, placed by a block scan (no shared atomics).
-// Returns how many candidates matched (every thread gets the same value).
-template <typename Pred>
-__device__ int emit_matching(const CandSource& src, Pred pred, int32_t* out, int base, int limit, int* tmp,
-                             int* s_tot) {
-    int mine = 0;
-    src.for_each([&](uint32_t key, int) { mine += pred(key) ? 1 : 0; });
-    int pos = block_inclusive_scan(mine, tmp, s_tot) - mine;
-    const int total = *s_tot;
-    if (mine) {
-        src.for_each([&](uint32_t key, int t) {
-            if (pred(key)) {
-                if (pos < limit) out[base + pos] = t;
-                ++pos;
-            }
-        });
-    }
-    __syncthreads();
-    return total;
-}
-
-// Top `need` of at most kRankMax candidates held in shared memory, by rank
-// counting: rank(c) = candidates with a larger key, plus equal keys earlier in
-// the list.  Ranks are distinct, so exactly min(need, ncand) positions are
-// written.  Four threads share a candidate, each scanning every fourth group
-// of four keys of `keys` (a copy padded with zeros, which never outrank a real
-// key); two shuffles add their counts.
-constexpr int kRankMax = kSelThreads / 4;
-__device__ void rank_select(const uint2* c, uint32_t* keys, int ncand, int32_t* out, int above, int need) {
-    const int i = threadIdx.x;
-    const int padded = (ncand + 15) & ~15;
-    if (i < ncand) keys[i] = c[i].x;
-    else if (i < padded) keys[i] = 0u;
-    __syncthreads();
-    const int cand = i >> 2, part = i & 3;
-    uint2 me = make_uint2(0u, 0u);
-    int rank = 0;
-    if (cand < ncand) {
-        me = c[cand];
-        for (int j = part * 4; j < ncand; j += 16) {
-            const uint4 k4 = *reinterpret_cast<const uint4*>(keys + j);
-            rank += (k4.x > me.x || (k4.x == me.x && j + 0 < cand)) ? 1 : 0;
-            rank += (k4.y > me.x || (k4.y == me.x && j + 1 < cand)) ? 1 : 0;
-            rank += (k4.z > me.x || (k4.z == me.x && j + 2 < cand)) ? 1 : 0;
-            rank += (k4.w > me.x || (k4.w == me.x && j + 3 < cand)) ? 1 : 0;
-        }
-    }
-    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 1);
-    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 2);
-    if (cand < ncand && part == 0 && rank < need) out[above + rank] = static_cast<int>(me.y);
-}
-
-// Resolves the boundary bin of a row: `need` more positions come from the
-// candidates (keys whose top 11 bits equal the bin B), chosen by two more
-// radix levels (bits 20..10, then 9..0); positions go to out[above ..).
-__device__ void refine_boundary(const CandSource& src, uint32_t B, int32_t* out, int above, int need,
-                                unsigned* h, int* tmp, int* s_bin, int* s_above, int* s_tot) {
-    // level 2: bits [20:10]
-    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = 0;
-    if (threadIdx.x == 0) {
-        *s_bin = 0;
-        *s_above = 0;
-    }
-    __syncthreads();
-    src.for_each([&](uint32_t key, int) { atomicAdd(&h[(key >> 10) & 0x7FF], 1u); });
-    __syncthreads();
-    find_boundary(h, kHistBins, need, s_bin, s_above, tmp);
-    __syncthreads();
-    const uint32_t B2 = static_cast<uint32_t>(*s_bin);
-    const int n2 = emit_matching(src, [&](uint32_t key) { return ((key >> 10) & 0x7FF) > B2; }, out, above, need,
-                                 tmp, s_tot);
-    // level 3: bits [9:0] within level-2 bin B2
-    for (int i = threadIdx.x; i < 1024; i += kSelThreads) h[i] = 0;
-    if (threadIdx.x == 0) {
-        *s_bin = 0;
-        *s_above = 0;
-    }
-    __syncthreads();
-    src.for_each([&](uint32_t key, int) {
-        if (((key >> 10) & 0x7FF) == B2) atomicAdd(&h[key & 0x3FF], 1u);
-    });
-    __syncthreads();
-    const int need2 = need - n2;
-    find_boundary(h, 1024, need2, s_bin, s_above, tmp);
-    __syncthreads();
-    const uint32_t B3 = static_cast<uint32_t>(*s_bin);
-    const int n3 = emit_matching(
-        src, [&](uint32_t key) { return ((key >> 10) & 0x7FF) == B2 && (key & 0x3FF) > B3; }, out, above + n2,
-        need2, tmp, s_tot);
-    // equal keys at the boundary: the first ones in candidate order
-    const uint32_t kB = (B << (32 - kHistBits)) | (B2 << 10) | B3;
-    const int left = need2 - n3;
-    const int n4 = emit_matching(src, [&](uint32_t key) { return key == kB; }, out, above + n2 + n3, left, tmp,
-                                 s_tot);
-    // Short only when the histogram disagreed with the scores (an aborted scoring pass).
-    for (int e = n2 + n3 + min(n4, left) + threadIdx.x; e < need; e += kSelThreads) out[above + e] = -1;
-}
-
-// Rows of at most kSingleRow positions are selected by one CTA holding the
-// whole row in registers; longer rows are split into kChunk-position CTAs.
-constexpr int kSingleRow = 8192;
-constexpr int kSelDynSmem = kSingleRow * sizeof(float);   // the staged row
-
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a, int pdl) {
-    __shared__ __align__(16) unsigned h[kHistBins];   // histogram, then rank_select's key copy
+    __shared__ unsigned h1[kHistBins];   // level-1 histogram, then level 3
+    __shared__ unsigned h2[kHistBins];   // level-2 histogram
     __shared__ int tmp[32];
-    __shared__ int s_bin, s_above, s_last, s_wbase, s_cbase, s_tot;
-    __shared__ uint64_t s_bar;
-    __shared__ int s_ww[kSelThreads / 32], s_wb[kSelThreads / 32];
-    __shared__ uint2 cbuf[kRefineCap];
+    __shared__ int s_b1, s_a1, s_b2, s_a2, s_b3, s_a3;
+    __shared__ int s_win, s_cand, s_w2, s_c3, s_w3, s_tie, s_base_w, s_base_c, s_last;
+    extern __shared__ uint2 sel_dyn[];
+    uint2* cbuf = sel_dyn;                 // level-1 candidates of a one-chunk row
+    uint2* c3buf = sel_dyn + kRefineCap;   // level-3 candidates
     if (pdl) pdl_wait();
     const int row = blockIdx.x;
     const int64_t lo = static_cast<int64_t>(blockIdx.y) * kChunk;
@@ -258,184 +198,162 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
         for (int64_t pos = lo + threadIdx.x; pos < hi; pos += kSelThreads) out[pos] = pos < n ? static_cast<int>(pos) : -1;
         return;
     }
-    unsigned* ghist = a.hist + static_cast<int64_t>(row) * kHistBins;
-    const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
-
-    if (n <= kSingleRow) {
-        // ---- one CTA per row: the row staged in shared memory by one bulk
-        // copy (while the histogram is read), then compact loops over it.
-        if (blockIdx.y != 0) return;
-        extern __shared__ __align__(16) float srow[];
-        const int n4 = (n + 3) & ~3;
-        const bool bulk = (reinterpret_cast<uintptr_t>(src) % 16) == 0 && n4 <= a.ld;
-        if (threadIdx.x == 0) {
-            s_bin = 0;
-            s_above = 0;
-            if (bulk) {
-                mbar_init(&s_bar, 1);
-                mbar_fence_init();
-                mbar_arrive_expect_tx(&s_bar, static_cast<uint32_t>(n4) * 4u);
-                bulk_load(srow, src, static_cast<uint32_t>(n4) * 4u, &s_bar);
-            }
-        }
-        if (!bulk)
-            for (int t = threadIdx.x; t < n; t += kSelThreads) srow[t] = src[t];
-        load_hist(h, ghist);
-        __syncthreads();
-        find_boundary(h, kHistBins, k, &s_bin, &s_above, tmp);
-        if (bulk) mbar_drain(&s_bar, 0);   // bounded wait for the row
-        __syncthreads();
-        const uint32_t B = static_cast<uint32_t>(s_bin);
-        const int above = s_above;
-        // Place winners (bin > B) and candidates (bin == B) with warp ballots:
-        // each warp writes one contiguous run per iteration, so stores coalesce.
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        const unsigned lt = (1u << lane) - 1u;
-        int wwin = 0, wbnd = 0;
-        for (int t0 = 0; t0 < n; t0 += kSelThreads) {
-            const int t = t0 + threadIdx.x;
-            const uint32_t b = t < n ? order_key(srow[t]) >> (32 - kHistBits) : 0u;
-            wwin += __popc(__ballot_sync(0xFFFFFFFFu, t < n && b > B));
-            wbnd += __popc(__ballot_sync(0xFFFFFFFFu, t < n && b == B));
-        }
-        if (lane == 0) {
-            s_ww[warp] = wwin;
-            s_wb[warp] = wbnd;
-        }
-        __syncthreads();
-        int pw = 0, pc = 0, ncand = 0;
-        for (int i = 0; i < kSelThreads / 32; ++i) {
-            if (i < warp) {
-                pw += s_ww[i];
-                pc += s_wb[i];
-            }
-            ncand += s_wb[i];
-        }
-        for (int t0 = 0; t0 < n; t0 += kSelThreads) {
-            const int t = t0 + threadIdx.x;
-            const uint32_t key = t < n ? order_key(srow[t]) : 0u;
-            const uint32_t b = key >> (32 - kHistBits);
-            const unsigned mw = __ballot_sync(0xFFFFFFFFu, t < n && b > B);
-            const unsigned mb = __ballot_sync(0xFFFFFFFFu, t < n && b == B);
-            if (t < n && b > B) {
-                const int pos = pw + __popc(mw & lt);
-                if (pos < k) out[pos] = t;
-            } else if (t < n && b == B) {
-                const int pos = pc + __popc(mb & lt);
-                if (pos < kRefineCap) cbuf[pos] = make_uint2(key, static_cast<uint32_t>(t));
-            }
-            pw += __popc(mw);
-            pc += __popc(mb);
-        }
-        __syncthreads();
-        if (ncand <= kRankMax) {
-            rank_select(cbuf, h, ncand, out, above, k - above);
-        } else {
-            const CandSource srcs{cbuf, min(ncand, kRefineCap), ncand <= kRefineCap ? 0 : 2, src, n, B};
-            refine_boundary(srcs, B, out, above, k - above, h, tmp, &s_bin, &s_above, &s_tot);
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) ghist[i] = 0;
-        return;
-    }
-
-    // ---- several CTAs per row
     const int nch = (n + kChunk - 1) / kChunk;
-    if (blockIdx.y >= nch) return;
+    if (static_cast<int>(blockIdx.y) >= nch) return;
+    const bool multi = nch > 1;
+    unsigned* ghist = a.hist + static_cast<int64_t>(row) * kHistBins;
+    unsigned* ghist2 = a.hist2 + static_cast<int64_t>(row) * kHistBins;
     int* ctr = a.counters + static_cast<int64_t>(row) * 4;
-    uint2* cand = a.cand + static_cast<int64_t>(row) * kCandCap;
-    const int64_t hi = min(static_cast<int64_t>(n), lo + kChunk);
-    float v[kPerThread];   // this CTA's scores, loaded while the histogram is read
+    uint2* gcand = a.cand + static_cast<int64_t>(row) * kCandCap;
+    const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
+    const int lane = threadIdx.x & 31;
+    const int hi = static_cast<int>(min(static_cast<int64_t>(n), lo + kChunk));
+
+    // ---- level 1: this chunk's scores in registers, the row's histogram in shared memory
+    float v[kPerThread];
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
-        const int64_t t = lo + i * kSelThreads + threadIdx.x;
+        const int t = static_cast<int>(lo) + i * kSelThreads + threadIdx.x;
         v[i] = t < hi ? src[t] : 0.0f;
     }
-    load_hist(h, ghist);
+    load_hist(h1, ghist);
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0;
     if (threadIdx.x == 0) {
-        s_bin = 0;
-        s_above = 0;
+        s_b1 = 0; s_a1 = 0; s_b2 = 0; s_a2 = 0; s_b3 = 0; s_a3 = 0;
+        s_win = 0; s_cand = 0; s_w2 = 0; s_c3 = 0; s_w3 = 0; s_tie = 0;
     }
     __syncthreads();
-    find_boundary(h, kHistBins, k, &s_bin, &s_above, tmp);
+    find_boundary(h1, kHistBins, k, &s_b1, &s_a1, tmp);
     __syncthreads();
-    const uint32_t B = static_cast<uint32_t>(s_bin);
-    // Place winners and candidates with warp ballots (coalesced runs per warp
-    // and iteration); the CTA's bases come from one global add per counter.
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned lt = (1u << lane) - 1u;
-    int wwin = 0, wbnd = 0;
+    const uint32_t B1 = static_cast<uint32_t>(s_b1);
+    const int above1 = s_a1;
+    // Winners and candidates of the chunk: one shared add per warp for its
+    // totals (then one global add per CTA when the row has several chunks),
+    // ballots for the order within the warp.
+    int nw = 0, nc = 0;
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
-        const int64_t t = lo + i * kSelThreads + threadIdx.x;
+        const int t = static_cast<int>(lo) + i * kSelThreads + threadIdx.x;
         const uint32_t b = order_key(v[i]) >> (32 - kHistBits);
-        wwin += __popc(__ballot_sync(0xFFFFFFFFu, t < hi && b > B));
-        wbnd += __popc(__ballot_sync(0xFFFFFFFFu, t < hi && b == B));
+        nw += (t < hi && b > B1) ? 1 : 0;
+        nc += (t < hi && b == B1) ? 1 : 0;
     }
+    nw = __reduce_add_sync(0xFFFFFFFFu, nw);
+    nc = __reduce_add_sync(0xFFFFFFFFu, nc);
+    int ow = 0, oc = 0;
     if (lane == 0) {
-        s_ww[warp] = wwin;
-        s_wb[warp] = wbnd;
+        ow = nw ? atomicAdd(&s_win, nw) : 0;
+        oc = nc ? atomicAdd(&s_cand, nc) : 0;
     }
     __syncthreads();
-    int pw = 0, pc = 0, tot_w = 0, tot_b = 0;
-    for (int i = 0; i < kSelThreads / 32; ++i) {
-        if (i < warp) {
-            pw += s_ww[i];
-            pc += s_wb[i];
-        }
-        tot_w += s_ww[i];
-        tot_b += s_wb[i];
-    }
-    if (threadIdx.x == 0) {
-        s_wbase = tot_w ? atomicAdd(ctr + 0, tot_w) : 0;
-        s_cbase = tot_b ? atomicAdd(ctr + 1, tot_b) : 0;
+    if (multi && threadIdx.x == 0) {
+        s_base_w = s_win ? atomicAdd(ctr + 0, s_win) : 0;
+        s_base_c = s_cand ? atomicAdd(ctr + 1, s_cand) : 0;
     }
     __syncthreads();
-    pw += s_wbase;
-    pc += s_cbase;
+    ow = __shfl_sync(0xFFFFFFFFu, ow, 0) + (multi ? s_base_w : 0);
+    oc = __shfl_sync(0xFFFFFFFFu, oc, 0) + (multi ? s_base_c : 0);
+    const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
-        const int64_t t = lo + i * kSelThreads + threadIdx.x;
+        const int t = static_cast<int>(lo) + i * kSelThreads + threadIdx.x;
         const uint32_t key = order_key(v[i]);
         const uint32_t b = key >> (32 - kHistBits);
-        const unsigned mw = __ballot_sync(0xFFFFFFFFu, t < hi && b > B);
-        const unsigned mb = __ballot_sync(0xFFFFFFFFu, t < hi && b == B);
-        if (t < hi && b > B) {
-            const int pos = pw + __popc(mw & lt);
-            if (pos < k) out[pos] = static_cast<int>(t);
-        } else if (t < hi && b == B) {
-            const int pos = pc + __popc(mb & lt);
-            if (pos < kCandCap) cand[pos] = make_uint2(key, static_cast<uint32_t>(t));
+        const bool win = t < hi && b > B1, cand = t < hi && b == B1;
+        const unsigned mw = __ballot_sync(0xFFFFFFFFu, win);
+        const unsigned mc = __ballot_sync(0xFFFFFFFFu, cand);
+        if (win) {
+            const int pos = ow + __popc(mw & lt);
+            if (pos < k) out[pos] = t;
+        } else if (cand) {
+            const int pos = oc + __popc(mc & lt);
+            atomicAdd(&h2[(key >> 10) & 0x7FF], 1u);
+            if (!multi) {
+                if (pos < kRefineCap) cbuf[pos] = make_uint2(key, static_cast<uint32_t>(t));
+            } else if (pos < kCandCap) {
+                gcand[pos] = make_uint2(key, static_cast<uint32_t>(t));
+            }
         }
-        pw += __popc(mw);
-        pc += __popc(mb);
+        ow += __popc(mw);
+        oc += __popc(mc);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    int ncand;
+    if (multi) {
+        // Add this chunk's level-2 counts to the row's; the last chunk to
+        // finish reads them back and settles the row.
+        for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
+            if (h2[i]) atomicAdd(ghist2 + i, h2[i]);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            s_last = (atomicAdd(ctr + 2, 1) == nch - 1) ? 1 : 0;
+        }
+        __syncthreads();
+        if (!s_last) return;
         __threadfence();
-        s_last = (atomicAdd(ctr + 2, 1) == nch - 1) ? 1 : 0;
+        load_hist(h2, ghist2);
+        ncand = *reinterpret_cast<volatile int*>(ctr + 1);
+    } else {
+        ncand = s_cand;
     }
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h1[i] = 0;   // level 3 from here on
     __syncthreads();
-    if (!s_last) return;
-    __threadfence();
 
-    // Last CTA of the row: resolve the boundary bin.
-    const int above = s_above;
-    const int ncand = *reinterpret_cast<volatile int*>(ctr + 1);
-    CandSource srcs{cand, min(ncand, kCandCap), ncand > kCandCap ? 2 : 1, src, n, B};
-    if (ncand <= kRefineCap) {
-        for (int i = threadIdx.x; i < ncand; i += kSelThreads) cbuf[i] = cand[i];
-        srcs.buf = cbuf;
-        srcs.mode = 0;
+    // ---- level 2: one pass over the candidates
+    const int need = k - above1;
+    find_boundary(h2, kHistBins, need, &s_b2, &s_a2, tmp);
+    __syncthreads();
+    const uint32_t B2 = static_cast<uint32_t>(s_b2);
+    const int above2 = s_a2;
+    CandSource cs{nullptr, 0, src, n, B1};
+    if (!multi && ncand <= kRefineCap) cs.buf = cbuf;
+    else if (multi && ncand <= kCandCap) cs.buf = gcand;
+    cs.count = ncand;
+    const int base2 = above1, base3 = above1 + above2;
+    cs.for_each([&](bool valid, uint32_t key, int t) {
+        const uint32_t b2 = (key >> 10) & 0x7FF;
+        const int pw = warp_slot(valid && b2 > B2, &s_w2);
+        if (pw >= 0 && base2 + pw < k) out[base2 + pw] = t;
+        const bool c3 = valid && b2 == B2;
+        const int pc = warp_slot(c3, &s_c3);
+        if (c3) {
+            atomicAdd(&h1[key & 0x3FF], 1u);
+            if (pc < kLevel3Cap) c3buf[pc] = make_uint2(key, static_cast<uint32_t>(t));
+        }
+    });
+    __syncthreads();
+
+    // ---- level 3 and equal keys
+    const int need2 = need - above2;
+    find_boundary(h1, 1024, need2, &s_b3, &s_a3, tmp);
+    __syncthreads();
+    const uint32_t B3 = static_cast<uint32_t>(s_b3);
+    const int above3 = s_a3;
+    const int n3 = s_c3;
+    const int left = need2 - above3;   // equal keys to take
+    auto level3 = [&](bool valid, uint32_t key, int t) {
+        const uint32_t b3 = key & 0x3FF;
+        const int pw = warp_slot(valid && b3 > B3, &s_w3);
+        if (pw >= 0 && base3 + pw < k) out[base3 + pw] = t;
+        const int pt = warp_slot(valid && b3 == B3, &s_tie);
+        if (pt >= 0 && pt < left && base3 + above3 + pt < k) out[base3 + above3 + pt] = t;
+    };
+    if (n3 <= kLevel3Cap) {
+        const CandSource c3s{c3buf, n3, src, n, B1};
+        c3s.for_each(level3);
+    } else {
+        cs.for_each([&](bool valid, uint32_t key, int t) { level3(valid && ((key >> 10) & 0x7FF) == B2, key, t); });
     }
     __syncthreads();
-    if (srcs.mode == 0 && ncand <= kRankMax)
-        rank_select(cbuf, h, ncand, out, above, k - above);
-    else
-        refine_boundary(srcs, B, out, above, k - above, h, tmp, &s_bin, &s_above, &s_tot);
-    __syncthreads();
-    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) ghist[i] = 0;
-    if (threadIdx.x < 4) ctr[threadIdx.x] = 0;
+    // Short only when the histogram disagreed with the scores (an aborted scoring pass).
+    const int placed = base3 + above3 + min(s_tie, left);
+    for (int e = placed + threadIdx.x; e < k; e += kSelThreads) out[e] = -1;
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) {
+        ghist[i] = 0;
+        if (multi) ghist2[i] = 0;
+    }
+    if (multi && threadIdx.x < 4) ctr[threadIdx.x] = 0;
 }
 
 // ----------------------------------------------------------------- host utilities
@@ -456,6 +374,8 @@ WsLayout workspace_layout(int64_t rows, int64_t width, bool with_plan, bool with
     L.cta = off;
     off = align256(off + (with_plan ? kMaxScoreCtas * sizeof(int4) : 0));
     L.hist = off;
+    off = align256(off + r * kHistBins * sizeof(unsigned));
+    L.hist2 = off;
     off = align256(off + r * kHistBins * sizeof(unsigned));
     L.counters = off;
     off = align256(off + r * 4 * sizeof(int));
@@ -513,6 +433,7 @@ int launch_select(const float* logits, float* logits_fill, int64_t ld, int64_t w
     a.k = static_cast<int>(k);
     a.out = out;
     a.hist = reinterpret_cast<unsigned*>(ws + L.hist);
+    a.hist2 = reinterpret_cast<unsigned*>(ws + L.hist2);
     a.counters = reinterpret_cast<int*>(ws + L.counters);
     a.cand = reinterpret_cast<uint2*>(ws + L.cand);
     const int64_t span = (k > width) ? k : width;
@@ -582,7 +503,7 @@ extern "C" const char* dsa_version(void) { return "dsa-gb300 0.1.0"; }
 namespace dsa {
 
 constexpr size_t noalloc_align(size_t x) { return (x + 255) & ~size_t(255); }
-constexpr size_t kNoAllocBytes = noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kHistBins * sizeof(unsigned)) +
+constexpr size_t kNoAllocBytes = 2 * noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kHistBins * sizeof(unsigned)) +
                                  noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * 4 * sizeof(int)) +
                                  noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kCandCap * sizeof(uint2));
 
