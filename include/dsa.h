@@ -236,7 +236,7 @@ int dsa_topk(const float* logits, int64_t ld, const int32_t* row_ends,
  * cudaMalloc, or a plugin host that passes a kernel its inputs and outputs but
  * no allocator.  It computes what dsa_topk computes, with the same arguments
  * minus the workspace.  Its scratch is a file-scope device array of
- * DSA_TOPK_NOALLOC_MAX_ROWS rows (about 4.7 MB), held by every GPU that loads
+ * DSA_TOPK_NOALLOC_MAX_ROWS rows (512 KB), held by every GPU that loads
  * the library until the process exits.
  *
  *   - rows > DSA_TOPK_NOALLOC_MAX_ROWS returns DSA_ERR_UNSUPPORTED (split the rows

@@ -23,7 +23,7 @@ constexpr int kFp4KeyBytes = kPage * kDim / 2;    // 4096: codes of one MXFP4 pa
 // Top-k: 11-bit histogram of the order-preserving score bits.
 constexpr int kHistBits = 11;
 constexpr int kHistBins = 1 << kHistBits;
-constexpr int kCandCap = 8192;    // boundary-bin candidates kept per row
+constexpr int kCandCap = 8192;    // level-1 candidates kept per split row
 
 // Bounded waits give up after this long (ns) and flag DSA_STATUS_TIMEOUT.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
@@ -120,6 +120,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 // Plain bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
+// Per-thread asynchronous global -> shared copies (completion tracked per
+// thread by commit/wait groups; bytes past src_bytes are zero-filled and not
+// read).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

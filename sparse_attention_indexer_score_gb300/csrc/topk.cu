@@ -6,18 +6,20 @@
 //
 // Level 1 (fused into the scoring epilogue, or hist_kernel here): a 2048-bin
 // histogram of the top 11 bits of each row's order-preserving score keys.
-// select_kernel takes a row in chunks of 8192 positions, one 1024-thread CTA
-// per chunk, the chunk's scores in registers.  Every CTA finds the level-1
-// boundary bin B1 (where the count from the top reaches k); positions above
-// it are winners, placed at once; positions in B1 are candidates, kept in a
-// buffer and counted in a level-2 histogram (key bits 20..10).  The one CTA of
-// a short row, or the last CTA of a longer row (a done counter, no waiting),
-// then makes one pass over the candidates: level-2 winners are placed, the
-// candidates of the level-2 boundary bin are kept in shared memory with a
-// level-3 histogram (bits 9..0), and those settle the rest, equal keys last.
-// Positions within the top k come out in no particular order.  The row's
-// histograms and counters are cleared at the end, so the workspace is zero
-// for the next call.
+// select_kernel gives each span of a row (the whole row unless the batch has
+// too few rows to fill the GPU) one 512-thread CTA, two per SM.  A CTA finds
+// the level-1 boundary bin B1 (where the count from the top reaches k) and
+// streams its span in tiles of 4096 positions, two tiles of loads in flight:
+// positions above B1 are winners, positions in B1 are candidates, kept in
+// shared memory and counted in a level-2 histogram (key bits 20..10).  A row
+// of one span places its winners at once; the spans of a longer row publish
+// winners, candidates and level-2 counts to the row's global buffers, and the
+// last span to finish (a done counter, no waiting) settles the row.  One pass
+// over the candidates places the level-2 winners and keeps the candidates of
+// the level-2 boundary bin, which settle the rest (a rank count in one warp
+// when they are few, else a level-3 histogram of bits 9..0, equal keys last).
+// Positions within the top k come out in no particular order.  Histograms and
+// counters are cleared at the end, so the workspace is zero for the next call.
 #include <mutex>
 
 #include "host.h"
@@ -25,12 +27,16 @@
 
 namespace dsa {
 
-constexpr int kSelThreads = 1024;
-constexpr int kPerThread = 8;
-constexpr int kChunk = kSelThreads * kPerThread;   // positions per select CTA
-constexpr int kRefineCap = 4096;   // level-1 candidates of a one-chunk row kept in shared memory
-constexpr int kLevel3Cap = 2048;   // level-3 candidates kept in shared memory
-constexpr int kSelDynSmem = kRefineCap * sizeof(uint2) + kLevel3Cap * sizeof(uint2);
+constexpr int kSelThreads = 512;
+constexpr int kPerThread = 8;                       // values per thread in one tile
+constexpr int kChunk = kSelThreads * kPerThread;    // positions per tile (and per hist_kernel CTA)
+constexpr int kRefineCap = 3584;   // level-1 candidates kept in shared memory
+constexpr int kLevel3Cap = 512;    // level-3 candidates kept in shared memory
+constexpr int kWinCap = 4096;      // level-1 winners a CTA buffers in shared memory (k up to this)
+constexpr int kRing = 3;           // score tiles in flight per CTA (shared-memory ring)
+constexpr int kSpanMin = 2 * kChunk;   // shortest span worth a CTA of its own
+constexpr int kSelDynSmem = kRing * kChunk * sizeof(float) + kRefineCap * sizeof(uint2) +
+                            kLevel3Cap * sizeof(uint2) + kWinCap * sizeof(int);
 
 struct SelectArgs {
     const float* logits;
@@ -41,9 +47,10 @@ struct SelectArgs {
     int k;               // 0: fill only
     int32_t* out;
     unsigned* hist;      // level-1 histograms, [rows][2048]
-    unsigned* hist2;     // level-2 histograms of rows longer than one chunk, [rows][2048]
-    int* counters;       // [rows][4]: winners placed, candidates kept, chunks done, spare
-    uint2* cand;         // [rows][kCandCap]: level-1 candidates (key, position)
+    unsigned* hist2;     // level-2 histograms of split rows, [rows][2048]
+    int* counters;       // [rows][4]: winners published, candidates published, spans done, spare
+    uint2* cand;         // [rows][kCandCap]: level-1 candidates of split rows (key, position)
+    int span;            // positions per CTA, a multiple of kChunk
 };
 
 __device__ __forceinline__ int clamp_end(const int32_t* ends, int row, int64_t width) {
@@ -64,7 +71,7 @@ __device__ __forceinline__ void load_hist(unsigned* h, const unsigned* ghist) {
 // the top first reaches `need`; stores B and the count strictly above it.
 // Leaves both untouched when the counts never reach `need`.
 __device__ void find_boundary(const unsigned* h, int bins, int need, int* out_bin, int* out_above, int* tmp) {
-    const int per = bins / kSelThreads;   // bins per thread (2 or 1)
+    const int per = bins / kSelThreads;   // bins per thread
     const int first = bins - (threadIdx.x + 1) * per;   // thread 0 owns the top bins
     int local = 0;
     for (int i = 0; i < per; ++i) local += static_cast<int>(h[first + i]);
@@ -171,22 +178,37 @@ struct CandSource {
     }
 };
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a, int pdl) {
+// Top `need` of n3 <= 32 level-3 candidates by one warp: rank(c) = the
+// candidates with a larger key, plus equal keys earlier in the list.
+__device__ __forceinline__ void warp_rank_select(const uint2* c3, int n3, int32_t* out, int base, int need, int k) {
+    const int lane = threadIdx.x & 31;
+    const uint2 me = lane < n3 ? c3[lane] : make_uint2(0u, 0u);
+    int rank = 0;
+    for (int j = 0; j < n3; ++j) {
+        const uint32_t kj = __shfl_sync(0xFFFFFFFFu, me.x, j);
+        rank += (kj > me.x || (kj == me.x && j < lane)) ? 1 : 0;
+    }
+    if (lane < n3 && rank < need && base + rank < k) out[base + rank] = static_cast<int>(me.y);
+}
+
+__global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs a, int pdl) {
     __shared__ unsigned h1[kHistBins];   // level-1 histogram, then level 3
     __shared__ unsigned h2[kHistBins];   // level-2 histogram
     __shared__ int tmp[32];
     __shared__ int s_b1, s_a1, s_b2, s_a2, s_b3, s_a3;
-    __shared__ int s_win, s_cand, s_w2, s_c3, s_w3, s_tie, s_base_w, s_base_c, s_last;
-    extern __shared__ uint2 sel_dyn[];
-    uint2* cbuf = sel_dyn;                 // level-1 candidates of a one-chunk row
-    uint2* c3buf = sel_dyn + kRefineCap;   // level-3 candidates
+    __shared__ int s_win, s_cand, s_w2, s_c3, s_w3, s_tie, s_last, s_wbase, s_cbase;
+    extern __shared__ float4 sel_dyn[];
+    float4* ring = sel_dyn;                                                    // kRing tiles of scores
+    uint2* cbuf = reinterpret_cast<uint2*>(sel_dyn + kRing * kChunk / 4);     // level-1 candidates
+    uint2* c3buf = cbuf + kRefineCap;                                          // level-3 candidates
+    int* wbuf = reinterpret_cast<int*>(c3buf + kLevel3Cap);                    // level-1 winners
     if (pdl) pdl_wait();
     const int row = blockIdx.x;
-    const int64_t lo = static_cast<int64_t>(blockIdx.y) * kChunk;
+    const int64_t lo = static_cast<int64_t>(blockIdx.y) * a.span;
     const int n = clamp_end(a.ends, row, a.width);
     if (a.fill) {
         float* dst = a.fill + static_cast<int64_t>(row) * a.ld;
-        const int64_t hi = min(a.width, lo + kChunk);
+        const int64_t hi = min(a.width, lo + a.span);
         for (int64_t t = max(lo, static_cast<int64_t>(n)) + threadIdx.x; t < hi; t += kSelThreads)
             dst[t] = -__int_as_float(0x7F800000);
     }
@@ -194,29 +216,51 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     if (k <= 0) return;
     int32_t* out = a.out + static_cast<int64_t>(row) * k;
     if (n <= k) {
-        const int64_t hi = min(static_cast<int64_t>(k), lo + kChunk);
+        const int64_t hi = min(static_cast<int64_t>(k), lo + a.span);
         for (int64_t pos = lo + threadIdx.x; pos < hi; pos += kSelThreads) out[pos] = pos < n ? static_cast<int>(pos) : -1;
         return;
     }
-    const int nch = (n + kChunk - 1) / kChunk;
-    if (static_cast<int>(blockIdx.y) >= nch) return;
-    const bool multi = nch > 1;
+    const int nsp = static_cast<int>((n + a.span - 1) / a.span);
+    if (static_cast<int>(blockIdx.y) >= nsp) return;
+    const bool split = nsp > 1;
     unsigned* ghist = a.hist + static_cast<int64_t>(row) * kHistBins;
     unsigned* ghist2 = a.hist2 + static_cast<int64_t>(row) * kHistBins;
     int* ctr = a.counters + static_cast<int64_t>(row) * 4;
     uint2* gcand = a.cand + static_cast<int64_t>(row) * kCandCap;
     const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
     const int lane = threadIdx.x & 31;
-    const int hi = static_cast<int>(min(static_cast<int64_t>(n), lo + kChunk));
+    const int lo32 = static_cast<int>(lo);
+    const int hi = static_cast<int>(min(static_cast<int64_t>(n), lo + a.span));
+    // Winners wait in shared memory (written out coalesced after the pass)
+    // when k allows; else they go straight to the output.
+    const bool wbuffered = k <= kWinCap;
 
-    // ---- level 1: this chunk's scores in registers, the row's histogram in shared memory
-    float v[kPerThread];
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-        const int t = static_cast<int>(lo) + i * kSelThreads + threadIdx.x;
-        v[i] = t < hi ? src[t] : 0.0f;
-    }
+    // ---- level 1: the row's histogram, then the span in tiles through a
+    // ring of kRing tiles in shared memory.  Each thread copies, and later
+    // reads, the same 8 scores of a tile: positions base + 4 * tid + j and
+    // base + kChunk / 2 + 4 * tid + j (j < 4), so no barrier guards the ring.
     load_hist(h1, ghist);
+    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+    auto issue_tile = [&](int i) {   // tile i of the span into ring slot i % kRing
+        const int base = lo32 + i * kChunk;
+        float4* slot = ring + (i % kRing) * (kChunk / 4);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = base + h * (kChunk / 2) + 4 * threadIdx.x;
+            const int avail = max(0, min(4, hi - p));
+            float4* d = slot + h * (kChunk / 8) + threadIdx.x;
+            if (vec) {
+                cp_async16(d, avail ? src + p : src, 4u * avail);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    cp_async4(reinterpret_cast<float*>(d) + j, j < avail ? src + p + j : src, j < avail ? 4u : 0u);
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int i = 0; i < kRing; ++i) issue_tile(i);
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0;
     if (threadIdx.x == 0) {
         s_b1 = 0; s_a1 = 0; s_b2 = 0; s_a2 = 0; s_b3 = 0; s_a3 = 0;
@@ -227,75 +271,115 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     __syncthreads();
     const uint32_t B1 = static_cast<uint32_t>(s_b1);
     const int above1 = s_a1;
-    // Winners and candidates of the chunk: one shared add per warp for its
-    // totals (then one global add per CTA when the row has several chunks),
-    // ballots for the order within the warp.
-    int nw = 0, nc = 0;
+    const uint32_t kwin = (B1 + 1u) << (32 - kHistBits);   // keys >= kwin: winners (0 when B1 is the top bin)
+    const uint32_t kcand = B1 << (32 - kHistBits);         // keys in [kcand, kwin): candidates
+    const bool top_bin = B1 == kHistBins - 1;
+    // Classifies tile i (waiting for this thread's copies of it), then reuses
+    // its slot for tile i + kRing.  Bit u of wm / cm marks value u as a winner
+    // (key > kw) / candidate (kcand <= key <= kw); the warp's runs come from
+    // one scan of both counts and one shared add each, and only marked values
+    // are placed.
+    const uint32_t kw = top_bin ? 0xFFFFFFFFu : kwin - 1u;
+    const uint32_t crange = kw - kcand;
+    const int ntiles = (hi - lo32 + kChunk - 1) / kChunk;
+    const float* ringf = reinterpret_cast<const float*>(ring);
+    for (int i = 0; i < ntiles; ++i) {
+        cp_async_wait<kRing - 1>();
+        const int base = lo32 + i * kChunk;
+        const int slot = (i % kRing) * kChunk;   // float offset of the slot
+        const float4 va = ring[slot / 4 + threadIdx.x], vb = ring[slot / 4 + kChunk / 8 + threadIdx.x];
+        const float x[kPerThread] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+        uint32_t wm = 0, cm = 0;
 #pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-        const int t = static_cast<int>(lo) + i * kSelThreads + threadIdx.x;
-        const uint32_t b = order_key(v[i]) >> (32 - kHistBits);
-        nw += (t < hi && b > B1) ? 1 : 0;
-        nc += (t < hi && b == B1) ? 1 : 0;
-    }
-    nw = __reduce_add_sync(0xFFFFFFFFu, nw);
-    nc = __reduce_add_sync(0xFFFFFFFFu, nc);
-    int ow = 0, oc = 0;
-    if (lane == 0) {
-        ow = nw ? atomicAdd(&s_win, nw) : 0;
-        oc = nc ? atomicAdd(&s_cand, nc) : 0;
-    }
-    __syncthreads();
-    if (multi && threadIdx.x == 0) {
-        s_base_w = s_win ? atomicAdd(ctr + 0, s_win) : 0;
-        s_base_c = s_cand ? atomicAdd(ctr + 1, s_cand) : 0;
-    }
-    __syncthreads();
-    ow = __shfl_sync(0xFFFFFFFFu, ow, 0) + (multi ? s_base_w : 0);
-    oc = __shfl_sync(0xFFFFFFFFu, oc, 0) + (multi ? s_base_c : 0);
-    const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-        const int t = static_cast<int>(lo) + i * kSelThreads + threadIdx.x;
-        const uint32_t key = order_key(v[i]);
-        const uint32_t b = key >> (32 - kHistBits);
-        const bool win = t < hi && b > B1, cand = t < hi && b == B1;
-        const unsigned mw = __ballot_sync(0xFFFFFFFFu, win);
-        const unsigned mc = __ballot_sync(0xFFFFFFFFu, cand);
-        if (win) {
-            const int pos = ow + __popc(mw & lt);
-            if (pos < k) out[pos] = t;
-        } else if (cand) {
-            const int pos = oc + __popc(mc & lt);
-            atomicAdd(&h2[(key >> 10) & 0x7FF], 1u);
-            if (!multi) {
-                if (pos < kRefineCap) cbuf[pos] = make_uint2(key, static_cast<uint32_t>(t));
-            } else if (pos < kCandCap) {
-                gcand[pos] = make_uint2(key, static_cast<uint32_t>(t));
-            }
+        for (int u = 0; u < kPerThread; ++u) {
+            const uint32_t key = order_key(x[u]);
+            if (key > kw) wm |= 1u << u;
+            if (key - kcand <= crange) cm |= 1u << u;
         }
-        ow += __popc(mw);
-        oc += __popc(mc);
+        if (base + kChunk > hi) {   // last, partial tile: drop positions past the end
+            uint32_t inm = 0;
+#pragma unroll
+            for (int u = 0; u < kPerThread; ++u)
+                if (base + (u >> 2) * (kChunk / 2) + 4 * threadIdx.x + (u & 3) < hi) inm |= 1u << u;
+            wm &= inm;
+            cm &= inm;
+        }
+        const int cw = __popc(wm), cc = __popc(cm);
+        int inc = (cw << 16) | cc;   // both counts stay below 2^16
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if (lane >= d) inc += y;
+        }
+        int ow = 0, oc = 0;
+        if (lane == 31) {
+            if (inc >> 16) ow = atomicAdd(&s_win, inc >> 16);
+            if (inc & 0xFFFF) oc = atomicAdd(&s_cand, inc & 0xFFFF);
+        }
+        int pw = __shfl_sync(0xFFFFFFFFu, ow, 31) + (inc >> 16) - cw;
+        int pc = __shfl_sync(0xFFFFFFFFu, oc, 31) + (inc & 0xFFFF) - cc;
+        const int tb = base + 4 * threadIdx.x;   // position of value 0 of this thread
+        while (wm) {
+            const int u = __ffs(wm) - 1;
+            wm &= wm - 1u;
+            const int t = tb + (u >> 2) * (kChunk / 2) + (u & 3);
+            if (wbuffered) {
+                if (pw < kWinCap) wbuf[pw] = t;
+            } else if (!split) {
+                if (pw < k) out[pw] = t;
+            } else {
+                const int g = atomicAdd(ctr + 0, 1);
+                if (g < k) out[g] = t;
+            }
+            ++pw;
+        }
+        while (cm) {
+            const int u = __ffs(cm) - 1;
+            cm &= cm - 1u;
+            const int off = (u >> 2) * (kChunk / 2) + (u & 3);
+            const uint32_t key = order_key(ringf[slot + 4 * threadIdx.x + off]);
+            atomicAdd(&h2[(key >> 10) & 0x7FF], 1u);
+            if (pc < kRefineCap) cbuf[pc] = make_uint2(key, static_cast<uint32_t>(tb + off));
+            ++pc;
+        }
+        issue_tile(i + kRing);   // this thread is done with the slot
     }
+    cp_async_wait<0>();
     __syncthreads();
-    int ncand;
-    if (multi) {
-        // Add this chunk's level-2 counts to the row's; the last chunk to
-        // finish reads them back and settles the row.
+    int ncand = s_cand;
+    const uint2* cand_src = ncand <= kRefineCap ? cbuf : nullptr;
+    if (!split && wbuffered)
+        for (int i = threadIdx.x; i < s_win; i += kSelThreads)
+            if (i < k) out[i] = wbuf[i];
+    if (split) {
+        // Publish this span's winners, candidates and level-2 counts; the last
+        // span of the row to finish reads the row's totals back and settles it.
+        if (threadIdx.x == 0) {
+            s_wbase = (wbuffered && s_win) ? atomicAdd(ctr + 0, s_win) : 0;
+            s_cbase = s_cand ? atomicAdd(ctr + 1, s_cand) : 0;
+        }
+        __syncthreads();
+        if (wbuffered)
+            for (int i = threadIdx.x; i < s_win; i += kSelThreads)
+                if (s_wbase + i < k) out[s_wbase + i] = wbuf[i];
+        if (ncand <= kRefineCap)
+            for (int i = threadIdx.x; i < ncand; i += kSelThreads)
+                if (s_cbase + i < kCandCap) gcand[s_cbase + i] = cbuf[i];
         for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
             if (h2[i]) atomicAdd(ghist2 + i, h2[i]);
+        if (threadIdx.x == 0 && ncand > kRefineCap) atomicAdd(ctr + 3, 1);   // candidates dropped
         __syncthreads();
         if (threadIdx.x == 0) {
             __threadfence();
-            s_last = (atomicAdd(ctr + 2, 1) == nch - 1) ? 1 : 0;
+            s_last = (atomicAdd(ctr + 2, 1) == nsp - 1) ? 1 : 0;
         }
         __syncthreads();
         if (!s_last) return;
         __threadfence();
         load_hist(h2, ghist2);
         ncand = *reinterpret_cast<volatile int*>(ctr + 1);
-    } else {
-        ncand = s_cand;
+        const bool dropped = *reinterpret_cast<volatile int*>(ctr + 3) != 0;
+        cand_src = (!dropped && ncand <= kCandCap) ? gcand : nullptr;
     }
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h1[i] = 0;   // level 3 from here on
     __syncthreads();
@@ -306,54 +390,59 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
     __syncthreads();
     const uint32_t B2 = static_cast<uint32_t>(s_b2);
     const int above2 = s_a2;
-    CandSource cs{nullptr, 0, src, n, B1};
-    if (!multi && ncand <= kRefineCap) cs.buf = cbuf;
-    else if (multi && ncand <= kCandCap) cs.buf = gcand;
-    cs.count = ncand;
+    const CandSource cs{cand_src, ncand, src, n, B1};
     const int base2 = above1, base3 = above1 + above2;
-    cs.for_each([&](bool valid, uint32_t key, int t) {
-        const uint32_t b2 = (key >> 10) & 0x7FF;
+    cs.for_each([&](bool valid, uint32_t kk, int t) {
+        if (!__any_sync(0xFFFFFFFFu, valid)) return;   // uniform over the warp
+        const uint32_t b2 = (kk >> 10) & 0x7FF;
         const int pw = warp_slot(valid && b2 > B2, &s_w2);
         if (pw >= 0 && base2 + pw < k) out[base2 + pw] = t;
         const bool c3 = valid && b2 == B2;
         const int pc = warp_slot(c3, &s_c3);
         if (c3) {
-            atomicAdd(&h1[key & 0x3FF], 1u);
-            if (pc < kLevel3Cap) c3buf[pc] = make_uint2(key, static_cast<uint32_t>(t));
+            atomicAdd(&h1[kk & 0x3FF], 1u);
+            if (pc < kLevel3Cap) c3buf[pc] = make_uint2(kk, static_cast<uint32_t>(t));
         }
     });
     __syncthreads();
 
     // ---- level 3 and equal keys
     const int need2 = need - above2;
-    find_boundary(h1, 1024, need2, &s_b3, &s_a3, tmp);
-    __syncthreads();
-    const uint32_t B3 = static_cast<uint32_t>(s_b3);
-    const int above3 = s_a3;
     const int n3 = s_c3;
-    const int left = need2 - above3;   // equal keys to take
-    auto level3 = [&](bool valid, uint32_t key, int t) {
-        const uint32_t b3 = key & 0x3FF;
-        const int pw = warp_slot(valid && b3 > B3, &s_w3);
-        if (pw >= 0 && base3 + pw < k) out[base3 + pw] = t;
-        const int pt = warp_slot(valid && b3 == B3, &s_tie);
-        if (pt >= 0 && pt < left && base3 + above3 + pt < k) out[base3 + above3 + pt] = t;
-    };
-    if (n3 <= kLevel3Cap) {
-        const CandSource c3s{c3buf, n3, src, n, B1};
-        c3s.for_each(level3);
+    int placed;
+    if (n3 <= 32) {
+        // few enough to rank in one warp (their keys agree on bits 31..10)
+        if (threadIdx.x < 32) warp_rank_select(c3buf, n3, out, base3, need2, k);
+        placed = base3 + min(n3, need2);
     } else {
-        cs.for_each([&](bool valid, uint32_t key, int t) { level3(valid && ((key >> 10) & 0x7FF) == B2, key, t); });
+        find_boundary(h1, 1024, need2, &s_b3, &s_a3, tmp);
+        __syncthreads();
+        const uint32_t B3 = static_cast<uint32_t>(s_b3);
+        const int above3 = s_a3;
+        const int left = need2 - above3;   // equal keys to take
+        auto level3 = [&](bool valid, uint32_t kk, int t) {
+            const uint32_t b3 = kk & 0x3FF;
+            const int pw = warp_slot(valid && b3 > B3, &s_w3);
+            if (pw >= 0 && base3 + pw < k) out[base3 + pw] = t;
+            const int pt = warp_slot(valid && b3 == B3, &s_tie);
+            if (pt >= 0 && pt < left && base3 + above3 + pt < k) out[base3 + above3 + pt] = t;
+        };
+        if (n3 <= kLevel3Cap) {
+            const CandSource c3s{c3buf, n3, src, n, B1};
+            c3s.for_each(level3);
+        } else {
+            cs.for_each([&](bool valid, uint32_t kk, int t) { level3(valid && ((kk >> 10) & 0x7FF) == B2, kk, t); });
+        }
+        __syncthreads();
+        placed = base3 + above3 + min(s_tie, left);
     }
-    __syncthreads();
     // Short only when the histogram disagreed with the scores (an aborted scoring pass).
-    const int placed = base3 + above3 + min(s_tie, left);
     for (int e = placed + threadIdx.x; e < k; e += kSelThreads) out[e] = -1;
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) {
         ghist[i] = 0;
-        if (multi) ghist2[i] = 0;
+        if (split) ghist2[i] = 0;
     }
-    if (multi && threadIdx.x < 4) ctr[threadIdx.x] = 0;
+    if (split && threadIdx.x < 4) ctr[threadIdx.x] = 0;
 }
 
 // ----------------------------------------------------------------- host utilities
@@ -436,18 +525,29 @@ int launch_select(const float* logits, float* logits_fill, int64_t ld, int64_t w
     a.hist2 = reinterpret_cast<unsigned*>(ws + L.hist2);
     a.counters = reinterpret_cast<int*>(ws + L.counters);
     a.cand = reinterpret_cast<uint2*>(ws + L.cand);
-    const int64_t span = (k > width) ? k : width;
-    const int64_t chunks = (span + kChunk - 1) / kChunk;
-    if (chunks == 0 || rows == 0) return DSA_OK;
-    if (chunks > 65535 || rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
-    const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(chunks));
+    if (rows == 0 || (k == 0 && (!logits_fill || width == 0))) return DSA_OK;
+    if (rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    // Span per CTA: about two CTAs per SM over rows x width, at least kSpanMin
+    // positions, a multiple of kChunk.
+    const int64_t target = 2 * static_cast<int64_t>(device_sm_count());
+    int64_t span = (rows * width + target - 1) / target;
+    span = span < kSpanMin ? kSpanMin : span;
+    span = (span + kChunk - 1) / kChunk * kChunk;
+    if (span > (int64_t(1) << 30)) span = int64_t(1) << 30;
+    a.span = static_cast<int>(span);
+    const int64_t reach = (k > width) ? k : width;
+    const int64_t spans = (reach + span - 1) / span;
+    if (spans > 65535) return DSA_ERR_UNSUPPORTED;
+    const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(spans > 0 ? spans : 1));
     cudaError_t err;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
     if (!attr_set[dev]) {
         if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelDynSmem) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return DSA_ERR_CUDA;
         attr_set[dev] = true;
     }

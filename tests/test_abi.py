@@ -41,7 +41,7 @@ def test_workspace_sizes_are_host_only(lib):
     a = lib.dsa_workspace_size(0, 64, 64, 128, 2048)
     b = lib.dsa_workspace_size(0, 128, 64, 128, 2048)
     assert a > 64 * 128 * 64 * 4 and b > a
-    assert lib.dsa_topk_workspace_size(10, 64) > 10 * 2048 * 4
+    assert lib.dsa_topk_workspace_size(10, 64) >= 10 * 2048 * 4
 
 
 def test_host_argument_checks(lib):
