@@ -61,7 +61,14 @@ constexpr int OFF_QSF = OFF_SFA + kStages * 512;
 constexpr int OFF_SFB = OFF_QSF + 2 * 512;
 constexpr int OFF_KS = OFF_SFB + 2 * 512;
 constexpr int OFF_W = OFF_KS + kAcc * 128 * 4;            // float[kEpiWarps][4 rows][32 heads]: w per warp
-constexpr int OFF_SINFO = OFF_W + kEpiWarps * kSegRows * kHeads * 4;   // int2[kStages]: {tile in segment, segment}
+// Score histogram of each epilogue group for its current segment: 4 rows x
+// 2048 bins of 16-bit counts, two per word; added to the rows' histograms in
+// global memory when the segment changes and at least every kHistFlushTiles
+// tiles (so that no count passes 2^16 - 1).
+constexpr int kHistFlushTiles = 256;
+constexpr int OFF_HIST = OFF_W + kEpiWarps * kSegRows * kHeads * 4;
+constexpr int kGroupHistWords = kSegRows * kHistBins / 2;
+constexpr int OFF_SINFO = OFF_HIST + kEpiGroups * kGroupHistWords * 4;   // int2[kStages]: {tile in segment, segment}
 constexpr int OFF_AINFO = OFF_SINFO + kStages * 8;        // int2[kAcc]: the same per accumulator
 constexpr int OFF_BAR = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 * kAcc + 1;
@@ -112,8 +119,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
                                                     int max_keys, int* __restrict__ info, int4* __restrict__ segs,
                                                     int* __restrict__ seg_prefix, int* __restrict__ eff_end,
                                                     int4* __restrict__ cta, int G, int32_t* status) {
-    pdl_launch_dependents();
+    // The scoring CTAs (persistent, one per SM, most of its registers) are let
+    // in only once the work before this kernel has finished, so that they do
+    // not crowd out a still-running predecessor; their prologue then overlaps
+    // this kernel.
     pdl_wait();
+    pdl_launch_dependents();
     __shared__ int warp_tmp[32];
     __shared__ int chunk_total;
     __shared__ int sp[kPlanSmemSegs + 1];   // tile prefix, when the segments fit
@@ -495,19 +506,50 @@ __device__ __forceinline__ float head_sum(const uint32_t* v, const float* wr, fl
 }
 
 // Logit store and histogram count of one row's 32 scores (one per lane);
-// the warp adds one count per distinct bin to the row's histogram in global
-// memory.
+// hrow is the row's part of the group's shared histogram.
 __device__ __forceinline__ void emit_row(const ScoreArgs& p, int row, int tpos, float sc, int end, bool hist_on,
-                                         int lane) {
+                                         uint32_t* hrow) {
     const bool valid = tpos < end;
     if (valid) p.logits[static_cast<int64_t>(row) * p.ld + tpos] = sc;
-    const unsigned counted = __ballot_sync(0xFFFFFFFFu, valid && hist_on);
     if (valid && hist_on) {
         const uint32_t bin = hist_bin(sc);
-        const unsigned peers = __match_any_sync(counted, bin);
-        if (lane == __ffs(peers) - 1)
-            atomicAdd(p.hist + static_cast<int64_t>(row) * kHistBins + bin, static_cast<unsigned>(__popc(peers)));
+        atomicAdd(hrow + (bin >> 1), 1u << ((bin & 1u) << 4));
     }
+}
+
+// Named barrier over the 128 threads of epilogue group g, returning the OR of `pred`.
+__device__ __forceinline__ bool group_sync_any(int g, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(1 + g)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void group_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
+
+// Adds the group's shared histogram of segment rows row0 .. row0 + nrows
+// (those whose bit is set in hist_m) to the rows' global histograms and
+// clears it.  e: thread index within the group.
+__device__ __forceinline__ void flush_group_hist(const ScoreArgs& p, uint32_t* gh, int g, int row0, int nrows,
+                                                 unsigned hist_m, int e) {
+    group_sync(g);
+    for (int r = 0; r < nrows; ++r) {
+        if (!((hist_m >> r) & 1u)) continue;
+        uint32_t* hr = gh + r * (kHistBins / 2);
+        unsigned* dst = p.hist + static_cast<int64_t>(row0 + r) * kHistBins;
+        for (int w = e; w < kHistBins / 2; w += 128) {
+            const uint32_t c = hr[w];
+            if (c) {
+                if (c & 0xFFFFu) atomicAdd(dst + 2 * w, c & 0xFFFFu);
+                if (c >> 16) atomicAdd(dst + 2 * w + 1, c >> 16);
+                hr[w] = 0u;
+            }
+        }
+    }
+    group_sync(g);
 }
 
 // Warps 2 .. 2 + kEpiWarps.  Group g = (warp - 2) / 4 drains the accumulators
@@ -523,15 +565,29 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
     const int2* ainfo = reinterpret_cast<const int2*>(smem + OFF_AINFO);
     const bool f32scale = (p.fmt == DSA_FMT_FP8);
     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC;
-    int cur = -1, row0 = 0, nrows = 0;
+    uint32_t* gh = reinterpret_cast<uint32_t*>(smem + OFF_HIST) + group * kGroupHistWords;
+    const int e = threadIdx.x - 64 - group * 128;   // thread index within the group
+    int cur = -1, row0 = 0, nrows = 0, seg_tiles = 0;
     int end_l = 0;        // lane r < nrows: bound of row row0 + r
     unsigned hist_m = 0;  // bit r: row r gets a histogram
+    bool aborted = false;
     for (int it = group;; it += kEpiGroups) {
         const int a = it % kAcc;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull + a, (it / kAcc) & 1, abort, p.status))) break;
+        // One decision for the group's four warps: all stop if any wait gave up
+        // (they share the histogram and its flush barriers).
+        const bool ok = mbar_wait(tfull + a, (it / kAcc) & 1, abort, p.status);
+        if (group_sync_any(group, !ok)) {
+            aborted = true;
+            break;
+        }
         tc_fence_after();
         const int2 tag = ainfo[a];   // {tile in segment, segment}; segment -1 ends the sequence
         if (tag.y < 0) break;
+        if (tag.y != cur || seg_tiles == kHistFlushTiles) {
+            if (cur >= 0 && hist_m) flush_group_hist(p, gh, group, row0, nrows, hist_m, e);
+            seg_tiles = 0;
+        }
+        ++seg_tiles;
         if (tag.y != cur) {
             cur = tag.y;
             const int4 si = p.segs[cur];
@@ -553,21 +609,24 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
             tc_wait_ld_regs<64>(v);
             const float s0 = head_sum(v, wsm + r * kHeads, ksm);
             const float s1 = head_sum(v + 32, wsm + (r + 1) * kHeads, ksm);
-            emit_row(p, row0 + r, tpos, s0, __shfl_sync(0xFFFFFFFFu, end_l, r), (hist_m >> r) & 1, lane);
+            emit_row(p, row0 + r, tpos, s0, __shfl_sync(0xFFFFFFFFu, end_l, r), (hist_m >> r) & 1,
+                     gh + r * (kHistBins / 2));
             emit_row(p, row0 + r + 1, tpos, s1, __shfl_sync(0xFFFFFFFFu, end_l, r + 1), (hist_m >> (r + 1)) & 1,
-                     lane);
+                     gh + (r + 1) * (kHistBins / 2));
         }
         if (r < nrows) {
             uint32_t v[32];
             tc_ld_32x32b_x32(acc + r * 32, v);
             tc_wait_ld_regs<32>(v);
             const float s0 = head_sum(v, wsm + r * kHeads, ksm);
-            emit_row(p, row0 + r, tpos, s0, __shfl_sync(0xFFFFFFFFu, end_l, r), (hist_m >> r) & 1, lane);
+            emit_row(p, row0 + r, tpos, s0, __shfl_sync(0xFFFFFFFFu, end_l, r), (hist_m >> r) & 1,
+                     gh + r * (kHistBins / 2));
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty + a);
     }
+    if (cur >= 0 && !aborted && hist_m) flush_group_hist(p, gh, group, row0, nrows, hist_m, e);
 }
 
 __global__ void __launch_bounds__(kScoreThreads, 1)
@@ -608,6 +667,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         tma_prefetch(&qmap);
     }
     if (warp == 1) tc_alloc(tmem_slot, TM_COLS);
+    for (int i = threadIdx.x; i < kEpiGroups * kGroupHistWords; i += blockDim.x)
+        reinterpret_cast<uint32_t*>(smem + OFF_HIST)[i] = 0u;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
