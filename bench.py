@@ -238,6 +238,24 @@ def run_reference(args, wl):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------- ranks
+def max_over_ranks(values, device=None) -> list:
+    """Element-wise maximum of ``values`` over the ranks of the default
+    process group (the values themselves when there is no group)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_step_per_rank: float, steps: int, world: int, total_ms: float) -> float:
+    """Units all ranks processed per second: every rank runs the same
+    per-step work (weak scaling), timed by the slowest rank."""
+    return units_per_step_per_rank * steps * world / (total_ms / 1e3)
+
+
 # ----------------------------------------------------------------- GPU
 def run_ours(args, wl, rank, world, local_rank):
     import torch
@@ -352,14 +370,10 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in eev) * args.steps / e2e_steps
 
-    times = torch.tensor([step_ms, e2e_ms, kernel_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    step_ms, e2e_ms, kernel_ms = times.tolist()
+    step_ms, e2e_ms, kernel_ms = max_over_ranks([step_ms, e2e_ms, kernel_ms], dev)
     if rank != 0:
         return
-    keys_total = ab["scored"] * args.steps * world
-    value = keys_total / (step_ms / 1e3)
+    value = whole_job_rate(ab["scored"], args.steps, world, step_ms)
     peaks = measured_peaks()
     achieved = ab["score_kernel"] / (kernel_ms / 1e3) / 1e9
     traffic = ncu_traffic(wl.name, ab["score_kernel"])
@@ -381,7 +395,7 @@ def run_ours(args, wl, rank, world, local_rank):
                      "kernel": "score_kernel", "kernel_us": kernel_ms * 1e3,
                      "peak_source": f"{peaks['source']} HBM copy bandwidth",
                      "step_frac": (ab["step"] / (step_ms / args.steps / 1e3) / 1e9) / peaks["hbm_gbs"]},
-        "e2e": {"value": keys_total / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "how": "eager public-API calls, host copies in the timed region"},
         "gpu_launches": STEP_KERNELS * args.steps,
         "clocks": clk,

@@ -1,0 +1,71 @@
+"""The multi-rank plumbing of bench.py, on CPU with the gloo backend: the
+max-over-ranks timing, the whole-job rate, and the reference arm under
+torchrun (rank 0 alone prints its line)."""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r took 1 + r, 10 - r, r / 2 milliseconds on the three timers
+        q.put((rank, bench.max_over_ranks([1.0 + rank, 10.0 - rank, 0.5 * rank])))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got[0] == got[1] == [2.0, 10.0, 0.5]
+
+
+def test_max_over_ranks_without_group_is_identity():
+    assert bench.max_over_ranks([3.0, 4.5]) == [3.0, 4.5]
+
+
+def test_whole_job_rate_counts_every_rank():
+    # 1000 keys per step per rank, 10 steps, 2 ranks, 5 ms for the slowest rank
+    assert bench.whole_job_rate(1000, 10, 2, 5.0) == 1000 * 10 * 2 / 0.005
+    assert bench.whole_job_rate(1000, 10, 1, 5.0) * 2 == bench.whole_job_rate(1000, 10, 2, 5.0)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--config", "tiny_fp8", "--steps", "1", "--warmup", "3"]
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1")
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [line for line in out.stdout.splitlines() if line.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
