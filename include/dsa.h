@@ -149,6 +149,35 @@ int dsa_decode_layout(const int32_t* seq_lens, int64_t num_seq,
                       void* stream);
 
 /*
+ * dsa_prepare_step - dsa_quantize_query, dsa_insert_key and dsa_decode_layout
+ * of one decode step in a single launch.
+ *
+ * Page "cutedsl.dsa.index" (DsaIndex) handles the query and the new key of a
+ * token together; page "cutedsl.dsa.overlap" runs this preparation ahead of
+ * scoring.  The three parts read and write disjoint buffers, so the results
+ * are exactly those of the three calls (in any order); the arguments keep
+ * their meaning, layout and checks:
+ *   fmt, q, q_row_stride, wv, wv_row_stride, rows, q_out, w_out   as dsa_quantize_query;
+ *   k, k_row_stride, gamma, beta, eps, slots, n, cache, page_stride,
+ *   num_pages, status                                            as dsa_insert_key;
+ *   seq_lens, num_seq, query_lens, num_requests, num_rows,
+ *   starts, row_ends                                             as dsa_decode_layout.
+ * Any argument error of a part returns that error and launches nothing.
+ * Ownership: every buffer belongs to the caller; nothing is allocated.
+ */
+int dsa_prepare_step(int fmt, const void* q, int64_t q_row_stride,
+                     const void* wv, int64_t wv_row_stride, int64_t rows,
+                     void* q_out, void* w_out,
+                     const void* k, int64_t k_row_stride,
+                     const float* gamma, const float* beta, float eps,
+                     const int64_t* slots, int64_t n,
+                     void* cache, int64_t page_stride, int64_t num_pages,
+                     const int32_t* seq_lens, int64_t num_seq,
+                     const int32_t* query_lens, int64_t num_requests,
+                     int64_t num_rows, int32_t* starts, int32_t* row_ends,
+                     int32_t* status, void* stream);
+
+/*
  * dsa_workspace_size - bytes of scratch dsa_score_paged needs for these sizes
  * (rows query rows, num_requests requests, max_pages block-table columns, top-k k).
  * The workspace must be zero-filled before its first use; every call that

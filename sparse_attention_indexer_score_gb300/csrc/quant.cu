@@ -5,6 +5,7 @@
 // insert_key, insert_fp4_key, mxfp4_scale (definition only), e2m1x2.
 #include "host.h"
 #include "common.cuh"
+#include "layout_body.cuh"
 
 namespace dsa {
 
@@ -47,15 +48,13 @@ __device__ __forceinline__ int mx_exponent(float amax) {
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 // ----------------------------------------------------------------- a1: query rows
-// One warp per (row, head); lane l holds columns 4l..4l+3.
-__global__ void __launch_bounds__(256) quantize_query_kernel(int fmt, const uint16_t* __restrict__ q,
-                                                             int64_t q_stride, const uint16_t* __restrict__ wv,
-                                                             int64_t wv_stride, int64_t rows,
-                                                             uint8_t* __restrict__ q_out,
-                                                             __nv_bfloat16* __restrict__ w_out) {
-    pdl_launch_dependents();
-    pdl_wait();
-    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+// One warp per (row, head); lane l holds columns 4l..4l+3.  `block` is the
+// block index within this part of the grid (256 threads per block).
+__device__ __forceinline__ void quantize_query_block(int fmt, const uint16_t* __restrict__ q, int64_t q_stride,
+                                                     const uint16_t* __restrict__ wv, int64_t wv_stride,
+                                                     int64_t rows, uint8_t* __restrict__ q_out,
+                                                     __nv_bfloat16* __restrict__ w_out, int64_t block) {
+    const int64_t gw = (block * 256 + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (gw >= rows * kHeads) return;
     const int64_t row = gw >> 5;
@@ -99,17 +98,25 @@ __global__ void __launch_bounds__(256) quantize_query_kernel(int fmt, const uint
     }
 }
 
-// ----------------------------------------------------------------- a2: keys
-// One half-warp per key; lane j of the half holds columns 8j..8j+7.
-__global__ void __launch_bounds__(256) insert_key_kernel(int fmt, const uint16_t* __restrict__ k, int64_t k_stride,
-                                                         const float* __restrict__ gamma,
-                                                         const float* __restrict__ beta, float eps,
-                                                         const int64_t* __restrict__ slots, int64_t n,
-                                                         uint8_t* __restrict__ cache, int64_t page_stride,
-                                                         int64_t num_pages, int32_t* status) {
+__global__ void __launch_bounds__(256) quantize_query_kernel(int fmt, const uint16_t* __restrict__ q,
+                                                             int64_t q_stride, const uint16_t* __restrict__ wv,
+                                                             int64_t wv_stride, int64_t rows,
+                                                             uint8_t* __restrict__ q_out,
+                                                             __nv_bfloat16* __restrict__ w_out) {
     pdl_launch_dependents();
     pdl_wait();
-    const int64_t key = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+    quantize_query_block(fmt, q, q_stride, wv, wv_stride, rows, q_out, w_out, blockIdx.x);
+}
+
+// ----------------------------------------------------------------- a2: keys
+// One half-warp per key; lane j of the half holds columns 8j..8j+7.  `block`
+// is the block index within this part of the grid (256 threads per block).
+__device__ __forceinline__ void insert_key_block(int fmt, const uint16_t* __restrict__ k, int64_t k_stride,
+                                                 const float* __restrict__ gamma, const float* __restrict__ beta,
+                                                 float eps, const int64_t* __restrict__ slots, int64_t n,
+                                                 uint8_t* __restrict__ cache, int64_t page_stride,
+                                                 int64_t num_pages, int32_t* status, int64_t block) {
+    const int64_t key = (block * 256 + threadIdx.x) >> 4;
     const int j = threadIdx.x & 15;
     const unsigned hmask = (threadIdx.x & 16) ? 0xFFFF0000u : 0x0000FFFFu;
     if (key >= n) return;
@@ -198,23 +205,123 @@ __global__ void __launch_bounds__(256) insert_key_kernel(int fmt, const uint16_t
     }
 }
 
+__global__ void __launch_bounds__(256) insert_key_kernel(int fmt, const uint16_t* __restrict__ k, int64_t k_stride,
+                                                         const float* __restrict__ gamma,
+                                                         const float* __restrict__ beta, float eps,
+                                                         const int64_t* __restrict__ slots, int64_t n,
+                                                         uint8_t* __restrict__ cache, int64_t page_stride,
+                                                         int64_t num_pages, int32_t* status) {
+    pdl_launch_dependents();
+    pdl_wait();
+    insert_key_block(fmt, k, k_stride, gamma, beta, eps, slots, n, cache, page_stride, num_pages, status, blockIdx.x);
+}
+
+// ----------------------------------------------------------------- fused step preparation
+// One launch for the three independent parts of a decode step's preparation:
+// block 0 computes the request starts and row bounds, the next blocks insert
+// the step's keys, the rest quantise the query rows.  The parts write
+// disjoint buffers, so the result is that of the three calls in any order.
+struct PrepareArgs {
+    int fmt;
+    // query rows
+    const uint16_t* q;
+    int64_t q_stride;
+    const uint16_t* wv;
+    int64_t wv_stride;
+    int64_t rows;
+    uint8_t* q_out;
+    __nv_bfloat16* w_out;
+    int64_t q_blocks;
+    // keys
+    const uint16_t* k;
+    int64_t k_stride;
+    const float* gamma;
+    const float* beta;
+    float eps;
+    const int64_t* slots;
+    int64_t n;
+    uint8_t* cache;
+    int64_t page_stride;
+    int64_t num_pages;
+    int32_t* status;
+    int64_t k_blocks;
+    // layout
+    const int32_t* seq_lens;
+    const int32_t* query_lens;
+    int num_req;
+    int64_t num_rows;
+    int32_t* starts;
+    int32_t* row_ends;
+};
+
+__global__ void __launch_bounds__(256) prepare_step_kernel(const PrepareArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t b = blockIdx.x;
+    if (b == 0) {
+        decode_layout_block(a.seq_lens, a.query_lens, a.num_req, a.num_rows, a.starts, a.row_ends);
+    } else if (b <= a.k_blocks) {
+        insert_key_block(a.fmt, a.k, a.k_stride, a.gamma, a.beta, a.eps, a.slots, a.n, a.cache, a.page_stride,
+                         a.num_pages, a.status, b - 1);
+    } else {
+        quantize_query_block(a.fmt, a.q, a.q_stride, a.wv, a.wv_stride, a.rows, a.q_out, a.w_out,
+                             b - 1 - a.k_blocks);
+    }
+}
+
 }  // namespace dsa
 
 using namespace dsa;
 
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-extern "C" int dsa_quantize_query(int fmt, const void* q, int64_t q_row_stride, const void* wv,
-                                  int64_t wv_row_stride, int64_t rows, void* q_out, void* w_out, void* stream) {
+// Argument checks shared by the single calls and dsa_prepare_step; each
+// returns DSA_OK and the number of 256-thread blocks its part needs (0 when
+// there is nothing to do).
+static int check_quantize(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride,
+                          int64_t rows, const void* q_out, const void* w_out, int64_t* blocks) {
+    *blocks = 0;
     if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4) return DSA_ERR_UNSUPPORTED;
     if (rows < 0) return DSA_ERR_INVALID;
     if (rows == 0) return DSA_OK;
     if (!q || !wv || !q_out || !w_out) return DSA_ERR_INVALID;
     if (q_row_stride < kHeads * kDim || q_row_stride % 8 || wv_row_stride < kHeads) return DSA_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(q_out, 16) || !aligned(w_out, 2) || !aligned(wv, 2)) return DSA_ERR_INVALID;
-    const int64_t warps = rows * kHeads;
-    const int64_t blocks = (warps * 32 + 255) / 256;
-    if (blocks > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    *blocks = (rows * kHeads * 32 + 255) / 256;
+    return *blocks > 0x7FFFFFFF ? DSA_ERR_UNSUPPORTED : DSA_OK;
+}
+
+static int check_insert(int fmt, const void* k, int64_t k_row_stride, const float* gamma, const float* beta,
+                        const int64_t* slots, int64_t n, const void* cache, int64_t page_stride, int64_t num_pages,
+                        int64_t* blocks) {
+    *blocks = 0;
+    if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4) return DSA_ERR_UNSUPPORTED;
+    if (n < 0 || num_pages < 0) return DSA_ERR_INVALID;
+    if (n == 0) return DSA_OK;
+    if (!k || !gamma || !beta || !slots || !cache) return DSA_ERR_INVALID;
+    const int64_t min_stride = (fmt == DSA_FMT_MXFP4) ? DSA_FP4_PAGE_BYTES : DSA_FP8_PAGE_BYTES;
+    if (page_stride < min_stride || page_stride % 16) return DSA_ERR_INVALID;
+    if (k_row_stride < kDim || k_row_stride % 8) return DSA_ERR_INVALID;
+    if (!aligned(k, 16) || !aligned(gamma, 16) || !aligned(beta, 16) || !aligned(cache, 16) || !aligned(slots, 8))
+        return DSA_ERR_INVALID;
+    *blocks = (n * 16 + 255) / 256;
+    return *blocks > 0x7FFFFFFF ? DSA_ERR_UNSUPPORTED : DSA_OK;
+}
+
+static int check_layout(const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens, int64_t num_requests,
+                        int64_t num_rows, const int32_t* starts, const int32_t* row_ends) {
+    if (num_rows < 0 || num_requests < 0 || num_seq < num_requests) return DSA_ERR_INVALID;
+    if (num_requests > 0x7FFFFFFF - 1 || num_rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    if (!starts || (num_rows > 0 && !row_ends) || (num_requests > 0 && (!seq_lens || !query_lens)))
+        return DSA_ERR_INVALID;
+    return DSA_OK;
+}
+
+extern "C" int dsa_quantize_query(int fmt, const void* q, int64_t q_row_stride, const void* wv,
+                                  int64_t wv_row_stride, int64_t rows, void* q_out, void* w_out, void* stream) {
+    int64_t blocks = 0;
+    const int rc = check_quantize(fmt, q, q_row_stride, wv, wv_row_stride, rows, q_out, w_out, &blocks);
+    if (rc != DSA_OK || blocks == 0) return rc;
     const cudaError_t err = launch_pdl(quantize_query_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
                                        static_cast<cudaStream_t>(stream), fmt, static_cast<const uint16_t*>(q),
                                        q_row_stride, static_cast<const uint16_t*>(wv), wv_row_stride, rows,
@@ -225,20 +332,59 @@ extern "C" int dsa_quantize_query(int fmt, const void* q, int64_t q_row_stride, 
 extern "C" int dsa_insert_key(int fmt, const void* k, int64_t k_row_stride, const float* gamma, const float* beta,
                               float eps, const int64_t* slots, int64_t n, void* cache, int64_t page_stride,
                               int64_t num_pages, int32_t* status, void* stream) {
-    if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4) return DSA_ERR_UNSUPPORTED;
-    if (n < 0 || num_pages < 0) return DSA_ERR_INVALID;
-    if (n == 0) return DSA_OK;
-    if (!k || !gamma || !beta || !slots || !cache) return DSA_ERR_INVALID;
-    const int64_t min_stride = (fmt == DSA_FMT_MXFP4) ? DSA_FP4_PAGE_BYTES : DSA_FP8_PAGE_BYTES;
-    if (page_stride < min_stride || page_stride % 16) return DSA_ERR_INVALID;
-    if (k_row_stride < kDim || k_row_stride % 8) return DSA_ERR_INVALID;
-    if (!aligned(k, 16) || !aligned(gamma, 16) || !aligned(beta, 16) || !aligned(cache, 16) || !aligned(slots, 8))
-        return DSA_ERR_INVALID;
-    const int64_t blocks = (n * 16 + 255) / 256;
-    if (blocks > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    int64_t blocks = 0;
+    const int rc = check_insert(fmt, k, k_row_stride, gamma, beta, slots, n, cache, page_stride, num_pages, &blocks);
+    if (rc != DSA_OK || blocks == 0) return rc;
     const cudaError_t err = launch_pdl(insert_key_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
                                        static_cast<cudaStream_t>(stream), fmt, static_cast<const uint16_t*>(k),
                                        k_row_stride, gamma, beta, eps, slots, n, static_cast<uint8_t*>(cache),
                                        page_stride, num_pages, status);
+    return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+extern "C" int dsa_prepare_step(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride,
+                                int64_t rows, void* q_out, void* w_out, const void* k, int64_t k_row_stride,
+                                const float* gamma, const float* beta, float eps, const int64_t* slots, int64_t n,
+                                void* cache, int64_t page_stride, int64_t num_pages, const int32_t* seq_lens,
+                                int64_t num_seq, const int32_t* query_lens, int64_t num_requests, int64_t num_rows,
+                                int32_t* starts, int32_t* row_ends, int32_t* status, void* stream) {
+    int64_t qb = 0, kb = 0;
+    int rc = check_quantize(fmt, q, q_row_stride, wv, wv_row_stride, rows, q_out, w_out, &qb);
+    if (rc != DSA_OK) return rc;
+    rc = check_insert(fmt, k, k_row_stride, gamma, beta, slots, n, cache, page_stride, num_pages, &kb);
+    if (rc != DSA_OK) return rc;
+    rc = check_layout(seq_lens, num_seq, query_lens, num_requests, num_rows, starts, row_ends);
+    if (rc != DSA_OK) return rc;
+    if (1 + kb + qb > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    PrepareArgs a;
+    a.fmt = fmt;
+    a.q = static_cast<const uint16_t*>(q);
+    a.q_stride = q_row_stride;
+    a.wv = static_cast<const uint16_t*>(wv);
+    a.wv_stride = wv_row_stride;
+    a.rows = rows;
+    a.q_out = static_cast<uint8_t*>(q_out);
+    a.w_out = static_cast<__nv_bfloat16*>(w_out);
+    a.q_blocks = qb;
+    a.k = static_cast<const uint16_t*>(k);
+    a.k_stride = k_row_stride;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.eps = eps;
+    a.slots = slots;
+    a.n = n;
+    a.cache = static_cast<uint8_t*>(cache);
+    a.page_stride = page_stride;
+    a.num_pages = num_pages;
+    a.status = status;
+    a.k_blocks = kb;
+    a.seq_lens = seq_lens;
+    a.query_lens = query_lens;
+    a.num_req = static_cast<int>(num_requests);
+    a.num_rows = num_rows;
+    a.starts = starts;
+    a.row_ends = row_ends;
+    const cudaError_t err = launch_pdl(prepare_step_kernel, dim3(static_cast<unsigned>(1 + kb + qb)), dim3(256), 0,
+                                       static_cast<cudaStream_t>(stream), a);
     return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

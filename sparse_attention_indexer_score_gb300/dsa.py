@@ -33,6 +33,8 @@ _SIGS = {
     "dsa_quantize_query": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P]),
     "dsa_insert_key": (_c.c_int, [_c.c_int, _P, _I64, _P, _P, _c.c_float, _P, _I64, _P, _I64, _I64, _P, _P]),
     "dsa_decode_layout": (_c.c_int, [_P, _I64, _P, _I64, _I64, _P, _P, _P]),
+    "dsa_prepare_step": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _c.c_float, _P,
+                                    _I64, _P, _I64, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P, _P]),
     "dsa_workspace_size": (_c.c_size_t, [_c.c_int, _I64, _I64, _I64, _I64]),
     "dsa_score_paged": (_c.c_int, [_c.c_int, _P, _P, _P, _I64, _I64, _P, _I64, _I64, _P, _P, _I64, _I64, _I64,
                                    _P, _I64, _I64, _P, _P, _c.c_size_t, _P, _P]),
@@ -81,11 +83,7 @@ def _fmt(fmt: str) -> int:
     return FORMATS[fmt]
 
 
-def quantize_query(fmt: str, q: torch.Tensor, wv: torch.Tensor,
-                   q_out: Optional[torch.Tensor] = None,
-                   w_out: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """q: BF16 [rows, 32, 128] (row stride >= 4096); wv: BF16 [rows, 32].
-    Returns (uint8 [rows, 4096] quantised rows, BF16 [rows, 32] head weights)."""
+def _query_args(q, wv, q_out, w_out):
     if q.dtype != torch.bfloat16 or q.dim() != 3 or tuple(q.shape[1:]) != (32, 128) or q.stride(2) != 1 \
             or q.stride(1) != 128:
         raise ValueError("q must be BF16 [rows, 32, 128] with contiguous heads")
@@ -96,16 +94,10 @@ def quantize_query(fmt: str, q: torch.Tensor, wv: torch.Tensor,
         q_out = torch.zeros((rows, Q_ROW_BYTES), dtype=torch.uint8, device=q.device)
     if w_out is None:
         w_out = torch.empty((rows, 32), dtype=torch.bfloat16, device=q.device)
-    rc = lib().dsa_quantize_query(_fmt(fmt), _ptr(q), q.stride(0), _ptr(wv), wv.stride(0), rows,
-                                  _ptr(q_out), _ptr(w_out), _stream(q.device))
-    _check(rc, "dsa_quantize_query")
     return q_out, w_out
 
 
-def insert_key(fmt: str, k: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,
-               slots: torch.Tensor, cache: torch.Tensor, page_stride: int, num_pages: int,
-               status: Optional[torch.Tensor] = None) -> None:
-    """k: BF16 [n, 128]; gamma, beta: FP32 [128]; slots: int64 [n]; cache: uint8 buffer."""
+def _key_args(k, gamma, beta, slots):
     if k.dtype != torch.bfloat16 or k.dim() != 2 or k.shape[1] != 128 or k.stride(1) != 1:
         raise ValueError("k must be BF16 [n, 128] with contiguous rows")
     if slots.dtype != torch.int64 or slots.dim() != 1 or slots.numel() != k.shape[0] or \
@@ -113,16 +105,9 @@ def insert_key(fmt: str, k: torch.Tensor, gamma: torch.Tensor, beta: torch.Tenso
         raise ValueError("slots must be int64 [n], one per key")
     if gamma.dtype != torch.float32 or beta.dtype != torch.float32 or gamma.numel() != 128 or beta.numel() != 128:
         raise ValueError("gamma and beta must be FP32 [128]")
-    rc = lib().dsa_insert_key(_fmt(fmt), _ptr(k), k.stride(0), _ptr(gamma), _ptr(beta), float(eps),
-                              _ptr(slots), k.shape[0], _ptr(cache), int(page_stride), int(num_pages),
-                              _ptr(status), _stream(k.device))
-    _check(rc, "dsa_insert_key")
 
 
-def decode_layout(seq_lens: torch.Tensor, query_lens: torch.Tensor, num_rows: int,
-                  starts: Optional[torch.Tensor] = None,
-                  row_ends: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """int32 seq_lens [>= R], query_lens [R] -> (starts int32 [R + 1], row_ends int32 [num_rows])."""
+def _layout_args(seq_lens, query_lens, num_rows, starts, row_ends):
     if seq_lens.dim() != 1 or query_lens.dim() != 1:
         raise ValueError("Sequence and query lengths must be one-dimensional")
     if seq_lens.dtype != torch.int32 or query_lens.dtype != torch.int32:
@@ -133,10 +118,64 @@ def decode_layout(seq_lens: torch.Tensor, query_lens: torch.Tensor, num_rows: in
         starts = torch.empty(R + 1, dtype=torch.int32, device=dev)
     if row_ends is None:
         row_ends = torch.empty(max(num_rows, 0), dtype=torch.int32, device=dev)
+    return starts, row_ends
+
+
+def quantize_query(fmt: str, q: torch.Tensor, wv: torch.Tensor,
+                   q_out: Optional[torch.Tensor] = None,
+                   w_out: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """q: BF16 [rows, 32, 128] (row stride >= 4096); wv: BF16 [rows, 32].
+    Returns (uint8 [rows, 4096] quantised rows, BF16 [rows, 32] head weights)."""
+    q_out, w_out = _query_args(q, wv, q_out, w_out)
+    rows = q.shape[0]
+    rc = lib().dsa_quantize_query(_fmt(fmt), _ptr(q), q.stride(0), _ptr(wv), wv.stride(0), rows,
+                                  _ptr(q_out), _ptr(w_out), _stream(q.device))
+    _check(rc, "dsa_quantize_query")
+    return q_out, w_out
+
+
+def insert_key(fmt: str, k: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,
+               slots: torch.Tensor, cache: torch.Tensor, page_stride: int, num_pages: int,
+               status: Optional[torch.Tensor] = None) -> None:
+    """k: BF16 [n, 128]; gamma, beta: FP32 [128]; slots: int64 [n]; cache: uint8 buffer."""
+    _key_args(k, gamma, beta, slots)
+    rc = lib().dsa_insert_key(_fmt(fmt), _ptr(k), k.stride(0), _ptr(gamma), _ptr(beta), float(eps),
+                              _ptr(slots), k.shape[0], _ptr(cache), int(page_stride), int(num_pages),
+                              _ptr(status), _stream(k.device))
+    _check(rc, "dsa_insert_key")
+
+
+def decode_layout(seq_lens: torch.Tensor, query_lens: torch.Tensor, num_rows: int,
+                  starts: Optional[torch.Tensor] = None,
+                  row_ends: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """int32 seq_lens [>= R], query_lens [R] -> (starts int32 [R + 1], row_ends int32 [num_rows])."""
+    starts, row_ends = _layout_args(seq_lens, query_lens, num_rows, starts, row_ends)
+    R = query_lens.numel()
+    dev = query_lens.device
     rc = lib().dsa_decode_layout(_ptr(seq_lens), seq_lens.numel(), _ptr(query_lens), R, int(num_rows),
                                  _ptr(starts), _ptr(row_ends), _stream(dev))
     _check(rc, "dsa_decode_layout")
     return starts, row_ends
+
+
+def prepare_step(fmt: str, q: torch.Tensor, wv: torch.Tensor, k: torch.Tensor, gamma: torch.Tensor,
+                 beta: torch.Tensor, eps: float, slots: torch.Tensor, cache: torch.Tensor, page_stride: int,
+                 num_pages: int, seq_lens: torch.Tensor, query_lens: torch.Tensor, num_rows: int,
+                 q_out: Optional[torch.Tensor] = None, w_out: Optional[torch.Tensor] = None,
+                 starts: Optional[torch.Tensor] = None, row_ends: Optional[torch.Tensor] = None,
+                 status: Optional[torch.Tensor] = None):
+    """quantize_query + insert_key + decode_layout in one launch (same arguments
+    and results).  Returns (q_rows, w, starts, row_ends)."""
+    q_out, w_out = _query_args(q, wv, q_out, w_out)
+    _key_args(k, gamma, beta, slots)
+    starts, row_ends = _layout_args(seq_lens, query_lens, num_rows, starts, row_ends)
+    rc = lib().dsa_prepare_step(_fmt(fmt), _ptr(q), q.stride(0), _ptr(wv), wv.stride(0), q.shape[0],
+                                _ptr(q_out), _ptr(w_out), _ptr(k), k.stride(0), _ptr(gamma), _ptr(beta), float(eps),
+                                _ptr(slots), k.shape[0], _ptr(cache), int(page_stride), int(num_pages),
+                                _ptr(seq_lens), seq_lens.numel(), _ptr(query_lens), query_lens.numel(),
+                                int(num_rows), _ptr(starts), _ptr(row_ends), _ptr(status), _stream(q.device))
+    _check(rc, "dsa_prepare_step")
+    return q_out, w_out, starts, row_ends
 
 
 def workspace_size(fmt: str, rows: int, num_requests: int, max_pages: int, k: int) -> int:

@@ -2,8 +2,8 @@
 
 ``DecodeIndexer`` owns the device state a serving loop keeps between steps
 (the paged key cache, the block table, a zero-filled workspace) and runs the
-step's five calls on the current stream:
-quantize_query -> insert_key -> decode_layout -> score_paged (+ fused top-k).
+step on the current stream: prepare_step (quantize_query + insert_key +
+decode_layout in one launch) -> score_paged (+ fused top-k).
 """
 
 from __future__ import annotations
@@ -54,9 +54,9 @@ class DecodeIndexer:
              want_logits: bool = False, topk_out: Optional[torch.Tensor] = None,
              q_out: Optional[torch.Tensor] = None, w_out: Optional[torch.Tensor] = None) -> StepOutput:
         rows = q.shape[0]
-        q_rows, w = dsa.quantize_query(self.fmt, q, wv, q_out, w_out)
-        self.insert(keys, slots)
-        starts, row_ends = dsa.decode_layout(seq_lens, query_lens, rows)
+        q_rows, w, starts, row_ends = dsa.prepare_step(
+            self.fmt, q, wv, keys, self.gamma, self.beta, self.eps, slots, self.cache, self.page_stride,
+            self.num_pages, seq_lens, query_lens, rows, q_out=q_out, w_out=w_out, status=self.status)
         logits, top = dsa.score_paged(self.fmt, q_rows, w, self.cache, self.page_stride, self.num_pages,
                                       self.block_table, starts, row_ends, max_query_len, k=self.k,
                                       want_logits=want_logits, workspace=self.workspace, status=self.status,

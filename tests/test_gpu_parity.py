@@ -89,6 +89,61 @@ def test_decode_layout_parity(cuda_lib):
         assert np.array_equal(st.cpu().numpy(), ws) and np.array_equal(en.cpu().numpy(), we)
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+def test_prepare_step_bit_exact(cuda_lib, fmt):
+    """The fused launch equals the oracle's quantize_query, insert_key and
+    decode_layout, and the three separate calls, byte for byte."""
+    import torch
+    rng = np.random.default_rng(6)
+    rows, n, num_pages = 41, 57, 5
+    qb = _special_queries(rng, rows)
+    wvb = ((rng.standard_normal((rows, 32)).astype(np.float32).view(np.uint32) >> 16)).astype(np.uint16)
+    x = (rng.standard_normal((n, 128)) * 3.0).astype(np.float32)
+    x[0] = -1.5                                   # zero variance
+    kb = ((x.view(np.uint32).astype(np.uint64) + 0x7FFF + ((x.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+    gamma = (1 + 0.1 * rng.standard_normal(128)).astype(np.float32)
+    beta = (0.1 * rng.standard_normal(128)).astype(np.float32)
+    slots = rng.permutation(num_pages * 64)[:n].astype(np.int64)
+    slots[3] = -1                                 # padding
+    slots[4] = num_pages * 64                     # past the pool
+    R = 17
+    qlen = rng.integers(0, 4, R).astype(np.int32)
+    seq = rng.integers(0, 9000, R + 2).astype(np.int32)
+    num_rows = int(qlen.sum()) + 3                # three padding rows
+    stride = O.page_bytes(fmt) + 32
+    dev = "cuda"
+
+    def run(fused):
+        cache = torch.zeros(num_pages * stride, dtype=torch.uint8, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        args = (bf16_tensor(qb, dev), bf16_tensor(wvb, dev))
+        kargs = (bf16_tensor(kb, dev), torch.from_numpy(gamma).to(dev), torch.from_numpy(beta).to(dev), 1e-6,
+                 torch.from_numpy(slots).to(dev))
+        lens = (torch.from_numpy(seq).to(dev), torch.from_numpy(qlen).to(dev))
+        if fused:
+            q_rows, w, st, en = cuda_lib.prepare_step(fmt, *args, kargs[0], kargs[1], kargs[2], kargs[3], kargs[4],
+                                                      cache, stride, num_pages, *lens, num_rows, status=status)
+        else:
+            q_rows, w = cuda_lib.quantize_query(fmt, *args)
+            cuda_lib.insert_key(fmt, *kargs, cache, stride, num_pages, status)
+            st, en = cuda_lib.decode_layout(*lens, num_rows)
+        torch.cuda.synchronize()
+        return [t.cpu().numpy() for t in (q_rows, w.float(), cache, st, en, status)]
+
+    fused, separate = run(True), run(False)
+    for a, b in zip(fused, separate):
+        assert np.array_equal(a, b)
+    want_rows, want_w = O.quantize_query(fmt, bf16_bits_to_f32(qb), bf16_bits_to_f32(wvb))
+    used = 4096 if fmt != "mxfp4" else 2176
+    assert np.array_equal(fused[0][:, :used], want_rows[:, :used]) and not fused[0][:, used:].any()
+    assert np.array_equal(fused[1], want_w)
+    want_cache = np.zeros(num_pages * stride, np.uint8)
+    bad = O.insert_key(fmt, want_cache, stride, num_pages, bf16_bits_to_f32(kb), gamma, beta, 1e-6, slots)
+    assert bad == 1 and np.array_equal(fused[2], want_cache) and int(fused[5][0]) & 1
+    ws, we = O.decode_layout(seq, qlen, num_rows)
+    assert np.array_equal(fused[3], ws) and np.array_equal(fused[4], we)
+
+
 SMALL = [
     dict(R=2, seq=(256, 256), qlen=(1, 1)),
     dict(R=5, seq=(100, 700), qlen=(1, 1)),
