@@ -114,11 +114,15 @@ __device__ __forceinline__ int find_segment(const int* prefix, int S, int t) {
 // ----------------------------------------------------------------- plan
 // One CTA: validates request starts and row bounds, splits requests into
 // segments of up to 4 rows and lays their 128-key tiles out in one index space.
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ starts,
-                                                    const int32_t* __restrict__ row_ends, int R, int rows,
-                                                    int max_keys, int* __restrict__ info, int4* __restrict__ segs,
-                                                    int* __restrict__ seg_prefix, int* __restrict__ eff_end,
-                                                    int4* __restrict__ cta, int G, int32_t* status) {
+constexpr int kPlanThreads = 256;
+constexpr int kPlanSmemRows = 4096;   // row bounds the plan keeps on chip
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ starts,
+                                                            const int32_t* __restrict__ row_ends, int R, int rows,
+                                                            int max_keys, int* __restrict__ info,
+                                                            int4* __restrict__ segs, int* __restrict__ seg_prefix,
+                                                            int* __restrict__ eff_end, int4* __restrict__ cta, int G,
+                                                            int32_t* status) {
     // The scoring CTAs (persistent, one per SM, most of its registers) are let
     // in only once the work before this kernel has finished, so that they do
     // not crowd out a still-running predecessor; their prologue then overlaps
@@ -127,8 +131,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     pdl_launch_dependents();
     __shared__ int warp_tmp[32];
     __shared__ int chunk_total;
-    __shared__ int sp[kPlanSmemSegs + 1];   // tile prefix, when the segments fit
-    for (int r = threadIdx.x; r < rows; r += blockDim.x) eff_end[r] = 0;
+    __shared__ int sp[kPlanSmemSegs + 1];   // tiles per segment, then the tile prefix (when the segments fit)
+    __shared__ int se[kPlanSmemRows];       // row bounds (when the rows fit)
+    const bool rows_fit = rows <= kPlanSmemRows;
+    // The first chunk's request starts and all row bounds are loaded together.
+    int a0 = 0, b0 = 0;
+    if (threadIdx.x < R) {
+        a0 = starts[threadIdx.x];
+        b0 = starts[threadIdx.x + 1];
+    }
+    if (rows_fit)
+        for (int r = threadIdx.x; r < rows; r += blockDim.x) se[r] = row_ends[r];
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) eff_end[r] = 0;   // rows outside every request keep 0
     __syncthreads();
     int carry = 0;
     bool bad = false;
@@ -136,7 +150,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         const int q = base + threadIdx.x;
         int s0 = 0, s1 = 0;
         if (q < R) {
-            const int a = starts[q], b = starts[q + 1];
+            const int a = base == 0 ? a0 : starts[q], b = base == 0 ? b0 : starts[q + 1];
             if (a < 0 || b < a || b > rows) bad = true;
             s0 = min(max(a, 0), rows);
             s1 = min(max(b, s0), rows);
@@ -150,28 +164,29 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
             const int nr = min(kSegRows, s1 - row0);
             int maxend = 0;
             for (int r = row0; r < row0 + nr; ++r) {
-                int e = row_ends[r];
+                int e = rows_fit ? se[r] : row_ends[r];
                 if (e > max_keys) { bad = true; e = max_keys; }
                 e = max(e, 0);
                 eff_end[r] = e;
                 maxend = max(maxend, e);
             }
             segs[sbase + i] = make_int4(q, row0, nr, maxend);
+            if (sbase + i < kPlanSmemSegs) sp[sbase + i] = (maxend + kTileRows - 1) / kTileRows;
         }
         carry += chunk_total;
         __syncthreads();
     }
     if (bad && status) atomicOr(status, DSA_STATUS_BAD_GEOMETRY);
     const int S = min(carry, rows + 1);
-    __syncthreads();
     carry = 0;
     for (int base = 0; base < S; base += blockDim.x) {
         const int i = base + threadIdx.x;
-        const int tiles = (i < S) ? (segs[i].w + kTileRows - 1) / kTileRows : 0;
+        int tiles = 0;
+        if (i < S) tiles = i < kPlanSmemSegs ? sp[i] : (segs[i].w + kTileRows - 1) / kTileRows;
         const int inc = block_inclusive_scan(tiles, warp_tmp, &chunk_total);
         if (i < S) {
             seg_prefix[i] = carry + inc - tiles;
-            if (i < kPlanSmemSegs) sp[i] = carry + inc - tiles;
+            if (i < kPlanSmemSegs) sp[i] = carry + inc - tiles;   // this thread's own entry
         }
         carry += chunk_total;
         __syncthreads();
@@ -808,7 +823,7 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     int* eff_end = reinterpret_cast<int*>(ws + L.eff_end);
     int4* cta = reinterpret_cast<int4*>(ws + L.cta);
     const int grid = device_sm_count() < kMaxScoreCtas ? device_sm_count() : kMaxScoreCtas;
-    if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, starts, row_ends, static_cast<int>(num_requests),
+    if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, starts, row_ends, static_cast<int>(num_requests),
                    static_cast<int>(rows), static_cast<int>(width), info, segs, seg_prefix, eff_end, cta, grid,
                    status) != cudaSuccess)
         return DSA_ERR_CUDA;
