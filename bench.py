@@ -416,6 +416,49 @@ def run_ours(args, wl, rank, world, local_rank):
     print(json.dumps(line))
 
 
+def run_query_norm(args):
+    """QueryNorm (q_a RMSNorm) of a batch of 1536-column BF16 rows, both forms:
+    HBM-bound (2 B read + 2 B written per element), timed with CUDA events on
+    the stream over K launches after W warm-up launches."""
+    import torch
+    from sparse_attention_indexer_score_gb300 import build as _b
+    _b.build()
+    from sparse_attention_indexer_score_gb300 import dsa
+    dev = torch.device("cuda", 0)
+    batch = args.norm_rows
+    g = torch.Generator(device="cpu").manual_seed(7)
+    x = torch.randn((batch, 1536), generator=g).to(torch.bfloat16).to(dev)
+    w = (1 + 0.1 * torch.randn(1536, generator=g)).to(torch.bfloat16).to(dev)
+    out = torch.empty_like(x)
+    peaks = measured_peaks()
+    bytes_per = batch * 1536 * 2 * 2 + 1536 * 2
+    lines = {}
+    for variant in ("row", "tiled"):
+        for _ in range(args.warmup):
+            dsa.query_norm(x, w, 1e-6, variant, out)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(args.steps):
+            dsa.query_norm(x, w, 1e-6, variant, out)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        gbs = bytes_per / (ms / 1e3) / 1e9
+        lines[variant] = {"us": ms * 1e3, "rows_per_s": batch / (ms / 1e3), "achieved_gbs": gbs,
+                          "frac": gbs / peaks["hbm_gbs"]}
+    best = max(lines, key=lambda v: lines[v]["rows_per_s"])
+    print(json.dumps({
+        "metric": "query_norm rows/s (q_a RMSNorm, 1536 BF16 columns)", "value": lines[best]["rows_per_s"],
+        "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic", "config": {"workload": f"query_norm {batch} rows x 1536",
+                                                         "variants": lines},
+        "roofline": {"bound": "hbm", "achieved": lines[best]["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": lines[best]["frac"], "traffic": None,
+                     "bytes_per_launch": bytes_per, "variant": best},
+        "gpu_launches": args.steps}))
+
+
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -425,9 +468,15 @@ def main():
     p.add_argument("--config", default="fp8_decode")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--op", choices=["step", "query_norm"], default="step",
+                   help="step: the decode step (the headline); query_norm: the q_a RMSNorm alone")
+    p.add_argument("--norm-rows", type=int, default=16384)
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.op == "query_norm":
+        run_query_norm(args)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))

@@ -178,6 +178,30 @@ int dsa_prepare_step(int fmt, const void* q, int64_t q_row_stride,
                      int32_t* status, void* stream);
 
 /*
+ * dsa_query_norm - the q_a RMSNorm of the packed projection -> q_c (QueryNorm).
+ *
+ * Page "cutedsl.dsa.overlap", class QueryNorm: row r of q_c is
+ * BF16((x[r] * rr) * w) with rr = 1 / sqrt(sum_c x[r][c]^2 / 1536 + eps), in
+ * FP32, in one of the page's two summation orders:
+ *   variant 0  per-row form: one row per CTA, 8 columns per thread, sequential
+ *              FMAs, warp butterfly sums added in warp order;
+ *   variant 1  tiled form: one row per warp, 48 columns per lane in four FMA
+ *              chains by value index mod 4;
+ *   variant -1 the tiled form from 64 rows on, else the per-row form (the
+ *              pages do not print their threshold).
+ *   x        BF16 [batch][x_row_stride >= 1536, multiple of 8]: columns 0..1535
+ *            of each row are q_a; 16-byte aligned.
+ *   w        BF16 [1536] weights, 16-byte aligned.
+ *   eps      added to the mean square.
+ *   out      BF16 [batch][out_row_stride >= 1536, multiple of 8], 16-byte aligned.
+ * batch == 0 launches nothing.  Errors: DSA_ERR_INVALID for a negative batch,
+ * a bad variant, null pointers, strides or alignment as above.
+ */
+int dsa_query_norm(const void* x, int64_t x_row_stride, const void* w, float eps,
+                   int64_t batch, void* out, int64_t out_row_stride, int variant,
+                   void* stream);
+
+/*
  * dsa_workspace_size - bytes of scratch dsa_score_paged needs for these sizes
  * (rows query rows, num_requests requests, max_pages block-table columns, top-k k).
  * The workspace must be zero-filled before its first use; every call that

@@ -35,6 +35,7 @@ _SIGS = {
     "dsa_decode_layout": (_c.c_int, [_P, _I64, _P, _I64, _I64, _P, _P, _P]),
     "dsa_prepare_step": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _c.c_float, _P,
                                     _I64, _P, _I64, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P, _P]),
+    "dsa_query_norm": (_c.c_int, [_P, _I64, _P, _c.c_float, _I64, _P, _I64, _c.c_int, _P]),
     "dsa_workspace_size": (_c.c_size_t, [_c.c_int, _I64, _I64, _I64, _I64]),
     "dsa_score_paged": (_c.c_int, [_c.c_int, _P, _P, _P, _I64, _I64, _P, _I64, _I64, _P, _P, _I64, _I64, _I64,
                                    _P, _I64, _I64, _P, _P, _c.c_size_t, _P, _P]),
@@ -156,6 +157,27 @@ def decode_layout(seq_lens: torch.Tensor, query_lens: torch.Tensor, num_rows: in
                                  _ptr(starts), _ptr(row_ends), _stream(dev))
     _check(rc, "dsa_decode_layout")
     return starts, row_ends
+
+
+NORM_VARIANTS = {"auto": -1, "row": 0, "tiled": 1}
+
+
+def query_norm(x: torch.Tensor, w: torch.Tensor, eps: float, variant: str = "auto",
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """QueryNorm: x BF16 [batch, >= 1536] (columns 0..1535 are q_a), w BF16 [1536]
+    -> q_c BF16 [batch, 1536] (or ``out``).  variant: "row", "tiled" or "auto"."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] < 1536 or x.stride(1) != 1:
+        raise ValueError("x must be BF16 [batch, >= 1536] with contiguous columns")
+    if w.dtype != torch.bfloat16 or w.numel() != 1536:
+        raise ValueError("w must be BF16 [1536]")
+    if variant not in NORM_VARIANTS:
+        raise ValueError(f"variant must be one of {sorted(NORM_VARIANTS)}")
+    if out is None:
+        out = torch.empty((x.shape[0], 1536), dtype=torch.bfloat16, device=x.device)
+    rc = lib().dsa_query_norm(_ptr(x), x.stride(0), _ptr(w), float(eps), x.shape[0], _ptr(out), out.stride(0),
+                              NORM_VARIANTS[variant], _stream(x.device))
+    _check(rc, "dsa_query_norm")
+    return out
 
 
 def prepare_step(fmt: str, q: torch.Tensor, wv: torch.Tensor, k: torch.Tensor, gamma: torch.Tensor,
