@@ -459,6 +459,43 @@ def run_query_norm(args):
         "gpu_launches": args.steps}))
 
 
+def run_topk_merge(args):
+    """The DCP top-k merge of 64 rows, 8 ranks x 2048 candidates each -> 2048:
+    reads 8 B per candidate (score, local position), timed with CUDA events
+    over K calls after W warm-up calls."""
+    import torch
+    from sparse_attention_indexer_score_gb300 import build as _b
+    _b.build()
+    from sparse_attention_indexer_score_gb300 import dsa
+    dev = torch.device("cuda", 0)
+    rows, world, k, k_out, inter = 64, 8, 2048, 2048, 64
+    g = torch.Generator(device="cpu").manual_seed(9)
+    scores = torch.randn((rows, world * k), generator=g).to(dev)
+    idx = torch.randint(0, 1 << 16, (rows, world * k), generator=g, dtype=torch.int32).to(dev)
+    ws = dsa.new_workspace(dsa.topk_workspace_size(rows, k_out), dev)
+    for _ in range(args.warmup):
+        dsa.topk_merge(scores, idx, world, k, inter, k_out, rank=0, workspace=ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(args.steps):
+        dsa.topk_merge(scores, idx, world, k, inter, k_out, rank=0, workspace=ws)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    cands = rows * world * k
+    nbytes = cands * 8 + rows * k_out * 8
+    peaks = measured_peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "DCP top-k merge candidates/s", "value": cands / (ms / 1e3), "unit": "candidates/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": f"topk_merge {rows} rows, {world} ranks x {k} -> {k_out}"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": nbytes},
+        "gpu_launches": 3 * args.steps}))
+
+
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -468,14 +505,18 @@ def main():
     p.add_argument("--config", default="fp8_decode")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--op", choices=["step", "query_norm"], default="step",
-                   help="step: the decode step (the headline); query_norm: the q_a RMSNorm alone")
+    p.add_argument("--op", choices=["step", "query_norm", "topk_merge"], default="step",
+                   help="step: the decode step (the headline); query_norm: the q_a RMSNorm alone; "
+                        "topk_merge: the DCP top-k merge alone")
     p.add_argument("--norm-rows", type=int, default=16384)
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.op == "query_norm":
         run_query_norm(args)
+        return
+    if args.op == "topk_merge":
+        run_topk_merge(args)
         return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

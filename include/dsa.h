@@ -149,6 +149,26 @@ int dsa_decode_layout(const int32_t* seq_lens, int64_t num_seq,
                       void* stream);
 
 /*
+ * dsa_decode_layout_dcp - dsa_decode_layout with decode context parallelism.
+ *
+ * Page "amd.ops.fp4_indexer", decode_layout(..., dcp_rank, dcp_world_size,
+ * interleave): a request's key positions are dealt to dcp_world_size ranks
+ * in runs of `interleave` consecutive positions (run n to rank n mod world);
+ * each rank scores only its own keys, numbered consecutively.  starts are as
+ * without DCP; row_ends are rank-local: for a global bound E,
+ *   full = E / (world * interleave) * interleave,
+ *   row_ends = full + clamp(E - full * world - dcp_rank * interleave, 0, interleave).
+ * dcp_world_size == 1 gives dsa_decode_layout's result.
+ * Errors (DSA_ERR_INVALID): dcp_rank outside [0, dcp_world_size),
+ * dcp_world_size < 1, interleave < 1, and dsa_decode_layout's cases.
+ */
+int dsa_decode_layout_dcp(const int32_t* seq_lens, int64_t num_seq,
+                          const int32_t* query_lens, int64_t num_requests,
+                          int64_t num_rows, int64_t dcp_rank,
+                          int64_t dcp_world_size, int64_t interleave,
+                          int32_t* starts, int32_t* row_ends, void* stream);
+
+/*
  * dsa_prepare_step - dsa_quantize_query, dsa_insert_key and dsa_decode_layout
  * of one decode step in a single launch.
  *
@@ -279,6 +299,34 @@ size_t dsa_topk_workspace_size(int64_t rows, int64_t k);
 int dsa_topk(const float* logits, int64_t ld, const int32_t* row_ends,
              int64_t rows, int64_t width, int64_t k, int32_t* out,
              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_topk_merge - the DCP top-k merge and the local slots.
+ *
+ * Page "cutedsl.dsa.overlap" names this step of the indexer path under DCP
+ * (it prints no code).  Every rank has selected its local top-k of a row;
+ * the caller gathers all ranks' candidates (for instance with an all-gather)
+ * and this call keeps the k_out best of them:
+ *   scores     FP32 [rows][scores_ld >= world * k]: rank w's candidates at
+ *              columns w*k .. w*k + k - 1; empty candidates -inf.
+ *   idx        int32 [rows][idx_ld >= world * k]: their rank-local key
+ *              positions (as dsa_decode_layout_dcp numbers them), -1 empty.
+ *   interleave the DCP run length.
+ *   out        int32 [rows][k_out] out: global key positions of the k_out best
+ *              candidates, in no particular order; -1 where a row has fewer
+ *              valid candidates (those -1 entries may sit anywhere in the row).
+ *   rank, out_local  optional (out_local may be NULL): rank-local positions of
+ *              the selected keys that `rank` owns, -1 elsewhere.
+ *   workspace  at least dsa_topk_workspace_size(rows, k_out) bytes, 256-byte
+ *              aligned, zero-filled before first use (left zero-filled).
+ * Errors (DSA_ERR_INVALID): negative sizes, world < 1, interleave < 1, short
+ * leading dimensions, null pointers, rank outside [0, world) with out_local.
+ */
+int dsa_topk_merge(const float* scores, int64_t scores_ld, const int32_t* idx,
+                   int64_t idx_ld, int64_t rows, int64_t world, int64_t k,
+                   int64_t interleave, int64_t k_out, int32_t* out,
+                   int64_t rank, int32_t* out_local, void* workspace,
+                   size_t workspace_bytes, void* stream);
 
 /*
  * dsa_topk_noalloc - dsa_topk for callers that cannot allocate device memory.

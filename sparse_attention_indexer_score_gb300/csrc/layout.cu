@@ -11,10 +11,11 @@ namespace dsa {
 __global__ void __launch_bounds__(1024) decode_layout_kernel(const int32_t* __restrict__ seq_lens,
                                                              const int32_t* __restrict__ query_lens, int num_req,
                                                              int64_t num_rows, int32_t* __restrict__ starts,
-                                                             int32_t* __restrict__ row_ends) {
+                                                             int32_t* __restrict__ row_ends, int64_t dcp_rank,
+                                                             int64_t dcp_world, int64_t interleave) {
     pdl_launch_dependents();
     pdl_wait();
-    decode_layout_block(seq_lens, query_lens, num_req, num_rows, starts, row_ends);
+    decode_layout_block(seq_lens, query_lens, num_req, num_rows, starts, row_ends, dcp_rank, dcp_world, interleave);
 }
 
 }  // namespace dsa
@@ -30,6 +31,22 @@ extern "C" int dsa_decode_layout(const int32_t* seq_lens, int64_t num_seq, const
         return DSA_ERR_INVALID;   // (the same checks as dsa_prepare_step's layout part)
     const cudaError_t err = launch_pdl(decode_layout_kernel, dim3(1), dim3(1024), 0, static_cast<cudaStream_t>(stream),
                                        seq_lens, query_lens, static_cast<int>(num_requests), num_rows, starts,
-                                       row_ends);
+                                       row_ends, int64_t(0), int64_t(1), int64_t(1));
+    return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+extern "C" int dsa_decode_layout_dcp(const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens,
+                                     int64_t num_requests, int64_t num_rows, int64_t dcp_rank,
+                                     int64_t dcp_world_size, int64_t interleave, int32_t* starts,
+                                     int32_t* row_ends, void* stream) {
+    if (dcp_world_size < 1 || dcp_rank < 0 || dcp_rank >= dcp_world_size || interleave < 1) return DSA_ERR_INVALID;
+    if (dcp_world_size > (int64_t(1) << 20) || interleave > (int64_t(1) << 30)) return DSA_ERR_UNSUPPORTED;
+    if (num_rows < 0 || num_requests < 0 || num_seq < num_requests) return DSA_ERR_INVALID;
+    if (num_requests > 0x7FFFFFFF - 1 || num_rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    if (!starts || (num_rows > 0 && !row_ends) || (num_requests > 0 && (!seq_lens || !query_lens)))
+        return DSA_ERR_INVALID;
+    const cudaError_t err = launch_pdl(decode_layout_kernel, dim3(1), dim3(1024), 0, static_cast<cudaStream_t>(stream),
+                                       seq_lens, query_lens, static_cast<int>(num_requests), num_rows, starts,
+                                       row_ends, dcp_rank, dcp_world_size, interleave);
     return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

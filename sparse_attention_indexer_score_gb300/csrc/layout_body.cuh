@@ -5,7 +5,11 @@
 // Page "amd.ops.fp4_indexer", decode_layout: starts = [0, cumsum(query_lens)];
 // row r belongs to the request searchsorted(starts[1:], r, right=True) capped at
 // R - 1, and scores keys t < max(0, seq_len - query_len + (r - start) + 1);
-// rows at or past starts[R] are padding with bound 0.
+// rows at or past starts[R] are padding with bound 0.  Under DCP (world > 1)
+// key runs of `interleave` positions go to the ranks round-robin and the bound
+// becomes the number of the rank's own keys below it: with
+// full = E / (world * interleave) * interleave,
+// E_local = full + clamp(E - full * world - rank * interleave, 0, interleave).
 #pragma once
 
 #include "scan.cuh"
@@ -15,7 +19,8 @@ namespace dsa {
 __device__ __forceinline__ void decode_layout_block(const int32_t* __restrict__ seq_lens,
                                                     const int32_t* __restrict__ query_lens, int num_req,
                                                     int64_t num_rows, int32_t* __restrict__ starts,
-                                                    int32_t* __restrict__ row_ends) {
+                                                    int32_t* __restrict__ row_ends, int64_t dcp_rank = 0,
+                                                    int64_t dcp_world = 1, int64_t interleave = 1) {
     __shared__ int warp_tmp[32];
     __shared__ int chunk_total;
     int carry = 0;
@@ -40,8 +45,14 @@ __device__ __forceinline__ void decode_layout_block(const int32_t* __restrict__ 
                 if (static_cast<int64_t>(starts[mid + 1]) > r) hi = mid; else lo = mid + 1;
             }
             const int q = min(lo, num_req - 1);
-            const int64_t e = static_cast<int64_t>(seq_lens[q]) - query_lens[q] + (r - starts[q]) + 1;
-            end = static_cast<int>(e > 0 ? e : 0);
+            int64_t e = static_cast<int64_t>(seq_lens[q]) - query_lens[q] + (r - starts[q]) + 1;
+            e = e > 0 ? e : 0;
+            if (dcp_world > 1) {
+                const int64_t full = e / (dcp_world * interleave) * interleave;
+                const int64_t part = e - full * dcp_world - dcp_rank * interleave;
+                e = full + (part < 0 ? 0 : (part > interleave ? interleave : part));
+            }
+            end = static_cast<int>(e);
         }
         row_ends[r] = end;
     }

@@ -43,7 +43,7 @@ struct SelectArgs {
     float* fill;         // when non-null: write -inf at [end, width) of each row
     int64_t ld;
     int64_t width;
-    const int32_t* ends;
+    const int32_t* ends;  // row bounds; null: every row holds `width` scores
     int k;               // 0: fill only
     int32_t* out;
     unsigned* hist;      // level-1 histograms, [rows][2048]
@@ -54,6 +54,7 @@ struct SelectArgs {
 };
 
 __device__ __forceinline__ int clamp_end(const int32_t* ends, int row, int64_t width) {
+    if (!ends) return static_cast<int>(width);   // every row holds width scores
     const int64_t e = ends[row];
     return static_cast<int>(e < 0 ? 0 : (e > width ? width : e));
 }
@@ -652,4 +653,75 @@ extern "C" int dsa_topk_noalloc(const float* logits, int64_t ld, const int32_t* 
             return DSA_ERR_CUDA;
     }
     return launch_select(logits, nullptr, ld, width, row_ends, rows, k, out, ws, L, stream, true);
+}
+
+// ----------------------------------------------------------------- DCP top-k merge
+// Page "cutedsl.dsa.overlap": under DCP the indexer path ends with the top-k
+// merge and the local slots.  Each row holds every rank's local top-k
+// candidates (rank w's at columns w*k .. w*k + k - 1: scores, rank-local
+// positions); the select above picks the k_out best columns, and this kernel
+// turns a column into the candidate's global key position (and, for one
+// rank, its rank-local slot when that rank owns it).
+namespace dsa {
+
+__global__ void __launch_bounds__(256) merge_positions_kernel(int32_t* __restrict__ out, int64_t rows, int64_t k_out,
+                                                              const int32_t* __restrict__ idx, int64_t idx_ld,
+                                                              int64_t k, int64_t world, int64_t inter, int64_t rank,
+                                                              int32_t* __restrict__ out_local) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= rows * k_out) return;
+    const int64_t r = i / k_out;
+    const int c = out[i];
+    int64_t g = -1;
+    if (c >= 0) {
+        const int64_t l = idx[r * idx_ld + c];
+        if (l >= 0) g = (l / inter) * (world * inter) + (c / k) * inter + l % inter;
+    }
+    out[i] = static_cast<int32_t>(g);
+    if (out_local) {
+        const bool mine = g >= 0 && (g / inter) % world == rank;
+        out_local[i] = mine ? static_cast<int32_t>((g / (world * inter)) * inter + g % inter) : -1;
+    }
+}
+
+}  // namespace dsa
+
+extern "C" int dsa_topk_merge(const float* scores, int64_t scores_ld, const int32_t* idx, int64_t idx_ld,
+                              int64_t rows, int64_t world, int64_t k, int64_t interleave, int64_t k_out,
+                              int32_t* out, int64_t rank, int32_t* out_local, void* workspace,
+                              size_t workspace_bytes, void* stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (rows < 0 || world < 1 || k < 0 || interleave < 1 || k_out < 0) return DSA_ERR_INVALID;
+    if (rows == 0 || k_out == 0) return DSA_OK;
+    const int64_t width = world * k;
+    if (scores_ld < width || idx_ld < width) return DSA_ERR_INVALID;
+    if (!out || !workspace || (width > 0 && (!scores || !idx))) return DSA_ERR_INVALID;
+    if (out_local && (rank < 0 || rank >= world)) return DSA_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return DSA_ERR_INVALID;
+    if (k_out > (int64_t(1) << 30) || width > (int64_t(1) << 30) || interleave > (int64_t(1) << 30) ||
+        world > (int64_t(1) << 20))
+        return DSA_ERR_UNSUPPORTED;
+    const WsLayout L = workspace_layout(rows, 0, false, false);
+    if (workspace_bytes < L.total) return DSA_ERR_INVALID;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int64_t chunks = (width + kChunk - 1) / kChunk;
+    if (chunks > 65535 || rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    if (chunks > 0) {
+        if (launch_pdl(hist_kernel, dim3(static_cast<unsigned>(rows), static_cast<unsigned>(chunks)),
+                       dim3(kSelThreads), 0, stream, scores, scores_ld, width, static_cast<const int32_t*>(nullptr),
+                       static_cast<int>(k_out), reinterpret_cast<unsigned*>(ws + L.hist)) != cudaSuccess)
+            return DSA_ERR_CUDA;
+    }
+    int rc = launch_select(scores, nullptr, scores_ld, width, nullptr, rows, k_out, out, ws, L, stream, true);
+    if (rc != DSA_OK) return rc;
+    const int64_t n = rows * k_out;
+    const int64_t blocks = (n + 255) / 256;
+    if (blocks > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    return launch_pdl(merge_positions_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, out, rows,
+                      k_out, idx, idx_ld, k, world, interleave, out_local ? rank : int64_t(0), out_local) ==
+                   cudaSuccess
+               ? DSA_OK
+               : DSA_ERR_CUDA;
 }

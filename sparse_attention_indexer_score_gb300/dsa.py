@@ -35,6 +35,9 @@ _SIGS = {
     "dsa_decode_layout": (_c.c_int, [_P, _I64, _P, _I64, _I64, _P, _P, _P]),
     "dsa_prepare_step": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _c.c_float, _P,
                                     _I64, _P, _I64, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P, _P]),
+    "dsa_decode_layout_dcp": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P]),
+    "dsa_topk_merge": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _I64, _P, _P,
+                                  _c.c_size_t, _P]),
     "dsa_query_norm": (_c.c_int, [_P, _I64, _P, _c.c_float, _I64, _P, _I64, _c.c_int, _P]),
     "dsa_workspace_size": (_c.c_size_t, [_c.c_int, _I64, _I64, _I64, _I64]),
     "dsa_score_paged": (_c.c_int, [_c.c_int, _P, _P, _P, _I64, _I64, _P, _I64, _I64, _P, _P, _I64, _I64, _I64,
@@ -157,6 +160,39 @@ def decode_layout(seq_lens: torch.Tensor, query_lens: torch.Tensor, num_rows: in
                                  _ptr(starts), _ptr(row_ends), _stream(dev))
     _check(rc, "dsa_decode_layout")
     return starts, row_ends
+
+
+def decode_layout_dcp(seq_lens: torch.Tensor, query_lens: torch.Tensor, num_rows: int, dcp_rank: int,
+                      dcp_world_size: int, interleave: int = 1) -> Tuple[torch.Tensor, torch.Tensor]:
+    """decode_layout with rank-local row bounds under DCP."""
+    starts, row_ends = _layout_args(seq_lens, query_lens, num_rows, None, None)
+    rc = lib().dsa_decode_layout_dcp(_ptr(seq_lens), seq_lens.numel(), _ptr(query_lens), query_lens.numel(),
+                                     int(num_rows), int(dcp_rank), int(dcp_world_size), int(interleave),
+                                     _ptr(starts), _ptr(row_ends), _stream(query_lens.device))
+    _check(rc, "dsa_decode_layout_dcp")
+    return starts, row_ends
+
+
+def topk_merge(scores: torch.Tensor, idx: torch.Tensor, world: int, k: int, interleave: int, k_out: int,
+               rank: Optional[int] = None, workspace: Optional[torch.Tensor] = None):
+    """scores FP32 [rows, >= world*k] and idx int32 [rows, >= world*k] (rank w's
+    candidates at columns w*k ..) -> (int32 [rows, k_out] global positions,
+    int32 [rows, k_out] local slots of ``rank`` or None)."""
+    if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be FP32 [rows, world * k]")
+    if idx.dtype != torch.int32 or idx.dim() != 2 or idx.stride(1) != 1 or idx.shape[0] != scores.shape[0]:
+        raise ValueError("idx must be int32 [rows, world * k]")
+    rows = scores.shape[0]
+    dev = scores.device
+    if workspace is None:
+        workspace = new_workspace(topk_workspace_size(rows, k_out), dev)
+    out = torch.empty((rows, k_out), dtype=torch.int32, device=dev)
+    out_local = torch.empty((rows, k_out), dtype=torch.int32, device=dev) if rank is not None else None
+    rc = lib().dsa_topk_merge(_ptr(scores), scores.stride(0), _ptr(idx), idx.stride(0), rows, int(world), int(k),
+                              int(interleave), int(k_out), _ptr(out), int(rank or 0), _ptr(out_local),
+                              _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(rc, "dsa_topk_merge")
+    return out, out_local
 
 
 NORM_VARIANTS = {"auto": -1, "row": 0, "tiled": 1}
