@@ -528,9 +528,9 @@ int launch_select(const float* logits, float* logits_fill, int64_t ld, int64_t w
     a.cand = reinterpret_cast<uint2*>(ws + L.cand);
     if (rows == 0 || (k == 0 && (!logits_fill || width == 0))) return DSA_OK;
     if (rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
-    // Span per CTA: about two CTAs per SM over rows x width, at least kSpanMin
+    // Span per CTA: about four CTAs per SM over rows x width, at least kSpanMin
     // positions, a multiple of kChunk.
-    const int64_t target = 2 * static_cast<int64_t>(device_sm_count());
+    const int64_t target = 4 * static_cast<int64_t>(device_sm_count());
     int64_t span = (rows * width + target - 1) / target;
     span = span < kSpanMin ? kSpanMin : span;
     span = (span + kChunk - 1) / kChunk * kChunk;
