@@ -401,18 +401,16 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                                          uint64_t* empty, uint64_t* qfull, uint64_t* qempty, uint64_t* tfull,
                                          uint64_t* tempty, uint64_t* done_bar, volatile int* abort) {
     const int lane = threadIdx.x & 31;
-    const bool f32scale = (p.fmt == DSA_FMT_FP8);
+    // FP8 keys carry one scale per key: an FP32 power of two, or (FP8-MX) one
+    // UE8M0 exponent repeated in the four bytes of the scale word, so the
+    // product with the (unscaled) FP8 query is 2^e * sum q8 k8 either way; both
+    // take the plain FP8 MMA and apply the key scale in the epilogue.  Only
+    // MXFP4 uses the block-scaled MMA.
+    const bool key_scale = (p.fmt != DSA_FMT_MXFP4);
+    const bool mx_byte = (p.fmt == DSA_FMT_FP8_MX);
     const bool fp4 = (p.fmt == DSA_FMT_MXFP4);
     const int2* sinfo = reinterpret_cast<const int2*>(smem + OFF_SINFO);
     int2* ainfo = reinterpret_cast<int2*>(smem + OFF_AINFO);
-    if (p.fmt == DSA_FMT_FP8_MX) {
-        // FP8 queries carry no block scales (their scale is folded into w): 2^0 everywhere.
-        reinterpret_cast<uint4*>(smem + OFF_SFB)[lane] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc_cp_32x128b_warpx4(tmem + TM_SFB, desc_rows16(smem_u32(smem + OFF_SFB)));
-        __syncwarp();
-    }
     int cur = -1, qb = 0, i_seg = 0, nrows = 0;
     for (int it = 0;; ++it) {
         const int s = it % kStages;
@@ -462,12 +460,13 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
         tc_fence_after();
         const uint32_t* rs = reinterpret_cast<const uint32_t*>(smem + OFF_RAWSC + s * 512);
         const uint32_t w0 = rs[lane], w1 = rs[32 + lane], w2 = rs[64 + lane], w3 = rs[96 + lane];
-        if (f32scale) {
+        if (key_scale) {
+            // FP8-MX: byte 0 of the word is e + 127, and 2^e has exactly those exponent bits
             float* ks = reinterpret_cast<float*>(smem + OFF_KS + a * 512);
-            ks[lane] = __uint_as_float(w0);
-            ks[32 + lane] = __uint_as_float(w1);
-            ks[64 + lane] = __uint_as_float(w2);
-            ks[96 + lane] = __uint_as_float(w3);
+            ks[lane] = __uint_as_float(mx_byte ? (w0 & 0xFFu) << 23 : w0);
+            ks[32 + lane] = __uint_as_float(mx_byte ? (w1 & 0xFFu) << 23 : w1);
+            ks[64 + lane] = __uint_as_float(mx_byte ? (w2 & 0xFFu) << 23 : w2);
+            ks[96 + lane] = __uint_as_float(mx_byte ? (w3 & 0xFFu) << 23 : w3);
         } else {
             reinterpret_cast<uint4*>(smem + OFF_SFA + s * 512)[lane] = make_uint4(w0, w1, w2, w3);
             fence_proxy_async_smem();
@@ -478,7 +477,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             const uint64_t ad = desc_sw128(smem_u32(smem + OFF_TILES + s * kTileBytes));
             const uint64_t bd = desc_sw128(smem_u32(smem + OFF_QBUF + qb * kQBufBytes));
             const uint32_t n = 32u * nrows;
-            if (f32scale) {
+            if (key_scale) {
                 const uint32_t id = idesc_f8f6f4(kMmaE4M3, kMmaE4M3, 128, n);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) tc_mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, id, kk > 0);
@@ -486,7 +485,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                 const uint32_t sfa = tmem + TM_SFA + s * 4;
                 tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
                 const uint32_t fm = fp4 ? kMmaE2M1 : kMmaE4M3;
-                const uint32_t sfb = tmem + TM_SFB + (fp4 ? qb * 4 : 0);
+                const uint32_t sfb = tmem + TM_SFB + qb * 4;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc_mx(fm, fm, 128, n, kk, kk), sfa, sfb, kk > 0);
@@ -578,7 +577,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
     const int m = quarter * 32 + lane;       // key of the tile this thread owns
     float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - 2) * (kSegRows * kHeads);
     const int2* ainfo = reinterpret_cast<const int2*>(smem + OFF_AINFO);
-    const bool f32scale = (p.fmt == DSA_FMT_FP8);
+    const bool f32scale = (p.fmt != DSA_FMT_MXFP4);   // FP8 and FP8-MX: one scale per key
     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC;
     uint32_t* gh = reinterpret_cast<uint32_t*>(smem + OFF_HIST) + group * kGroupHistWords;
     const int e = threadIdx.x - 64 - group * 128;   // thread index within the group
