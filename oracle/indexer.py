@@ -44,11 +44,20 @@ FP4_WEIGHT = WEIGHT_SCALE              # A7: "the indexer weight scale"
 FP8_AMAX_FLOOR = np.float32(1e-10)     # ``DsaIndex.fp8_query``: amax starts at 1e-10
 MX_AMAX_FLOOR = 6.0 * 2.0 ** -126      # ``mxfp4_scale``: max(amax, 6 * 2^-126)
 
-FORMATS = ("fp8", "fp8_mx", "mxfp4")
+FORMATS = ("fp8", "fp8_mx", "mxfp4", "mxfp4_rg")
+# "mxfp4_rg" (page *amd.ops.fp4_indexer*, ``cache_views``): the MXFP4 codes and
+# scales of "mxfp4" placed group-major ("row-group") within the 4352-byte page
+# section: payload byte j of column group g of token t at g * 1024 + t * 16 + j,
+# the group's UE8M0 byte at 4096 + g * 64 + t (A23).
+RG_GROUP_BYTES, RG_SCALE_GROUP = 1024, 64
+
+
+def _fp4(fmt: str) -> bool:
+    return fmt in ("mxfp4", "mxfp4_rg")
 
 
 def page_bytes(fmt: str) -> int:
-    return FP4_PAGE_BYTES if fmt == "mxfp4" else FP8_PAGE_BYTES
+    return FP4_PAGE_BYTES if _fp4(fmt) else FP8_PAGE_BYTES
 
 
 # --------------------------------------------------------------------------
@@ -95,7 +104,7 @@ def quantize_query(fmt: str, q, wv):
         scale = np.ldexp(np.float32(1.0), e).astype(np.float32)
         fold = (wv * scale).astype(np.float32) * np.float32(WEIGHT_SCALE)
         w = bf16_round(fold.astype(np.float32))
-    elif fmt == "mxfp4":
+    elif _fp4(fmt):
         blocks = q.reshape(rows, HEADS, 4, 32).astype(np.float64)
         e = mx_scale_exponent(np.abs(blocks).max(axis=3))                   # [rows, 32, 4]
         codes = e2m1_encode(blocks * np.ldexp(1.0, -e)[..., None]).reshape(rows, HEADS, DIM)
@@ -171,7 +180,7 @@ def quantize_key(fmt: str, normed):
         else:
             scale_bytes = np.repeat((e + 127).astype(np.uint8)[:, None], 4, axis=1)
         return codes.astype(np.uint8), scale_bytes
-    if fmt == "mxfp4":
+    if _fp4(fmt):
         blocks = normed.reshape(n, 4, 32).astype(np.float64)
         e = mx_scale_exponent(np.abs(blocks).max(axis=2))
         codes = e2m1_encode(blocks * np.ldexp(1.0, -e)[..., None]).reshape(n, DIM)
@@ -198,7 +207,21 @@ def insert_key(fmt: str, cache: np.ndarray, page_stride: int, num_pages: int,
     codes, scale_bytes = quantize_key(fmt, normed)
     flat = cache.reshape(-1)
     bad = 0
-    code_bytes = DIM if fmt != "mxfp4" else DIM // 2
+    if fmt == "mxfp4_rg":
+        for i, slot in enumerate(slots):
+            if slot < 0:
+                continue
+            if slot >= num_pages * PAGE:
+                bad += 1
+                continue
+            page, off = divmod(int(slot), PAGE)
+            base = page * page_stride
+            for g in range(4):
+                a = base + g * RG_GROUP_BYTES + off * 16
+                flat[a: a + 16] = codes[i][g * 16:(g + 1) * 16]
+                flat[base + FP4_KEY_BYTES + g * RG_SCALE_GROUP + off] = scale_bytes[i][g]
+        return bad
+    code_bytes = DIM if not _fp4(fmt) else DIM // 2
     scale_base = PAGE * code_bytes
     for i, slot in enumerate(slots):
         if slot < 0:
@@ -281,9 +304,14 @@ def decode_keys(fmt: str, cache: np.ndarray, page_stride: int, pages, n: int) ->
             return vals * scale[:, None]
         e = sb.astype(np.int64) - 127
         return (vals.reshape(n, 4, 32) * np.ldexp(1.0, e)[..., None]).reshape(n, DIM)
-    code_idx = (base + off * (DIM // 2))[:, None] + np.arange(DIM // 2)
+    if fmt == "mxfp4_rg":
+        j = np.arange(DIM // 2)
+        code_idx = base[:, None] + (j // 16) * RG_GROUP_BYTES + off[:, None] * 16 + j % 16
+        sidx = base[:, None] + FP4_KEY_BYTES + np.arange(4) * RG_SCALE_GROUP + off[:, None]
+    else:
+        code_idx = (base + off * (DIM // 2))[:, None] + np.arange(DIM // 2)
+        sidx = (base + FP4_KEY_BYTES + off * 4)[:, None] + np.arange(4)
     codes = unpack_e2m1(flat[code_idx])
-    sidx = (base + FP4_KEY_BYTES + off * 4)[:, None] + np.arange(4)
     e = flat[sidx].astype(np.int64) - 127
     return (e2m1_decode(codes).reshape(n, 4, 32) * np.ldexp(1.0, e)[..., None]).reshape(n, DIM)
 
