@@ -40,12 +40,14 @@ import numpy as np  # noqa: E402
 METRIC = "indexer scored keys/sec and cache GB/s (score+top-k) vs roofline, 1 GB300"
 UNIT = "keys/s"
 STEP_KERNELS = 4   # prepare_step (quantize + insert + layout), plan, score, select
+FP4_FORMATS = ("mxfp4", "mxfp4_rg")
 
 
 def workload_desc(wl) -> str:
     kind = {"fp8": "FP8 E4M3 keys, FP32 scales (132 B/token)",
             "fp8_mx": "FP8 E4M3 keys, UE8M0 scales (132 B/token)",
-            "mxfp4": "MXFP4 keys (68 B/token)"}[wl.fmt]
+            "mxfp4": "MXFP4 keys (68 B/token)",
+            "mxfp4_rg": "MXFP4 keys, row-group page layout (68 B/token)"}[wl.fmt]
     return (f"{wl.name}: {wl.R} requests, {int(wl.query_lens.sum())} rows (+{wl.num_rows - int(wl.query_lens.sum())}"
             f" padding), seq {int(wl.seq_lens.min())}..{int(wl.seq_lens.max())}, {kind}, top-{wl.topk}")
 
@@ -54,7 +56,7 @@ def algorithmic_bytes(wl, row_ends) -> dict:
     """Bytes the step must move at least: unique cache bytes of the scored keys
     (each request's keys once), the quantised query rows and head weights, the
     block-table entries read, and the top-k indices written."""
-    per_token = 68 if wl.fmt == "mxfp4" else 132
+    per_token = 68 if wl.fmt in FP4_FORMATS else 132
     starts = np.concatenate([[0], np.cumsum(wl.query_lens)])
     keys_unique = 0
     pages = 0
@@ -63,7 +65,7 @@ def algorithmic_bytes(wl, row_ends) -> dict:
         m = int(e.max()) if e.size else 0
         keys_unique += m
         pages += (m + 63) // 64
-    q_bytes = 2176 if wl.fmt == "mxfp4" else 4096
+    q_bytes = 2176 if wl.fmt in FP4_FORMATS else 4096
     cache = keys_unique * per_token
     other = wl.num_rows * (q_bytes + 64 + 4) + pages * 4
     topk = wl.num_rows * wl.topk * 4
@@ -149,6 +151,13 @@ def score_source_hash() -> str:
     for f in ("score.cu", "common.cuh", "scan.cuh"):
         h.update(open(os.path.join(ROOT, "sparse_attention_indexer_score_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def traffic_key(wl) -> str:
+    """Name of a workload's entry in the traffic record: the workload's name,
+    with ``/<format>`` when its cache format was overridden."""
+    from synth.workloads import CONFIGS
+    return wl.name if wl.fmt == CONFIGS[wl.name]["fmt"] else f"{wl.name}/{wl.fmt}"
 
 
 def ncu_traffic(workload: str, units_per_launch: int):
@@ -384,11 +393,11 @@ def run_ours(args, wl, rank, world, local_rank):
     value = whole_job_rate(ab["scored"], args.steps, world, step_ms)
     peaks = measured_peaks()
     achieved = ab["score_kernel"] / (kernel_ms / 1e3) / 1e9
-    traffic = ncu_traffic(wl.name, ab["score_kernel"])
+    traffic = ncu_traffic(traffic_key(wl), ab["score_kernel"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": {"fp8": "fp8_e4m3", "fp8_mx": "fp8_e4m3", "mxfp4": "fp4_e2m1"}[wl.fmt],
+        "vs_baseline": None, "dtype": "fp4_e2m1" if wl.fmt in FP4_FORMATS else "fp8_e4m3",
         "data": "synthetic",
         "config": {"workload": workload_desc(wl), "rows": wl.num_rows, "requests": wl.R,
                    "scored_keys_per_step": ab["scored"], "unique_keys_per_step": ab["keys_unique"],
@@ -503,6 +512,7 @@ def main():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="fp8_decode")
+    p.add_argument("--fmt", default=None, help="override the workload's cache format (e.g. mxfp4_rg)")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--op", choices=["step", "query_norm", "topk_merge"], default="step",
@@ -522,7 +532,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     from synth import make_workload
-    wl = make_workload(args.config)
+    wl = make_workload(args.config, **({"fmt": args.fmt} if args.fmt else {}))
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, wl)

@@ -58,11 +58,18 @@ extern "C" {
  *                  byte b as the scale of columns 32b..32b+31, which for the
  *                  four equal bytes the writer stores is the token's one scale.
  *  DSA_FMT_MXFP4   E2M1 keys and queries, one UE8M0 scale per 32 columns
- *                  (68 B/token); the head weights carry only the 1/64 factor. */
+ *                  (68 B/token); the head weights carry only the 1/64 factor.
+ *  DSA_FMT_MXFP4_RG  the codes and scales of DSA_FMT_MXFP4, placed group-major
+ *                  ("row-group") in the 4352-byte page section (page
+ *                  "amd.ops.fp4_indexer", cache_views): the 16 code bytes of
+ *                  column group g (columns 32g..32g+31) of token t at
+ *                  g * 1024 + t * 16, its UE8M0 byte at 4096 + g * 64 + t.
+ *                  Queries and weights as DSA_FMT_MXFP4. */
 typedef enum {
     DSA_FMT_FP8 = 0,
     DSA_FMT_FP8_MX = 1,
-    DSA_FMT_MXFP4 = 2
+    DSA_FMT_MXFP4 = 2,
+    DSA_FMT_MXFP4_RG = 3
 } dsa_format;
 
 /* Return codes. */
@@ -116,6 +123,8 @@ int dsa_quantize_query(int fmt, const void* q, int64_t q_row_stride,
  *                scales at 8192 + offset * 4 (FP32 2^e, or the byte e + 127 four
  *                times for DSA_FMT_FP8_MX).  MXFP4 page: 64 x 64 B E2M1 at
  *                offset * 64, then 64 x 4 UE8M0 at 4096 + offset * 4.
+ *                DSA_FMT_MXFP4_RG page: the same bytes group-major (see the
+ *                format list); page_stride >= 4352 and a multiple of 16.
  *   status       optional int32 device word (may be NULL).
  *
  * The LayerNorm is computed in a fixed order: per 8-column group a sequential
@@ -239,11 +248,12 @@ size_t dsa_workspace_size(int fmt, int64_t rows, int64_t num_requests,
  * max_pages * 64); page "cutedsl.dsa.overlap" (scoring and top-k).
  *
  *   q_rows        uint8 [rows][4096] from dsa_quantize_query (16-byte aligned;
- *                 32-byte aligned for MXFP4).
+ *                 32-byte aligned for DSA_FMT_MXFP4).
  *   w             BF16 [rows][32] head weights from dsa_quantize_query.
  *   cache         paged cache written by dsa_insert_key (same layout rules;
  *                 for MXFP4 the base must be 32-byte aligned and page_stride a
- *                 multiple of 32).
+ *                 multiple of 32; for MXFP4_RG 16-byte alignment and stride
+ *                 multiples of 16 suffice).
  *   block_table   int32, request q's page j at block_table[q * bt_stride + j],
  *                 max_pages columns.
  *   starts        int32 [num_requests + 1]: rows starts[q] .. starts[q+1]-1 form

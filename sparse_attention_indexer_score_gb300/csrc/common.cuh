@@ -19,6 +19,15 @@ constexpr int kQRowBytes = 4096;
 constexpr int kFp4Scales = 2048;
 constexpr int kFp8KeyBytes = kPage * kDim;        // 8192: codes of one FP8 page
 constexpr int kFp4KeyBytes = kPage * kDim / 2;    // 4096: codes of one MXFP4 page
+// Row-group MXFP4 page: column group g's 64 x 16 code bytes at g * 1024, its
+// 64 scale bytes at 4096 + g * 64.
+constexpr int kRgGroupBytes = kPage * 16;
+constexpr int kRgScaleGroup = kPage;
+
+// MXFP4 codes in either placement.
+__host__ __device__ __forceinline__ bool fmt_fp4(int fmt) {
+    return fmt == DSA_FMT_MXFP4 || fmt == DSA_FMT_MXFP4_RG;
+}
 
 // Top-k: 11-bit histogram of the order-preserving score bits.
 constexpr int kHistBits = 11;
@@ -111,6 +120,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
                                             uint64_t* bar) {
     asm volatile(
@@ -191,6 +208,18 @@ __device__ __forceinline__ void tc_mma_mxf8f6f4(uint32_t d, uint64_t a, uint64_t
         "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
         : "memory");
 }
+// Packed E2M1 operands (two per byte, K = 64 per instruction) with two UE8M0
+// scales per row per instruction: bytes id and id + 1 (id = 0 or 2) of each
+// row's scale word, for K-elements 0-31 and 32-63.
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], "
+        "p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
 // Copy a 32-row x 16-byte matrix from shared memory into TMEM lanes 0-31
 // (4 columns), replicated into the other three 32-lane quarters.
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
@@ -262,6 +291,18 @@ __device__ __forceinline__ uint64_t desc_rows16(uint32_t saddr) {
     return d;
 }
 
+// Descriptor of an unswizzled K-major operand built of 8-row x 16-byte core
+// matrices (128 contiguous bytes each): `lbo` bytes between core matrices
+// adjacent in K, `sbo` bytes between those adjacent in M (or N).
+__device__ __forceinline__ uint64_t desc_kmajor_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;                    // descriptor version; layout type 0: no swizzle
+    return d;
+}
+
 // Instruction descriptor, kind::f8f6f4, FP32 accumulate, K-major A and B.
 __host__ __device__ __forceinline__ uint32_t idesc_f8f6f4(uint32_t a_fmt, uint32_t b_fmt, uint32_t m,
                                                            uint32_t n) {
@@ -276,6 +317,7 @@ __host__ __device__ __forceinline__ uint32_t idesc_mx(uint32_t a_fmt, uint32_t b
 }
 constexpr uint32_t kMmaE4M3 = 0;
 constexpr uint32_t kMmaE2M1 = 5;
+constexpr uint32_t kMmaMxf4E2M1 = 1;   // the E2M1 code of kind::mxf4
 
 // ----------------------------------------------------------------- top-k keys
 // Order-preserving map of an FP32 onto uint32 (larger float -> larger key).

@@ -65,7 +65,7 @@ __device__ __forceinline__ void quantize_query_block(int fmt, const uint16_t* __
     float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
     uint8_t* out_row = q_out + row * kQRowBytes;
     const float wvf = bf16_bits_to_f32(wv[row * wv_stride + head]);
-    if (fmt != DSA_FMT_MXFP4) {
+    if (!fmt_fp4(fmt)) {
         amax = fmaxf(amax, 1e-10f);
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
@@ -169,7 +169,7 @@ __device__ __forceinline__ void insert_key_block(int fmt, const uint16_t* __rest
     const int64_t page = slot / kPage;
     const int off = static_cast<int>(slot % kPage);
     uint8_t* base = cache + page * page_stride;
-    if (fmt != DSA_FMT_MXFP4) {
+    if (!fmt_fp4(fmt)) {
 #pragma unroll
         for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, d, 16));
         const int e = fp8_exponent(fmaxf(amax, 1e-10f));
@@ -195,13 +195,21 @@ __device__ __forceinline__ void insert_key_block(int fmt, const uint16_t* __rest
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             word |= e2m1x2(__fmul_rn(normed[2 * i], inv), __fmul_rn(normed[2 * i + 1], inv)) << (8 * i);
-        *reinterpret_cast<uint32_t*>(base + off * (kDim / 2) + j * 4) = word;
         const uint32_t byte = static_cast<uint32_t>(e + 127);
-        const uint32_t b1 = __shfl_sync(hmask, byte, 4, 16);
-        const uint32_t b2 = __shfl_sync(hmask, byte, 8, 16);
-        const uint32_t b3 = __shfl_sync(hmask, byte, 12, 16);
-        if (j == 0)
-            *reinterpret_cast<uint32_t*>(base + kFp4KeyBytes + off * 4) = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        if (fmt == DSA_FMT_MXFP4_RG) {
+            // lane j: bytes 4(j mod 4) .. +3 of group j / 4's 16 bytes; its first lane writes the scale
+            const int g = j >> 2;
+            *reinterpret_cast<uint32_t*>(base + g * kRgGroupBytes + off * 16 + (j & 3) * 4) = word;
+            if ((j & 3) == 0) base[kFp4KeyBytes + g * kRgScaleGroup + off] = static_cast<uint8_t>(byte);
+        } else {
+            *reinterpret_cast<uint32_t*>(base + off * (kDim / 2) + j * 4) = word;
+            const uint32_t b1 = __shfl_sync(hmask, byte, 4, 16);
+            const uint32_t b2 = __shfl_sync(hmask, byte, 8, 16);
+            const uint32_t b3 = __shfl_sync(hmask, byte, 12, 16);
+            if (j == 0)
+                *reinterpret_cast<uint32_t*>(base + kFp4KeyBytes + off * 4) =
+                    byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        }
     }
 }
 
@@ -281,7 +289,7 @@ static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 static int check_quantize(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride,
                           int64_t rows, const void* q_out, const void* w_out, int64_t* blocks) {
     *blocks = 0;
-    if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4) return DSA_ERR_UNSUPPORTED;
+    if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4_RG) return DSA_ERR_UNSUPPORTED;
     if (rows < 0) return DSA_ERR_INVALID;
     if (rows == 0) return DSA_OK;
     if (!q || !wv || !q_out || !w_out) return DSA_ERR_INVALID;
@@ -295,11 +303,11 @@ static int check_insert(int fmt, const void* k, int64_t k_row_stride, const floa
                         const int64_t* slots, int64_t n, const void* cache, int64_t page_stride, int64_t num_pages,
                         int64_t* blocks) {
     *blocks = 0;
-    if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4) return DSA_ERR_UNSUPPORTED;
+    if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4_RG) return DSA_ERR_UNSUPPORTED;
     if (n < 0 || num_pages < 0) return DSA_ERR_INVALID;
     if (n == 0) return DSA_OK;
     if (!k || !gamma || !beta || !slots || !cache) return DSA_ERR_INVALID;
-    const int64_t min_stride = (fmt == DSA_FMT_MXFP4) ? DSA_FP4_PAGE_BYTES : DSA_FP8_PAGE_BYTES;
+    const int64_t min_stride = fmt_fp4(fmt) ? DSA_FP4_PAGE_BYTES : DSA_FP8_PAGE_BYTES;
     if (page_stride < min_stride || page_stride % 16) return DSA_ERR_INVALID;
     if (k_row_stride < kDim || k_row_stride % 8) return DSA_ERR_INVALID;
     if (!aligned(k, 16) || !aligned(gamma, 16) || !aligned(beta, 16) || !aligned(cache, 16) || !aligned(slots, 8))

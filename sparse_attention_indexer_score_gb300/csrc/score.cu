@@ -19,10 +19,14 @@
 //              ReLU-weighted head sum, FP32 key scale, logits store, and a
 //              shared-memory histogram of the scores for the top-k pass.
 //
-// Formats: FP8 uses kind::f8f6f4 (E4M3 x E4M3) and multiplies the FP32 key
-// scale in the epilogue.  FP8-MX and MXFP4 use kind::mxf8f6f4 with UE8M0 block
-// scales in TMEM (one per 32 columns); MXFP4 keys and queries are unpacked by
-// TMA into the 16-byte-aligned E2M1 layout the MMA reads.
+// Formats: FP8 and FP8-MX use kind::f8f6f4 (E4M3 x E4M3) and multiply the
+// per-key scale in the epilogue.  MXFP4 uses kind::mxf8f6f4 with UE8M0 block
+// scales in TMEM (one per 32 columns); its keys and queries are unpacked by
+// TMA into the 16-byte-aligned E2M1 layout that MMA kind reads.  Row-group
+// MXFP4 keeps the codes packed: each column group's 64 x 16 bytes of a page
+// is one TMA box that lands as 8 unswizzled core matrices, the two pages'
+// boxes of a group side by side, and kind::mxf4 (K = 64, two scales per row)
+// reads groups 2m and 2m + 1 in instruction m.
 #include "host.h"
 #include "scan.cuh"
 
@@ -37,6 +41,11 @@ constexpr int kPageSmem = 64 * 128;           // one page's codes in shared memo
 // an MXFP4 query row 2048.
 constexpr uint32_t kFp8PageTx = 64 * 128, kFp4PageTx = 64 * 64;
 constexpr uint32_t kFp8QRowTx = kQRowBytes, kFp4QRowTx = kQRowBytes / 2;
+// Row-group MXFP4 in shared memory: a tile's column group g at g * 2048 (the
+// two pages' 1024-byte boxes in key order); query chunk c (16 bytes = 32
+// columns of every head) at c * 2048, query row r's 32 heads at + r * 512.
+constexpr int kRgTileGroup = 2 * kRgGroupBytes;
+constexpr int kRgQChunk = 2048;
 constexpr int kSegRows = 4;                   // query rows per segment
 constexpr int kQBufBytes = kSegRows * kQRowBytes;
 // Two epilogue groups of four warps (one per TMEM lane quarter) drain
@@ -288,7 +297,8 @@ struct Producer {
     uint64_t* qfull;
     uint64_t* qempty;
     volatile int* abort;
-    bool fp4;
+    bool fp4;            // MXFP4 codes (either placement): transaction sizes
+    bool rg;             // row-group placement: packed boxes per column group
     int cur = -1, i_seg = 0, it = 0;
 
     __device__ __forceinline__ bool issue(const ScoreArgs& p, int sg, int j, int p0, int p1) {
@@ -301,7 +311,14 @@ struct Producer {
             mbar_arrive_expect_tx(qfull + qb, bytes);
             uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
             for (int r = 0; r < si.z; ++r) {
-                tma_load_3d(qdst + r * kQRowBytes, qmap, 0, 0, si.y + r, qfull + qb);
+                if (rg) {
+                    // packed: 16-byte column chunk c of the 32 heads at c * 2048 + r * 512
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_3d(qdst + c * kRgQChunk + r * 512, qmap, 16 * c, 0, si.y + r, qfull + qb);
+                } else {
+                    tma_load_3d(qdst + r * kQRowBytes, qmap, 0, 0, si.y + r, qfull + qb);
+                }
                 if (fp4)
                     bulk_load(smem + OFF_QSF + qb * 512 + r * 128,
                               p.q_rows + static_cast<int64_t>(si.y + r) * kQRowBytes + kFp4Scales, 128, qfull + qb);
@@ -318,13 +335,28 @@ struct Producer {
         } else {
             mbar_arrive_expect_tx(full + s, bytes);
             uint8_t* dst = smem + OFF_TILES + s * kTileBytes;
-            if (p0 >= 0) {
-                tma_load_3d(dst, kmap, 0, 0, p0, full + s);
-                tma_load_2d(smem + OFF_RAWSC + s * 512, smap, 0, p0, full + s);
-            }
-            if (p1 >= 0) {
-                tma_load_3d(dst + kPageSmem, kmap, 0, 0, p1, full + s);
-                tma_load_2d(smem + OFF_RAWSC + s * 512 + 256, smap, 0, p1, full + s);
+            if (rg) {
+                // group g of page h at g * 2048 + h * 1024: keys 0..127 of a group are 128 x 16 bytes in order
+                if (p0 >= 0) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) tma_load_4d(dst + g * kRgTileGroup, kmap, 0, 0, g, p0, full + s);
+                    tma_load_2d(smem + OFF_RAWSC + s * 512, smap, 0, p0, full + s);
+                }
+                if (p1 >= 0) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        tma_load_4d(dst + g * kRgTileGroup + kRgGroupBytes, kmap, 0, 0, g, p1, full + s);
+                    tma_load_2d(smem + OFF_RAWSC + s * 512 + 256, smap, 0, p1, full + s);
+                }
+            } else {
+                if (p0 >= 0) {
+                    tma_load_3d(dst, kmap, 0, 0, p0, full + s);
+                    tma_load_2d(smem + OFF_RAWSC + s * 512, smap, 0, p0, full + s);
+                }
+                if (p1 >= 0) {
+                    tma_load_3d(dst + kPageSmem, kmap, 0, 0, p1, full + s);
+                    tma_load_2d(smem + OFF_RAWSC + s * 512 + 256, smap, 0, p1, full + s);
+                }
             }
         }
         ++it;
@@ -406,9 +438,10 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
     // product with the (unscaled) FP8 query is 2^e * sum q8 k8 either way; both
     // take the plain FP8 MMA and apply the key scale in the epilogue.  Only
     // MXFP4 uses the block-scaled MMA.
-    const bool key_scale = (p.fmt != DSA_FMT_MXFP4);
+    const bool key_scale = !fmt_fp4(p.fmt);
     const bool mx_byte = (p.fmt == DSA_FMT_FP8_MX);
-    const bool fp4 = (p.fmt == DSA_FMT_MXFP4);
+    const bool fp4 = fmt_fp4(p.fmt);
+    const bool rg = (p.fmt == DSA_FMT_MXFP4_RG);
     const int2* sinfo = reinterpret_cast<const int2*>(smem + OFF_SINFO);
     int2* ainfo = reinterpret_cast<int2*>(smem + OFF_AINFO);
     int cur = -1, qb = 0, i_seg = 0, nrows = 0;
@@ -459,7 +492,25 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty + a, ((it / kAcc) & 1) ^ 1, abort, p.status))) break;
         tc_fence_after();
         const uint32_t* rs = reinterpret_cast<const uint32_t*>(smem + OFF_RAWSC + s * 512);
-        const uint32_t w0 = rs[lane], w1 = rs[32 + lane], w2 = rs[64 + lane], w3 = rs[96 + lane];
+        uint32_t w0, w1, w2, w3;
+        if (rg) {
+            // page h's scale bytes are [group][64 keys]: gather key t's four into one word
+            const uint8_t* rb = smem + OFF_RAWSC + s * 512;
+            auto word = [&](int t) {
+                const uint8_t* b = rb + (t >> 6) * 256 + (t & 63);
+                return static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[64]) << 8) |
+                       (static_cast<uint32_t>(b[128]) << 16) | (static_cast<uint32_t>(b[192]) << 24);
+            };
+            w0 = word(lane);
+            w1 = word(32 + lane);
+            w2 = word(64 + lane);
+            w3 = word(96 + lane);
+        } else {
+            w0 = rs[lane];
+            w1 = rs[32 + lane];
+            w2 = rs[64 + lane];
+            w3 = rs[96 + lane];
+        }
         if (key_scale) {
             // FP8-MX: byte 0 of the word is e + 127, and 2^e has exactly those exponent bits
             float* ks = reinterpret_cast<float*>(smem + OFF_KS + a * 512);
@@ -481,6 +532,17 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                 const uint32_t id = idesc_f8f6f4(kMmaE4M3, kMmaE4M3, 128, n);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) tc_mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, id, kk > 0);
+            } else if (rg) {
+                const uint32_t sfa = tmem + TM_SFA + s * 4;
+                tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
+                const uint32_t sfb = tmem + TM_SFB + qb * 4;
+                const uint32_t ka = smem_u32(smem + OFF_TILES + s * kTileBytes);
+                const uint32_t kb = smem_u32(smem + OFF_QBUF + qb * kQBufBytes);
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+                    tc_mma_mxf4(d, desc_kmajor_plain(ka + 2 * m * kRgTileGroup, kRgTileGroup, 128),
+                                desc_kmajor_plain(kb + 2 * m * kRgQChunk, kRgQChunk, 128),
+                                idesc_mx(kMmaMxf4E2M1, kMmaMxf4E2M1, 128, n, 2 * m, 2 * m), sfa, sfb, m > 0);
             } else {
                 const uint32_t sfa = tmem + TM_SFA + s * 4;
                 tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
@@ -577,7 +639,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
     const int m = quarter * 32 + lane;       // key of the tile this thread owns
     float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - 2) * (kSegRows * kHeads);
     const int2* ainfo = reinterpret_cast<const int2*>(smem + OFF_AINFO);
-    const bool f32scale = (p.fmt != DSA_FMT_MXFP4);   // FP8 and FP8-MX: one scale per key
+    const bool f32scale = !fmt_fp4(p.fmt);   // FP8 and FP8-MX: one scale per key
     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC;
     uint32_t* gh = reinterpret_cast<uint32_t*>(smem + OFF_HIST) + group * kGroupHistWords;
     const int e = threadIdx.x - 64 - group * 128;   // thread index within the group
@@ -696,7 +758,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int T = args.claim[-1], Ts = args.claim[1];
         const int t0 = range.x, t1 = range.y, S = range.w;
         const int seg = (t0 < t1 && range.z < 0) ? find_segment(args.seg_prefix, S, t0) : range.z;
-        Producer pr{&kmap, &smap, &qmap, smem, full, empty, qfull, qempty, abort, args.fmt == DSA_FMT_MXFP4};
+        Producer pr{&kmap, &smap, &qmap, smem, full, empty, qfull, qempty, abort, fmt_fp4(args.fmt),
+                    args.fmt == DSA_FMT_MXFP4_RG};
         producer_role(pr, args, t0, t1, seg, S, Ts, T);
     } else if (warp == 1) {
         mma_role(args, smem, tmem, full, empty, qfull, qempty, tfull, tempty, done_bar, abort);
@@ -760,11 +823,13 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
                                int64_t max_query_len, float* logits, int64_t logits_ld, int64_t k, int32_t* topk,
                                void* workspace, size_t workspace_bytes, int32_t* status, void* stream_) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4) return DSA_ERR_UNSUPPORTED;
+    if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4_RG) return DSA_ERR_UNSUPPORTED;
     if (rows < 0 || num_requests < 0 || max_pages < 0 || num_pages < 0 || k < 0 || max_query_len < 0)
         return DSA_ERR_INVALID;
     if (rows == 0) return DSA_OK;
-    const bool fp4 = (fmt == DSA_FMT_MXFP4);
+    const bool fp4 = fmt_fp4(fmt);
+    const bool rg = (fmt == DSA_FMT_MXFP4_RG);
+    const bool unpack = fp4 && !rg;   // 16U4_ALIGN16B copies: 32-byte bases and strides
     const int64_t width = max_pages * kPage;
     if (rows > (1 << 30) || num_requests > (1 << 30) || width > (int64_t(1) << 30) || num_pages > 0x7FFFFFFF)
         return DSA_ERR_UNSUPPORTED;
@@ -772,8 +837,8 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     if (num_pages > 0 && !cache) return DSA_ERR_INVALID;
     if (max_pages > 0 && num_requests > 0 && (!block_table || bt_stride < max_pages)) return DSA_ERR_INVALID;
     const int64_t min_stride = fp4 ? DSA_FP4_PAGE_BYTES : DSA_FP8_PAGE_BYTES;
-    if (page_stride < min_stride || page_stride % (fp4 ? 32 : 16)) return DSA_ERR_INVALID;
-    if (!aligned(cache, fp4 ? 32 : 16) || !aligned(q_rows, fp4 ? 32 : 16) || !aligned(workspace, 256) ||
+    if (page_stride < min_stride || page_stride % (unpack ? 32 : 16)) return DSA_ERR_INVALID;
+    if (!aligned(cache, unpack ? 32 : 16) || !aligned(q_rows, unpack ? 32 : 16) || !aligned(workspace, 256) ||
         !aligned(w, 2))
         return DSA_ERR_INVALID;
     if (logits && (logits_ld < width || !aligned(logits, 4))) return DSA_ERR_INVALID;
@@ -790,7 +855,15 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     const cuuint64_t np = static_cast<cuuint64_t>(num_pages > 0 ? num_pages : 1);
     uint8_t* cache_b = static_cast<uint8_t*>(const_cast<void*>(cache));
     void* cache_addr = cache_b ? static_cast<void*>(cache_b) : workspace;   // unused when there are no pages
-    {
+    if (rg) {
+        // {16 code bytes, 64 keys, 4 column groups, pages}: one box = one group of one page
+        const cuuint64_t dims[4] = {16, 64, 4, np};
+        const cuuint64_t strides[3] = {16, kRgGroupBytes, static_cast<cuuint64_t>(page_stride)};
+        const cuuint32_t box[4] = {16, 64, 1, 1};
+        if (encode_tiled(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, cache_addr, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+            return DSA_ERR_CUDA;
+    } else {
         const cuuint64_t dims[3] = {128, 64, np};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(fp4 ? 64 : 128), static_cast<cuuint64_t>(page_stride)};
         const cuuint32_t box[3] = {128, 64, 1};
@@ -807,7 +880,15 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
                          CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
             return DSA_ERR_CUDA;
     }
-    {
+    if (rg) {
+        // {64 code bytes, 32 heads, rows}: one box = one 16-byte column chunk of a row's heads
+        const cuuint64_t dims[3] = {64, 32, static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[2] = {64, kQRowBytes};
+        const cuuint32_t box[3] = {16, 32, 1};
+        if (encode_tiled(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q_rows), dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+            return DSA_ERR_CUDA;
+    } else {
         const cuuint64_t dims[3] = {128, 32, static_cast<cuuint64_t>(rows)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(fp4 ? 64 : 128), kQRowBytes};
         const cuuint32_t box[3] = {128, 32, 1};

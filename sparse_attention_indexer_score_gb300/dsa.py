@@ -18,11 +18,11 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libdsa.so")
 
-FORMATS = {"fp8": 0, "fp8_mx": 1, "mxfp4": 2}
+FORMATS = {"fp8": 0, "fp8_mx": 1, "mxfp4": 2, "mxfp4_rg": 3}
 ERRORS = {-1: "invalid argument", -2: "unsupported", -3: "CUDA launch or driver error"}
 STATUS_BITS = {1: "bad slot", 2: "bad page", 4: "bad geometry", 8: "timeout"}
 Q_ROW_BYTES = 4096
-PAGE_BYTES = {"fp8": 8448, "fp8_mx": 8448, "mxfp4": 4352}
+PAGE_BYTES = {"fp8": 8448, "fp8_mx": 8448, "mxfp4": 4352, "mxfp4_rg": 4352}
 
 _lib = None
 

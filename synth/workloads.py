@@ -40,7 +40,7 @@ DIM = 128
 PAGE = 64
 
 # Format names shared by both sides; each side maps them to its own enum.
-FORMATS = ("fp8", "fp8_mx", "mxfp4")
+FORMATS = ("fp8", "fp8_mx", "mxfp4", "mxfp4_rg")
 
 CONFIGS = {
     "tiny_fp8": dict(fmt="fp8", R=2, qlen=(1, 1), seq=(256, 256), pad_rows=0,
@@ -121,7 +121,7 @@ class Workload:
         return (np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts]))
 
     def cache_bytes(self) -> int:
-        return self.num_pages * PAGE * (68 if self.fmt == "mxfp4" else 132)
+        return self.num_pages * PAGE * (68 if self.fmt in ("mxfp4", "mxfp4_rg") else 132)
 
 
 def make_workload(name: str = "tiny_fp8", **overrides) -> Workload:

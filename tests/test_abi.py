@@ -54,7 +54,12 @@ def test_host_argument_checks(lib):
     assert lib.dsa_insert_key(2, 16, 128, 16, 16, 1e-6, 16, 0, 16, 4352, 1, None, None) == 0
     assert lib.dsa_decode_layout(None, 0, None, 0, -1, None, None, None) == -1
     assert lib.dsa_decode_layout(16, 1, 16, 2, 2, 16, 16, None) == -1        # fewer seq_lens than requests
-    assert lib.dsa_score_paged(3, *([0] * 21)) == -2
+    assert lib.dsa_score_paged(4, *([0] * 21)) == -2
+    assert lib.dsa_insert_key(4, 16, 128, 16, 16, 1e-6, 16, 0, 16, 4352, 1, None, None) == -2
+    assert lib.dsa_insert_key(3, 16, 128, 16, 16, 1e-6, 16, 0, 16, 4352, 1, None, None) == 0   # row-group MXFP4
+    assert lib.dsa_insert_key(3, 16, 128, 16, 16, 1e-6, 16, 1, 16, 4352 - 16, 1, None, None) == -1
+    assert lib.dsa_score_paged(3, 32, 32, 32, 4352 + 8, 1, 16, 1, 1, 16, 16, 1, 1, 1, None, 0, 4, None, 256,
+                               10**9, None, None) == -1                         # row-group stride not a multiple of 16
     assert lib.dsa_score_paged(0, 16, 16, 16, 8448, 1, 16, 1, 1, 16, 16, 1, 0, 1, None, 0, 4, None, 256, 10**9,
                                None, None) == 0                                 # zero rows
     assert lib.dsa_score_paged(2, 32, 32, 32, 4352 + 16, 1, 16, 1, 1, 16, 16, 1, 1, 1, None, 0, 4, None, 256,

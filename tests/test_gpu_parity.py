@@ -8,7 +8,12 @@ from oracle import indexer as O
 from synth import bf16_bits_to_f32, make_workload
 
 pytestmark = pytest.mark.gpu
-FMTS = ["fp8", "fp8_mx", "mxfp4"]
+FMTS = ["fp8", "fp8_mx", "mxfp4", "mxfp4_rg"]
+
+
+def _used(fmt):
+    """Bytes of a quantised query row that carry data."""
+    return 2176 if fmt in ("mxfp4", "mxfp4_rg") else 4096
 
 
 def _special_queries(rng, rows):
@@ -35,7 +40,7 @@ def test_quantize_query_bit_exact(cuda_lib, fmt):
     wvb = ((rng.standard_normal((rows, 32)).astype(np.float32).view(np.uint32) >> 16)).astype(np.uint16)
     q_rows, w = cuda_lib.quantize_query(fmt, bf16_tensor(qb, "cuda"), bf16_tensor(wvb, "cuda"))
     want_rows, want_w = O.quantize_query(fmt, bf16_bits_to_f32(qb), bf16_bits_to_f32(wvb))
-    used = 4096 if fmt != "mxfp4" else 2176
+    used = _used(fmt)
     got = q_rows.cpu().numpy()
     assert np.array_equal(got[:, :used], want_rows[:, :used])
     assert not got[:, used:].any()
@@ -134,7 +139,7 @@ def test_prepare_step_bit_exact(cuda_lib, fmt):
     for a, b in zip(fused, separate):
         assert np.array_equal(a, b)
     want_rows, want_w = O.quantize_query(fmt, bf16_bits_to_f32(qb), bf16_bits_to_f32(wvb))
-    used = 4096 if fmt != "mxfp4" else 2176
+    used = _used(fmt)
     assert np.array_equal(fused[0][:, :used], want_rows[:, :used]) and not fused[0][:, used:].any()
     assert np.array_equal(fused[1], want_w)
     want_cache = np.zeros(num_pages * stride, np.uint8)
@@ -163,7 +168,7 @@ def test_score_topk_parity_small(cuda_lib, fmt, case):
     o = oracle_run(wl)
     assert g["status"] == 0
     assert np.array_equal(g["starts"], o["starts"]) and np.array_equal(g["row_ends"], o["row_ends"])
-    used = 4096 if fmt != "mxfp4" else 2176
+    used = _used(fmt)
     assert np.array_equal(g["q_rows"][:, :used], o["q_rows"][:, :used])
     rows = range(wl.num_rows)
     check_logits(g["logits"], o["scores"], o["row_ends"], rows)
@@ -181,6 +186,23 @@ def test_score_cache_bytes_match_oracle(cuda_lib, fmt):
     for p_gpu, p_or in o["remap"].items():
         assert np.array_equal(cache[p_gpu * stride:p_gpu * stride + O.page_bytes(fmt)],
                               o["cache"][p_or * stride:p_or * stride + O.page_bytes(fmt)]), p_gpu
+
+
+@pytest.mark.parametrize("case", [1, 2, 3, 5])
+def test_score_rowgroup_page_stride(cuda_lib, case):
+    """Row-group MXFP4 in a pool whose physical page stride (4400 bytes) is
+    above the 4352-byte section and not a multiple of 32."""
+    spec = dict(SMALL[case])
+    wl = make_workload("tiny_fp8", fmt="mxfp4_rg", seed=300 + case, topk=[16, 64, 100, 5, 2, 512][case], **spec)
+    g = gpu_run(wl, page_stride=4400)
+    o = oracle_run(wl, page_stride=4400)
+    assert g["status"] == 0
+    cache = g["cache"].cpu().numpy()
+    for p_gpu, p_or in o["remap"].items():
+        assert np.array_equal(cache[p_gpu * 4400:p_gpu * 4400 + 4352], o["cache"][p_or * 4400:p_or * 4400 + 4352])
+    rows = range(wl.num_rows)
+    check_logits(g["logits"], o["scores"], o["row_ends"], rows)
+    check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, rows)
 
 
 def test_topk_standalone_exact(cuda_lib):
@@ -246,11 +268,14 @@ def test_empty_and_degenerate(cuda_lib):
     assert np.all(np.isneginf(g["logits"][1:])) and np.all(g["topk"][1:] == -1)
 
 
-@pytest.mark.parametrize("name", ["tiny_fp8", "fp8_decode", "mxfp4_decode", "spec_verify", "long_mxfp4"])
+@pytest.mark.parametrize("name", ["tiny_fp8", "fp8_decode", "mxfp4_decode", "spec_verify", "long_mxfp4",
+                                  "long_mxfp4/mxfp4_rg"])
 def test_full_size_sampled_rows(cuda_lib, name):
     """The named decode-step workloads at full size, in the launch configuration
-    the bench times; the oracle checks a sample of rows (all for the tiny one)."""
-    wl = make_workload(name)
+    the bench times (``name/format`` overrides the cache format); the oracle
+    checks a sample of rows (all for the tiny one)."""
+    name, _, fmt = name.partition("/")
+    wl = make_workload(name, **({"fmt": fmt} if fmt else {}))
     g = gpu_run(wl, want_logits=True)
     assert g["status"] == 0
     rng = np.random.default_rng(0)
@@ -263,7 +288,7 @@ def test_full_size_sampled_rows(cuda_lib, name):
             rows += [wl.num_rows - 1]     # a padding row
     o = oracle_run(wl, rows=rows)
     assert np.array_equal(g["row_ends"], o["row_ends"])
-    used = 4096 if wl.fmt != "mxfp4" else 2176
+    used = _used(wl.fmt)
     assert np.array_equal(g["q_rows"][:, :used], o["q_rows"][:, :used])
     check_logits(g["logits"], o["scores"], o["row_ends"], rows)
     check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, rows)
