@@ -108,6 +108,18 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// Shared-memory counter with release / acquire ordering (a thread's earlier
+// accesses, tcgen05 ones fenced with tcgen05.fence::before_thread_sync, happen
+// before those of a thread that observes the count).
+__device__ __forceinline__ void smem_add_release(uint32_t* c, uint32_t v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(c)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t smem_ld_acquire(const uint32_t* c) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(c)) : "memory");
+    return v;
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");

@@ -13,11 +13,14 @@
 // Warp roles of the persistent CTA (one per SM):
 //   warp 0     TMA producer: block-table gather of key pages (+ their scales)
 //              into an 8-stage shared-memory ring; query rows per segment.
-//   warp 1     tcgen05 issuer: scale factors into TMEM, 4 MMAs (K = 32 each)
-//              per tile into one of three TMEM accumulators.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = key),
-//              ReLU-weighted head sum, FP32 key scale, logits store, and a
-//              shared-memory histogram of the scores for the top-k pass.
+//   warps 1-2  tcgen05 issuers of alternate tiles: scale factors into TMEM,
+//              4 MMAs (K = 32 each) per tile into one of three TMEM
+//              accumulators.  One issuer's per-tile chain of waits, tag and
+//              scale handling and MMA issue is longer than a tile's copy time.
+//   warps 3-10 epilogue, two groups of four: tcgen05.ld of the accumulator
+//              (thread = key), ReLU-weighted head sum, FP32 key scale, logits
+//              store, and a shared-memory histogram of the scores for the
+//              top-k pass.
 //
 // Formats: FP8 and FP8-MX use kind::f8f6f4 (E4M3 x E4M3) and multiply the
 // per-key scale in the epilogue.  MXFP4 uses kind::mxf8f6f4 with UE8M0 block
@@ -52,7 +55,13 @@ constexpr int kQBufBytes = kSegRows * kQRowBytes;
 // alternate tiles, so two accumulators are read out at once.
 constexpr int kEpiGroups = 2;
 constexpr int kEpiWarps = 4 * kEpiGroups;
-constexpr int kScoreThreads = 64 + 32 * kEpiWarps;
+// Two MMA-issuing warps: warp 1 + w issues the tiles of sequence positions
+// w, w + 2, ... (so it alone uses ring stages of that parity), which epilogue
+// group w drains.
+constexpr int kMmaWarps = 2;
+constexpr int kFirstEpiWarp = 1 + kMmaWarps;
+constexpr int kScoreThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+static_assert(kMmaWarps == kEpiGroups && kStages % kMmaWarps == 0, "issuer w owns stages and group w");
 constexpr int kAcc = 3;                       // TMEM accumulators in flight (MMA latency is hidden behind 2)
 constexpr int kPlanSmemSegs = 4096;           // segments whose tile prefix the plan keeps on chip
 // Tile assignment: every CTA owns an equal contiguous range of the first
@@ -68,7 +77,7 @@ constexpr int OFF_RAWSC = OFF_QBUF + 2 * kQBufBytes;
 constexpr int OFF_SFA = OFF_RAWSC + kStages * 512;
 constexpr int OFF_QSF = OFF_SFA + kStages * 512;
 constexpr int OFF_SFB = OFF_QSF + 2 * 512;
-constexpr int OFF_KS = OFF_SFB + 2 * 512;
+constexpr int OFF_KS = OFF_SFB + 2 * kMmaWarps * 512;   // query scale atoms per (buffer, issuer)
 constexpr int OFF_W = OFF_KS + kAcc * 128 * 4;            // float[kEpiWarps][4 rows][32 heads]: w per warp
 // Score histogram of each epilogue group for its current segment: 4 rows x
 // 2048 bins of 16-bit counts, two per word; added to the rows' histograms in
@@ -77,18 +86,24 @@ constexpr int OFF_W = OFF_KS + kAcc * 128 * 4;            // float[kEpiWarps][4 
 constexpr int kHistFlushTiles = 256;
 constexpr int OFF_HIST = OFF_W + kEpiWarps * kSegRows * kHeads * 4;
 constexpr int kGroupHistWords = kSegRows * kHistBins / 2;
-constexpr int OFF_SINFO = OFF_HIST + kEpiGroups * kGroupHistWords * 4;   // int2[kStages]: {tile in segment, segment}
-constexpr int OFF_AINFO = OFF_SINFO + kStages * 8;        // int2[kAcc]: the same per accumulator
+// int4[kStages]: {tile in segment, segment, segment ordinal in this CTA's sequence}
+constexpr int OFF_SINFO = OFF_HIST + kEpiGroups * kGroupHistWords * 4;
+constexpr int OFF_AINFO = OFF_SINFO + kStages * 16;       // int2[kAcc]: {tile in segment, segment} per accumulator
 constexpr int OFF_BAR = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 * kAcc + 1;
-constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
-constexpr int kScoreSmem = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
+// full, empty, qfull, tfull (per accumulator and epilogue group), done.  A
+// group's accumulator barrier is used by the sequence positions it, it + 6, ...
+// of that group alone: one barrier per accumulator, filled by both issuers,
+// could show a group a phase of the other group's fill (the two issuers'
+// MMAs complete in no common order) and its parity wait would take it.
+constexpr int kNumBars = 2 * kStages + 2 + kAcc * kEpiGroups + 1;
+constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;       // TMEM address, abort flag, then released[kAcc]
+constexpr int kScoreSmem = OFF_MISC + 32 + 1024;       // + slack to align the base to 1024
 static_assert(kScoreSmem <= 227 * 1024, "scoring CTA exceeds the shared memory of an SM");
 
 // TMEM columns: kAcc accumulators of up to 128 columns, then scale factors.
 constexpr uint32_t TM_ACC = 0;
 constexpr uint32_t TM_SFA = kAcc * 128;           // kStages x 4 columns
-constexpr uint32_t TM_SFB = TM_SFA + 4 * kStages; // 2 x 4 columns
+constexpr uint32_t TM_SFB = TM_SFA + 4 * kStages; // (2 buffers x kMmaWarps) x 4 columns
 constexpr uint32_t TM_COLS = 512;
 
 struct ScoreArgs {
@@ -286,7 +301,13 @@ __device__ __forceinline__ int warp_find_segment(const int* prefix, int S, int t
 
 // Issues the loads of one tile (lane 0 of the producer warp): the segment's
 // query rows when the segment changes, then the key pages and scales into the
-// next ring stage, tagged with {tile in segment, segment}.
+// next ring stage, tagged with {tile in segment, segment, segment ordinal}.
+//
+// Query buffer b holds the segments of ordinals b, b + 2, ...  Before it is
+// refilled, the MMAs of the segment it held must be done: every issuer's last
+// tile of that segment has released its ring stage (an issuer's MMAs complete
+// in order), which the producer waits for unless it has already waited for
+// that release when it refilled the stage.
 struct Producer {
     const CUtensorMap* kmap;
     const CUtensorMap* smap;
@@ -295,18 +316,37 @@ struct Producer {
     uint64_t* full;
     uint64_t* empty;
     uint64_t* qfull;
-    uint64_t* qempty;
     volatile int* abort;
     bool fp4;            // MXFP4 codes (either placement): transaction sizes
     bool rg;             // row-group placement: packed boxes per column group
     int cur = -1, i_seg = 0, it = 0;
+    int last00 = -1, last01 = -1, last10 = -1, last11 = -1;   // last tile of query buffer b for issuer w
+
+    __device__ __forceinline__ int last_tile(int b, int w) const {
+        return b ? (w ? last11 : last10) : (w ? last01 : last00);
+    }
+    __device__ __forceinline__ void set_last_tile(int b, int w, int v) {
+        if (b) {
+            if (w) last11 = v; else last10 = v;
+        } else {
+            if (w) last01 = v; else last00 = v;
+        }
+    }
 
     __device__ __forceinline__ bool issue(const ScoreArgs& p, int sg, int j, int p0, int p1) {
         if (sg != cur) {
             cur = sg;
             const int4 si = p.segs[sg];
             const int qb = i_seg & 1;
-            if (!mbar_wait(qempty + qb, ((i_seg >> 1) & 1) ^ 1, abort, p.status)) return false;
+            for (int w = 0; w < kMmaWarps; ++w) {
+                // release of tile l: phase l / kStages of its stage's empty barrier; while
+                // it - l <= kStages the stage's next use (tile l + kStages) is not yet issued
+                const int l = last_tile(qb, w);
+                if (l >= 0 && it - l <= kStages &&
+                    !mbar_wait(empty + l % kStages, (l / kStages) & 1, abort, p.status))
+                    return false;
+                set_last_tile(qb, w, -1);
+            }
             const uint32_t bytes = si.z * (fp4 ? kFp4QRowTx + 128u : kFp8QRowTx);
             mbar_arrive_expect_tx(qfull + qb, bytes);
             uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
@@ -327,7 +367,8 @@ struct Producer {
         }
         const int s = it % kStages;
         if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status)) return false;
-        reinterpret_cast<int2*>(smem + OFF_SINFO)[s] = make_int2(j, sg);
+        reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(j, sg, i_seg - 1, 0);
+        set_last_tile((i_seg - 1) & 1, it % kMmaWarps, it);
         const uint32_t page_tx = (fp4 ? kFp4PageTx : kFp8PageTx) + 256;
         const uint32_t bytes = (p0 >= 0 ? page_tx : 0u) + (p1 >= 0 ? page_tx : 0u);
         if (bytes == 0) {
@@ -363,13 +404,15 @@ struct Producer {
         return true;
     }
 
-    // End of this CTA's sequence: a stage tagged -1 with no copies.
+    // End of this CTA's sequence: one stage tagged -1, with no copies, per issuer.
     __device__ __forceinline__ bool finish(const ScoreArgs& p) {
-        const int s = it % kStages;
-        if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status)) return false;
-        reinterpret_cast<int2*>(smem + OFF_SINFO)[s] = make_int2(-1, -1);
-        mbar_arrive(full + s);
-        ++it;
+        for (int w = 0; w < kMmaWarps; ++w) {
+            const int s = it % kStages;
+            if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status)) return false;
+            reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(-1, -1, -1, 0);
+            mbar_arrive(full + s);
+            ++it;
+        }
         return true;
     }
 };
@@ -427,12 +470,35 @@ __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, 
     __syncwarp();
 }
 
-// Warp 1.  Follows the producer's stage tags; hands each accumulator's tag
-// to the epilogue (and the end-of-sequence tag as the last one).
+// Bounded wait until a release counter reaches `need` (wrap-safe compare);
+// same give-up rules as mbar_wait.
+__device__ __forceinline__ bool count_wait(const uint32_t* c, uint32_t need, volatile int* abort, int32_t* status) {
+    if (static_cast<int>(smem_ld_acquire(c) - need) >= 0) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (static_cast<int>(smem_ld_acquire(c) - need) >= 0) return true;
+        if ((i & 31) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                if (status) atomicOr(status, DSA_STATUS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Warps 1 .. kMmaWarps.  Issuer w follows the stage tags of sequence
+// positions w, w + kMmaWarps, ...; hands each accumulator's tag to the
+// epilogue (its end-of-sequence tag as the last one).  An accumulator is
+// used by both issuers in turn, so its release is a count (four epilogue
+// warps per use) rather than an mbarrier phase, which an issuer running
+// ahead could mistake for a later one.
 __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* full,
-                                         uint64_t* empty, uint64_t* qfull, uint64_t* qempty, uint64_t* tfull,
-                                         uint64_t* tempty, uint64_t* done_bar, volatile int* abort) {
+                                         uint64_t* empty, uint64_t* qfull, uint64_t* tfull, const uint32_t* released,
+                                         uint64_t* done_bar, volatile int* abort) {
     const int lane = threadIdx.x & 31;
+    const int w = (threadIdx.x >> 5) - 1;
     // FP8 keys carry one scale per key: an FP32 power of two, or (FP8-MX) one
     // UE8M0 exponent repeated in the four bytes of the scale word, so the
     // product with the (unscaled) FP8 query is 2^e * sum q8 k8 either way; both
@@ -442,54 +508,49 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
     const bool mx_byte = (p.fmt == DSA_FMT_FP8_MX);
     const bool fp4 = fmt_fp4(p.fmt);
     const bool rg = (p.fmt == DSA_FMT_MXFP4_RG);
-    const int2* sinfo = reinterpret_cast<const int2*>(smem + OFF_SINFO);
+    const int4* sinfo = reinterpret_cast<const int4*>(smem + OFF_SINFO);
     int2* ainfo = reinterpret_cast<int2*>(smem + OFF_AINFO);
-    int cur = -1, qb = 0, i_seg = 0, nrows = 0;
-    for (int it = 0;; ++it) {
+    int cur = -1, qb = 0, nrows = 0;
+    for (int it = w;; it += kMmaWarps) {
         const int s = it % kStages;
         const int a = it % kAcc;
+        const uint32_t need = 4u * static_cast<uint32_t>(it / kAcc);   // releases of its earlier uses
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(full + s, (it / kStages) & 1, abort, p.status))) break;
-        const int2 tag = sinfo[s];
+        const int4 tag = sinfo[s];
         if (tag.y < 0) {
-            // one end tag for each epilogue group (they take alternate accumulators)
-            for (int q = 0; q < kEpiGroups; ++q) {
-                const int aq = (it + q) % kAcc;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty + aq, (((it + q) / kAcc) & 1) ^ 1, abort, p.status)))
-                    break;
-                if (lane == 0) {
-                    ainfo[aq] = tag;
-                    mbar_arrive(tfull + aq);
-                    mbar_arrive(tfull + aq);
-                }
-                __syncwarp();
+            // this issuer's epilogue group takes the end tag
+            if (!__all_sync(0xFFFFFFFFu, count_wait(released + a, need, abort, p.status))) break;
+            if (lane == 0) {
+                ainfo[a] = make_int2(tag.x, tag.y);
+                mbar_arrive(tfull + a * kEpiGroups + w);
+                mbar_arrive(tfull + a * kEpiGroups + w);
             }
+            __syncwarp();
             break;
         }
-        const int seg = tag.y;
-        if (seg != cur) {
-            if (cur >= 0 && lane == 0) tc_commit(qempty + qb);
-            cur = seg;
-            nrows = p.segs[seg].z;
-            qb = i_seg & 1;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(qfull + qb, (i_seg >> 1) & 1, abort, p.status))) break;
+        if (tag.z != cur) {
+            cur = tag.z;
+            nrows = p.segs[tag.y].z;
+            qb = cur & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(qfull + qb, (cur >> 1) & 1, abort, p.status))) break;
             if (fp4) {
                 // Query block scales: line L of the atom holds the words of MMA
                 // rows L, 32 + L, 64 + L, 96 + L (row r * 32 + h = head h of query row r).
                 const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + OFF_QSF + qb * 512);
+                uint8_t* atom = smem + OFF_SFB + (qb * kMmaWarps + w) * 512;
                 uint4 line;
                 line.x = raw[lane];
                 line.y = nrows > 1 ? raw[32 + lane] : 0x7F7F7F7Fu;
                 line.z = nrows > 2 ? raw[64 + lane] : 0x7F7F7F7Fu;
                 line.w = nrows > 3 ? raw[96 + lane] : 0x7F7F7F7Fu;
-                reinterpret_cast<uint4*>(smem + OFF_SFB + qb * 512)[lane] = line;
+                reinterpret_cast<uint4*>(atom)[lane] = line;
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0)
-                    tc_cp_32x128b_warpx4(tmem + TM_SFB + qb * 4, desc_rows16(smem_u32(smem + OFF_SFB + qb * 512)));
+                    tc_cp_32x128b_warpx4(tmem + TM_SFB + (qb * kMmaWarps + w) * 4, desc_rows16(smem_u32(atom)));
             }
-            ++i_seg;
         }
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty + a, ((it / kAcc) & 1) ^ 1, abort, p.status))) break;
+        if (!__all_sync(0xFFFFFFFFu, count_wait(released + a, need, abort, p.status))) break;
         tc_fence_after();
         const uint32_t* rs = reinterpret_cast<const uint32_t*>(smem + OFF_RAWSC + s * 512);
         uint32_t w0, w1, w2, w3;
@@ -535,7 +596,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             } else if (rg) {
                 const uint32_t sfa = tmem + TM_SFA + s * 4;
                 tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
-                const uint32_t sfb = tmem + TM_SFB + qb * 4;
+                const uint32_t sfb = tmem + TM_SFB + (qb * kMmaWarps + w) * 4;
                 const uint32_t ka = smem_u32(smem + OFF_TILES + s * kTileBytes);
                 const uint32_t kb = smem_u32(smem + OFF_QBUF + qb * kQBufBytes);
 #pragma unroll
@@ -547,15 +608,15 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                 const uint32_t sfa = tmem + TM_SFA + s * 4;
                 tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
                 const uint32_t fm = fp4 ? kMmaE2M1 : kMmaE4M3;
-                const uint32_t sfb = tmem + TM_SFB + qb * 4;
+                const uint32_t sfb = tmem + TM_SFB + (qb * kMmaWarps + w) * 4;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc_mx(fm, fm, 128, n, kk, kk), sfa, sfb, kk > 0);
             }
-            ainfo[a] = tag;
+            ainfo[a] = make_int2(tag.x, tag.y);
             tc_commit(empty + s);
-            tc_commit(tfull + a);
-            mbar_arrive(tfull + a);   // releases the key scales and the tag written above
+            tc_commit(tfull + a * kEpiGroups + w);
+            mbar_arrive(tfull + a * kEpiGroups + w);   // releases the key scales and the tag written above
         }
         __syncwarp();
     }
@@ -628,21 +689,21 @@ __device__ __forceinline__ void flush_group_hist(const ScoreArgs& p, uint32_t* g
     group_sync(g);
 }
 
-// Warps 2 .. 2 + kEpiWarps.  Group g = (warp - 2) / 4 drains the accumulators
-// of sequence positions g, g + kEpiGroups, ...; every warp works on its own
-// (per-warp head weights, row bounds in registers, one arrival per tile).
+// Warps kFirstEpiWarp .. + kEpiWarps.  Group g drains the accumulators of
+// sequence positions g, g + kEpiGroups, ...; every warp works on its own
+// (per-warp head weights, row bounds in registers, one release count per tile).
 __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* tfull,
-                                              uint64_t* tempty, volatile int* abort) {
+                                              uint32_t* released, volatile int* abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int group = (warp - 2) >> 2;
+    const int group = (warp - kFirstEpiWarp) >> 2;
     const int quarter = warp & 3;            // TMEM lanes this warp may access
     const int m = quarter * 32 + lane;       // key of the tile this thread owns
-    float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - 2) * (kSegRows * kHeads);
+    float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - kFirstEpiWarp) * (kSegRows * kHeads);
     const int2* ainfo = reinterpret_cast<const int2*>(smem + OFF_AINFO);
     const bool f32scale = !fmt_fp4(p.fmt);   // FP8 and FP8-MX: one scale per key
     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC;
     uint32_t* gh = reinterpret_cast<uint32_t*>(smem + OFF_HIST) + group * kGroupHistWords;
-    const int e = threadIdx.x - 64 - group * 128;   // thread index within the group
+    const int e = threadIdx.x - 32 * kFirstEpiWarp - group * 128;   // thread index within the group
     int cur = -1, row0 = 0, nrows = 0, seg_tiles = 0;
     int end_l = 0;        // lane r < nrows: bound of row row0 + r
     unsigned hist_m = 0;  // bit r: row r gets a histogram
@@ -651,7 +712,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
         const int a = it % kAcc;
         // One decision for the group's four warps: all stop if any wait gave up
         // (they share the histogram and its flush barriers).
-        const bool ok = mbar_wait(tfull + a, (it / kAcc) & 1, abort, p.status);
+        const bool ok = mbar_wait(tfull + a * kEpiGroups + group, (it / (kAcc * kEpiGroups)) & 1, abort, p.status);
         if (group_sync_any(group, !ok)) {
             aborted = true;
             break;
@@ -700,7 +761,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty + a);
+        if (lane == 0) smem_add_release(released + a, 1u);
     }
     if (cur >= 0 && !aborted && hist_m) flush_group_hist(p, gh, group, row0, nrows, hist_m, e);
 }
@@ -714,12 +775,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     uint64_t* qfull = bars + 2 * kStages;
-    uint64_t* qempty = qfull + 2;
-    uint64_t* tfull = qempty + 2;
-    uint64_t* tempty = tfull + kAcc;
-    uint64_t* done_bar = tempty + kAcc;
+    uint64_t* tfull = qfull + 2;
+    uint64_t* done_bar = tfull + kAcc * kEpiGroups;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    uint32_t* released = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 16);   // per accumulator
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
@@ -727,15 +787,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(qfull + b, 1);
-            mbar_init(qempty + b, 1);
-        }
-        for (int b = 0; b < kAcc; ++b) {
-            mbar_init(tfull + b, 2);
-            mbar_init(tempty + b, 4);
-        }
-        mbar_init(done_bar, 1);
+        for (int b = 0; b < 2; ++b) mbar_init(qfull + b, 1);
+        for (int b = 0; b < kAcc * kEpiGroups; ++b) mbar_init(tfull + b, 2);
+        for (int b = 0; b < kAcc; ++b) released[b] = 0u;
+        mbar_init(done_bar, kMmaWarps);
         *abort = 0;
         mbar_fence_init();
         tma_prefetch(&kmap);
@@ -758,13 +813,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int T = args.claim[-1], Ts = args.claim[1];
         const int t0 = range.x, t1 = range.y, S = range.w;
         const int seg = (t0 < t1 && range.z < 0) ? find_segment(args.seg_prefix, S, t0) : range.z;
-        Producer pr{&kmap, &smap, &qmap, smem, full, empty, qfull, qempty, abort, fmt_fp4(args.fmt),
+        Producer pr{&kmap, &smap, &qmap, smem, full, empty, qfull, abort, fmt_fp4(args.fmt),
                     args.fmt == DSA_FMT_MXFP4_RG};
         producer_role(pr, args, t0, t1, seg, S, Ts, T);
-    } else if (warp == 1) {
-        mma_role(args, smem, tmem, full, empty, qfull, qempty, tfull, tempty, done_bar, abort);
+    } else if (warp < kFirstEpiWarp) {
+        mma_role(args, smem, tmem, full, empty, qfull, tfull, released, done_bar, abort);
     } else {
-        epilogue_role(args, smem, tmem, tfull, tempty, abort);
+        epilogue_role(args, smem, tmem, tfull, released, abort);
     }
     tc_fence_before();
     __syncthreads();
