@@ -100,11 +100,36 @@ typedef enum {
  *           DSA_FMT_MXFP4: head h's 64 bytes of E2M1 pairs at h * 64 (column 2j in the
  *             low nibble of byte j), its four UE8M0 bytes (column block b at byte b)
  *             at 2048 + h * 4; bytes 2176..4095 are not written.
+ *           DSA_FMT_MXFP4_RG: the same pairs; the UE8M0 byte of block b of head h
+ *             at 2048 + b * 64 + h (the row-group order of dsa_quantize_queries_rg);
+ *             the slots of heads 32..63 and bytes 2304..4095 are not written.
  *   w_out   BF16 [rows][32]: FP8: BF16(wv * 2^e / 64); MXFP4: BF16(wv / 64).
  */
 int dsa_quantize_query(int fmt, const void* q, int64_t q_row_stride,
                        const void* wv, int64_t wv_row_stride, int64_t rows,
                        void* q_out, void* w_out, void* stream);
+
+/*
+ * dsa_quantize_queries_rg - MXFP4 of [rows, heads, 128] queries in the
+ * row-group layout, no scale folded into head weights.
+ *
+ * Page "amd.ops.fp4_indexer": quantize_queries (payload [rows, heads, 64],
+ * scales [rows, 1, 4, 16, 4]; heads 16, 32 or 64).  The page fixes the scale
+ * tensor's shape but not its order; the order taken is group-major, like the
+ * cache's scale view [pages, 1, 4, 64]: the byte of column block g of head h at
+ * flat position g * 64 + h of the row's 256 bytes.
+ *
+ *   q        BF16, row r head h column c at q[r * q_row_stride + h * q_head_stride + c];
+ *            q_head_stride >= 128 and both strides multiples of 4 elements; q 8-byte aligned.
+ *   heads    16, 32 or 64 (else DSA_ERR_UNSUPPORTED).
+ *   payload  uint8 [rows][heads][64], 2-byte aligned: head h's E2M1 pairs (column 2j
+ *            in the low nibble of byte j), codes of v / 2^e for its block scale 2^e.
+ *   scales   uint8 [rows][256]; the slots of heads >= `heads` are written 0.
+ * The codec is dsa_quantize_query's MXFP4 one, bit for bit.
+ */
+int dsa_quantize_queries_rg(const void* q, int64_t q_row_stride, int64_t q_head_stride,
+                            int64_t heads, int64_t rows, void* payload, void* scales,
+                            void* stream);
 
 /*
  * dsa_insert_key - LayerNorm (FP32) + BF16 + quantise + insert of indexer keys.

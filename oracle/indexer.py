@@ -50,6 +50,11 @@ FORMATS = ("fp8", "fp8_mx", "mxfp4", "mxfp4_rg")
 # section: payload byte j of column group g of token t at g * 1024 + t * 16 + j,
 # the group's UE8M0 byte at 4096 + g * 64 + t (A23).
 RG_GROUP_BYTES, RG_SCALE_GROUP = 1024, 64
+# Row-group query scales (page *amd.ops.fp4_indexer*, ``quantize_queries``: a
+# [rows, 1, 4, 16, 4] uint8 tensor, 256 bytes a row): the scale of block g of
+# head h at g * 64 + h, group-major like the cache's scale views (A27).
+RG_QUERY_HEAD_SLOTS = 64
+RG_QUERY_HEADS = (16, 32, 64)
 
 
 def _fp4(fmt: str) -> bool:
@@ -91,7 +96,10 @@ def quantize_query(fmt: str, q, wv):
     Returns (q_rows uint8 [rows, 4096], w float32 [rows, 32] holding BF16 values).
     FP8 rows hold head h's 128 E4M3 codes at ``h * 128``.  MXFP4 rows hold
     head h's E2M1 pairs at ``h * 64`` and its four UE8M0 bytes (block b at
-    byte b, A5) at ``2048 + h * 4``; bytes from 2176 on are left zero."""
+    byte b, A5) at ``2048 + h * 4``; bytes from 2176 on are left zero.
+    Row-group MXFP4 ("mxfp4_rg") rows hold the same pairs and the scale of
+    block b of head h at ``2048 + b * 64 + h`` (A27); the slots of heads 32..63
+    and bytes from 2304 on are left zero."""
     q = np.asarray(q, dtype=np.float32)
     wv = np.asarray(wv, dtype=np.float32)
     rows = q.shape[0]
@@ -109,11 +117,39 @@ def quantize_query(fmt: str, q, wv):
         e = mx_scale_exponent(np.abs(blocks).max(axis=3))                   # [rows, 32, 4]
         codes = e2m1_encode(blocks * np.ldexp(1.0, -e)[..., None]).reshape(rows, HEADS, DIM)
         out[:, :FP4_SCALES] = pack_e2m1(codes).reshape(rows, FP4_SCALES)
-        out[:, FP4_SCALES:FP4_QUERY_ROW] = (e + 127).astype(np.uint8).reshape(rows, HEADS * 4)
+        if fmt == "mxfp4_rg":
+            sc = np.zeros((rows, 4, RG_QUERY_HEAD_SLOTS), np.uint8)
+            sc[:, :, :HEADS] = (e + 127).astype(np.uint8).transpose(0, 2, 1)
+            out[:, FP4_SCALES:FP4_SCALES + sc.shape[1] * sc.shape[2]] = sc.reshape(rows, -1)
+        else:
+            out[:, FP4_SCALES:FP4_QUERY_ROW] = (e + 127).astype(np.uint8).reshape(rows, HEADS * 4)
         w = bf16_round((wv * np.float32(FP4_WEIGHT)).astype(np.float32))
     else:
         raise ValueError(f"unknown format {fmt!r}")
     return out, w
+
+
+def quantize_queries(q):
+    """Page *amd.ops.fp4_indexer*, ``quantize_queries``: MXFP4 of q float32
+    [rows, heads, 128] (BF16 values), heads in {16, 32, 64}, with no scale
+    folded into head weights.  Returns (payload uint8 [rows, heads, 64]: head
+    h's E2M1 pairs, column 2j in the low nibble of byte j; scales uint8
+    [rows, 1, 4, 16, 4]: the UE8M0 byte of block g of head h at flat position
+    g * 64 + h of the row's 256 bytes, A27; slots of heads >= ``heads`` zero).
+    The codec is the one of ``quantize_query``'s MXFP4 rows."""
+    q = np.asarray(q, dtype=np.float32)
+    if q.ndim != 3 or q.shape[2] != DIM:
+        raise ValueError("queries must be [rows, heads, 128]")
+    rows, heads = q.shape[0], q.shape[1]
+    if heads not in RG_QUERY_HEADS:
+        raise ValueError("row-group queries support 16, 32 or 64 heads")
+    blocks = q.reshape(rows, heads, 4, 32).astype(np.float64)
+    e = mx_scale_exponent(np.abs(blocks).max(axis=3))                       # [rows, heads, 4]
+    codes = e2m1_encode(blocks * np.ldexp(1.0, -e)[..., None]).reshape(rows, heads, DIM)
+    payload = pack_e2m1(codes).reshape(rows, heads, DIM // 2)
+    flat = np.zeros((rows, 4, RG_QUERY_HEAD_SLOTS), np.uint8)
+    flat[:, :, :heads] = (e + 127).astype(np.uint8).transpose(0, 2, 1)
+    return payload, flat.reshape(rows, 1, 4, 16, 4)
 
 
 # --------------------------------------------------------------------------
@@ -279,7 +315,11 @@ def decode_query(fmt: str, q_row) -> np.ndarray:
     if fmt in ("fp8", "fp8_mx"):
         return e4m3_decode(q_row[:Q_ROW_BYTES]).reshape(HEADS, DIM)
     codes = unpack_e2m1(q_row[:FP4_SCALES].reshape(HEADS, DIM // 2))
-    e = q_row[FP4_SCALES:FP4_QUERY_ROW].reshape(HEADS, 4).astype(np.int64) - 127
+    if fmt == "mxfp4_rg":
+        sc = q_row[FP4_SCALES:FP4_SCALES + 4 * RG_QUERY_HEAD_SLOTS].reshape(4, RG_QUERY_HEAD_SLOTS)
+        e = sc[:, :HEADS].T.astype(np.int64) - 127
+    else:
+        e = q_row[FP4_SCALES:FP4_QUERY_ROW].reshape(HEADS, 4).astype(np.int64) - 127
     return (e2m1_decode(codes).reshape(HEADS, 4, 32) * np.ldexp(1.0, e)[..., None]).reshape(HEADS, DIM)
 
 

@@ -10,6 +10,7 @@ from .dsa import (  # noqa: F401
     FORMATS,
     decode_layout,
     insert_key,
+    quantize_queries_rg,
     quantize_query,
     score_paged,
     topk,

@@ -23,6 +23,8 @@ constexpr int kFp4KeyBytes = kPage * kDim / 2;    // 4096: codes of one MXFP4 pa
 // 64 scale bytes at 4096 + g * 64.
 constexpr int kRgGroupBytes = kPage * 16;
 constexpr int kRgScaleGroup = kPage;
+// Row-group query scales: block g of head slot h at g * 64 + h (256 bytes a row).
+constexpr int kRgQuerySlots = 64;
 
 // MXFP4 codes in either placement.
 __host__ __device__ __forceinline__ bool fmt_fp4(int fmt) {

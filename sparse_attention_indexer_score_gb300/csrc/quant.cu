@@ -47,6 +47,22 @@ __device__ __forceinline__ int mx_exponent(float amax) {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// MXFP4 of a 128-column head held by a warp (lane l: columns 4l..4l+3; amax:
+// the lane's max |x|): returns the lane's two bytes of E2M1 pairs (column 4l
+// in the low nibble) and sets *scale_byte to the UE8M0 byte of its 32-column
+// block (8 lanes per block).
+__device__ __forceinline__ uint32_t mxfp4_lane(float x0, float x1, float x2, float x3, float amax,
+                                               uint32_t* scale_byte) {
+#pragma unroll
+    for (int d = 4; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
+    const int e = mx_exponent(amax);
+    const float inv = exp2i(-e);
+    const uint32_t b01 = e2m1x2(__fmul_rn(x0, inv), __fmul_rn(x1, inv));
+    const uint32_t b23 = e2m1x2(__fmul_rn(x2, inv), __fmul_rn(x3, inv));
+    *scale_byte = static_cast<uint32_t>(e + 127);
+    return b01 | (b23 << 8);
+}
+
 // ----------------------------------------------------------------- a1: query rows
 // One warp per (row, head); lane l holds columns 4l..4l+3.  `block` is the
 // block index within this part of the grid (256 threads per block).
@@ -78,23 +94,21 @@ __device__ __forceinline__ void quantize_query_block(int fmt, const uint16_t* __
             w_out[row * kHeads + head] = __float2bfloat16_rn(fold);
         }
     } else {
-        // 8 lanes hold one 32-column block
-#pragma unroll
-        for (int d = 4; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
-        const int e = mx_exponent(amax);
-        const float inv = exp2i(-e);
-        const uint32_t b01 = e2m1x2(__fmul_rn(x0, inv), __fmul_rn(x1, inv));
-        const uint32_t b23 = e2m1x2(__fmul_rn(x2, inv), __fmul_rn(x3, inv));
+        uint32_t byte;
         *reinterpret_cast<uint16_t*>(out_row + head * (kDim / 2) + lane * 2) =
-            static_cast<uint16_t>(b01 | (b23 << 8));
-        const uint32_t byte = static_cast<uint32_t>(e + 127);
-        const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, byte, 8);
-        const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, byte, 16);
-        const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, byte, 24);
-        if (lane == 0) {
-            *reinterpret_cast<uint32_t*>(out_row + kFp4Scales + head * 4) = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            w_out[row * kHeads + head] = __float2bfloat16_rn(__fmul_rn(wvf, 0.015625f));
+            static_cast<uint16_t>(mxfp4_lane(x0, x1, x2, x3, amax, &byte));
+        if (fmt == DSA_FMT_MXFP4_RG) {
+            // row-group scales: block g of head h at g * 64 + h
+            if ((lane & 7) == 0) out_row[kFp4Scales + (lane >> 3) * kRgQuerySlots + head] = static_cast<uint8_t>(byte);
+        } else {
+            const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, byte, 8);
+            const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, byte, 16);
+            const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, byte, 24);
+            if (lane == 0)
+                *reinterpret_cast<uint32_t*>(out_row + kFp4Scales + head * 4) =
+                    byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
         }
+        if (lane == 0) w_out[row * kHeads + head] = __float2bfloat16_rn(__fmul_rn(wvf, 0.015625f));
     }
 }
 
@@ -224,6 +238,35 @@ __global__ void __launch_bounds__(256) insert_key_kernel(int fmt, const uint16_t
     insert_key_block(fmt, k, k_stride, gamma, beta, eps, slots, n, cache, page_stride, num_pages, status, blockIdx.x);
 }
 
+// ----------------------------------------------------------------- row-group queries
+// Page "amd.ops.fp4_indexer", quantize_queries: one warp per (row, head slot
+// of 64); slots past `heads` only clear their four scale bytes.
+__global__ void __launch_bounds__(256) quantize_queries_rg_kernel(const uint16_t* __restrict__ q, int64_t row_stride,
+                                                                  int64_t head_stride, int heads, int64_t rows,
+                                                                  uint8_t* __restrict__ payload,
+                                                                  uint8_t* __restrict__ scales) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= rows * kRgQuerySlots) return;
+    const int64_t row = gw / kRgQuerySlots;
+    const int h = static_cast<int>(gw % kRgQuerySlots);
+    uint8_t* srow = scales + row * (4 * kRgQuerySlots);
+    if (h >= heads) {
+        if (lane < 4) srow[lane * kRgQuerySlots + h] = 0;
+        return;
+    }
+    const uint2 raw = *reinterpret_cast<const uint2*>(q + row * row_stride + h * head_stride + lane * 4);
+    const float x0 = bf16_bits_to_f32(raw.x & 0xFFFFu), x1 = bf16_bits_to_f32(raw.x >> 16);
+    const float x2 = bf16_bits_to_f32(raw.y & 0xFFFFu), x3 = bf16_bits_to_f32(raw.y >> 16);
+    const float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+    uint32_t byte;
+    *reinterpret_cast<uint16_t*>(payload + (row * heads + h) * (kDim / 2) + lane * 2) =
+        static_cast<uint16_t>(mxfp4_lane(x0, x1, x2, x3, amax, &byte));
+    if ((lane & 7) == 0) srow[(lane >> 3) * kRgQuerySlots + h] = static_cast<uint8_t>(byte);
+}
+
 // ----------------------------------------------------------------- fused step preparation
 // One launch for the three independent parts of a decode step's preparation:
 // block 0 computes the request starts and row bounds, the next blocks insert
@@ -334,6 +377,24 @@ extern "C" int dsa_quantize_query(int fmt, const void* q, int64_t q_row_stride, 
                                        static_cast<cudaStream_t>(stream), fmt, static_cast<const uint16_t*>(q),
                                        q_row_stride, static_cast<const uint16_t*>(wv), wv_row_stride, rows,
                                        static_cast<uint8_t*>(q_out), static_cast<__nv_bfloat16*>(w_out));
+    return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+extern "C" int dsa_quantize_queries_rg(const void* q, int64_t q_row_stride, int64_t q_head_stride, int64_t heads,
+                                       int64_t rows, void* payload, void* scales, void* stream) {
+    if (heads != 16 && heads != 32 && heads != 64) return DSA_ERR_UNSUPPORTED;
+    if (rows < 0) return DSA_ERR_INVALID;
+    if (rows == 0) return DSA_OK;
+    if (!q || !payload || !scales) return DSA_ERR_INVALID;
+    if (q_head_stride < kDim || q_head_stride % 4 || q_row_stride < 0 || q_row_stride % 4) return DSA_ERR_INVALID;
+    if (!aligned(q, 8) || !aligned(payload, 2)) return DSA_ERR_INVALID;
+    if (rows > (int64_t(1) << 40) / (kRgQuerySlots * 32)) return DSA_ERR_UNSUPPORTED;
+    const int64_t blocks = (rows * kRgQuerySlots * 32 + 255) / 256;
+    if (blocks > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+    const cudaError_t err =
+        launch_pdl(quantize_queries_rg_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                   static_cast<cudaStream_t>(stream), static_cast<const uint16_t*>(q), q_row_stride, q_head_stride,
+                   static_cast<int>(heads), rows, static_cast<uint8_t*>(payload), static_cast<uint8_t*>(scales));
     return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -50,6 +50,9 @@ constexpr uint32_t kFp8QRowTx = kQRowBytes, kFp4QRowTx = kQRowBytes / 2;
 constexpr int kRgTileGroup = 2 * kRgGroupBytes;
 constexpr int kRgQChunk = 2048;
 constexpr int kSegRows = 4;                   // query rows per segment
+// Raw query scale bytes staged per row: 32 heads x 4 (token-major MXFP4) or
+// the row's 4 x 64 row-group slots.
+constexpr int kQsfRow = 128, kQsfRowRg = 4 * kRgQuerySlots;
 constexpr int kQBufBytes = kSegRows * kQRowBytes;
 // Two epilogue groups of four warps (one per TMEM lane quarter) drain
 // alternate tiles, so two accumulators are read out at once.
@@ -76,7 +79,8 @@ constexpr int OFF_QBUF = OFF_TILES + kStages * kTileBytes;
 constexpr int OFF_RAWSC = OFF_QBUF + 2 * kQBufBytes;
 constexpr int OFF_SFA = OFF_RAWSC + kStages * 512;
 constexpr int OFF_QSF = OFF_SFA + kStages * 512;
-constexpr int OFF_SFB = OFF_QSF + 2 * 512;
+constexpr int kQsfBytes = 4 * kQsfRowRg;                 // raw query scales of a buffer's rows
+constexpr int OFF_SFB = OFF_QSF + 2 * kQsfBytes;
 constexpr int OFF_KS = OFF_SFB + 2 * kMmaWarps * 512;   // query scale atoms per (buffer, issuer)
 constexpr int OFF_W = OFF_KS + kAcc * 128 * 4;            // float[kEpiWarps][4 rows][32 heads]: w per warp
 // Score histogram of each epilogue group for its current segment: 4 rows x
@@ -347,7 +351,8 @@ struct Producer {
                     return false;
                 set_last_tile(qb, w, -1);
             }
-            const uint32_t bytes = si.z * (fp4 ? kFp4QRowTx + 128u : kFp8QRowTx);
+            const uint32_t qsf = rg ? kQsfRowRg : kQsfRow;
+            const uint32_t bytes = si.z * (fp4 ? kFp4QRowTx + qsf : kFp8QRowTx);
             mbar_arrive_expect_tx(qfull + qb, bytes);
             uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
             for (int r = 0; r < si.z; ++r) {
@@ -360,8 +365,8 @@ struct Producer {
                     tma_load_3d(qdst + r * kQRowBytes, qmap, 0, 0, si.y + r, qfull + qb);
                 }
                 if (fp4)
-                    bulk_load(smem + OFF_QSF + qb * 512 + r * 128,
-                              p.q_rows + static_cast<int64_t>(si.y + r) * kQRowBytes + kFp4Scales, 128, qfull + qb);
+                    bulk_load(smem + OFF_QSF + qb * kQsfBytes + r * qsf,
+                              p.q_rows + static_cast<int64_t>(si.y + r) * kQRowBytes + kFp4Scales, qsf, qfull + qb);
             }
             ++i_seg;
         }
@@ -536,13 +541,23 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             if (fp4) {
                 // Query block scales: line L of the atom holds the words of MMA
                 // rows L, 32 + L, 64 + L, 96 + L (row r * 32 + h = head h of query row r).
-                const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + OFF_QSF + qb * 512);
+                const uint8_t* raw = smem + OFF_QSF + qb * kQsfBytes;
+                // word of head `lane` of row r: token-major rows hold it as is; row-group
+                // rows hold block g's byte at g * 64 + head
+                auto word = [&](int r) -> uint32_t {
+                    if (r >= nrows) return 0x7F7F7F7Fu;
+                    if (!rg) return reinterpret_cast<const uint32_t*>(raw + r * kQsfRow)[lane];
+                    const uint8_t* b = raw + r * kQsfRowRg + lane;
+                    return static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[kRgQuerySlots]) << 8) |
+                           (static_cast<uint32_t>(b[2 * kRgQuerySlots]) << 16) |
+                           (static_cast<uint32_t>(b[3 * kRgQuerySlots]) << 24);
+                };
                 uint8_t* atom = smem + OFF_SFB + (qb * kMmaWarps + w) * 512;
                 uint4 line;
-                line.x = raw[lane];
-                line.y = nrows > 1 ? raw[32 + lane] : 0x7F7F7F7Fu;
-                line.z = nrows > 2 ? raw[64 + lane] : 0x7F7F7F7Fu;
-                line.w = nrows > 3 ? raw[96 + lane] : 0x7F7F7F7Fu;
+                line.x = word(0);
+                line.y = word(1);
+                line.z = word(2);
+                line.w = word(3);
                 reinterpret_cast<uint4*>(atom)[lane] = line;
                 fence_proxy_async_smem();
                 __syncwarp();

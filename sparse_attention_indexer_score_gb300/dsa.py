@@ -31,6 +31,7 @@ _P = _c.c_void_p
 _I64 = _c.c_int64
 _SIGS = {
     "dsa_quantize_query": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P]),
+    "dsa_quantize_queries_rg": (_c.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P]),
     "dsa_insert_key": (_c.c_int, [_c.c_int, _P, _I64, _P, _P, _c.c_float, _P, _I64, _P, _I64, _I64, _P, _P]),
     "dsa_decode_layout": (_c.c_int, [_P, _I64, _P, _I64, _I64, _P, _P, _P]),
     "dsa_prepare_step": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _c.c_float, _P,
@@ -136,6 +137,21 @@ def quantize_query(fmt: str, q: torch.Tensor, wv: torch.Tensor,
                                   _ptr(q_out), _ptr(w_out), _stream(q.device))
     _check(rc, "dsa_quantize_query")
     return q_out, w_out
+
+
+def quantize_queries_rg(q: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """q: BF16 [rows, heads, 128], heads 16, 32 or 64, unit column stride.
+    Returns (uint8 [rows, heads, 64] E2M1 payload, uint8 [rows, 1, 4, 16, 4]
+    row-group block scales)."""
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != 128 or q.stride(2) != 1:
+        raise ValueError("q must be BF16 [rows, heads, 128] with contiguous heads")
+    rows, heads = q.shape[0], q.shape[1]
+    payload = torch.empty((rows, heads, 64), dtype=torch.uint8, device=q.device)
+    scales = torch.empty((rows, 1, 4, 16, 4), dtype=torch.uint8, device=q.device)
+    rc = lib().dsa_quantize_queries_rg(_ptr(q), q.stride(0), q.stride(1), heads, rows, _ptr(payload),
+                                       _ptr(scales), _stream(q.device))
+    _check(rc, "dsa_quantize_queries_rg")
+    return payload, scales
 
 
 def insert_key(fmt: str, k: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,

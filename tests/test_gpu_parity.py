@@ -12,8 +12,8 @@ FMTS = ["fp8", "fp8_mx", "mxfp4", "mxfp4_rg"]
 
 
 def _used(fmt):
-    """Bytes of a quantised query row that carry data."""
-    return 2176 if fmt in ("mxfp4", "mxfp4_rg") else 4096
+    """Bytes of a quantised query row that carry data (row-group: 4 x 64 scale slots)."""
+    return {"mxfp4": 2176, "mxfp4_rg": 2304}.get(fmt, 4096)
 
 
 def _special_queries(rng, rows):
@@ -45,6 +45,29 @@ def test_quantize_query_bit_exact(cuda_lib, fmt):
     assert np.array_equal(got[:, :used], want_rows[:, :used])
     assert not got[:, used:].any()
     assert np.array_equal(w.float().cpu().numpy(), want_w)
+
+
+@pytest.mark.parametrize("heads", [16, 32, 64])
+def test_quantize_queries_rg_bit_exact(cuda_lib, heads):
+    """Page "amd.ops.fp4_indexer", quantize_queries: payload and row-group
+    scales equal the oracle's byte for byte, in a strided input view."""
+    import torch
+    rng = np.random.default_rng(10 + heads)
+    rows = 29
+    x = rng.standard_normal((rows, heads, 128)).astype(np.float32)
+    x[0, 0] = 0.0
+    x[0, 1, :32] = 0.0
+    x[0, 2] *= 1e30
+    x[1] *= np.float32(2.0 ** -100)
+    x[2, :, ::5] = -0.0
+    u = x.view(np.uint32).astype(np.uint64)
+    qb = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    big = torch.zeros((rows, heads, 160), dtype=torch.bfloat16, device="cuda")   # head stride 160
+    big[:, :, :128] = bf16_tensor(qb, "cuda")
+    payload, scales = cuda_lib.quantize_queries_rg(big[:, :, :128])
+    want_p, want_s = O.quantize_queries(bf16_bits_to_f32(qb))
+    assert np.array_equal(payload.cpu().numpy(), want_p)
+    assert np.array_equal(scales.cpu().numpy(), want_s)
 
 
 @pytest.mark.parametrize("fmt", FMTS)
