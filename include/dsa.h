@@ -272,13 +272,10 @@ size_t dsa_workspace_size(int fmt, int64_t rows, int64_t num_requests,
  * score_paged (block table, query_starts, row_ends, logits width
  * max_pages * 64); page "cutedsl.dsa.overlap" (scoring and top-k).
  *
- *   q_rows        uint8 [rows][4096] from dsa_quantize_query (16-byte aligned;
- *                 32-byte aligned for DSA_FMT_MXFP4).
+ *   q_rows        uint8 [rows][4096] from dsa_quantize_query, 16-byte aligned.
  *   w             BF16 [rows][32] head weights from dsa_quantize_query.
- *   cache         paged cache written by dsa_insert_key (same layout rules;
- *                 for MXFP4 the base must be 32-byte aligned and page_stride a
- *                 multiple of 32; for MXFP4_RG 16-byte alignment and stride
- *                 multiples of 16 suffice).
+ *   cache         paged cache written by dsa_insert_key (same layout rules:
+ *                 base 16-byte aligned, page_stride a multiple of 16).
  *   block_table   int32, request q's page j at block_table[q * bt_stride + j],
  *                 max_pages columns.
  *   starts        int32 [num_requests + 1]: rows starts[q] .. starts[q+1]-1 form

@@ -211,17 +211,6 @@ __device__ __forceinline__ void tc_mma_f8f6f4(uint32_t d, uint64_t a, uint64_t b
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// Block-scaled variant: one UE8M0 scale per 32 K-elements of each row of A
-// and of B, read from tensor memory.
-__device__ __forceinline__ void tc_mma_mxf8f6f4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                                uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], "
-        "p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-        : "memory");
-}
 // Packed E2M1 operands (two per byte, K = 64 per instruction) with two UE8M0
 // scales per row per instruction: bytes id and id + 1 (id = 0 or 2) of each
 // row's scale word, for K-elements 0-31 and 32-63.
@@ -294,6 +283,17 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
     return d;
 }
+// Descriptor of a K-major operand with 64-byte rows in 64-byte-swizzled
+// 8-row atoms of 512 bytes, as TMA writes them with CU_TENSOR_MAP_SWIZZLE_64B.
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(512 >> 4) << 32;             // stride byte offset: next 8 rows
+    d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+    d |= static_cast<uint64_t>(4) << 61;                    // 64-byte swizzle
+    return d;
+}
 // Descriptor of an unswizzled 32-row x 16-byte matrix (rows 16 bytes apart),
 // the source of tc_cp_32x128b_warpx4.
 __device__ __forceinline__ uint64_t desc_rows16(uint32_t saddr) {
@@ -322,15 +322,15 @@ __host__ __device__ __forceinline__ uint32_t idesc_f8f6f4(uint32_t a_fmt, uint32
                                                            uint32_t n) {
     return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
-// Instruction descriptor, kind::mxf8f6f4 with UE8M0 scales; sf ids pick the
-// byte of each 32-bit scale column.
+// Instruction descriptor of the block-scaled kinds with UE8M0 scales (FP32
+// accumulate, K-major A and B); sf ids pick the first byte of each row's
+// scale word that the instruction uses (0 or 2 for kind::mxf4's two scales).
 __host__ __device__ __forceinline__ uint32_t idesc_mx(uint32_t a_fmt, uint32_t b_fmt, uint32_t m, uint32_t n,
                                                        uint32_t a_sf_id, uint32_t b_sf_id) {
     return (b_sf_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | (1u << 23) |
            ((m >> 4) << 24) | (a_sf_id << 29);
 }
 constexpr uint32_t kMmaE4M3 = 0;
-constexpr uint32_t kMmaE2M1 = 5;
 constexpr uint32_t kMmaMxf4E2M1 = 1;   // the E2M1 code of kind::mxf4
 
 // ----------------------------------------------------------------- top-k keys

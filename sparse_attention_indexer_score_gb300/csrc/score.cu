@@ -23,25 +23,26 @@
 //              top-k pass.
 //
 // Formats: FP8 and FP8-MX use kind::f8f6f4 (E4M3 x E4M3) and multiply the
-// per-key scale in the epilogue.  MXFP4 uses kind::mxf8f6f4 with UE8M0 block
-// scales in TMEM (one per 32 columns); its keys and queries are unpacked by
-// TMA into the 16-byte-aligned E2M1 layout that MMA kind reads.  Row-group
-// MXFP4 keeps the codes packed: each column group's 64 x 16 bytes of a page
-// is one TMA box that lands as 8 unswizzled core matrices, the two pages'
-// boxes of a group side by side, and kind::mxf4 (K = 64, two scales per row)
-// reads groups 2m and 2m + 1 in instruction m.
+// per-key scale in the epilogue.  MXFP4 keeps its codes packed and uses
+// kind::mxf4 (K = 64, two UE8M0 scales per row from TMEM, scale bytes 2m and
+// 2m + 1 in instruction m).  Token-major pages are 64 rows of 64 bytes, which
+// one TMA box lands in the 64-byte-swizzled K-major layout; as packed stages
+// take half the shared memory, that format runs a 16-stage ring.  Row-group
+// pages place each column group's 64 x 16 bytes together: one TMA box per
+// group lands as 8 unswizzled core matrices, the two pages' boxes of a group
+// side by side.
 #include "host.h"
 #include "scan.cuh"
 
 namespace dsa {
 
-constexpr int kStages = 8;
+constexpr int kStages = 8;                    // ring stages of 16 KB (FP8 codes)
+constexpr int kMaxStages = 16;                // ring stages of 8 KB (packed token-major MXFP4)
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * 128;   // codes of 128 keys in shared memory
-constexpr int kPageSmem = 64 * 128;           // one page's codes in shared memory
-// Transaction bytes of one TMA copy count the packed source: a 64-key MXFP4
-// page (16U4_ALIGN16B, unpacked to 8192 bytes of shared memory) counts 4096,
-// an MXFP4 query row 2048.
+constexpr int kPageSmem = 64 * 128;           // one FP8 page's codes in shared memory
+// Transaction bytes of one TMA copy: an MXFP4 page's codes 4096, an MXFP4
+// query row 2048 (packed, as in shared memory).
 constexpr uint32_t kFp8PageTx = 64 * 128, kFp4PageTx = 64 * 64;
 constexpr uint32_t kFp8QRowTx = kQRowBytes, kFp4QRowTx = kQRowBytes / 2;
 // Row-group MXFP4 in shared memory: a tile's column group g at g * 2048 (the
@@ -64,7 +65,8 @@ constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kMmaWarps = 2;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kScoreThreads = 32 * (kFirstEpiWarp + kEpiWarps);
-static_assert(kMmaWarps == kEpiGroups && kStages % kMmaWarps == 0, "issuer w owns stages and group w");
+static_assert(kMmaWarps == kEpiGroups && kStages % kMmaWarps == 0 && kMaxStages % kMmaWarps == 0,
+              "issuer w owns stages and group w");
 constexpr int kAcc = 3;                       // TMEM accumulators in flight (MMA latency is hidden behind 2)
 constexpr int kPlanSmemSegs = 4096;           // segments whose tile prefix the plan keeps on chip
 // Tile assignment: every CTA owns an equal contiguous range of the first
@@ -76,9 +78,9 @@ constexpr int kChunkTiles = 4;
 
 constexpr int OFF_TILES = 0;
 constexpr int OFF_QBUF = OFF_TILES + kStages * kTileBytes;
-constexpr int OFF_RAWSC = OFF_QBUF + 2 * kQBufBytes;
-constexpr int OFF_SFA = OFF_RAWSC + kStages * 512;
-constexpr int OFF_QSF = OFF_SFA + kStages * 512;
+constexpr int OFF_RAWSC = OFF_QBUF + 2 * kQBufBytes;   // key scales per stage
+constexpr int OFF_SFA = OFF_RAWSC + kMaxStages * 512;
+constexpr int OFF_QSF = OFF_SFA + kMaxStages * 512;
 constexpr int kQsfBytes = 4 * kQsfRowRg;                 // raw query scales of a buffer's rows
 constexpr int OFF_SFB = OFF_QSF + 2 * kQsfBytes;
 constexpr int OFF_KS = OFF_SFB + 2 * kMmaWarps * 512;   // query scale atoms per (buffer, issuer)
@@ -90,25 +92,36 @@ constexpr int OFF_W = OFF_KS + kAcc * 128 * 4;            // float[kEpiWarps][4 
 constexpr int kHistFlushTiles = 256;
 constexpr int OFF_HIST = OFF_W + kEpiWarps * kSegRows * kHeads * 4;
 constexpr int kGroupHistWords = kSegRows * kHistBins / 2;
-// int4[kStages]: {tile in segment, segment, segment ordinal in this CTA's sequence}
+// int4[kMaxStages]: {tile in segment, segment, segment ordinal in this CTA's sequence}
 constexpr int OFF_SINFO = OFF_HIST + kEpiGroups * kGroupHistWords * 4;
-constexpr int OFF_AINFO = OFF_SINFO + kStages * 16;       // int2[kAcc]: {tile in segment, segment} per accumulator
+constexpr int OFF_AINFO = OFF_SINFO + kMaxStages * 16;       // int2[kAcc]: {tile in segment, segment} per accumulator
 constexpr int OFF_BAR = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;
 // full, empty, qfull, tfull (per accumulator and epilogue group), done.  A
 // group's accumulator barrier is used by the sequence positions it, it + 6, ...
 // of that group alone: one barrier per accumulator, filled by both issuers,
 // could show a group a phase of the other group's fill (the two issuers'
 // MMAs complete in no common order) and its parity wait would take it.
-constexpr int kNumBars = 2 * kStages + 2 + kAcc * kEpiGroups + 1;
+constexpr int kNumBars = 2 * kMaxStages + 2 + kAcc * kEpiGroups + 1;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;       // TMEM address, abort flag, then released[kAcc]
 constexpr int kScoreSmem = OFF_MISC + 32 + 1024;       // + slack to align the base to 1024
 static_assert(kScoreSmem <= 227 * 1024, "scoring CTA exceeds the shared memory of an SM");
 
 // TMEM columns: kAcc accumulators of up to 128 columns, then scale factors.
 constexpr uint32_t TM_ACC = 0;
-constexpr uint32_t TM_SFA = kAcc * 128;           // kStages x 4 columns
-constexpr uint32_t TM_SFB = TM_SFA + 4 * kStages; // (2 buffers x kMmaWarps) x 4 columns
+constexpr uint32_t TM_SFA = kAcc * 128;              // kMaxStages x 4 columns
+constexpr uint32_t TM_SFB = TM_SFA + 4 * kMaxStages; // (2 buffers x kMmaWarps) x 4 columns
 constexpr uint32_t TM_COLS = 512;
+
+// Ring geometry of a format: packed token-major MXFP4 tiles take half the
+// shared memory of the others, so twice as many are in flight.
+// Stage counts are powers of two: position it uses stage it & (n - 1) in its
+// (it >> log2 n)-th round (no division on the per-tile paths).
+__host__ __device__ __forceinline__ int ring_stages_log2(int fmt) { return fmt == DSA_FMT_MXFP4 ? 4 : 3; }
+static_assert(kStages == 1 << 3 && kMaxStages == 1 << 4, "stage counts as their log2 above");
+__host__ __device__ __forceinline__ int ring_stage_bytes(int fmt) {
+    return fmt == DSA_FMT_MXFP4 ? kTileBytes / 2 : kTileBytes;
+}
+static_assert(kMaxStages * (kTileBytes / 2) == kStages * kTileBytes, "both rings fill the tile area");
 
 struct ScoreArgs {
     int fmt;
@@ -323,6 +336,8 @@ struct Producer {
     volatile int* abort;
     bool fp4;            // MXFP4 codes (either placement): transaction sizes
     bool rg;             // row-group placement: packed boxes per column group
+    int lg;              // log2 of the ring's stage count
+    int stage_bytes;     // shared memory of a stage's codes
     int cur = -1, i_seg = 0, it = 0;
     int last00 = -1, last01 = -1, last10 = -1, last11 = -1;   // last tile of query buffer b for issuer w
 
@@ -343,11 +358,11 @@ struct Producer {
             const int4 si = p.segs[sg];
             const int qb = i_seg & 1;
             for (int w = 0; w < kMmaWarps; ++w) {
-                // release of tile l: phase l / kStages of its stage's empty barrier; while
-                // it - l <= kStages the stage's next use (tile l + kStages) is not yet issued
+                // release of tile l: round l >> lg of its stage's empty barrier; while
+                // it - l <= stages the stage's next use is not yet issued
                 const int l = last_tile(qb, w);
-                if (l >= 0 && it - l <= kStages &&
-                    !mbar_wait(empty + l % kStages, (l / kStages) & 1, abort, p.status))
+                if (l >= 0 && it - l <= (1 << lg) &&
+                    !mbar_wait(empty + (l & ((1 << lg) - 1)), (l >> lg) & 1, abort, p.status))
                     return false;
                 set_last_tile(qb, w, -1);
             }
@@ -362,7 +377,8 @@ struct Producer {
                     for (int c = 0; c < 4; ++c)
                         tma_load_3d(qdst + c * kRgQChunk + r * 512, qmap, 16 * c, 0, si.y + r, qfull + qb);
                 } else {
-                    tma_load_3d(qdst + r * kQRowBytes, qmap, 0, 0, si.y + r, qfull + qb);
+                    // FP8 rows of 4096 bytes, packed MXFP4 rows of 2048 (32 heads x 64 B)
+                    tma_load_3d(qdst + r * (fp4 ? kFp4QRowTx : kQRowBytes), qmap, 0, 0, si.y + r, qfull + qb);
                 }
                 if (fp4)
                     bulk_load(smem + OFF_QSF + qb * kQsfBytes + r * qsf,
@@ -370,8 +386,8 @@ struct Producer {
             }
             ++i_seg;
         }
-        const int s = it % kStages;
-        if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status)) return false;
+        const int s = it & ((1 << lg) - 1);
+        if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
         reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(j, sg, i_seg - 1, 0);
         set_last_tile((i_seg - 1) & 1, it % kMmaWarps, it);
         const uint32_t page_tx = (fp4 ? kFp4PageTx : kFp8PageTx) + 256;
@@ -380,7 +396,7 @@ struct Producer {
             mbar_arrive(full + s);   // no valid page: scores of these keys are unspecified
         } else {
             mbar_arrive_expect_tx(full + s, bytes);
-            uint8_t* dst = smem + OFF_TILES + s * kTileBytes;
+            uint8_t* dst = smem + OFF_TILES + s * stage_bytes;
             if (rg) {
                 // group g of page h at g * 2048 + h * 1024: keys 0..127 of a group are 128 x 16 bytes in order
                 if (p0 >= 0) {
@@ -400,7 +416,7 @@ struct Producer {
                     tma_load_2d(smem + OFF_RAWSC + s * 512, smap, 0, p0, full + s);
                 }
                 if (p1 >= 0) {
-                    tma_load_3d(dst + kPageSmem, kmap, 0, 0, p1, full + s);
+                    tma_load_3d(dst + (fp4 ? kFp4KeyBytes : kPageSmem), kmap, 0, 0, p1, full + s);
                     tma_load_2d(smem + OFF_RAWSC + s * 512 + 256, smap, 0, p1, full + s);
                 }
             }
@@ -412,8 +428,8 @@ struct Producer {
     // End of this CTA's sequence: one stage tagged -1, with no copies, per issuer.
     __device__ __forceinline__ bool finish(const ScoreArgs& p) {
         for (int w = 0; w < kMmaWarps; ++w) {
-            const int s = it % kStages;
-            if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort, p.status)) return false;
+            const int s = it & ((1 << lg) - 1);
+            if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
             reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(-1, -1, -1, 0);
             mbar_arrive(full + s);
             ++it;
@@ -468,8 +484,8 @@ __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, 
     if (lane == 0) {
         if (ok) pr.finish(p);
         // Drain: every copy issued must have landed before the CTA exits.
-        const int it = pr.it, i_seg = pr.i_seg;
-        for (int i = max(0, it - kStages); i < it; ++i) mbar_drain(pr.full + (i % kStages), (i / kStages) & 1);
+        const int it = pr.it, i_seg = pr.i_seg, lg = pr.lg;
+        for (int i = max(0, it - (1 << lg)); i < it; ++i) mbar_drain(pr.full + (i & ((1 << lg) - 1)), (i >> lg) & 1);
         for (int i = max(0, i_seg - 2); i < i_seg; ++i) mbar_drain(pr.qfull + (i & 1), (i >> 1) & 1);
     }
     __syncwarp();
@@ -513,14 +529,16 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
     const bool mx_byte = (p.fmt == DSA_FMT_FP8_MX);
     const bool fp4 = fmt_fp4(p.fmt);
     const bool rg = (p.fmt == DSA_FMT_MXFP4_RG);
+    const int lg = ring_stages_log2(p.fmt);
+    const int stage_bytes = ring_stage_bytes(p.fmt);
     const int4* sinfo = reinterpret_cast<const int4*>(smem + OFF_SINFO);
     int2* ainfo = reinterpret_cast<int2*>(smem + OFF_AINFO);
     int cur = -1, qb = 0, nrows = 0;
     for (int it = w;; it += kMmaWarps) {
-        const int s = it % kStages;
+        const int s = it & ((1 << lg) - 1);
         const int a = it % kAcc;
         const uint32_t need = 4u * static_cast<uint32_t>(it / kAcc);   // releases of its earlier uses
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full + s, (it / kStages) & 1, abort, p.status))) break;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full + s, (it >> lg) & 1, abort, p.status))) break;
         const int4 tag = sinfo[s];
         if (tag.y < 0) {
             // this issuer's epilogue group takes the end tag
@@ -601,10 +619,11 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
         __syncwarp();
         if (lane == 0) {
             const uint32_t d = tmem + TM_ACC + a * 128;
-            const uint64_t ad = desc_sw128(smem_u32(smem + OFF_TILES + s * kTileBytes));
-            const uint64_t bd = desc_sw128(smem_u32(smem + OFF_QBUF + qb * kQBufBytes));
+            const uint32_t ka = smem_u32(smem + OFF_TILES + s * stage_bytes);
+            const uint32_t kb = smem_u32(smem + OFF_QBUF + qb * kQBufBytes);
             const uint32_t n = 32u * nrows;
             if (key_scale) {
+                const uint64_t ad = desc_sw128(ka), bd = desc_sw128(kb);
                 const uint32_t id = idesc_f8f6f4(kMmaE4M3, kMmaE4M3, 128, n);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) tc_mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, id, kk > 0);
@@ -612,21 +631,22 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                 const uint32_t sfa = tmem + TM_SFA + s * 4;
                 tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
                 const uint32_t sfb = tmem + TM_SFB + (qb * kMmaWarps + w) * 4;
-                const uint32_t ka = smem_u32(smem + OFF_TILES + s * kTileBytes);
-                const uint32_t kb = smem_u32(smem + OFF_QBUF + qb * kQBufBytes);
 #pragma unroll
                 for (int m = 0; m < 2; ++m)
                     tc_mma_mxf4(d, desc_kmajor_plain(ka + 2 * m * kRgTileGroup, kRgTileGroup, 128),
                                 desc_kmajor_plain(kb + 2 * m * kRgQChunk, kRgQChunk, 128),
                                 idesc_mx(kMmaMxf4E2M1, kMmaMxf4E2M1, 128, n, 2 * m, 2 * m), sfa, sfb, m > 0);
             } else {
+                // token-major: 64-byte rows (128 E2M1 per key or head); instruction m reads
+                // the row's bytes 32m .. 32m + 31
                 const uint32_t sfa = tmem + TM_SFA + s * 4;
                 tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
-                const uint32_t fm = fp4 ? kMmaE2M1 : kMmaE4M3;
                 const uint32_t sfb = tmem + TM_SFB + (qb * kMmaWarps + w) * 4;
+                const uint64_t ad = desc_sw64(ka), bd = desc_sw64(kb);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc_mx(fm, fm, 128, n, kk, kk), sfa, sfb, kk > 0);
+                for (int m = 0; m < 2; ++m)
+                    tc_mma_mxf4(d, ad + 2 * m, bd + 2 * m, idesc_mx(kMmaMxf4E2M1, kMmaMxf4E2M1, 128, n, 2 * m, 2 * m),
+                                sfa, sfb, m > 0);
             }
             ainfo[a] = make_int2(tag.x, tag.y);
             tc_commit(empty + s);
@@ -788,8 +808,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* full = bars;
-    uint64_t* empty = bars + kStages;
-    uint64_t* qfull = bars + 2 * kStages;
+    uint64_t* empty = bars + kMaxStages;
+    uint64_t* qfull = bars + 2 * kMaxStages;
     uint64_t* tfull = qfull + 2;
     uint64_t* done_bar = tfull + kAcc * kEpiGroups;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
@@ -798,7 +818,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kMaxStages; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
@@ -829,7 +849,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int t0 = range.x, t1 = range.y, S = range.w;
         const int seg = (t0 < t1 && range.z < 0) ? find_segment(args.seg_prefix, S, t0) : range.z;
         Producer pr{&kmap, &smap, &qmap, smem, full, empty, qfull, abort, fmt_fp4(args.fmt),
-                    args.fmt == DSA_FMT_MXFP4_RG};
+                    args.fmt == DSA_FMT_MXFP4_RG, ring_stages_log2(args.fmt), ring_stage_bytes(args.fmt)};
         producer_role(pr, args, t0, t1, seg, S, Ts, T);
     } else if (warp < kFirstEpiWarp) {
         mma_role(args, smem, tmem, full, empty, qfull, tfull, released, done_bar, abort);
@@ -899,7 +919,6 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     if (rows == 0) return DSA_OK;
     const bool fp4 = fmt_fp4(fmt);
     const bool rg = (fmt == DSA_FMT_MXFP4_RG);
-    const bool unpack = fp4 && !rg;   // 16U4_ALIGN16B copies: 32-byte bases and strides
     const int64_t width = max_pages * kPage;
     if (rows > (1 << 30) || num_requests > (1 << 30) || width > (int64_t(1) << 30) || num_pages > 0x7FFFFFFF)
         return DSA_ERR_UNSUPPORTED;
@@ -907,8 +926,8 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     if (num_pages > 0 && !cache) return DSA_ERR_INVALID;
     if (max_pages > 0 && num_requests > 0 && (!block_table || bt_stride < max_pages)) return DSA_ERR_INVALID;
     const int64_t min_stride = fp4 ? DSA_FP4_PAGE_BYTES : DSA_FP8_PAGE_BYTES;
-    if (page_stride < min_stride || page_stride % (unpack ? 32 : 16)) return DSA_ERR_INVALID;
-    if (!aligned(cache, unpack ? 32 : 16) || !aligned(q_rows, unpack ? 32 : 16) || !aligned(workspace, 256) ||
+    if (page_stride < min_stride || page_stride % 16) return DSA_ERR_INVALID;
+    if (!aligned(cache, 16) || !aligned(q_rows, 16) || !aligned(workspace, 256) ||
         !aligned(w, 2))
         return DSA_ERR_INVALID;
     if (logits && (logits_ld < width || !aligned(logits, 4))) return DSA_ERR_INVALID;
@@ -934,11 +953,14 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
                          CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
             return DSA_ERR_CUDA;
     } else {
-        const cuuint64_t dims[3] = {128, 64, np};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(fp4 ? 64 : 128), static_cast<cuuint64_t>(page_stride)};
-        const cuuint32_t box[3] = {128, 64, 1};
-        if (encode_tiled(&kmap, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
-                         cache_addr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        // {row bytes, 64 keys, pages}: FP8 rows of 128 bytes (128-byte swizzle), MXFP4 rows of
+        // 64 packed bytes (64-byte swizzle)
+        const cuuint64_t row = fp4 ? 64 : 128;
+        const cuuint64_t dims[3] = {row, 64, np};
+        const cuuint64_t strides[2] = {row, static_cast<cuuint64_t>(page_stride)};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(row), 64, 1};
+        if (encode_tiled(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, cache_addr, dims, strides, box,
+                         fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return DSA_ERR_CUDA;
     }
     {
@@ -959,11 +981,12 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
                          CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
             return DSA_ERR_CUDA;
     } else {
-        const cuuint64_t dims[3] = {128, 32, static_cast<cuuint64_t>(rows)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(fp4 ? 64 : 128), kQRowBytes};
-        const cuuint32_t box[3] = {128, 32, 1};
-        if (encode_tiled(&qmap, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
-                         const_cast<void*>(q_rows), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        const cuuint64_t row = fp4 ? 64 : 128;
+        const cuuint64_t dims[3] = {row, 32, static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[2] = {row, kQRowBytes};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(row), 32, 1};
+        if (encode_tiled(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q_rows), dims, strides, box,
+                         fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return DSA_ERR_CUDA;
     }
 

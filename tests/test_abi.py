@@ -65,6 +65,6 @@ def test_host_argument_checks(lib):
                                10**9, None, None) == -1                         # row-group stride not a multiple of 16
     assert lib.dsa_score_paged(0, 16, 16, 16, 8448, 1, 16, 1, 1, 16, 16, 1, 0, 1, None, 0, 4, None, 256, 10**9,
                                None, None) == 0                                 # zero rows
-    assert lib.dsa_score_paged(2, 32, 32, 32, 4352 + 16, 1, 16, 1, 1, 16, 16, 1, 1, 1, None, 0, 4, None, 256,
-                               10**9, None, None) == -1                         # MXFP4 stride not a multiple of 32
+    assert lib.dsa_score_paged(2, 32, 32, 32, 4352 + 8, 1, 16, 1, 1, 16, 16, 1, 1, 1, None, 0, 4, None, 256,
+                               10**9, None, None) == -1                         # MXFP4 stride not a multiple of 16
     assert lib.dsa_topk(None, 10, None, 1, 20, 4, None, None, 0, None) == -1  # ld < width

@@ -211,12 +211,13 @@ def test_score_cache_bytes_match_oracle(cuda_lib, fmt):
                               o["cache"][p_or * stride:p_or * stride + O.page_bytes(fmt)]), p_gpu
 
 
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp4_rg"])
 @pytest.mark.parametrize("case", [1, 2, 3, 5])
-def test_score_rowgroup_page_stride(cuda_lib, case):
-    """Row-group MXFP4 in a pool whose physical page stride (4400 bytes) is
-    above the 4352-byte section and not a multiple of 32."""
+def test_score_mxfp4_page_stride(cuda_lib, fmt, case):
+    """MXFP4 in either placement in a pool whose physical page stride (4400
+    bytes) is above the 4352-byte section and not a multiple of 32."""
     spec = dict(SMALL[case])
-    wl = make_workload("tiny_fp8", fmt="mxfp4_rg", seed=300 + case, topk=[16, 64, 100, 5, 2, 512][case], **spec)
+    wl = make_workload("tiny_fp8", fmt=fmt, seed=300 + case, topk=[16, 64, 100, 5, 2, 512][case], **spec)
     g = gpu_run(wl, page_stride=4400)
     o = oracle_run(wl, page_stride=4400)
     assert g["status"] == 0
