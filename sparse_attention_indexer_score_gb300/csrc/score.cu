@@ -112,14 +112,14 @@ constexpr uint32_t TM_SFA = kAcc * 128;              // kMaxStages x 4 columns
 constexpr uint32_t TM_SFB = TM_SFA + 4 * kMaxStages; // (2 buffers x kMmaWarps) x 4 columns
 constexpr uint32_t TM_COLS = 512;
 
-// Ring geometry of a format: packed token-major MXFP4 tiles take half the
-// shared memory of the others, so twice as many are in flight.
+// Ring geometry of a format: packed MXFP4 tiles (either placement) take half
+// the shared memory of FP8 ones, so twice as many are in flight.
 // Stage counts are powers of two: position it uses stage it & (n - 1) in its
 // (it >> log2 n)-th round (no division on the per-tile paths).
-__host__ __device__ __forceinline__ int ring_stages_log2(int fmt) { return fmt == DSA_FMT_MXFP4 ? 4 : 3; }
+__host__ __device__ __forceinline__ int ring_stages_log2(int fmt) { return fmt_fp4(fmt) ? 4 : 3; }
 static_assert(kStages == 1 << 3 && kMaxStages == 1 << 4, "stage counts as their log2 above");
 __host__ __device__ __forceinline__ int ring_stage_bytes(int fmt) {
-    return fmt == DSA_FMT_MXFP4 ? kTileBytes / 2 : kTileBytes;
+    return fmt_fp4(fmt) ? kTileBytes / 2 : kTileBytes;
 }
 static_assert(kMaxStages * (kTileBytes / 2) == kStages * kTileBytes, "both rings fill the tile area");
 
