@@ -12,11 +12,13 @@
 //
 // Warp roles of the persistent CTA (one per SM):
 //   warp 0     TMA producer: block-table gather of key pages (+ their scales)
-//              into an 8-stage shared-memory ring; query rows per segment.
+//              into a shared-memory ring (8 stages of 16 KB for FP8, 16 of
+//              8 KB for packed MXFP4); query rows per segment.
 //   warps 1-2  tcgen05 issuers of alternate tiles: scale factors into TMEM,
-//              4 MMAs (K = 32 each) per tile into one of three TMEM
-//              accumulators.  One issuer's per-tile chain of waits, tag and
-//              scale handling and MMA issue is longer than a tile's copy time.
+//              the tile's MMAs (FP8: 4 with K = 32; MXFP4: 2 with K = 64) into
+//              one of three TMEM accumulators.  One issuer's per-tile chain of
+//              waits, tag and scale handling and MMA issue is longer than a
+//              tile's copy time.
 //   warps 3-10 epilogue, two groups of four: tcgen05.ld of the accumulator
 //              (thread = key), ReLU-weighted head sum, FP32 key scale, logits
 //              store, and a shared-memory histogram of the scores for the
