@@ -23,6 +23,8 @@
 //              (thread = key), ReLU-weighted head sum, FP32 key scale, logits
 //              store, and a shared-memory histogram of the scores for the
 //              top-k pass.
+//   warp 11    second copy issuer: each tile's second page (warp 0 issues the
+//              first), so two threads feed the copy engine.
 //
 // Formats: FP8 and FP8-MX use kind::f8f6f4 (E4M3 x E4M3) and multiply the
 // per-key scale in the epilogue.  MXFP4 keeps its codes packed and uses
@@ -66,7 +68,11 @@ constexpr int kEpiWarps = 4 * kEpiGroups;
 // group w drains.
 constexpr int kMmaWarps = 2;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
-constexpr int kScoreThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr int kPageWarp = kFirstEpiWarp + kEpiWarps;   // issues the second page of every tile
+constexpr int kScoreThreads = 32 * (kPageWarp + 1);
+// Second-page ids handed from warp 0 to the page warp: a ring of kPageRing
+// entries (>= 0 page, kNoPage none, kEndMark end of sequence).
+constexpr int kPageRing = 64, kNoPage = -1, kEndMark = -2;
 static_assert(kMmaWarps == kEpiGroups && kStages % kMmaWarps == 0 && kMaxStages % kMmaWarps == 0,
               "issuer w owns stages and group w");
 constexpr int kAcc = 3;                       // TMEM accumulators in flight (MMA latency is hidden behind 2)
@@ -97,15 +103,17 @@ constexpr int kGroupHistWords = kSegRows * kHistBins / 2;
 // int4[kMaxStages]: {tile in segment, segment, segment ordinal in this CTA's sequence}
 constexpr int OFF_SINFO = OFF_HIST + kEpiGroups * kGroupHistWords * 4;
 constexpr int OFF_AINFO = OFF_SINFO + kMaxStages * 16;       // int2[kAcc]: {tile in segment, segment} per accumulator
-constexpr int OFF_BAR = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;
+constexpr int OFF_PRING = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;   // int[kPageRing]
+constexpr int OFF_BAR = OFF_PRING + kPageRing * 4;
 // full, empty, qfull, tfull (per accumulator and epilogue group), done.  A
 // group's accumulator barrier is used by the sequence positions it, it + 6, ...
 // of that group alone: one barrier per accumulator, filled by both issuers,
 // could show a group a phase of the other group's fill (the two issuers'
 // MMAs complete in no common order) and its parity wait would take it.
 constexpr int kNumBars = 2 * kMaxStages + 2 + kAcc * kEpiGroups + 1;
-constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;       // TMEM address, abort flag, then released[kAcc]
-constexpr int kScoreSmem = OFF_MISC + 32 + 1024;       // + slack to align the base to 1024
+// TMEM address, abort flag, released[kAcc] at +16, page ring published / consumed at +32 / +36
+constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
+constexpr int kScoreSmem = OFF_MISC + 48 + 1024;       // + slack to align the base to 1024
 static_assert(kScoreSmem <= 227 * 1024, "scoring CTA exceeds the shared memory of an SM");
 
 // TMEM columns: kAcc accumulators of up to 128 columns, then scale factors.
@@ -318,6 +326,39 @@ __device__ __forceinline__ int warp_find_segment(const int* prefix, int S, int t
     return lo;
 }
 
+// Bounded wait until a release counter reaches `need` (wrap-safe compare);
+// same give-up rules as mbar_wait.
+__device__ __forceinline__ bool count_wait(const uint32_t* c, uint32_t need, volatile int* abort, int32_t* status) {
+    if (static_cast<int>(smem_ld_acquire(c) - need) >= 0) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (static_cast<int>(smem_ld_acquire(c) - need) >= 0) return true;
+        if ((i & 31) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                if (status) atomicOr(status, DSA_STATUS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Copies page h (0 or 1) of a tile, id pid, into stage s: its codes (FP8: one
+// 128-byte-swizzled box; MXFP4: one 64-byte-swizzled box; row-group: one box
+// per column group, group g at g * 2048 + h * 1024) and its 256 scale bytes.
+__device__ __forceinline__ void issue_page(const CUtensorMap* kmap, const CUtensorMap* smap, uint8_t* smem,
+                                           uint64_t* bar, int s, int stage_bytes, bool fp4, bool rg, int h, int pid) {
+    uint8_t* dst = smem + OFF_TILES + s * stage_bytes;
+    if (rg) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tma_load_4d(dst + g * kRgTileGroup + h * kRgGroupBytes, kmap, 0, 0, g, pid, bar);
+    } else {
+        tma_load_3d(dst + h * (fp4 ? kFp4KeyBytes : kPageSmem), kmap, 0, 0, pid, bar);
+    }
+    tma_load_2d(smem + OFF_RAWSC + s * 512 + h * 256, smap, 0, pid, bar);
+}
+
 // Issues the loads of one tile (lane 0 of the producer warp): the segment's
 // query rows when the segment changes, then the key pages and scales into the
 // next ring stage, tagged with {tile in segment, segment, segment ordinal}.
@@ -340,7 +381,19 @@ struct Producer {
     bool rg;             // row-group placement: packed boxes per column group
     int lg;              // log2 of the ring's stage count
     int stage_bytes;     // shared memory of a stage's codes
+    int* page_ring;      // second-page ids for the page warp
+    uint32_t* published; // entries written (release)
+    const uint32_t* consumed;   // entries the page warp has taken (acquire)
     int cur = -1, i_seg = 0, it = 0;
+
+    // Hands position it's second-page entry to the page warp (ring of kPageRing).
+    __device__ __forceinline__ bool publish(const ScoreArgs& p, int v) {
+        if (it >= kPageRing && !count_wait(consumed, static_cast<uint32_t>(it - kPageRing + 1), abort, p.status))
+            return false;
+        page_ring[it & (kPageRing - 1)] = v;
+        smem_add_release(published, 1u);
+        return true;
+    }
     int last00 = -1, last01 = -1, last10 = -1, last11 = -1;   // last tile of query buffer b for issuer w
 
     __device__ __forceinline__ int last_tile(int b, int w) const {
@@ -392,36 +445,13 @@ struct Producer {
         if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
         reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(j, sg, i_seg - 1, 0);
         set_last_tile((i_seg - 1) & 1, it % kMmaWarps, it);
-        const uint32_t page_tx = (fp4 ? kFp4PageTx : kFp8PageTx) + 256;
-        const uint32_t bytes = (p0 >= 0 ? page_tx : 0u) + (p1 >= 0 ? page_tx : 0u);
-        if (bytes == 0) {
+        // the stage's full barrier takes two arrivals: this warp's (first page) and the page warp's
+        if (!publish(p, p1 >= 0 ? p1 : kNoPage)) return false;
+        if (p0 < 0) {
             mbar_arrive(full + s);   // no valid page: scores of these keys are unspecified
         } else {
-            mbar_arrive_expect_tx(full + s, bytes);
-            uint8_t* dst = smem + OFF_TILES + s * stage_bytes;
-            if (rg) {
-                // group g of page h at g * 2048 + h * 1024: keys 0..127 of a group are 128 x 16 bytes in order
-                if (p0 >= 0) {
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) tma_load_4d(dst + g * kRgTileGroup, kmap, 0, 0, g, p0, full + s);
-                    tma_load_2d(smem + OFF_RAWSC + s * 512, smap, 0, p0, full + s);
-                }
-                if (p1 >= 0) {
-#pragma unroll
-                    for (int g = 0; g < 4; ++g)
-                        tma_load_4d(dst + g * kRgTileGroup + kRgGroupBytes, kmap, 0, 0, g, p1, full + s);
-                    tma_load_2d(smem + OFF_RAWSC + s * 512 + 256, smap, 0, p1, full + s);
-                }
-            } else {
-                if (p0 >= 0) {
-                    tma_load_3d(dst, kmap, 0, 0, p0, full + s);
-                    tma_load_2d(smem + OFF_RAWSC + s * 512, smap, 0, p0, full + s);
-                }
-                if (p1 >= 0) {
-                    tma_load_3d(dst + (fp4 ? kFp4KeyBytes : kPageSmem), kmap, 0, 0, p1, full + s);
-                    tma_load_2d(smem + OFF_RAWSC + s * 512 + 256, smap, 0, p1, full + s);
-                }
-            }
+            mbar_arrive_expect_tx(full + s, (fp4 ? kFp4PageTx : kFp8PageTx) + 256);
+            issue_page(kmap, smap, smem, full + s, s, stage_bytes, fp4, rg, 0, p0);
         }
         ++it;
         return true;
@@ -433,6 +463,7 @@ struct Producer {
             const int s = it & ((1 << lg) - 1);
             if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
             reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(-1, -1, -1, 0);
+            if (!publish(p, kEndMark)) return false;
             mbar_arrive(full + s);
             ++it;
         }
@@ -493,21 +524,31 @@ __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, 
     __syncwarp();
 }
 
-// Bounded wait until a release counter reaches `need` (wrap-safe compare);
-// same give-up rules as mbar_wait.
-__device__ __forceinline__ bool count_wait(const uint32_t* c, uint32_t need, volatile int* abort, int32_t* status) {
-    if (static_cast<int>(smem_ld_acquire(c) - need) >= 0) return true;
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (static_cast<int>(smem_ld_acquire(c) - need) >= 0) return true;
-        if ((i & 31) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                *abort = 1;
-                if (status) atomicOr(status, DSA_STATUS_TIMEOUT);
-                return false;
-            }
+// Warp kPageWarp.  Follows warp 0's positions through the page ring and
+// copies each tile's second page into the same stage, arming the stage's full
+// barrier for its own bytes (it waits for the same free-stage phase as warp 0;
+// the stage cannot move on before this warp's arrival).
+__device__ __forceinline__ void page_role(const ScoreArgs& p, const CUtensorMap* kmap, const CUtensorMap* smap,
+                                          uint8_t* smem, uint64_t* full, uint64_t* empty, const uint32_t* published,
+                                          uint32_t* consumed, volatile int* abort) {
+    if ((threadIdx.x & 31) != 0) return;
+    const bool fp4 = fmt_fp4(p.fmt), rg = (p.fmt == DSA_FMT_MXFP4_RG);
+    const int lg = ring_stages_log2(p.fmt), stage_bytes = ring_stage_bytes(p.fmt);
+    const int* ring = reinterpret_cast<const int*>(smem + OFF_PRING);
+    int ends = 0;
+    for (int j = 0; ends < kMmaWarps; ++j) {
+        if (!count_wait(published, static_cast<uint32_t>(j + 1), abort, p.status)) break;
+        const int v = ring[j & (kPageRing - 1)];
+        const int s = j & ((1 << lg) - 1);
+        if (!mbar_wait(empty + s, ((j >> lg) & 1) ^ 1, abort, p.status)) break;
+        if (v >= 0) {
+            mbar_arrive_expect_tx(full + s, (fp4 ? kFp4PageTx : kFp8PageTx) + 256);
+            issue_page(kmap, smap, smem, full + s, s, stage_bytes, fp4, rg, 1, v);
+        } else {
+            mbar_arrive(full + s);
         }
+        smem_add_release(consumed, 1u);
+        if (v == kEndMark) ++ends;
     }
 }
 
@@ -817,16 +858,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     uint32_t* released = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 16);   // per accumulator
+    uint32_t* published = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 32);
+    uint32_t* consumed = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 36);
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMaxStages; ++s) {
-            mbar_init(full + s, 1);
+            mbar_init(full + s, 2);   // warp 0 (first page) and the page warp (second page)
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) mbar_init(qfull + b, 1);
         for (int b = 0; b < kAcc * kEpiGroups; ++b) mbar_init(tfull + b, 2);
         for (int b = 0; b < kAcc; ++b) released[b] = 0u;
+        *published = 0u;
+        *consumed = 0u;
         mbar_init(done_bar, kMmaWarps);
         *abort = 0;
         mbar_fence_init();
@@ -850,13 +895,28 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int T = args.claim[-1], Ts = args.claim[1];
         const int t0 = range.x, t1 = range.y, S = range.w;
         const int seg = (t0 < t1 && range.z < 0) ? find_segment(args.seg_prefix, S, t0) : range.z;
-        Producer pr{&kmap, &smap, &qmap, smem, full, empty, qfull, abort, fmt_fp4(args.fmt),
-                    args.fmt == DSA_FMT_MXFP4_RG, ring_stages_log2(args.fmt), ring_stage_bytes(args.fmt)};
+        Producer pr{&kmap,
+                    &smap,
+                    &qmap,
+                    smem,
+                    full,
+                    empty,
+                    qfull,
+                    abort,
+                    fmt_fp4(args.fmt),
+                    args.fmt == DSA_FMT_MXFP4_RG,
+                    ring_stages_log2(args.fmt),
+                    ring_stage_bytes(args.fmt),
+                    reinterpret_cast<int*>(smem + OFF_PRING),
+                    published,
+                    consumed};
         producer_role(pr, args, t0, t1, seg, S, Ts, T);
     } else if (warp < kFirstEpiWarp) {
         mma_role(args, smem, tmem, full, empty, qfull, tfull, released, done_bar, abort);
-    } else {
+    } else if (warp < kPageWarp) {
         epilogue_role(args, smem, tmem, tfull, released, abort);
+    } else {
+        page_role(args, &kmap, &smap, smem, full, empty, published, consumed, abort);
     }
     tc_fence_before();
     __syncthreads();
