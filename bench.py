@@ -274,7 +274,7 @@ def run_ours(args, wl, rank, world, local_rank):
     from sparse_attention_indexer_score_gb300 import build as _b
     _b.build()
     from sparse_attention_indexer_score_gb300 import dsa
-    from sparse_attention_indexer_score_gb300.step import DecodeIndexer
+    from sparse_attention_indexer_score_gb300.step import DecodeIndexer, GraphedStep
     from dsa_case import bf16_tensor
 
     dev = torch.device("cuda", local_rank)
@@ -369,25 +369,41 @@ def run_ours(args, wl, rank, world, local_rank):
         kernel_ms += a.elapsed_ms(b)
     kernel_ms /= args.steps
 
-    # end to end through the public API (eager calls) from pinned host buffers
+    # End to end through the public API from pinned host buffers, every step
+    # copying its inputs in and its top-k back: the graph-captured step a
+    # serving loop replays (one GraphedStep per cache replica), and eager calls.
     pinned = {k: v.pin_memory() for k, v in host.items()}
     h_top = torch.empty((wl.num_rows, wl.topk), dtype=torch.int32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = h_top.numel() * 4
     e2e_steps = min(args.steps, 200)
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
-    torch.cuda.synchronize()
-    for i, (a, b) in enumerate(eev):
-        a.record()
+
+    def timed_e2e(run_step):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(ev):
+            a.record()
+            run_step(i)
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) * args.steps / e2e_steps
+
+    named = dict(q=pinned["q"], wv=pinned["wv"], keys=pinned["keys"], slots=pinned["slots"],
+                 seq_lens=pinned["seq"], query_lens=pinned["qlen"])
+    gsteps = []
+    for r in range(n_rep):
+        ix.cache = caches[r]
+        gsteps.append(GraphedStep(ix, named, max_q, h_top))
+    e2e_ms = timed_e2e(lambda i: gsteps[i % n_rep].replay())
+
+    def eager_step(i):
         for k in d:
             d[k].copy_(pinned[k], non_blocking=True)
         step(d, i % n_rep)
         h_top.copy_(topk_out, non_blocking=True)
-        b.record()
-    torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) * args.steps / e2e_steps
+    e2e_eager_ms = timed_e2e(eager_step)
 
-    step_ms, e2e_ms, kernel_ms = max_over_ranks([step_ms, e2e_ms, kernel_ms], dev)
+    step_ms, e2e_ms, e2e_eager_ms, kernel_ms = max_over_ranks([step_ms, e2e_ms, e2e_eager_ms, kernel_ms], dev)
     if rank != 0:
         return
     value = whole_job_rate(ab["scored"], args.steps, world, step_ms)
@@ -413,7 +429,12 @@ def run_ours(args, wl, rank, world, local_rank):
                      "peak_source": f"{peaks['source']} HBM copy bandwidth",
                      "step_frac": (ab["step"] / (step_ms / args.steps / 1e3) / 1e9) / peaks["hbm_gbs"]},
         "e2e": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "how": "eager public-API calls, host copies in the timed region"},
+                "d2h_bytes_per_step": d2h,
+                "how": ("DecodeIndexer GraphedStep replayed once per step: the inputs' copies from pinned host "
+                        "memory, the step and the top-k copy back, all in the timed region")},
+        "e2e_eager": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_eager_ms), "unit": UNIT,
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "how": "eager public-API calls per step, the same host copies in the timed region"},
         "gpu_launches": STEP_KERNELS * args.steps,
         "clocks": clk,
     }

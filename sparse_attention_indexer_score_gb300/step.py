@@ -3,7 +3,8 @@
 ``DecodeIndexer`` owns the device state a serving loop keeps between steps
 (the paged key cache, the block table, a zero-filled workspace) and runs the
 step on the current stream: prepare_step (quantize_query + insert_key +
-decode_layout in one launch) -> score_paged (+ fused top-k).
+decode_layout in one launch) -> score_paged (+ fused top-k).  ``GraphedStep``
+captures a step with its host copies as one CUDA graph.
 """
 
 from __future__ import annotations
@@ -65,3 +66,47 @@ class DecodeIndexer:
 
     def status_bits(self) -> int:
         return int(self.status.item())
+
+
+class GraphedStep:
+    """A decode step captured as one CUDA graph, as a serving loop runs it:
+    the host-to-device copies of the step's inputs from pinned host buffers,
+    the step itself (prepare_step, scoring, top-k), and the copy of the top-k
+    positions back to a pinned host buffer.  ``replay()`` runs all of it on
+    the current stream; the caller refills the pinned inputs between replays
+    and synchronises before reading ``host_topk``.
+
+    host_inputs: pinned CPU tensors ``q``, ``wv``, ``keys``, ``slots``,
+    ``seq_lens``, ``query_lens`` with the shapes and dtypes ``step`` takes.
+    """
+
+    NAMES = ("q", "wv", "keys", "slots", "seq_lens", "query_lens")
+
+    def __init__(self, ix: DecodeIndexer, host_inputs: dict, max_query_len: int, host_topk: torch.Tensor):
+        for name in self.NAMES:
+            if not host_inputs[name].is_pinned():
+                raise ValueError(f"host input {name!r} must be in pinned memory")
+        if not host_topk.is_pinned() or host_topk.dtype != torch.int32:
+            raise ValueError("host_topk must be a pinned int32 tensor")
+        self.ix = ix
+        self.host = {name: host_inputs[name] for name in self.NAMES}
+        self.host_topk = host_topk
+        self.dev = {name: torch.empty_like(t, device=ix.device) for name, t in self.host.items()}
+        self.topk = torch.empty(tuple(host_topk.shape), dtype=torch.int32, device=ix.device)
+        self.max_query_len = int(max_query_len)
+        self._run()                      # first use outside capture (library and allocator set up)
+        torch.cuda.synchronize(ix.device)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._run()
+
+    def _run(self) -> None:
+        for name in self.NAMES:
+            self.dev[name].copy_(self.host[name], non_blocking=True)
+        d = self.dev
+        self.ix.step(d["q"], d["wv"], d["keys"], d["slots"], d["seq_lens"], d["query_lens"], self.max_query_len,
+                     topk_out=self.topk)
+        self.host_topk.copy_(self.topk, non_blocking=True)
+
+    def replay(self) -> None:
+        self.graph.replay()
