@@ -69,31 +69,44 @@ class DecodeIndexer:
 
 
 class GraphedStep:
-    """A decode step captured as one CUDA graph, as a serving loop runs it:
-    the host-to-device copies of the step's inputs from pinned host buffers,
-    the step itself (prepare_step, scoring, top-k), and the copy of the top-k
-    positions back to a pinned host buffer.  ``replay()`` runs all of it on
-    the current stream; the caller refills the pinned inputs between replays
-    and synchronises before reading ``host_topk``.
+    """A decode step captured as one CUDA graph, as a serving loop runs it: one
+    host-to-device copy of the step's inputs from a pinned staging buffer, the
+    step itself (prepare_step, scoring, top-k), and one copy of the top-k
+    positions back to a pinned host buffer.
 
-    host_inputs: pinned CPU tensors ``q``, ``wv``, ``keys``, ``slots``,
-    ``seq_lens``, ``query_lens`` with the shapes and dtypes ``step`` takes.
+    ``inputs`` holds pinned views ``q``, ``wv``, ``keys``, ``slots``,
+    ``seq_lens`` and ``query_lens`` into the staging buffer, shaped and typed
+    like the ``like`` tensors given; the caller fills them, calls ``replay()``
+    (current stream) and synchronises before reading ``host_topk``.
     """
 
     NAMES = ("q", "wv", "keys", "slots", "seq_lens", "query_lens")
+    ALIGN = 256
 
-    def __init__(self, ix: DecodeIndexer, host_inputs: dict, max_query_len: int, host_topk: torch.Tensor):
+    def __init__(self, ix: DecodeIndexer, like: dict, max_query_len: int):
+        offs, total = {}, 0
         for name in self.NAMES:
-            if not host_inputs[name].is_pinned():
-                raise ValueError(f"host input {name!r} must be in pinned memory")
-        if not host_topk.is_pinned() or host_topk.dtype != torch.int32:
-            raise ValueError("host_topk must be a pinned int32 tensor")
+            t = like[name]
+            offs[name] = total
+            total += -(-t.numel() * t.element_size() // self.ALIGN) * self.ALIGN
+        self.staging_bytes = total
+        self.host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.dev_buf = torch.empty(total, dtype=torch.uint8, device=ix.device)
+
+        def view(buf, name):
+            t = like[name]
+            n = t.numel() * t.element_size()
+            return buf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+
+        self.inputs = {name: view(self.host_buf, name) for name in self.NAMES}
+        self.dev = {name: view(self.dev_buf, name) for name in self.NAMES}
+        rows = like["q"].shape[0]
+        self.topk = torch.empty((rows, ix.k), dtype=torch.int32, device=ix.device)
+        self.host_topk = torch.empty((rows, ix.k), dtype=torch.int32).pin_memory()
         self.ix = ix
-        self.host = {name: host_inputs[name] for name in self.NAMES}
-        self.host_topk = host_topk
-        self.dev = {name: torch.empty_like(t, device=ix.device) for name, t in self.host.items()}
-        self.topk = torch.empty(tuple(host_topk.shape), dtype=torch.int32, device=ix.device)
         self.max_query_len = int(max_query_len)
+        for name in self.NAMES:
+            self.inputs[name].copy_(like[name])
         self._run()                      # first use outside capture (library and allocator set up)
         torch.cuda.synchronize(ix.device)
         self.graph = torch.cuda.CUDAGraph()
@@ -101,8 +114,7 @@ class GraphedStep:
             self._run()
 
     def _run(self) -> None:
-        for name in self.NAMES:
-            self.dev[name].copy_(self.host[name], non_blocking=True)
+        self.dev_buf.copy_(self.host_buf, non_blocking=True)
         d = self.dev
         self.ix.step(d["q"], d["wv"], d["keys"], d["slots"], d["seq_lens"], d["query_lens"], self.max_query_len,
                      topk_out=self.topk)

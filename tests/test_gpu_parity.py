@@ -319,8 +319,9 @@ def test_full_size_sampled_rows(cuda_lib, name):
 
 
 def test_graphed_step_matches_eager(cuda_lib):
-    """The graph-captured step (host copies in, step, top-k copy back) gives the
-    eager step's top-k sets, replay after replay, and reads fresh host inputs."""
+    """The graph-captured step (one staging copy in, step, top-k copy back)
+    gives the eager step's top-k sets, replay after replay, and reads what the
+    caller writes into its staging views."""
     import torch
     from sparse_attention_indexer_score_gb300.step import DecodeIndexer, GraphedStep
     wl = make_workload("tiny_fp8", fmt="mxfp4", seed=21, R=5, seq=(300, 900), qlen=(1, 3), pad_rows=1, topk=64)
@@ -332,23 +333,24 @@ def test_graphed_step_matches_eager(cuda_lib):
         kb, sl = wl.prefill(q)
         if kb.shape[0]:
             ix.insert(bf16_tensor(kb, dev), torch.from_numpy(sl).to(dev))
-    host = dict(q=bf16_tensor(wl.q_bits, "cpu").pin_memory(), wv=bf16_tensor(wl.wv_bits, "cpu").pin_memory(),
-                keys=bf16_tensor(wl.step_key_bits, "cpu").pin_memory(),
-                slots=torch.from_numpy(wl.step_slots).pin_memory(), seq_lens=torch.from_numpy(wl.seq_lens).pin_memory(),
-                query_lens=torch.from_numpy(wl.query_lens).pin_memory())
-    h_top = torch.full((wl.num_rows, wl.topk), -7, dtype=torch.int32).pin_memory()
-    with pytest.raises(ValueError):
-        GraphedStep(ix, dict(host, q=bf16_tensor(wl.q_bits, "cpu")), int(wl.query_lens.max()), h_top)   # not pinned
-    g = GraphedStep(ix, host, int(wl.query_lens.max()), h_top)
+    like = dict(q=bf16_tensor(wl.q_bits, "cpu"), wv=bf16_tensor(wl.wv_bits, "cpu"),
+                keys=bf16_tensor(wl.step_key_bits, "cpu"), slots=torch.from_numpy(wl.step_slots),
+                seq_lens=torch.from_numpy(wl.seq_lens), query_lens=torch.from_numpy(wl.query_lens))
+    g = GraphedStep(ix, like, int(wl.query_lens.max()))
+    assert all(g.inputs[k].is_pinned() for k in g.NAMES) and g.host_topk.is_pinned()
     for _ in range(3):
-        h_top.fill_(-7)
+        g.host_topk.fill_(-7)
         g.replay()
         torch.cuda.synchronize()
-        got = h_top.numpy()
+        got = g.host_topk.numpy()
         for r in range(wl.num_rows):
             assert sorted(got[r].tolist()) == sorted(want[r].tolist()), r
-    # fresh inputs through the same pinned buffers: all-zero queries score 0 everywhere
-    host["q"].zero_()
+    # rows whose request length the caller sets to 1 now select only position 0
+    g.inputs["seq_lens"].fill_(1)
+    g.inputs["query_lens"].fill_(1)
     g.replay()
     torch.cuda.synchronize()
+    got = g.host_topk.numpy()
     assert ix.status_bits() == 0
+    for r in range(min(wl.R, wl.num_rows)):
+        assert got[r, 0] == 0 and np.all(got[r, 1:] == -1), r
