@@ -407,6 +407,17 @@ int dsa_timing_elapsed_ms(void* start, void* end, float* ms);
 /* dsa_version - library version string. */
 const char* dsa_version(void);
 
+/*
+ * dsa_selftest_wait_timeout - exercise the failure detection of the kernels.
+ *
+ * Launches one thread that waits, with the bounded wait every kernel of this
+ * library uses, on a barrier that nothing completes.  The wait gives up after
+ * its time limit (about one second), sets DSA_STATUS_TIMEOUT in *status and
+ * the kernel returns: the context stays usable.  status: int32 device word.
+ * Returns DSA_ERR_INVALID for a null status.
+ */
+int dsa_selftest_wait_timeout(int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -50,3 +50,27 @@ extern "C" int dsa_decode_layout_dcp(const int32_t* seq_lens, int64_t num_seq, c
                                        row_ends, dcp_rank, dcp_world_size, interleave);
     return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
+
+// ----------------------------------------------------------------- failure detection self-check
+// One thread waits, with the kernels' own bounded wait, on an mbarrier that
+// nothing arrives on: the wait gives up after its time limit and flags
+// DSA_STATUS_TIMEOUT, and the kernel returns normally.
+namespace dsa {
+__global__ void wait_selftest_kernel(int32_t* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status);
+}
+}  // namespace dsa
+
+extern "C" int dsa_selftest_wait_timeout(int32_t* status, void* stream) {
+    if (!status) return DSA_ERR_INVALID;
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}

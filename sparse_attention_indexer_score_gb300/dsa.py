@@ -32,6 +32,7 @@ _I64 = _c.c_int64
 _SIGS = {
     "dsa_quantize_query": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P]),
     "dsa_quantize_queries_rg": (_c.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P]),
+    "dsa_selftest_wait_timeout": (_c.c_int, [_P, _P]),
     "dsa_insert_key": (_c.c_int, [_c.c_int, _P, _I64, _P, _P, _c.c_float, _P, _I64, _P, _I64, _I64, _P, _P]),
     "dsa_decode_layout": (_c.c_int, [_P, _I64, _P, _I64, _I64, _P, _P, _P]),
     "dsa_prepare_step": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _c.c_float, _P,
@@ -152,6 +153,14 @@ def quantize_queries_rg(q: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
                                        _ptr(scales), _stream(q.device))
     _check(rc, "dsa_quantize_queries_rg")
     return payload, scales
+
+
+def selftest_wait_timeout(status: torch.Tensor) -> None:
+    """Runs the failure-detection self-check: a bounded wait that runs out
+    (about one second) and sets the timeout bit of ``status`` (int32 [1])."""
+    if status.dtype != torch.int32 or status.numel() < 1 or not status.is_cuda:
+        raise ValueError("status must be an int32 CUDA tensor")
+    _check(lib().dsa_selftest_wait_timeout(_ptr(status), _stream(status.device)), "dsa_selftest_wait_timeout")
 
 
 def insert_key(fmt: str, k: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,

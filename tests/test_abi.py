@@ -55,6 +55,7 @@ def test_host_argument_checks(lib):
     assert lib.dsa_decode_layout(None, 0, None, 0, -1, None, None, None) == -1
     assert lib.dsa_decode_layout(16, 1, 16, 2, 2, 16, 16, None) == -1        # fewer seq_lens than requests
     assert lib.dsa_score_paged(4, *([0] * 21)) == -2
+    assert lib.dsa_selftest_wait_timeout(None, None) == -1
     assert lib.dsa_quantize_queries_rg(16, 4096, 128, 48, 1, 16, 16, None) == -2      # 48 heads
     assert lib.dsa_quantize_queries_rg(None, 0, 128, 64, 0, None, None, None) == 0    # no rows
     assert lib.dsa_quantize_queries_rg(16, 4096, 100, 32, 1, 16, 16, None) == -1     # head stride < 128

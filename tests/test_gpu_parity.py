@@ -354,3 +354,21 @@ def test_graphed_step_matches_eager(cuda_lib):
     assert ix.status_bits() == 0
     for r in range(min(wl.R, wl.num_rows)):
         assert got[r, 0] == 0 and np.all(got[r, 1:] == -1), r
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable(cuda_lib):
+    """Failure detection: a pipeline wait on a barrier nothing completes gives
+    up after its limit, the host reads the timeout bit, and the next calls run."""
+    import time
+    import torch
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    cuda_lib.selftest_wait_timeout(status)
+    torch.cuda.synchronize()
+    assert 0.5 < time.time() - t0 < 30.0
+    assert int(status.item()) == 8
+    wl = make_workload("tiny_fp8", fmt="fp8", seed=4, R=2, seq=(200, 300), qlen=(1, 2), topk=16)
+    g = gpu_run(wl)
+    o = oracle_run(wl)
+    assert g["status"] == 0
+    check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, range(wl.num_rows))
