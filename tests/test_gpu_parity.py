@@ -372,3 +372,19 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable(cuda_lib):
     o = oracle_run(wl)
     assert g["status"] == 0
     check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, range(wl.num_rows))
+
+
+def test_more_rows_and_segments_than_the_plan_keeps_on_chip(cuda_lib):
+    """4200 one-row requests: more row bounds and segments than the plan keeps
+    in shared memory (4096 of each), so its global-memory paths run; sampled
+    rows against the oracle, all rows' bounds exactly."""
+    wl = make_workload("tiny_fp8", fmt="fp8", seed=33, R=4200, seq=(1, 300), qlen=(1, 1), pad_rows=5, topk=32)
+    assert wl.num_rows > 4096
+    g = gpu_run(wl)
+    assert g["status"] == 0
+    rng = np.random.default_rng(1)
+    rows = sorted(set(rng.choice(wl.num_rows - 5, 40, replace=False).tolist() + [0, 4095, 4096, 4199, wl.num_rows - 1]))
+    o = oracle_run(wl, rows=rows)
+    assert np.array_equal(g["row_ends"], o["row_ends"]) and np.array_equal(g["starts"], o["starts"])
+    check_logits(g["logits"], o["scores"], o["row_ends"], rows)
+    check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, rows)
