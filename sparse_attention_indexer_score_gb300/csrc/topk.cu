@@ -34,7 +34,7 @@ constexpr int kRefineCap = 3584;   // level-1 candidates kept in shared memory
 constexpr int kLevel3Cap = 512;    // level-3 candidates kept in shared memory
 constexpr int kWinCap = 4096;      // level-1 winners a CTA buffers in shared memory (k up to this)
 constexpr int kRing = 3;           // score tiles in flight per CTA (shared-memory ring)
-constexpr int kSpanMin = 2 * kChunk;   // shortest span worth a CTA of its own
+constexpr int kSpanMin = 2 * kChunk;   // shortest span worth a CTA of its own (rows this long stay whole)
 constexpr int kSelDynSmem = kRing * kChunk * sizeof(float) + kRefineCap * sizeof(uint2) +
                             kLevel3Cap * sizeof(uint2) + kWinCap * sizeof(int);
 
@@ -528,11 +528,16 @@ int launch_select(const float* logits, float* logits_fill, int64_t ld, int64_t w
     a.cand = reinterpret_cast<uint2*>(ws + L.cand);
     if (rows == 0 || (k == 0 && (!logits_fill || width == 0))) return DSA_OK;
     if (rows > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
-    // Span per CTA: about four CTAs per SM over rows x width, at least kSpanMin
-    // positions, a multiple of kChunk.
-    const int64_t target = 4 * static_cast<int64_t>(device_sm_count());
+    // Span per CTA: about four CTAs per SM over rows x width, a multiple of
+    // kChunk, at least kSpanMin positions (rows that short stay whole: a split
+    // row pays for its merge) -- unless spans of kSpanMin would leave fewer
+    // CTAs than SMs (a few long rows), when spans go down to kChunk.
+    const int64_t sms = device_sm_count();
+    const int64_t target = 4 * sms;
     int64_t span = (rows * width + target - 1) / target;
-    span = span < kSpanMin ? kSpanMin : span;
+    const bool few = width > kSpanMin && rows * ((width + kSpanMin - 1) / kSpanMin) < sms;
+    const int64_t span_min = few ? kChunk : kSpanMin;
+    span = span < span_min ? span_min : span;
     span = (span + kChunk - 1) / kChunk * kChunk;
     if (span > (int64_t(1) << 30)) span = int64_t(1) << 30;
     a.span = static_cast<int>(span);
