@@ -241,8 +241,6 @@ __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[3
           "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
         : "r"(taddr));
 }
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
 // 32 lanes x 64 consecutive 32-bit columns (two query rows of one tile).
 __device__ __forceinline__ void tc_ld_32x32b_x64(uint32_t taddr, uint32_t (&v)[64]) {
     asm volatile(
