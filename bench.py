@@ -274,7 +274,7 @@ def run_ours(args, wl, rank, world, local_rank):
     from sparse_attention_indexer_score_gb300 import build as _b
     _b.build()
     from sparse_attention_indexer_score_gb300 import dsa
-    from sparse_attention_indexer_score_gb300.step import DecodeIndexer, GraphedStep
+    from sparse_attention_indexer_score_gb300.step import DecodeIndexer, GraphedStep, StepPipeline
     from dsa_case import bf16_tensor
 
     dev = torch.device("cuda", local_rank)
@@ -370,8 +370,10 @@ def run_ours(args, wl, rank, world, local_rank):
     kernel_ms /= args.steps
 
     # End to end through the public API from pinned host buffers, every step
-    # copying its inputs in and its top-k back: the graph-captured step a
-    # serving loop replays (one GraphedStep per cache replica), and eager calls.
+    # copying its inputs in and its top-k back: the serving loop's pipeline
+    # (StepPipeline: copies of step i +- 1 overlapped with step i's compute,
+    # cycling the cache replicas), the graph-captured step replayed one at a
+    # time (one GraphedStep per cache replica), and eager calls.
     pinned = {k: v.pin_memory() for k, v in host.items()}
     h_top = torch.empty((wl.num_rows, wl.topk), dtype=torch.int32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
@@ -395,7 +397,13 @@ def run_ours(args, wl, rank, world, local_rank):
         ix.cache = caches[r]
         gsteps.append(GraphedStep(ix, like, max_q))      # staging buffers filled from `like`
     h2d_graph, d2h_graph = gsteps[0].staging_bytes, gsteps[0].host_topk.numel() * 4
-    e2e_ms = timed_e2e(lambda i: gsteps[i % n_rep].replay())
+    e2e_graphed_ms = timed_e2e(lambda i: gsteps[i % n_rep].replay())
+    pipe = StepPipeline(ix, like, max_q, caches=caches)
+    pipe.run(2 * n_rep)                                   # warm-up
+    torch.cuda.synchronize()
+    p_start, p_end = pipe.run(e2e_steps)
+    torch.cuda.synchronize()
+    e2e_ms = p_start.elapsed_time(p_end) * args.steps / e2e_steps
 
     def eager_step(i):
         for k in d:
@@ -404,7 +412,8 @@ def run_ours(args, wl, rank, world, local_rank):
         h_top.copy_(topk_out, non_blocking=True)
     e2e_eager_ms = timed_e2e(eager_step)
 
-    step_ms, e2e_ms, e2e_eager_ms, kernel_ms = max_over_ranks([step_ms, e2e_ms, e2e_eager_ms, kernel_ms], dev)
+    step_ms, e2e_ms, e2e_graphed_ms, e2e_eager_ms, kernel_ms = max_over_ranks(
+        [step_ms, e2e_ms, e2e_graphed_ms, e2e_eager_ms, kernel_ms], dev)
     if rank != 0:
         return
     value = whole_job_rate(ab["scored"], args.steps, world, step_ms)
@@ -431,8 +440,12 @@ def run_ours(args, wl, rank, world, local_rank):
                      "step_frac": (ab["step"] / (step_ms / args.steps / 1e3) / 1e9) / peaks["hbm_gbs"]},
         "e2e": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d_graph, "d2h_bytes_per_step": d2h_graph,
-                "how": ("GraphedStep replayed once per step: one copy of the step's inputs from a pinned "
-                        "staging buffer, the step, and the top-k copy back, all in the timed region")},
+                "how": ("StepPipeline: each step copies its inputs in from a pinned staging buffer and its "
+                        "top-k back, overlapped with the neighbouring steps' compute on two copy streams; "
+                        "device time from the first copy in to the last copy out")},
+        "e2e_graphed": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_graphed_ms), "unit": UNIT,
+                        "h2d_bytes_per_step": h2d_graph, "d2h_bytes_per_step": d2h_graph,
+                        "how": "GraphedStep replayed one step at a time: copy in, step, copy back, serialised"},
         "e2e_eager": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_eager_ms), "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "how": "eager public-API calls per step, the same host copies in the timed region"},

@@ -68,28 +68,20 @@ class DecodeIndexer:
         return int(self.status.item())
 
 
-class GraphedStep:
-    """A decode step captured as one CUDA graph, as a serving loop runs it: one
-    host-to-device copy of the step's inputs from a pinned staging buffer, the
-    step itself (prepare_step, scoring, top-k), and one copy of the top-k
-    positions back to a pinned host buffer.
-
-    ``inputs`` holds pinned views ``q``, ``wv``, ``keys``, ``slots``,
-    ``seq_lens`` and ``query_lens`` into the staging buffer, shaped and typed
-    like the ``like`` tensors given; the caller fills them, calls ``replay()``
-    (current stream) and synchronises before reading ``host_topk``.
-    """
+class _Staging:
+    """One step's pinned host staging buffer with its named input views, the
+    device copy, and the top-k on the device and in pinned host memory."""
 
     NAMES = ("q", "wv", "keys", "slots", "seq_lens", "query_lens")
     ALIGN = 256
 
-    def __init__(self, ix: DecodeIndexer, like: dict, max_query_len: int):
+    def __init__(self, ix: DecodeIndexer, like: dict):
         offs, total = {}, 0
         for name in self.NAMES:
             t = like[name]
             offs[name] = total
             total += -(-t.numel() * t.element_size() // self.ALIGN) * self.ALIGN
-        self.staging_bytes = total
+        self.nbytes = total
         self.host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
         self.dev_buf = torch.empty(total, dtype=torch.uint8, device=ix.device)
 
@@ -103,10 +95,34 @@ class GraphedStep:
         rows = like["q"].shape[0]
         self.topk = torch.empty((rows, ix.k), dtype=torch.int32, device=ix.device)
         self.host_topk = torch.empty((rows, ix.k), dtype=torch.int32).pin_memory()
-        self.ix = ix
-        self.max_query_len = int(max_query_len)
         for name in self.NAMES:
             self.inputs[name].copy_(like[name])
+
+    def compute(self, ix: DecodeIndexer, max_query_len: int) -> None:
+        d = self.dev
+        ix.step(d["q"], d["wv"], d["keys"], d["slots"], d["seq_lens"], d["query_lens"], max_query_len,
+                topk_out=self.topk)
+
+
+class GraphedStep:
+    """A decode step captured as one CUDA graph, as a serving loop runs it: one
+    host-to-device copy of the step's inputs from a pinned staging buffer, the
+    step itself (prepare_step, scoring, top-k), and one copy of the top-k
+    positions back to a pinned host buffer.
+
+    ``inputs`` holds pinned views ``q``, ``wv``, ``keys``, ``slots``,
+    ``seq_lens`` and ``query_lens`` into the staging buffer, shaped and typed
+    like the ``like`` tensors given; the caller fills them, calls ``replay()``
+    (current stream) and synchronises before reading ``host_topk``.
+    """
+
+    NAMES = _Staging.NAMES
+
+    def __init__(self, ix: DecodeIndexer, like: dict, max_query_len: int):
+        self.ix = ix
+        self.max_query_len = int(max_query_len)
+        self.st = _Staging(ix, like)
+        self.inputs, self.host_topk, self.staging_bytes = self.st.inputs, self.st.host_topk, self.st.nbytes
         self._run()                      # first use outside capture (library and allocator set up)
         torch.cuda.synchronize(ix.device)
         self.graph = torch.cuda.CUDAGraph()
@@ -114,11 +130,91 @@ class GraphedStep:
             self._run()
 
     def _run(self) -> None:
-        self.dev_buf.copy_(self.host_buf, non_blocking=True)
-        d = self.dev
-        self.ix.step(d["q"], d["wv"], d["keys"], d["slots"], d["seq_lens"], d["query_lens"], self.max_query_len,
-                     topk_out=self.topk)
-        self.host_topk.copy_(self.topk, non_blocking=True)
+        self.st.dev_buf.copy_(self.st.host_buf, non_blocking=True)
+        self.st.compute(self.ix, self.max_query_len)
+        self.st.host_topk.copy_(self.st.topk, non_blocking=True)
 
     def replay(self) -> None:
         self.graph.replay()
+
+
+class StepPipeline:
+    """Decode steps with their host copies overlapped, as a serving loop runs
+    them back to back: step i's inputs are copied in (one copy from a pinned
+    staging buffer, on an input stream) while step i - 1 computes, and step
+    i's top-k is copied back (on an output stream) while step i + 1 computes.
+    Two staging sets alternate; each step's compute is a CUDA graph replayed
+    on the stream current at construction, and events order the three
+    streams, so every step still copies its own inputs in and its own result
+    out.
+
+    caches: optional list of key-cache tensors laid out like ``ix.cache``;
+    step i reads caches[i % len(caches)] (one graph per set and cache).
+    A serving loop passes none: every step reads the indexer's own cache.
+    ``inputs(i)`` / ``host_topk(i)`` are the pinned views of step i's set.
+    ``run(n)`` issues n steps and returns the timing events (start, end)
+    bracketing them on the device.
+    """
+
+    def __init__(self, ix: DecodeIndexer, like: dict, max_query_len: int, caches=None):
+        self.ix = ix
+        self.sets = [_Staging(ix, like) for _ in range(2)]
+        self.staging_bytes = self.sets[0].nbytes
+        caches = list(caches) if caches else [ix.cache]
+        own = ix.cache
+        dev = ix.device
+        self.compute = torch.cuda.current_stream(dev)
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+        for st in self.sets:             # first use outside capture
+            st.dev_buf.copy_(st.host_buf)
+            st.compute(ix, max_query_len)
+        torch.cuda.synchronize(dev)
+        self.graphs = []                 # [cache][set]
+        for c in caches:
+            ix.cache = c
+            row = []
+            for st in self.sets:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    st.compute(ix, max_query_len)
+                row.append(g)
+            self.graphs.append(row)
+        ix.cache = own
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.out_done = [torch.cuda.Event() for _ in range(2)]
+        for e in self.computed + self.out_done:
+            e.record(self.compute)
+
+    def inputs(self, i: int) -> dict:
+        return self.sets[i % 2].inputs
+
+    def host_topk(self, i: int) -> torch.Tensor:
+        return self.sets[i % 2].host_topk
+
+    def run(self, n: int):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.compute):
+            start.record(self.compute)
+            self.s_in.wait_event(start)
+            self.s_out.wait_event(start)
+            for i in range(n):
+                k = i % 2
+                st = self.sets[k]
+                with torch.cuda.stream(self.s_in):
+                    self.s_in.wait_event(self.computed[k])      # the set's previous step has read its inputs
+                    st.dev_buf.copy_(st.host_buf, non_blocking=True)
+                    self.in_ready[k].record(self.s_in)
+                self.compute.wait_event(self.in_ready[k])
+                self.compute.wait_event(self.out_done[k])       # its previous top-k has left the device
+                self.graphs[i % len(self.graphs)][k].replay()
+                self.computed[k].record(self.compute)
+                with torch.cuda.stream(self.s_out):
+                    self.s_out.wait_event(self.computed[k])
+                    st.host_topk.copy_(st.topk, non_blocking=True)
+                    self.out_done[k].record(self.s_out)
+            self.compute.wait_stream(self.s_in)
+            self.compute.wait_stream(self.s_out)
+            end.record(self.compute)
+        return start, end

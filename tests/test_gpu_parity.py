@@ -337,7 +337,7 @@ def test_graphed_step_matches_eager(cuda_lib):
                 keys=bf16_tensor(wl.step_key_bits, "cpu"), slots=torch.from_numpy(wl.step_slots),
                 seq_lens=torch.from_numpy(wl.seq_lens), query_lens=torch.from_numpy(wl.query_lens))
     g = GraphedStep(ix, like, int(wl.query_lens.max()))
-    assert all(g.inputs[k].is_pinned() for k in g.NAMES) and g.host_topk.is_pinned()
+    assert all(g.inputs[k].is_pinned() for k in GraphedStep.NAMES) and g.host_topk.is_pinned()
     for _ in range(3):
         g.host_topk.fill_(-7)
         g.replay()
@@ -388,3 +388,33 @@ def test_more_rows_and_segments_than_the_plan_keeps_on_chip(cuda_lib):
     assert np.array_equal(g["row_ends"], o["row_ends"]) and np.array_equal(g["starts"], o["starts"])
     check_logits(g["logits"], o["scores"], o["row_ends"], rows)
     check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, rows)
+
+
+def test_step_pipeline_matches_eager(cuda_lib):
+    """Steps with their copies overlapped on separate streams give the eager
+    step's top-k sets in both staging sets, step after step."""
+    import torch
+    from sparse_attention_indexer_score_gb300.step import DecodeIndexer, StepPipeline
+    wl = make_workload("tiny_fp8", fmt="fp8", seed=22, R=6, seq=(300, 2000), qlen=(1, 4), pad_rows=2, topk=100)
+    want = gpu_run(wl)["topk"]
+    dev = torch.device("cuda")
+    ix = DecodeIndexer(wl.fmt, wl.num_pages, torch.from_numpy(wl.block_table), torch.from_numpy(wl.gamma),
+                       torch.from_numpy(wl.beta), wl.eps, wl.num_rows, wl.topk, dev)
+    for q in range(wl.R):
+        kb, sl = wl.prefill(q)
+        if kb.shape[0]:
+            ix.insert(bf16_tensor(kb, dev), torch.from_numpy(sl).to(dev))
+    like = dict(q=bf16_tensor(wl.q_bits, "cpu"), wv=bf16_tensor(wl.wv_bits, "cpu"),
+                keys=bf16_tensor(wl.step_key_bits, "cpu"), slots=torch.from_numpy(wl.step_slots),
+                seq_lens=torch.from_numpy(wl.seq_lens), query_lens=torch.from_numpy(wl.query_lens))
+    pipe = StepPipeline(ix, like, int(wl.query_lens.max()), caches=[ix.cache, ix.cache.clone()])
+    for rnd in range(3):
+        for i in range(2):
+            pipe.host_topk(i).fill_(-7)
+        pipe.run(6)
+        torch.cuda.synchronize()
+        for i in range(2):
+            got = pipe.host_topk(i).numpy()
+            for r in range(wl.num_rows):
+                assert sorted(got[r].tolist()) == sorted(want[r].tolist()), (rnd, i, r)
+    assert ix.status_bits() == 0
