@@ -70,8 +70,8 @@ constexpr int kMmaWarps = 2;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kPageWarp = kFirstEpiWarp + kEpiWarps;   // issues the second page of every tile
 constexpr int kScoreThreads = 32 * (kPageWarp + 1);
-// Second-page ids handed from warp 0 to the page warp: a ring of kPageRing
-// entries (>= 0 page, kNoPage none, kEndMark end of sequence).
+// Page ids handed from warp 0 to the page warp: a ring of kPageRing entries
+// {first page, second page} (>= 0 page, kNoPage none, kEndMark end of sequence).
 constexpr int kPageRing = 64, kNoPage = -1, kEndMark = -2;
 static_assert(kMmaWarps == kEpiGroups && kStages % kMmaWarps == 0 && kMaxStages % kMmaWarps == 0,
               "issuer w owns stages and group w");
@@ -104,7 +104,7 @@ constexpr int kGroupHistWords = kSegRows * kHistBins / 2;
 constexpr int OFF_SINFO = OFF_HIST + kEpiGroups * kGroupHistWords * 4;
 constexpr int OFF_AINFO = OFF_SINFO + kMaxStages * 16;       // int2[kAcc]: {tile in segment, segment} per accumulator
 constexpr int OFF_PRING = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;   // int[kPageRing]
-constexpr int OFF_BAR = OFF_PRING + kPageRing * 4;
+constexpr int OFF_BAR = OFF_PRING + kPageRing * 8;
 // full, empty, qfull, tfull (per accumulator and epilogue group), done.  A
 // group's accumulator barrier is used by the sequence positions it, it + 6, ...
 // of that group alone: one barrier per accumulator, filled by both issuers,
@@ -344,11 +344,11 @@ __device__ __forceinline__ bool count_wait(const uint32_t* c, uint32_t need, vol
     }
 }
 
-// Copies page h (0 or 1) of a tile, id pid, into stage s: its codes (FP8: one
-// 128-byte-swizzled box; MXFP4: one 64-byte-swizzled box; row-group: one box
-// per column group, group g at g * 2048 + h * 1024) and its 256 scale bytes.
-__device__ __forceinline__ void issue_page(const CUtensorMap* kmap, const CUtensorMap* smap, uint8_t* smem,
-                                           uint64_t* bar, int s, int stage_bytes, bool fp4, bool rg, int h, int pid) {
+// Copies the codes of page h (0 or 1) of a tile, id pid, into stage s (FP8:
+// one 128-byte-swizzled box; MXFP4: one 64-byte-swizzled box; row-group: one
+// box per column group, group g at g * 2048 + h * 1024).
+__device__ __forceinline__ void issue_codes(const CUtensorMap* kmap, uint8_t* smem, uint64_t* bar, int s,
+                                            int stage_bytes, bool fp4, bool rg, int h, int pid) {
     uint8_t* dst = smem + OFF_TILES + s * stage_bytes;
     if (rg) {
 #pragma unroll
@@ -356,6 +356,10 @@ __device__ __forceinline__ void issue_page(const CUtensorMap* kmap, const CUtens
     } else {
         tma_load_3d(dst + h * (fp4 ? kFp4KeyBytes : kPageSmem), kmap, 0, 0, pid, bar);
     }
+}
+// Copies the 256 scale bytes of page h of a tile into stage s.
+__device__ __forceinline__ void issue_scales(const CUtensorMap* smap, uint8_t* smem, uint64_t* bar, int s, int h,
+                                             int pid) {
     tma_load_2d(smem + OFF_RAWSC + s * 512 + h * 256, smap, 0, pid, bar);
 }
 
@@ -381,13 +385,13 @@ struct Producer {
     bool rg;             // row-group placement: packed boxes per column group
     int lg;              // log2 of the ring's stage count
     int stage_bytes;     // shared memory of a stage's codes
-    int* page_ring;      // second-page ids for the page warp
+    int2* page_ring;     // {first, second} page ids for the page warp
     uint32_t* published; // entries written (release)
     const uint32_t* consumed;   // entries the page warp has taken (acquire)
     int cur = -1, i_seg = 0, it = 0;
 
-    // Hands position it's second-page entry to the page warp (ring of kPageRing).
-    __device__ __forceinline__ bool publish(const ScoreArgs& p, int v) {
+    // Hands position it's page ids to the page warp (ring of kPageRing).
+    __device__ __forceinline__ bool publish(const ScoreArgs& p, int2 v) {
         if (it >= kPageRing && !count_wait(consumed, static_cast<uint32_t>(it - kPageRing + 1), abort, p.status))
             return false;
         page_ring[it & (kPageRing - 1)] = v;
@@ -445,13 +449,14 @@ struct Producer {
         if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
         reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(j, sg, i_seg - 1, 0);
         set_last_tile((i_seg - 1) & 1, it % kMmaWarps, it);
-        // the stage's full barrier takes two arrivals: this warp's (first page) and the page warp's
-        if (!publish(p, p1 >= 0 ? p1 : kNoPage)) return false;
+        // the stage's full barrier takes two arrivals: this warp's (the first page's codes) and
+        // the page warp's (the second page's codes, both pages' scales)
+        if (!publish(p, make_int2(p0 >= 0 ? p0 : kNoPage, p1 >= 0 ? p1 : kNoPage))) return false;
         if (p0 < 0) {
             mbar_arrive(full + s);   // no valid page: scores of these keys are unspecified
         } else {
-            mbar_arrive_expect_tx(full + s, (fp4 ? kFp4PageTx : kFp8PageTx) + 256);
-            issue_page(kmap, smap, smem, full + s, s, stage_bytes, fp4, rg, 0, p0);
+            mbar_arrive_expect_tx(full + s, fp4 ? kFp4PageTx : kFp8PageTx);
+            issue_codes(kmap, smem, full + s, s, stage_bytes, fp4, rg, 0, p0);
         }
         ++it;
         return true;
@@ -463,7 +468,7 @@ struct Producer {
             const int s = it & ((1 << lg) - 1);
             if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
             reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(-1, -1, -1, 0);
-            if (!publish(p, kEndMark)) return false;
+            if (!publish(p, make_int2(kEndMark, kEndMark))) return false;
             mbar_arrive(full + s);
             ++it;
         }
@@ -525,30 +530,36 @@ __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, 
 }
 
 // Warp kPageWarp.  Follows warp 0's positions through the page ring and
-// copies each tile's second page into the same stage, arming the stage's full
-// barrier for its own bytes (it waits for the same free-stage phase as warp 0;
-// the stage cannot move on before this warp's arrival).
+// copies each tile's second page and both pages' scales into the same stage,
+// arming the stage's full barrier for its own bytes (it waits for the same
+// free-stage phase as warp 0; the stage cannot move on before this warp's
+// arrival).
 __device__ __forceinline__ void page_role(const ScoreArgs& p, const CUtensorMap* kmap, const CUtensorMap* smap,
                                           uint8_t* smem, uint64_t* full, uint64_t* empty, const uint32_t* published,
                                           uint32_t* consumed, volatile int* abort) {
     if ((threadIdx.x & 31) != 0) return;
     const bool fp4 = fmt_fp4(p.fmt), rg = (p.fmt == DSA_FMT_MXFP4_RG);
     const int lg = ring_stages_log2(p.fmt), stage_bytes = ring_stage_bytes(p.fmt);
-    const int* ring = reinterpret_cast<const int*>(smem + OFF_PRING);
+    const int2* ring = reinterpret_cast<const int2*>(smem + OFF_PRING);
     int ends = 0;
     for (int j = 0; ends < kMmaWarps; ++j) {
         if (!count_wait(published, static_cast<uint32_t>(j + 1), abort, p.status)) break;
-        const int v = ring[j & (kPageRing - 1)];
+        const int2 v = ring[j & (kPageRing - 1)];
         const int s = j & ((1 << lg) - 1);
         if (!mbar_wait(empty + s, ((j >> lg) & 1) ^ 1, abort, p.status)) break;
-        if (v >= 0) {
-            mbar_arrive_expect_tx(full + s, (fp4 ? kFp4PageTx : kFp8PageTx) + 256);
-            issue_page(kmap, smap, smem, full + s, s, stage_bytes, fp4, rg, 1, v);
+        const uint32_t bytes = (v.x >= 0 ? 256u : 0u) + (v.y >= 0 ? (fp4 ? kFp4PageTx : kFp8PageTx) + 256u : 0u);
+        if (bytes) {
+            mbar_arrive_expect_tx(full + s, bytes);
+            if (v.x >= 0) issue_scales(smap, smem, full + s, s, 0, v.x);
+            if (v.y >= 0) {
+                issue_codes(kmap, smem, full + s, s, stage_bytes, fp4, rg, 1, v.y);
+                issue_scales(smap, smem, full + s, s, 1, v.y);
+            }
         } else {
             mbar_arrive(full + s);
         }
         smem_add_release(consumed, 1u);
-        if (v == kEndMark) ++ends;
+        if (v.x == kEndMark) ++ends;
     }
 }
 
@@ -907,7 +918,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     args.fmt == DSA_FMT_MXFP4_RG,
                     ring_stages_log2(args.fmt),
                     ring_stage_bytes(args.fmt),
-                    reinterpret_cast<int*>(smem + OFF_PRING),
+                    reinterpret_cast<int2*>(smem + OFF_PRING),
                     published,
                     consumed};
         producer_role(pr, args, t0, t1, seg, S, Ts, T);
