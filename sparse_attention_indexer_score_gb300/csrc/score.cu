@@ -23,8 +23,9 @@
 //              (thread = key), ReLU-weighted head sum, FP32 key scale, logits
 //              store, and a shared-memory histogram of the scores for the
 //              top-k pass.
-//   warp 11    second copy issuer: each tile's second page (warp 0 issues the
-//              first), so two threads feed the copy engine.
+//   warp 11    second copy issuer: each tile's second page and both pages'
+//              scales (warp 0 copies the first page's codes), so two threads
+//              feed the copy engine.
 //
 // Formats: FP8 and FP8-MX use kind::f8f6f4 (E4M3 x E4M3) and multiply the
 // per-key scale in the epilogue.  MXFP4 keeps its codes packed and uses
@@ -41,7 +42,7 @@
 namespace dsa {
 
 constexpr int kStages = 8;                    // ring stages of 16 KB (FP8 codes)
-constexpr int kMaxStages = 16;                // ring stages of 8 KB (packed token-major MXFP4)
+constexpr int kMaxStages = 16;                // ring stages of 8 KB (packed MXFP4, either placement)
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * 128;   // codes of 128 keys in shared memory
 constexpr int kPageSmem = 64 * 128;           // one FP8 page's codes in shared memory
@@ -68,7 +69,7 @@ constexpr int kEpiWarps = 4 * kEpiGroups;
 // group w drains.
 constexpr int kMmaWarps = 2;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
-constexpr int kPageWarp = kFirstEpiWarp + kEpiWarps;   // issues the second page of every tile
+constexpr int kPageWarp = kFirstEpiWarp + kEpiWarps;   // copies each tile's second page and both scale boxes
 constexpr int kScoreThreads = 32 * (kPageWarp + 1);
 // Page ids handed from warp 0 to the page warp: a ring of kPageRing entries
 // {first page, second page} (>= 0 page, kNoPage none, kEndMark end of sequence).
@@ -103,7 +104,7 @@ constexpr int kGroupHistWords = kSegRows * kHistBins / 2;
 // int4[kMaxStages]: {tile in segment, segment, segment ordinal in this CTA's sequence}
 constexpr int OFF_SINFO = OFF_HIST + kEpiGroups * kGroupHistWords * 4;
 constexpr int OFF_AINFO = OFF_SINFO + kMaxStages * 16;       // int2[kAcc]: {tile in segment, segment} per accumulator
-constexpr int OFF_PRING = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;   // int[kPageRing]
+constexpr int OFF_PRING = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;   // int2[kPageRing]
 constexpr int OFF_BAR = OFF_PRING + kPageRing * 8;
 // full, empty, qfull, tfull (per accumulator and epilogue group), done.  A
 // group's accumulator barrier is used by the sequence positions it, it + 6, ...
@@ -364,8 +365,9 @@ __device__ __forceinline__ void issue_scales(const CUtensorMap* smap, uint8_t* s
 }
 
 // Issues the loads of one tile (lane 0 of the producer warp): the segment's
-// query rows when the segment changes, then the key pages and scales into the
-// next ring stage, tagged with {tile in segment, segment, segment ordinal}.
+// query rows when the segment changes, then the first page's codes into the
+// next ring stage, tagged with {tile in segment, segment, segment ordinal};
+// the page ids go to the page warp, which copies the rest of the tile.
 //
 // Query buffer b holds the segments of ordinals b, b + 2, ...  Before it is
 // refilled, the MMAs of the segment it held must be done: every issuer's last
@@ -478,7 +480,7 @@ struct Producer {
 
 // Warp 0.  Its 32 lanes resolve the segments and block-table entries of 32
 // tiles at once (the next batch's loads are in flight while lane 0 issues the
-// current batch's TMA copies), so block-table latency is paid once per batch.
+// current batch's tiles), so block-table latency is paid once per batch.
 // After its own range the warp claims chunks of the pool until none is left.
 __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, int t0, int t1, int seg, int S,
                                               int Ts, int T) {
@@ -875,7 +877,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMaxStages; ++s) {
-            mbar_init(full + s, 2);   // warp 0 (first page) and the page warp (second page)
+            mbar_init(full + s, 2);   // warp 0 (first page's codes) and the page warp (the rest)
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) mbar_init(qfull + b, 1);
