@@ -9,8 +9,13 @@ Prints one JSON line.  ``value`` is scored keys per second (sum of the row
 bounds over the timed steps / device time) with inputs resident in HBM.  The
 K timed steps run as one captured CUDA graph; the key cache is replicated
 until the replicas exceed three times the L2 size and the steps use them in
-turn, so every step reads its keys from HBM.  ``--impl reference`` times the
-CPU oracle instead.
+turn, so every step reads its keys from HBM.  ``e2e`` is the same metric
+through the public API with every step copying its inputs in from pinned host
+memory and its top-k back (``StepPipeline``; ``e2e_graphed`` and
+``e2e_eager`` run the step one at a time).  ``--fmt`` runs a workload in
+another cache format (e.g. ``mxfp4_rg``); ``--op`` times QueryNorm or the
+DCP top-k merge instead of the step.  ``--impl reference`` times the CPU
+oracle instead.
 
 Multi-GPU (``torchrun``): every rank runs its own replica of the workload
 (the step has no exchange); the timing is the max over ranks and ``value``
