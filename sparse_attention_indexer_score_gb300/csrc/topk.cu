@@ -59,15 +59,6 @@ __device__ __forceinline__ int clamp_end(const int32_t* ends, int row, int64_t w
     return static_cast<int>(e < 0 ? 0 : (e > width ? width : e));
 }
 
-// Copies a row's 2048-bin histogram to shared memory, all loads in flight.
-__device__ __forceinline__ void load_hist(unsigned* h, const unsigned* ghist) {
-    unsigned r[kHistBins / kSelThreads];
-#pragma unroll
-    for (int i = 0; i < kHistBins / kSelThreads; ++i) r[i] = ghist[i * kSelThreads + threadIdx.x];
-#pragma unroll
-    for (int i = 0; i < kHistBins / kSelThreads; ++i) h[i * kSelThreads + threadIdx.x] = r[i];
-}
-
 // Finds, over `bins` counts in shared memory, the bin B where the count from
 // the top first reaches `need`; stores B and the count strictly above it.
 // Leaves both untouched when the counts never reach `need`.
@@ -86,6 +77,32 @@ __device__ void find_boundary(const unsigned* h, int bins, int need, int* out_bi
             *out_above = cum;
         }
         cum += c;
+    }
+}
+
+// This thread's four adjacent bins of a 2048-bin histogram, for
+// find_boundary4: bins 2048 - 4 (tid + 1) .. 2048 - 4 tid - 1, so that
+// thread 0 holds the top four.
+static_assert(kHistBins == 4 * kSelThreads, "four histogram bins per thread");
+__device__ __forceinline__ uint4 hist_quad(const unsigned* h) {
+    return reinterpret_cast<const uint4*>(h)[kHistBins / 4 - 1 - threadIdx.x];
+}
+
+// find_boundary over a 2048-bin histogram held as hist_quad in registers.
+__device__ void find_boundary4(uint4 q, int need, int* out_bin, int* out_above, int* tmp) {
+    const int first = kHistBins - 4 * (threadIdx.x + 1);
+    const int c[4] = {static_cast<int>(q.x), static_cast<int>(q.y), static_cast<int>(q.z), static_cast<int>(q.w)};
+    const int local = c[0] + c[1] + c[2] + c[3];
+    int total;
+    const int inc = block_inclusive_scan(local, tmp, &total);
+    int cum = inc - local;   // count in bins above this thread's four
+#pragma unroll
+    for (int j = 3; j >= 0; --j) {
+        if (cum < need && cum + c[j] >= need) {
+            *out_bin = first + j;
+            *out_above = cum;
+        }
+        cum += c[j];
     }
 }
 
@@ -194,7 +211,7 @@ __device__ __forceinline__ void warp_rank_select(const uint2* c3, int n3, int32_
 
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs a, int pdl) {
     __shared__ unsigned h1[kHistBins];   // level-1 histogram, then level 3
-    __shared__ unsigned h2[kHistBins];   // level-2 histogram
+    __shared__ __align__(16) unsigned h2[kHistBins];   // level-2 histogram (read as uint4)
     __shared__ int tmp[32];
     __shared__ int s_b1, s_a1, s_b2, s_a2, s_b3, s_a3;
     __shared__ int s_win, s_cand, s_w2, s_c3, s_w3, s_tie, s_last, s_wbase, s_cbase;
@@ -240,7 +257,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     // ring of kRing tiles in shared memory.  Each thread copies, and later
     // reads, the same 8 scores of a tile: positions base + 4 * tid + j and
     // base + kChunk / 2 + 4 * tid + j (j < 4), so no barrier guards the ring.
-    load_hist(h1, ghist);
     const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
     auto issue_tile = [&](int i) {   // tile i of the span into ring slot i % kRing
         const int base = lo32 + i * kChunk;
@@ -262,13 +278,14 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     };
 #pragma unroll
     for (int i = 0; i < kRing; ++i) issue_tile(i);
+    const uint4 hq1 = hist_quad(ghist);   // in flight with the tiles
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0;
     if (threadIdx.x == 0) {
         s_b1 = 0; s_a1 = 0; s_b2 = 0; s_a2 = 0; s_b3 = 0; s_a3 = 0;
         s_win = 0; s_cand = 0; s_w2 = 0; s_c3 = 0; s_w3 = 0; s_tie = 0;
     }
     __syncthreads();
-    find_boundary(h1, kHistBins, k, &s_b1, &s_a1, tmp);
+    find_boundary4(hq1, k, &s_b1, &s_a1, tmp);
     __syncthreads();
     const uint32_t B1 = static_cast<uint32_t>(s_b1);
     const int above1 = s_a1;
@@ -377,7 +394,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
         __syncthreads();
         if (!s_last) return;
         __threadfence();
-        load_hist(h2, ghist2);
         ncand = *reinterpret_cast<volatile int*>(ctr + 1);
         const bool dropped = *reinterpret_cast<volatile int*>(ctr + 3) != 0;
         cand_src = (!dropped && ncand <= kCandCap) ? gcand : nullptr;
@@ -387,7 +403,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
 
     // ---- level 2: one pass over the candidates
     const int need = k - above1;
-    find_boundary(h2, kHistBins, need, &s_b2, &s_a2, tmp);
+    find_boundary4(hist_quad(split ? ghist2 : h2), need, &s_b2, &s_a2, tmp);
     __syncthreads();
     const uint32_t B2 = static_cast<uint32_t>(s_b2);
     const int above2 = s_a2;
