@@ -226,6 +226,23 @@ def oracle_sample(wl, budget_s: float, rng_seed: int = 0):
     return keys, secs, f"{used} of {wl.R} requests of {wl.name} (score + top-k of their rows)"
 
 
+def oracle_one_core(wl, budget_s: float):
+    """``oracle_sample`` on one host core: a child process whose BLAS and
+    OpenMP pools hold one thread, on the same workload.  Returns (scored keys,
+    seconds, desc), or None when the child fails."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, bench\nfrom synth import make_workload\n"
+            f"wl = make_workload({wl.name!r}, fmt={wl.fmt!r})\n"
+            f"print(json.dumps(bench.oracle_sample(wl, {float(budget_s)!r})))")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                           timeout=600)
+        keys, secs, desc = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, OSError, ValueError, IndexError):
+        return None
+    return int(keys), float(secs), str(desc)
+
+
 def run_reference(args, wl):
     """The oracle on the host cores: each step a bounded sample of the workload."""
     cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
@@ -462,6 +479,11 @@ def run_ours(args, wl, rank, world, local_rank):
         line["cpu_baseline"] = {"value": keys / secs if secs else None, "unit": UNIT,
                                 "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", 1)), "kind": "oracle",
                                 "sample": f"{desc}; {secs:.1f} s"}
+        one = oracle_one_core(wl, min(args.cpu_seconds, 1.0))
+        if one is not None:
+            k1, s1, d1 = one
+            line["cpu_baseline"]["one_core"] = {"value": k1 / s1 if s1 else None, "unit": UNIT, "cores": 1,
+                                                "sample": f"{d1}; {s1:.1f} s"}
     print(json.dumps(line))
 
 

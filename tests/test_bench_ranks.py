@@ -69,3 +69,13 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_one_core_oracle_sample_runs_in_a_child():
+    """The CPU baseline's one-core figure: the oracle sample in a child process
+    holding one BLAS thread scores every key of a small workload."""
+    from synth import make_workload
+    wl = make_workload("tiny_fp8")
+    keys, secs, desc = bench.oracle_one_core(wl, 1.0)
+    assert keys == int(wl.seq_lens.sum()) and secs > 0
+    assert desc.startswith(f"{wl.R} of {wl.R} requests")
