@@ -147,8 +147,28 @@ def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         d = json.load(open(path))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops_sustained"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1700.0, "source": "fallback"}
+
+
+NOMINAL_HBM_GBS = 7900.0
+# Dense tensor rate of the score kernel's MMA kind over bf16's, from the nominal
+# per-GPU figures (bf16 2.25, fp8 4.5, fp4 13.5 PFLOP/s).
+TENSOR_RATIO = {"fp8": 2.0, "fp8_mx": 2.0, "mxfp4": 6.0, "mxfp4_rg": 6.0}
+FLOPS_PER_SCORED_KEY = 2 * 32 * 128   # one row's 32 head dot products of 128 columns
+
+
+def tensor_side(scored_keys: int, kernel_ms: float, fmt: str, peaks: dict) -> dict:
+    """The score kernel against the tensor-core roof: algorithmic FLOPs per
+    launch over its event time, against the measured sustained bf16 rate times
+    the nominal ratio of the MMA's operand type."""
+    flops = FLOPS_PER_SCORED_KEY * scored_keys
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"] * TENSOR_RATIO[fmt]
+    return {"flops_per_launch": flops, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "peak_source": f"{peaks['source']} sustained bf16 x {TENSOR_RATIO[fmt]:g} (nominal {fmt} / bf16)"}
 
 
 def score_source_hash() -> str:
@@ -459,7 +479,9 @@ def run_ours(args, wl, rank, world, local_rank):
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": "score_kernel", "kernel_us": kernel_ms * 1e3,
                      "peak_source": f"{peaks['source']} HBM copy bandwidth",
-                     "step_frac": (ab["step"] / (step_ms / args.steps / 1e3) / 1e9) / peaks["hbm_gbs"]},
+                     "step_frac": (ab["step"] / (step_ms / args.steps / 1e3) / 1e9) / peaks["hbm_gbs"],
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "tensor": tensor_side(ab["scored"], kernel_ms, wl.fmt, peaks)},
         "e2e": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d_graph, "d2h_bytes_per_step": d2h_graph,
                 "how": ("StepPipeline: each step copies its inputs in from a pinned staging buffer and its "

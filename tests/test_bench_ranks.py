@@ -79,3 +79,13 @@ def test_one_core_oracle_sample_runs_in_a_child():
     keys, secs, desc = bench.oracle_one_core(wl, 1.0)
     assert keys == int(wl.seq_lens.sum()) and secs > 0
     assert desc.startswith(f"{wl.R} of {wl.R} requests")
+
+
+def test_tensor_side_of_the_roofline():
+    """8192 FLOPs per scored key (32 heads x 128 columns x multiply-add) over
+    the kernel time, against bf16's rate times the operand type's ratio."""
+    t = bench.tensor_side(1000, 1.0, "fp8", {"bf16_tflops": 1000.0, "source": "measured"})
+    assert t["flops_per_launch"] == 8_192_000
+    assert abs(t["achieved"] - 8.192e-3) < 1e-12 and t["peak"] == 2000.0
+    assert abs(t["frac"] - 8.192e-3 / 2000.0) < 1e-15
+    assert bench.tensor_side(1, 1.0, "mxfp4_rg", {"bf16_tflops": 1.0, "source": "x"})["peak"] == 6.0
