@@ -214,7 +214,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     __shared__ __align__(16) unsigned h2[kHistBins];   // level-2 histogram (read as uint4)
     __shared__ int tmp[32];
     __shared__ int s_b1, s_a1, s_b2, s_a2, s_b3, s_a3;
-    __shared__ int s_win, s_cand, s_w2, s_c3, s_w3, s_tie, s_last, s_wbase, s_cbase;
+    __shared__ unsigned long long s_wc;   // level-1 winners (bits 63..32) and candidates (31..0) placed
+    __shared__ int s_w2, s_c3, s_w3, s_tie, s_last, s_wbase, s_cbase;
     extern __shared__ float4 sel_dyn[];
     float4* ring = sel_dyn;                                                    // kRing tiles of scores
     uint2* cbuf = reinterpret_cast<uint2*>(sel_dyn + kRing * kChunk / 4);     // level-1 candidates
@@ -258,11 +259,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     // reads, the same 8 scores of a tile: positions base + 4 * tid + j and
     // base + kChunk / 2 + 4 * tid + j (j < 4), so no barrier guards the ring.
     const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
-    auto issue_tile = [&](int i) {   // tile i of the span into ring slot i % kRing
+    auto issue_tile = [&](int i) {   // tile i of the span into ring slot i % kRing (none past the span)
         const int base = lo32 + i * kChunk;
         float4* slot = ring + (i % kRing) * (kChunk / 4);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2 && base < hi; ++h) {
             const int p = base + h * (kChunk / 2) + 4 * threadIdx.x;
             const int avail = max(0, min(4, hi - p));
             float4* d = slot + h * (kChunk / 8) + threadIdx.x;
@@ -276,13 +277,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
         }
         cp_async_commit();
     };
+    const uint4 hq1 = hist_quad(ghist);   // first in flight, then the tiles
 #pragma unroll
     for (int i = 0; i < kRing; ++i) issue_tile(i);
-    const uint4 hq1 = hist_quad(ghist);   // in flight with the tiles
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0;
     if (threadIdx.x == 0) {
         s_b1 = 0; s_a1 = 0; s_b2 = 0; s_a2 = 0; s_b3 = 0; s_a3 = 0;
-        s_win = 0; s_cand = 0; s_w2 = 0; s_c3 = 0; s_w3 = 0; s_tie = 0;
+        s_wc = 0; s_w2 = 0; s_c3 = 0; s_w3 = 0; s_tie = 0;
     }
     __syncthreads();
     find_boundary4(hq1, k, &s_b1, &s_a1, tmp);
@@ -295,8 +296,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     // Classifies tile i (waiting for this thread's copies of it), then reuses
     // its slot for tile i + kRing.  Bit u of wm / cm marks value u as a winner
     // (key > kw) / candidate (kcand <= key <= kw); the warp's runs come from
-    // one scan of both counts and one shared add each, and only marked values
-    // are placed.
+    // one scan of both counts and one shared 64-bit add of both, and only
+    // marked values are placed.
     const uint32_t kw = top_bin ? 0xFFFFFFFFu : kwin - 1u;
     const uint32_t crange = kw - kcand;
     const int ntiles = (hi - lo32 + kChunk - 1) / kChunk;
@@ -329,13 +330,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
             const int y = __shfl_up_sync(0xFFFFFFFFu, inc, d);
             if (lane >= d) inc += y;
         }
-        int ow = 0, oc = 0;
-        if (lane == 31) {
-            if (inc >> 16) ow = atomicAdd(&s_win, inc >> 16);
-            if (inc & 0xFFFF) oc = atomicAdd(&s_cand, inc & 0xFFFF);
-        }
-        int pw = __shfl_sync(0xFFFFFFFFu, ow, 31) + (inc >> 16) - cw;
-        int pc = __shfl_sync(0xFFFFFFFFu, oc, 31) + (inc & 0xFFFF) - cc;
+        unsigned long long o = 0;   // one shared add reserves both runs
+        if (lane == 31 && inc)
+            o = atomicAdd(&s_wc, (static_cast<unsigned long long>(inc >> 16) << 32) | static_cast<unsigned>(inc & 0xFFFF));
+        o = __shfl_sync(0xFFFFFFFFu, o, 31);
+        int pw = static_cast<int>(o >> 32) + (inc >> 16) - cw;
+        int pc = static_cast<int>(o & 0xFFFFFFFFu) + (inc & 0xFFFF) - cc;
         const int tb = base + 4 * threadIdx.x;   // position of value 0 of this thread
         while (wm) {
             const int u = __ffs(wm) - 1;
@@ -364,21 +364,22 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     }
     cp_async_wait<0>();
     __syncthreads();
-    int ncand = s_cand;
+    const int nwin = static_cast<int>(s_wc >> 32), mycand = static_cast<int>(s_wc & 0xFFFFFFFFu);
+    int ncand = mycand;
     const uint2* cand_src = ncand <= kRefineCap ? cbuf : nullptr;
     if (!split && wbuffered)
-        for (int i = threadIdx.x; i < s_win; i += kSelThreads)
+        for (int i = threadIdx.x; i < nwin; i += kSelThreads)
             if (i < k) out[i] = wbuf[i];
     if (split) {
         // Publish this span's winners, candidates and level-2 counts; the last
         // span of the row to finish reads the row's totals back and settles it.
         if (threadIdx.x == 0) {
-            s_wbase = (wbuffered && s_win) ? atomicAdd(ctr + 0, s_win) : 0;
-            s_cbase = s_cand ? atomicAdd(ctr + 1, s_cand) : 0;
+            s_wbase = (wbuffered && nwin) ? atomicAdd(ctr + 0, nwin) : 0;
+            s_cbase = mycand ? atomicAdd(ctr + 1, mycand) : 0;
         }
         __syncthreads();
         if (wbuffered)
-            for (int i = threadIdx.x; i < s_win; i += kSelThreads)
+            for (int i = threadIdx.x; i < nwin; i += kSelThreads)
                 if (s_wbase + i < k) out[s_wbase + i] = wbuf[i];
         if (ncand <= kRefineCap)
             for (int i = threadIdx.x; i < ncand; i += kSelThreads)
