@@ -12,7 +12,7 @@ bounds, paged logits, top-k).
 Parity unpinned: the pages' claim that the MXFP4 scale is bit-exact with a
 particular compiled ``log2`` sequence (page *cutedsl.dsa.index*,
 ``mxfp4_scale``) is not reproduced; the exact mathematical definition printed
-there is used instead (reading A3).
+there is used instead (a reading of ours).
 """
 
 from . import codecs, indexer  # noqa: F401

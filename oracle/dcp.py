@@ -11,8 +11,8 @@ rank scores only its own keys, numbered consecutively in rank-local space,
 so a row's global bound E becomes the number of its keys below E.
 
 Page *cutedsl.dsa.overlap*: under DCP the indexer path ends with "the top-k
-merge and the local slots".  The merge is not printed; the reading (A22 in
-the design doc) is the plain one: every rank contributes its local top-k
+merge and the local slots".  The merge is not printed; the reading taken
+here is the plain one: every rank contributes its local top-k
 candidates (score, rank-local position), the k best of all of them by
 (score desc, global position asc) are the row's top-k, and a rank's local
 slots are the rank-local positions of the selected keys it owns.

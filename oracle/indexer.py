@@ -8,8 +8,7 @@ It follows three pages: *cutedsl.dsa.index* (query quantisation, key
 LayerNorm + quantise + insert, cache and query-row layouts), *cutedsl.dsa.overlap*
 (the order "wq_b -> DsaIndex -> scoring and top-k") and *amd.ops.fp4_indexer*
 (``decode_layout``, ``score_paged``, ``store_keys``).  Where the pages leave
-a step open, the reading taken is named in the docstring (A1..A17) and listed
-in DESIGN.md.
+a step open, the docstring states the reading taken ("a reading").
 
 Precision: FP32 where the pages compute in FP32 (LayerNorm, the scale and
 weight folds), exact arithmetic for the scale exponents, FP64 for the scores.
@@ -35,12 +34,12 @@ from .codecs import (
 
 HEADS, DIM, PAGE = 32, 128, 64
 Q_ROW_BYTES = HEADS * DIM            # one FP8 query row: 32 heads x 128 E4M3
-FP4_SCALES = HEADS * DIM // 2        # A6: scale bytes follow the 32 x 64 B of E2M1
+FP4_SCALES = HEADS * DIM // 2        # not printed; a reading: scale bytes follow the 32 x 64 B of E2M1
 FP4_QUERY_ROW = FP4_SCALES + HEADS * 4
 FP8_KEY_BYTES, FP8_PAGE_BYTES = PAGE * DIM, PAGE * (DIM + 4)          # 8192, 8448
 FP4_KEY_BYTES, FP4_PAGE_BYTES = PAGE * DIM // 2, PAGE * (DIM // 2 + 4)  # 4096, 4352
 WEIGHT_SCALE = (HEADS * DIM) ** -0.5   # 1/64, page *cutedsl.dsa.index*, ``DsaIndex.fp8_query``
-FP4_WEIGHT = WEIGHT_SCALE              # A7: "the indexer weight scale"
+FP4_WEIGHT = WEIGHT_SCALE              # not printed ("the indexer weight scale"); a reading: the FP8 fold's 1/64
 FP8_AMAX_FLOOR = np.float32(1e-10)     # ``DsaIndex.fp8_query``: amax starts at 1e-10
 MX_AMAX_FLOOR = 6.0 * 2.0 ** -126      # ``mxfp4_scale``: max(amax, 6 * 2^-126)
 
@@ -48,11 +47,13 @@ FORMATS = ("fp8", "fp8_mx", "mxfp4", "mxfp4_rg")
 # "mxfp4_rg" (page *amd.ops.fp4_indexer*, ``cache_views``): the MXFP4 codes and
 # scales of "mxfp4" placed group-major ("row-group") within the 4352-byte page
 # section: payload byte j of column group g of token t at g * 1024 + t * 16 + j,
-# the group's UE8M0 byte at 4096 + g * 64 + t (A23).
+# the group's UE8M0 byte at 4096 + g * 64 + t (a reading: the page prints
+# the views' strides, not their writer).
 RG_GROUP_BYTES, RG_SCALE_GROUP = 1024, 64
 # Row-group query scales (page *amd.ops.fp4_indexer*, ``quantize_queries``: a
 # [rows, 1, 4, 16, 4] uint8 tensor, 256 bytes a row): the scale of block g of
-# head h at g * 64 + h, group-major like the cache's scale views (A27).
+# head h at g * 64 + h, group-major like the cache's scale views (a reading:
+# the page fixes the shape, not the order).
 RG_QUERY_HEAD_SLOTS = 64
 RG_QUERY_HEADS = (16, 32, 64)
 
@@ -71,7 +72,7 @@ def page_bytes(fmt: str) -> int:
 
 def fp8_scale_exponent(amax) -> np.ndarray:
     """Exponent e of the FP8 power-of-two scale: the smallest e with
-    ``448 * 2**e >= amax`` (A1: ``pow2_ceil(amax / 448)`` in exact arithmetic;
+    ``448 * 2**e >= amax`` (a reading: ``pow2_ceil(amax / 448)`` in exact arithmetic;
     page *cutedsl.dsa.index*, ``DsaIndex.fp8_query``)."""
     return pow2_exponent(np.asarray(amax, dtype=np.float64), 448.0)
 
@@ -79,13 +80,14 @@ def fp8_scale_exponent(amax) -> np.ndarray:
 def mx_scale_exponent(amax) -> np.ndarray:
     """Exponent of an MXFP4 block scale (page *cutedsl.dsa.index*, ``mxfp4_scale``):
     ``clamp(ceil(log2(max(amax, 6 * 2^-126) / 6)), -127, 127)``, taken as an exact
-    mathematical definition (A3)."""
+    mathematical definition (a reading: the page's compiled ``log2`` sequence is not
+    reproduced)."""
     a = np.maximum(np.asarray(amax, dtype=np.float64), MX_AMAX_FLOOR)
     return np.clip(pow2_exponent(a, 6.0), -127, 127)
 
 
 # --------------------------------------------------------------------------
-# a1: query quantisation
+# query quantisation
 # --------------------------------------------------------------------------
 
 def quantize_query(fmt: str, q, wv):
@@ -96,9 +98,9 @@ def quantize_query(fmt: str, q, wv):
     Returns (q_rows uint8 [rows, 4096], w float32 [rows, 32] holding BF16 values).
     FP8 rows hold head h's 128 E4M3 codes at ``h * 128``.  MXFP4 rows hold
     head h's E2M1 pairs at ``h * 64`` and its four UE8M0 bytes (block b at
-    byte b, A5) at ``2048 + h * 4``; bytes from 2176 on are left zero.
+    byte b, a reading) at ``2048 + h * 4``; bytes from 2176 on are left zero.
     Row-group MXFP4 ("mxfp4_rg") rows hold the same pairs and the scale of
-    block b of head h at ``2048 + b * 64 + h`` (A27); the slots of heads 32..63
+    block b of head h at ``2048 + b * 64 + h`` (group-major, a reading); the slots of heads 32..63
     and bytes from 2304 on are left zero."""
     q = np.asarray(q, dtype=np.float32)
     wv = np.asarray(wv, dtype=np.float32)
@@ -135,7 +137,7 @@ def quantize_queries(q):
     folded into head weights.  Returns (payload uint8 [rows, heads, 64]: head
     h's E2M1 pairs, column 2j in the low nibble of byte j; scales uint8
     [rows, 1, 4, 16, 4]: the UE8M0 byte of block g of head h at flat position
-    g * 64 + h of the row's 256 bytes, A27; slots of heads >= ``heads`` zero).
+    g * 64 + h of the row's 256 bytes, group-major (a reading); slots of heads >= ``heads`` zero).
     The codec is the one of ``quantize_query``'s MXFP4 rows."""
     q = np.asarray(q, dtype=np.float32)
     if q.ndim != 3 or q.shape[2] != DIM:
@@ -153,11 +155,12 @@ def quantize_queries(q):
 
 
 # --------------------------------------------------------------------------
-# a2: key LayerNorm + quantise + insert
+# key LayerNorm + quantise + insert
 # --------------------------------------------------------------------------
 
 def _half_warp_sum(lane_values: np.ndarray) -> np.ndarray:
-    """Sum over 16 lanes by an xor butterfly with distances 8, 4, 2, 1 (A8);
+    """Sum over 16 lanes by an xor butterfly with distances 8, 4, 2, 1 (a reading: the
+    order is not printed);
     every lane ends with the same FP32 value."""
     s = lane_values.astype(np.float32)
     lane = np.arange(16)
@@ -173,7 +176,8 @@ def layer_norm_bf16(x, gamma, beta, eps):
     mean = sum / 128; the variance repeats the scheme on (x - mean)^2;
     rstd = 1 / sqrt(var + eps) with a correctly rounded square root and
     division; y = ((x - mean) * rstd) * gamma + beta, every operation rounded
-    on its own (no fused multiply-add), then BF16 (A8)."""
+    on its own (no fused multiply-add), then BF16 (a reading: the order and
+    rounding are not printed)."""
     x = np.asarray(x, dtype=np.float32)
     n = x.shape[0]
     X = x.reshape(n, 16, 8)
@@ -197,7 +201,7 @@ def layer_norm_bf16(x, gamma, beta, eps):
 def quantize_key(fmt: str, normed):
     """Codes and scale bytes of BF16-valued normalised keys [n, 128].
 
-    FP8 (A10): amax over the 128 values, floored at 1e-10; scale ``2**e`` with e
+    FP8 (a reading: ``insert_fp8_key`` is not printed): amax over the 128 values, floored at 1e-10; scale ``2**e`` with e
     from ``fp8_scale_exponent``; 128 E4M3 codes and 4 scale bytes: FP32 ``2**e``
     little-endian ("fp8"), or the byte ``e + 127`` four times ("fp8_mx", page
     *cutedsl.dsa.index*, module docstring).
@@ -231,7 +235,7 @@ def insert_key(fmt: str, cache: np.ndarray, page_stride: int, num_pages: int,
     cache: uint8 array of at least ``num_pages * page_stride`` bytes.  A slot is
     ``page * 64 + offset`` (page *cutedsl.dsa.index*, ``insert_fp4_key``).  A page
     holds the 64 tokens' codes, then their 4-byte scales: FP8 codes at
-    ``offset * 128``, scales at ``8192 + offset * 4`` (A10); MXFP4 codes at
+    ``offset * 128``, scales at ``8192 + offset * 4`` (a reading); MXFP4 codes at
     ``offset * 64``, scales at ``64 * 64 + offset * 4``.  Slots < 0 are padding
     and write nothing (``insert_key``; *amd.ops.fp4_indexer*, ``store_keys``).
     Slots at or past ``num_pages * 64`` are skipped too; the return value
@@ -273,7 +277,7 @@ def insert_key(fmt: str, cache: np.ndarray, page_stride: int, num_pages: int,
 
 
 # --------------------------------------------------------------------------
-# a3: row bounds of grouped verify rows
+# row bounds of grouped verify rows
 # --------------------------------------------------------------------------
 
 def decode_layout(seq_lens, query_lens, num_rows: int):
@@ -283,7 +287,7 @@ def decode_layout(seq_lens, query_lens, num_rows: int):
     starts = [0, cumsum(query_lens)] (int32).  Row r belongs to the request
     found by ``searchsorted(starts[1:], r, right=True)`` capped at R - 1;
     its bound is ``max(0, seq_len - query_len + (r - start) + 1)``.  Rows at
-    or past ``starts[-1]`` are padding with bound 0 (A15)."""
+    or past ``starts[-1]`` are padding with bound 0 (as printed)."""
     if num_rows < 0:
         raise ValueError("Invalid DCP geometry or query row count")
     seq_lens = np.asarray(seq_lens)
@@ -304,7 +308,7 @@ def decode_layout(seq_lens, query_lens, num_rows: int):
 
 
 # --------------------------------------------------------------------------
-# a4: paged MQA logits
+# paged MQA logits
 # --------------------------------------------------------------------------
 
 def decode_query(fmt: str, q_row) -> np.ndarray:
@@ -368,7 +372,7 @@ def score_paged(fmt: str, q_rows, w, cache, page_stride: int, block_table,
                 starts, row_ends, rows_subset=None):
     """Logits float64 [rows, max_pages * 64] of every query row against the
     keys of its request's block-table row; positions at or past the row's
-    bound are -inf (A13).  ``rows_subset`` restricts the work to some rows
+    bound are -inf (a reading: the page leaves them unset).  ``rows_subset`` restricts the work to some rows
     (the others stay -inf)."""
     block_table = np.asarray(block_table)
     starts = np.asarray(starts, dtype=np.int64)
@@ -393,13 +397,13 @@ def score_paged(fmt: str, q_rows, w, cache, page_stride: int, block_table,
 
 
 # --------------------------------------------------------------------------
-# a5: top-k
+# top-k
 # --------------------------------------------------------------------------
 
 def topk(scores, row_ends, k: int) -> np.ndarray:
     """Per row, the positions t < row_end of the k largest scores, ordered by
     (score descending, t ascending); rows with fewer than k candidates are
-    filled with -1 (A14).  Indices are logical positions in the request."""
+    filled with -1 (a reading: the pages do not say).  Indices are logical positions in the request."""
     scores = np.asarray(scores)
     rows = scores.shape[0]
     out = np.full((rows, k), -1, dtype=np.int32)

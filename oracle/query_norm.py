@@ -19,14 +19,14 @@ results to the model's query kernel, and so fixes their FP32 operation order:
   to chain e mod 4 in increasing e (two packed pairs); the lane total is
   (c0 + c1) + (c2 + c3), then the warp sum.
 
-Readings where the page is silent (listed in the design doc as A18..A21):
-A18 ``warp_sum`` is an xor butterfly over 32 lanes with distances 16, 8, 4,
+Readings where the page is silent:
+- ``warp_sum`` is an xor butterfly over 32 lanes with distances 16, 8, 4,
 2, 1 (addition is commutative, so every lane ends with the same value).
-A19 ``query_norm_rsqrt(total, eps)`` = 1 / sqrt(total / 1536 + eps), each
+- ``query_norm_rsqrt(total, eps)`` = 1 / sqrt(total / 1536 + eps), each
 operation correctly rounded in FP32.
-A20 the output is BF16_rne((x * rr) * w) with two FP32 products, as both
+- the output is BF16_rne((x * rr) * w) with two FP32 products, as both
 kernels print them (left to right); the packed products round each lane.
-A21 ``tiled_from`` is not printed: the caller picks the variant.
+- ``tiled_from`` is not printed: the caller picks the variant.
 
 Every FP32 operation below is rounded on its own.  A fused multiply-add
 ``fma(x, x, c)`` is evaluated as FP64 ``x * x + c`` rounded to FP32: x is a
@@ -53,7 +53,7 @@ def _fma32(a, b, c):
 
 
 def _warp_sum(lanes: np.ndarray) -> np.ndarray:
-    """A18: xor butterfly over the last axis (32 lanes), distances 16..1."""
+    """Reading: xor butterfly over the last axis (32 lanes), distances 16..1."""
     s = lanes.astype(np.float32)
     lane = np.arange(32)
     for d in (16, 8, 4, 2, 1):
@@ -62,13 +62,13 @@ def _warp_sum(lanes: np.ndarray) -> np.ndarray:
 
 
 def _rsqrt(total: np.ndarray, eps: float) -> np.ndarray:
-    """A19: 1 / sqrt(total / 1536 + eps), each operation rounded to FP32."""
+    """Reading: 1 / sqrt(total / 1536 + eps), each operation rounded to FP32."""
     mean = (total.astype(np.float32) / np.float32(COLS)).astype(np.float32)
     return (np.float32(1.0) / np.sqrt((mean + np.float32(eps)).astype(np.float32))).astype(np.float32)
 
 
 def _scale(x: np.ndarray, rr: np.ndarray, w: np.ndarray) -> np.ndarray:
-    """A20: BF16((x * rr) * w), two FP32 products."""
+    """Reading: BF16((x * rr) * w), two FP32 products."""
     y = (x * rr[:, None]).astype(np.float32)
     return bf16_round((y * w[None, :]).astype(np.float32))
 

@@ -63,7 +63,7 @@ __device__ __forceinline__ uint32_t mxfp4_lane(float x0, float x1, float x2, flo
     return b01 | (b23 << 8);
 }
 
-// ----------------------------------------------------------------- a1: query rows
+// ----------------------------------------------------------------- query rows
 // One warp per (row, head); lane l holds columns 4l..4l+3.  `block` is the
 // block index within this part of the grid (256 threads per block).
 __device__ __forceinline__ void quantize_query_block(int fmt, const uint16_t* __restrict__ q, int64_t q_stride,
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(256) quantize_query_kernel(int fmt, const uint
     quantize_query_block(fmt, q, q_stride, wv, wv_stride, rows, q_out, w_out, blockIdx.x);
 }
 
-// ----------------------------------------------------------------- a2: keys
+// ----------------------------------------------------------------- keys
 // One half-warp per key; lane j of the half holds columns 8j..8j+7.  `block`
 // is the block index within this part of the grid (256 threads per block).
 __device__ __forceinline__ void insert_key_block(int fmt, const uint16_t* __restrict__ k, int64_t k_stride,

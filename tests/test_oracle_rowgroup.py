@@ -83,7 +83,7 @@ def _grid_queries(rng, rows, heads):
 def test_quantize_queries_closed_form():
     """Page *amd.ops.fp4_indexer*, ``quantize_queries``: payload [rows, heads, 64]
     and scales [rows, 1, 4, 16, 4] for 16, 32 and 64 heads; the scale of block
-    g of head h at flat g * 64 + h (A27), unused head slots zero."""
+    g of head h at flat g * 64 + h (the group-major reading), unused head slots zero."""
     rng = np.random.default_rng(7)
     for heads in (16, 32, 64):
         x, pairs, sbytes = _grid_queries(rng, 5, heads)
