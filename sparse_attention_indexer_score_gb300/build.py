@@ -1,7 +1,7 @@
 """Build the CUDA library ``libdsa.so`` in-tree for sm_103a (GB300).
 
 Each translation unit is compiled by nvcc in parallel, then linked into a
-shared library next to this file.  No CMake; a minute or two on the GPU machine.
+shared library next to this file.  No CMake; a minute or two on an Arm GB300 host.
 """
 
 from __future__ import annotations
