@@ -372,8 +372,8 @@ def score_paged(fmt: str, q_rows, w, cache, page_stride: int, block_table,
                 starts, row_ends, rows_subset=None):
     """Logits float64 [rows, max_pages * 64] of every query row against the
     keys of its request's block-table row; positions at or past the row's
-    bound are -inf (a reading: the page leaves them unset).  ``rows_subset`` restricts the work to some rows
-    (the others stay -inf)."""
+    bound are -inf (a reading: the page leaves them unset).  ``rows_subset``
+    restricts the work to some rows (the others stay -inf)."""
     block_table = np.asarray(block_table)
     starts = np.asarray(starts, dtype=np.int64)
     row_ends = np.asarray(row_ends, dtype=np.int64)
@@ -403,7 +403,8 @@ def score_paged(fmt: str, q_rows, w, cache, page_stride: int, block_table,
 def topk(scores, row_ends, k: int) -> np.ndarray:
     """Per row, the positions t < row_end of the k largest scores, ordered by
     (score descending, t ascending); rows with fewer than k candidates are
-    filled with -1 (a reading: the pages do not say).  Indices are logical positions in the request."""
+    filled with -1 (a reading: the pages do not say).  Indices are logical
+    positions in the request."""
     scores = np.asarray(scores)
     rows = scores.shape[0]
     out = np.full((rows, k), -1, dtype=np.int32)
