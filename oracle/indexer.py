@@ -39,7 +39,8 @@ FP4_QUERY_ROW = FP4_SCALES + HEADS * 4
 FP8_KEY_BYTES, FP8_PAGE_BYTES = PAGE * DIM, PAGE * (DIM + 4)          # 8192, 8448
 FP4_KEY_BYTES, FP4_PAGE_BYTES = PAGE * DIM // 2, PAGE * (DIM // 2 + 4)  # 4096, 4352
 WEIGHT_SCALE = (HEADS * DIM) ** -0.5   # 1/64, page *cutedsl.dsa.index*, ``DsaIndex.fp8_query``
-FP4_WEIGHT = WEIGHT_SCALE              # not printed ("the indexer weight scale"); a reading: the FP8 fold's 1/64
+# "the indexer weight scale" is not printed; a reading: the FP8 fold's 1/64
+FP4_WEIGHT = WEIGHT_SCALE
 FP8_AMAX_FLOOR = np.float32(1e-10)     # ``DsaIndex.fp8_query``: amax starts at 1e-10
 MX_AMAX_FLOOR = 6.0 * 2.0 ** -126      # ``mxfp4_scale``: max(amax, 6 * 2^-126)
 
@@ -201,8 +202,9 @@ def layer_norm_bf16(x, gamma, beta, eps):
 def quantize_key(fmt: str, normed):
     """Codes and scale bytes of BF16-valued normalised keys [n, 128].
 
-    FP8 (a reading: ``insert_fp8_key`` is not printed): amax over the 128 values, floored at 1e-10; scale ``2**e`` with e
-    from ``fp8_scale_exponent``; 128 E4M3 codes and 4 scale bytes: FP32 ``2**e``
+    FP8 (a reading: ``insert_fp8_key`` is not printed): amax over the 128
+    values, floored at 1e-10; scale ``2**e`` with e from
+    ``fp8_scale_exponent``; 128 E4M3 codes and 4 scale bytes: FP32 ``2**e``
     little-endian ("fp8"), or the byte ``e + 127`` four times ("fp8_mx", page
     *cutedsl.dsa.index*, module docstring).
     MXFP4 (``insert_fp4_key``): per 32-column block b a UE8M0 exponent as in
