@@ -138,8 +138,9 @@ def quantize_queries(q):
     folded into head weights.  Returns (payload uint8 [rows, heads, 64]: head
     h's E2M1 pairs, column 2j in the low nibble of byte j; scales uint8
     [rows, 1, 4, 16, 4]: the UE8M0 byte of block g of head h at flat position
-    g * 64 + h of the row's 256 bytes, group-major (a reading); slots of heads >= ``heads`` zero).
-    The codec is the one of ``quantize_query``'s MXFP4 rows."""
+    g * 64 + h of the row's 256 bytes, group-major (a reading); slots of
+    heads >= ``heads`` zero).  The codec is the one of ``quantize_query``'s
+    MXFP4 rows."""
     q = np.asarray(q, dtype=np.float32)
     if q.ndim != 3 or q.shape[2] != DIM:
         raise ValueError("queries must be [rows, heads, 128]")

@@ -7,14 +7,20 @@ import numpy as np
 import pytest
 
 from oracle import codecs as C
+from oracle import dcp as D
 from oracle import indexer as O
+from oracle import query_norm as QN
 
 import test_oracle_codecs as TC
+import test_oracle_dcp as TD
 import test_oracle_indexer as TI
+import test_oracle_query_norm as TQ
+import test_oracle_rowgroup as TR
 
 _orig = {name: getattr(O, name) for name in (
     "score_row", "decode_query", "decode_keys", "decode_layout", "topk", "fp8_scale_exponent",
-    "mx_scale_exponent", "layer_norm_bf16", "_half_warp_sum")}
+    "mx_scale_exponent", "layer_norm_bf16", "_half_warp_sum", "quantize_queries")}
+_orig_rank_local_ends = D.rank_local_ends
 
 
 # ---------------------------------------------------------------- planted mistakes
@@ -123,6 +129,82 @@ def e4m3_truncating(x):
     return (codes[np.maximum(idx, 0)] | (np.signbit(x).astype(np.int64) << 7)).astype(np.uint8)
 
 
+def queries_head_major_scales(q):
+    payload, scales = _orig["quantize_queries"](q)
+    rows, heads = payload.shape[0], payload.shape[1]
+    by_group = scales.reshape(rows, 4, 64)
+    flat = np.zeros((rows, 256), np.uint8)
+    for h in range(heads):
+        for g in range(4):
+            flat[:, h * 4 + g] = by_group[:, g, h]
+    return payload, flat.reshape(rows, 1, 4, 16, 4)
+
+
+def keys_rowgroup_scales_token_major(fmt, cache, page_stride, pages, n):
+    if fmt != "mxfp4_rg":
+        return _orig["decode_keys"](fmt, cache, page_stride, pages, n)
+    flat = cache.reshape(-1)
+    t = np.arange(n, dtype=np.int64)
+    base = np.asarray(pages, np.int64)[t // O.PAGE] * page_stride
+    off = t % O.PAGE
+    j = np.arange(O.DIM // 2)
+    codes = C.unpack_e2m1(flat[base[:, None] + (j // 16) * O.RG_GROUP_BYTES + off[:, None] * 16 + j % 16])
+    e = flat[(base + O.FP4_KEY_BYTES + off * 4)[:, None] + np.arange(4)].astype(np.int64) - 127
+    return (C.e2m1_decode(codes).reshape(n, 4, 32) * np.ldexp(1.0, e)[..., None]).reshape(n, O.DIM)
+
+
+def rsqrt_without_eps(total, eps):
+    mean = (total.astype(np.float32) / np.float32(QN.COLS)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return (np.float32(1.0) / np.sqrt(mean)).astype(np.float32)
+
+
+def rsqrt_mean_over_one_column_less(total, eps):
+    mean = (total.astype(np.float32) / np.float32(QN.COLS - 1)).astype(np.float32)
+    return (np.float32(1.0) / np.sqrt((mean + np.float32(eps)).astype(np.float32))).astype(np.float32)
+
+
+def warp_sum_left_to_right(lanes):
+    s = np.zeros(lanes.shape[:-1], np.float32)
+    for j in range(lanes.shape[-1]):
+        s = (s + lanes[..., j].astype(np.float32)).astype(np.float32)
+    return s
+
+
+def scale_weight_first(x, rr, w):
+    y = (x * w[None, :]).astype(np.float32)
+    return C.bf16_round((y * rr[:, None]).astype(np.float32))
+
+
+def owner_ignoring_interleave(t, world, interleave):
+    return np.asarray(t, np.int64) % world
+
+
+def rank_local_ends_partial_short(ends, rank, world, interleave):
+    e = np.asarray(ends, np.int64)
+    full = e // (world * interleave) * interleave
+    return (full + np.clip(e - full * world - rank * interleave, 0, max(interleave - 1, 0))).astype(np.int32)
+
+
+def local_to_global_without_rank(l, rank, world, interleave):
+    l = np.asarray(l, np.int64)
+    return (l // interleave) * (world * interleave) + l % interleave
+
+
+def merge_ties_toward_later_position(scores, idx, world, interleave, k_out):
+    scores = np.asarray(scores, np.float64)
+    idx = np.asarray(idx, np.int64)
+    out = np.full((scores.shape[0], k_out), -1, np.int32)
+    ranks = np.broadcast_to(np.arange(world)[None, :, None], idx.shape)
+    for r in range(scores.shape[0]):
+        keep = idx[r] >= 0
+        g = (idx[r][keep] // interleave) * (world * interleave) + idx[r][keep] % interleave + ranks[r][keep] * interleave
+        order = np.lexsort((-g, -scores[r][keep]))
+        m = min(k_out, order.size)
+        out[r, :m] = g[order[:m]]
+    return out
+
+
 # ---------------------------------------------------------------- cases
 
 CASES = [
@@ -148,9 +230,31 @@ CASES = [
     ("LayerNorm lanes summed left to right", O, "_half_warp_sum", lanes_left_to_right,
      [TI.test_layer_norm_lane_order_is_the_stated_one]),
     ("E4M3 rounding toward zero", C, "e4m3_encode", e4m3_truncating, [lambda: TC.test_e4m3_exhaustive_bf16(1.0)]),
+    ("row-group query scales head-major", O, "quantize_queries", queries_head_major_scales,
+     [TR.test_quantize_queries_closed_form]),
+    ("row-group key scales read token-major", O, "decode_keys", keys_rowgroup_scales_token_major,
+     [TR.test_decoded_keys_and_scores_agree]),
+    ("QueryNorm eps dropped", QN, "_rsqrt", rsqrt_without_eps,
+     [lambda: TQ.test_zero_row_with_eps_is_zero(QN.query_norm_cta)]),
+    ("QueryNorm mean over 1535 columns", QN, "_rsqrt", rsqrt_mean_over_one_column_less,
+     [TQ.test_orders_agree_when_sums_are_exact]),
+    ("QueryNorm warp sum left to right", QN, "_warp_sum", warp_sum_left_to_right,
+     [TQ.test_warp_sum_is_the_stated_butterfly]),
+    ("QueryNorm weight applied before rr", QN, "_scale", scale_weight_first,
+     [lambda: TQ.test_output_products_in_the_printed_order(QN.query_norm_cta),
+      lambda: TQ.test_output_products_in_the_printed_order(QN.query_norm_tiled)]),
+    ("DCP owner ignoring the interleave", D, "owner", owner_ignoring_interleave,
+     [TD.test_rank_local_ends_count_the_owned_keys]),
+    ("DCP partial round one key short", D, "rank_local_ends", rank_local_ends_partial_short,
+     [TD.test_rank_local_ends_count_the_owned_keys, TD.test_hand_case]),
+    ("DCP local to global without the rank's offset", D, "local_to_global", local_to_global_without_rank,
+     [TD.test_hand_case]),
+    ("DCP merge ties toward the later position", D, "topk_merge", merge_ties_toward_later_position,
+     [TD.test_merge_of_local_topks_is_the_global_topk]),
 ]
 
 
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")   # a planted mistake may divide by zero
 @pytest.mark.parametrize("name,module,attr,mutant,pins", CASES, ids=[c[0] for c in CASES])
 def test_pins_catch_the_planted_mistake(monkeypatch, name, module, attr, mutant, pins):
     for pin in pins:   # every pin passes on the oracle as it stands

@@ -75,6 +75,34 @@ def test_orders_agree_when_sums_are_exact():
     assert np.array_equal(a, want)
 
 
+def test_warp_sum_is_the_stated_butterfly():
+    """Lane 0 holds 2^26 (FP32 spacing 8 there), lanes 1..31 hold 4.  The xor
+    butterfly (16, 8, 4, 2, 1) loses lane 16's 4 in its first step (2^26 + 4
+    is a tie, rounded to even) and then adds 8, 16, 32 and 64 exactly: 2^26 +
+    120.  A left-to-right sum would lose every 4 and give 2^26; the exact sum
+    is 2^26 + 124."""
+    from oracle.query_norm import _warp_sum
+    lanes = np.full((1, 32), 4.0, np.float32)
+    lanes[0, 0] = 2.0 ** 26
+    assert _warp_sum(lanes)[0] == np.float32(2.0 ** 26 + 120)
+
+
+@pytest.mark.parametrize("norm", VARIANTS)
+def test_output_products_in_the_printed_order(norm):
+    """Both kernels print q_c = BF16((x * rr) * w).  Row [1.4140625, 1.40625,
+    0, ...] with eps 0: the sum of squares 3.97711181640625 is exact in any
+    order; in FP32 the mean is 0.0025892655830830336 and rr 19.652223587036133.
+    Column 0 with w = 0.81640625: x * rr = 27.789472579956055, times w =
+    22.6875 exactly, a BF16 tie that rounds to the even 22.75.  The other
+    order, x * w = 1.154449462890625 (exact) times rr = 22.687498..., would
+    give 22.625."""
+    x = np.zeros((1, COLS), np.float32)
+    x[0, 0], x[0, 1] = 1.4140625, 1.40625
+    w = np.ones(COLS, np.float32)
+    w[0] = 0.81640625
+    assert norm(x, w, 0.0)[0, 0] == np.float32(22.75)
+
+
 @pytest.mark.parametrize("norm", VARIANTS)
 def test_close_to_fp64_rmsnorm(norm):
     """Within one BF16 unit of the FP64 RMSNorm rounded to BF16; equal to it
