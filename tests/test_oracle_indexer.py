@@ -65,6 +65,32 @@ def test_layer_norm_lane_order_is_the_stated_one():
     assert normed[0, 0] == np.float32(8.0) and normed[0, 64] == np.float32(-8.0)
 
 
+def test_layer_norm_eps_inside_the_root():
+    """A row of +-2^-10 has variance 2^-20, the size of eps = 1e-6: the closed
+    form 2^-10 / sqrt(2^-20 + 1e-6) = 0.69867... rounds to the BF16 0.69921875
+    (eps added outside the root would give 0.99898... and 1.0)."""
+    d = 2.0 ** -10
+    x = np.tile(np.float32([d, -d]), 64)[None, :]
+    out = O.layer_norm_bf16(x, np.ones(128, np.float32), np.zeros(128, np.float32), 1e-6)[0]
+    closed = d / np.sqrt(d * d + 1e-6)
+    assert out[0] == C.bf16_round(np.float32(closed)) == np.float32(0.69921875)
+    assert out[1] == -out[0]
+
+
+def test_layer_norm_output_has_no_fused_multiply_add():
+    """Row of +-1.234375 (mean 0, variance 1.523681640625 exactly): in FP32
+    var + eps = 1.5236825942993164, rstd = 0.8101263642311096 and
+    (x - mean) * rstd = 0.9999997019767761 on column 0.  With gamma -0.2109375
+    and beta -0.80078125: the product rounds to -0.21093744039535522 and the
+    sum to -1.01171875 exactly, a BF16 tie that rounds to the even -1.015625.
+    A fused multiply-add would round the exact -1.01171863... once, to
+    -1.0117186307907104, and give -1.0078125."""
+    x = np.tile(np.float32([1.234375, -1.234375]), 64)[None, :]
+    gamma, beta = np.ones(128, np.float32), np.zeros(128, np.float32)
+    gamma[0], beta[0] = -0.2109375, -0.80078125
+    assert O.layer_norm_bf16(x, gamma, beta, 1e-6)[0, 0] == np.float32(-1.015625)
+
+
 # ---------------------------------------------------------------- cache layout
 
 @pytest.mark.parametrize("fmt", ["fp8", "fp8_mx", "mxfp4"])
@@ -279,6 +305,21 @@ def test_score_matches_dequantised_float_reference():
                 dot += qv[h, c] * Fraction(C.E2M1_TABLE[code]) * Fraction(2) ** ex
             total += Fraction(float(w[r, h])) * max(dot, Fraction(0))
         assert abs(float(total) - s[r, t]) <= 1e-12 * max(1.0, abs(float(total)))
+
+
+def test_mxfp4_weights_share_the_fp8_fold():
+    """The MXFP4 head weight carries the same 1/64 as the FP8 fold (pinned by
+    the scale fixtures) but no query scale: for one query, w_fp8 = w_mxfp4 *
+    2^e with e each head's FP8 exponent, exactly (powers of two, no underflow
+    at these sizes)."""
+    rng = np.random.default_rng(12)
+    q = _bf16_values(rng, (6, 32, 128), 2.0)
+    wv = _bf16_values(rng, (6, 32))
+    _, w8 = O.quantize_query("fp8", q, wv)
+    _, w4 = O.quantize_query("mxfp4", q, wv)
+    e = O.fp8_scale_exponent(np.maximum(np.abs(q).max(axis=2), O.FP8_AMAX_FLOOR))
+    assert np.array_equal(np.asarray(w8, np.float64), np.asarray(w4, np.float64) * np.ldexp(1.0, e))
+    assert np.any(w4 != wv)
 
 
 # ---------------------------------------------------------------- top-k

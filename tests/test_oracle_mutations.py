@@ -111,6 +111,37 @@ def layer_norm_without_beta(x, gamma, beta, eps):
     return _orig["layer_norm_bf16"](x, gamma, np.zeros_like(np.asarray(beta, np.float32)), eps)
 
 
+def _layer_norm_variant(eps_outside=False, fused=False):
+    """The oracle's LayerNorm with the square root's eps or the output's
+    rounding changed (the rest as in the oracle)."""
+    def ln(x, gamma, beta, eps):
+        x = np.asarray(x, np.float32)
+        n = x.shape[0]
+        X = x.reshape(n, 16, 8)
+        total = np.zeros((n, 16), np.float32)
+        for i in range(8):
+            total = (total + X[:, :, i]).astype(np.float32)
+        mean = (O._half_warp_sum(total) / np.float32(O.DIM)).astype(np.float32)
+        Dv = (X - mean[:, None, None]).astype(np.float32)
+        square = np.zeros((n, 16), np.float32)
+        for i in range(8):
+            square = (square + (Dv[:, :, i] * Dv[:, :, i]).astype(np.float32)).astype(np.float32)
+        var = (O._half_warp_sum(square) / np.float32(O.DIM)).astype(np.float32)
+        if eps_outside:
+            rstd = (np.float32(1.0) / (np.sqrt(var) + np.float32(eps))).astype(np.float32)
+        else:
+            rstd = (np.float32(1.0) / np.sqrt((var + np.float32(eps)).astype(np.float32))).astype(np.float32)
+        g = np.asarray(gamma, np.float32).reshape(16, 8)
+        b = np.asarray(beta, np.float32).reshape(16, 8)
+        p = (Dv * rstd[:, None, None]).astype(np.float32)
+        if fused:
+            y = (p.astype(np.float64) * g + b).astype(np.float32)
+        else:
+            y = ((p * g).astype(np.float32) + b).astype(np.float32)
+        return C.bf16_round(y).reshape(n, O.DIM)
+    return ln
+
+
 def lanes_left_to_right(lane_values):
     s = np.zeros(lane_values.shape[0], np.float32)
     for j in range(lane_values.shape[1]):
@@ -229,7 +260,13 @@ CASES = [
     ("LayerNorm without beta", O, "layer_norm_bf16", layer_norm_without_beta, [TI.test_layer_norm_special_cases]),
     ("LayerNorm lanes summed left to right", O, "_half_warp_sum", lanes_left_to_right,
      [TI.test_layer_norm_lane_order_is_the_stated_one]),
+    ("LayerNorm eps outside the square root", O, "layer_norm_bf16", _layer_norm_variant(eps_outside=True),
+     [TI.test_layer_norm_eps_inside_the_root]),
+    ("LayerNorm output with a fused multiply-add", O, "layer_norm_bf16", _layer_norm_variant(fused=True),
+     [TI.test_layer_norm_output_has_no_fused_multiply_add]),
     ("E4M3 rounding toward zero", C, "e4m3_encode", e4m3_truncating, [lambda: TC.test_e4m3_exhaustive_bf16(1.0)]),
+    ("FP8 weight fold without the 1/64", O, "WEIGHT_SCALE", 1.0, [TC.test_scales_golden]),
+    ("MXFP4 weight without the 1/64", O, "FP4_WEIGHT", 1.0, [TI.test_mxfp4_weights_share_the_fp8_fold]),
     ("row-group query scales head-major", O, "quantize_queries", queries_head_major_scales,
      [TR.test_quantize_queries_closed_form]),
     ("row-group key scales read token-major", O, "decode_keys", keys_rowgroup_scales_token_major,
@@ -268,3 +305,12 @@ def test_pins_catch_the_planted_mistake(monkeypatch, name, module, attr, mutant,
             caught.append(getattr(pin, "__name__", "pin"))
     assert caught, f"no pin caught: {name}"
 
+
+
+def test_the_layer_norm_variant_without_changes_is_the_oracle():
+    """The LayerNorm mutants differ from the oracle only in what they plant."""
+    rng = np.random.default_rng(4)
+    x = C.bf16_round((rng.standard_normal((64, 128)) * 3).astype(np.float32))
+    gamma = C.bf16_round((1 + 0.1 * rng.standard_normal(128)).astype(np.float32))
+    beta = C.bf16_round((0.1 * rng.standard_normal(128)).astype(np.float32))
+    assert np.array_equal(_layer_norm_variant()(x, gamma, beta, 1e-6), O.layer_norm_bf16(x, gamma, beta, 1e-6))
