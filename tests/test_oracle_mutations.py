@@ -21,6 +21,8 @@ _orig = {name: getattr(O, name) for name in (
     "score_row", "decode_query", "decode_keys", "decode_layout", "topk", "fp8_scale_exponent",
     "mx_scale_exponent", "layer_norm_bf16", "_half_warp_sum", "quantize_queries")}
 _orig_rank_local_ends = D.rank_local_ends
+_orig_quantize_query = O.quantize_query
+_orig_quantize_key = O.quantize_key
 
 
 # ---------------------------------------------------------------- planted mistakes
@@ -160,6 +162,46 @@ def e4m3_truncating(x):
     return (codes[np.maximum(idx, 0)] | (np.signbit(x).astype(np.int64) << 7)).astype(np.uint8)
 
 
+def query_nibbles_swapped(fmt, q, wv):
+    rows, w = _orig_quantize_query(fmt, q, wv)
+    if fmt in ("mxfp4", "mxfp4_rg"):
+        b = rows[:, :O.FP4_SCALES].copy()
+        rows[:, :O.FP4_SCALES] = ((b & 0xF) << 4) | (b >> 4)
+    return rows, w
+
+
+def fp8_query_heads_reversed(fmt, q, wv):
+    rows, w = _orig_quantize_query(fmt, q, wv)
+    if fmt in ("fp8", "fp8_mx"):
+        rows[:, :O.Q_ROW_BYTES] = rows[:, :O.Q_ROW_BYTES].reshape(-1, O.HEADS, O.DIM)[:, ::-1].reshape(-1, O.Q_ROW_BYTES)
+    return rows, w
+
+
+def mxfp4_query_scales_block_major(fmt, q, wv):
+    rows, w = _orig_quantize_query(fmt, q, wv)
+    if fmt == "mxfp4":
+        sc = rows[:, O.FP4_SCALES:O.FP4_QUERY_ROW]
+        rows[:, O.FP4_SCALES:O.FP4_QUERY_ROW] = sc.reshape(-1, O.HEADS, 4).transpose(0, 2, 1).reshape(-1, O.HEADS * 4)
+    return rows, w
+
+
+def fp8_key_scale_big_endian(fmt, normed):
+    codes, sc = _orig_quantize_key(fmt, normed)
+    return (codes, sc[:, ::-1].copy()) if fmt == "fp8" else (codes, sc)
+
+
+def mxfp4_key_scale_blocks_reversed(fmt, normed):
+    codes, sc = _orig_quantize_key(fmt, normed)
+    return (codes, sc[:, ::-1].copy()) if fmt == "mxfp4" else (codes, sc)
+
+
+def fp8_key_codes_unscaled(fmt, normed):
+    codes, sc = _orig_quantize_key(fmt, normed)
+    if fmt in ("fp8", "fp8_mx"):
+        codes = C.e4m3_encode(np.asarray(normed, np.float64)).reshape(codes.shape).astype(np.uint8)
+    return codes, sc
+
+
 def queries_head_major_scales(q):
     payload, scales = _orig["quantize_queries"](q)
     rows, heads = payload.shape[0], payload.shape[1]
@@ -267,6 +309,17 @@ CASES = [
     ("E4M3 rounding toward zero", C, "e4m3_encode", e4m3_truncating, [lambda: TC.test_e4m3_exhaustive_bf16(1.0)]),
     ("FP8 weight fold without the 1/64", O, "WEIGHT_SCALE", 1.0, [TC.test_scales_golden]),
     ("MXFP4 weight without the 1/64", O, "FP4_WEIGHT", 1.0, [TI.test_mxfp4_weights_share_the_fp8_fold]),
+    ("MXFP4 query nibbles swapped", O, "quantize_query", query_nibbles_swapped,
+     [TR.test_rowgroup_query_rows_carry_the_same_codes_and_scales]),
+    ("FP8 query heads in reverse order", O, "quantize_query", fp8_query_heads_reversed, [TC.test_scales_golden]),
+    ("MXFP4 query scale bytes block-major", O, "quantize_query", mxfp4_query_scales_block_major,
+     [TR.test_decoded_keys_and_scores_agree]),
+    ("FP8 key scale big-endian", O, "quantize_key", fp8_key_scale_big_endian,
+     [lambda: TI.test_insert_layout_golden("fp8")]),
+    ("MXFP4 key scale blocks reversed", O, "quantize_key", mxfp4_key_scale_blocks_reversed,
+     [TR.test_page_views_show_the_token_major_codes]),
+    ("FP8 key codes without the scale divided out", O, "quantize_key", fp8_key_codes_unscaled,
+     [lambda: TI.test_insert_layout_golden("fp8")]),
     ("row-group query scales head-major", O, "quantize_queries", queries_head_major_scales,
      [TR.test_quantize_queries_closed_form]),
     ("row-group key scales read token-major", O, "decode_keys", keys_rowgroup_scales_token_major,
