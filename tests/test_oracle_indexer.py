@@ -277,6 +277,18 @@ def test_nonnegative_weights_give_nonnegative_scores():
     assert np.any(s_pos[fin] > 0)
 
 
+def test_rows_of_a_request_stop_at_their_own_bounds():
+    """Verify rows of one request share its keys but each is scored only below
+    its own causal bound: row i of a request of length L with Q rows ends at
+    L - Q + i + 1; the logits there and past it are -inf."""
+    wl, qr, w, cache, starts, ends, s = _step("fp8", seed=8, R=2, seq=(100, 130), qlen=(3, 3))
+    for q in range(wl.R):
+        L, Q = int(wl.seq_lens[q]), int(wl.query_lens[q])
+        for i, r in enumerate(range(int(starts[q]), int(starts[q + 1]))):
+            assert ends[r] == L - Q + i + 1
+            assert np.all(np.isfinite(s[r, :ends[r]])) and np.all(np.isneginf(s[r, ends[r]:]))
+
+
 def test_score_matches_dequantised_float_reference():
     """The oracle's logits against an independent dequantisation: each cache
     byte decoded through the brute-force codebook tables and the layout

@@ -19,7 +19,7 @@ import test_oracle_rowgroup as TR
 
 _orig = {name: getattr(O, name) for name in (
     "score_row", "decode_query", "decode_keys", "decode_layout", "topk", "fp8_scale_exponent",
-    "mx_scale_exponent", "layer_norm_bf16", "_half_warp_sum", "quantize_queries")}
+    "mx_scale_exponent", "layer_norm_bf16", "_half_warp_sum", "quantize_queries", "score_paged")}
 _orig_rank_local_ends = D.rank_local_ends
 _orig_quantize_query = O.quantize_query
 _orig_quantize_key = O.quantize_key
@@ -202,6 +202,17 @@ def fp8_key_codes_unscaled(fmt, normed):
     return codes, sc
 
 
+def rows_scored_to_the_request_bound(fmt, q_rows, w, cache, page_stride, block_table, starts, row_ends,
+                                     rows_subset=None):
+    bounds = np.asarray(row_ends).copy()
+    st = np.asarray(starts)
+    for q in range(len(st) - 1):
+        a, b = int(st[q]), int(st[q + 1])
+        if b > a:
+            bounds[a:b] = bounds[a:b].max()
+    return _orig["score_paged"](fmt, q_rows, w, cache, page_stride, block_table, starts, bounds, rows_subset)
+
+
 def queries_head_major_scales(q):
     payload, scales = _orig["quantize_queries"](q)
     rows, heads = payload.shape[0], payload.shape[1]
@@ -290,6 +301,8 @@ CASES = [
     ("MXFP4 key block scales in reverse byte order", O, "decode_keys", keys_block_scales_reversed,
      [TI.test_score_matches_dequantised_float_reference]),
     ("row bound one short", O, "decode_layout", layout_bound_one_short, [TI.test_decode_layout_golden]),
+    ("verify rows scored to their request's largest bound", O, "score_paged", rows_scored_to_the_request_bound,
+     [TI.test_rows_of_a_request_stop_at_their_own_bounds]),
     ("row bounds shifted by one row", O, "decode_layout", layout_request_off_by_one,
      [TI.test_decode_layout_golden, TI.test_decode_layout_bruteforce_random]),
     ("top-k ascending", O, "topk", topk_ascending, [TI.test_topk_short_rows_return_all_positions]),
