@@ -213,6 +213,24 @@ def rows_scored_to_the_request_bound(fmt, q_rows, w, cache, page_stride, block_t
     return _orig["score_paged"](fmt, q_rows, w, cache, page_stride, block_table, starts, bounds, rows_subset)
 
 
+def every_request_reads_request_zero(fmt, q_rows, w, cache, page_stride, block_table, starts, row_ends,
+                                     rows_subset=None):
+    bt = np.asarray(block_table).copy()
+    bt[:] = bt[0]
+    return _orig["score_paged"](fmt, q_rows, w, cache, page_stride, bt, starts, row_ends, rows_subset)
+
+
+def positions_paged_column_major(fmt, cache, page_stride, pages, n):
+    """Position t read from page t mod P, offset t div P (P pages) instead of
+    page t div 64, offset t mod 64."""
+    if n == 0:
+        return _orig["decode_keys"](fmt, cache, page_stride, pages, 0)
+    npg = (n + 63) // 64
+    full = _orig["decode_keys"](fmt, cache, page_stride, pages, npg * 64)
+    t = np.arange(n)
+    return full[(t % npg) * 64 + t // npg]
+
+
 def queries_head_major_scales(q):
     payload, scales = _orig["quantize_queries"](q)
     rows, heads = payload.shape[0], payload.shape[1]
@@ -303,6 +321,10 @@ CASES = [
     ("row bound one short", O, "decode_layout", layout_bound_one_short, [TI.test_decode_layout_golden]),
     ("verify rows scored to their request's largest bound", O, "score_paged", rows_scored_to_the_request_bound,
      [TI.test_rows_of_a_request_stop_at_their_own_bounds]),
+    ("every request reads the first request's pages", O, "score_paged", every_request_reads_request_zero,
+     [TI.test_score_matches_dequantised_float_reference]),
+    ("positions paged column-major", O, "decode_keys", positions_paged_column_major,
+     [TI.test_score_matches_dequantised_float_reference]),
     ("row bounds shifted by one row", O, "decode_layout", layout_request_off_by_one,
      [TI.test_decode_layout_golden, TI.test_decode_layout_bruteforce_random]),
     ("top-k ascending", O, "topk", topk_ascending, [TI.test_topk_short_rows_return_all_positions]),
