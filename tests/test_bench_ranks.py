@@ -89,3 +89,27 @@ def test_tensor_side_of_the_roofline():
     assert abs(t["achieved"] - 8.192e-3) < 1e-12 and t["peak"] == 2000.0
     assert abs(t["frac"] - 8.192e-3 / 2000.0) < 1e-15
     assert bench.tensor_side(1, 1.0, "mxfp4_rg", {"bf16_tflops": 1.0, "source": "x"})["peak"] == 6.0
+
+
+def test_traffic_record_matches_the_scoring_source_and_scales_per_unit():
+    """The committed ncu traffic of the scoring kernel applies only to the
+    source it was taken on (a hash of the kernel's files) and scales with the
+    algorithmic bytes of the launch."""
+    import json
+    rec = json.load(open(os.path.join(ROOT, "profiles", "score_kernel_traffic.json")))
+    e = rec["fp8_decode"]
+    if e["source_hash"] == bench.score_source_hash():
+        assert bench.ncu_traffic("fp8_decode", e["units"]) == e["dram_bytes"]
+        assert bench.ncu_traffic("fp8_decode", 2 * e["units"]) == 2 * e["dram_bytes"]
+    else:   # the kernel changed since the capture: no traffic is reported
+        assert bench.ncu_traffic("fp8_decode", e["units"]) is None
+    assert bench.ncu_traffic("no_such_workload", 1) is None
+    # every recorded workload: traffic within 10 % above its algorithmic bytes
+    for name, v in rec.items():
+        assert 1.0 <= v["dram_bytes"] / v["units"] < 1.1, name
+
+
+def test_traffic_key_names_format_overrides():
+    from synth import make_workload
+    assert bench.traffic_key(make_workload("long_mxfp4")) == "long_mxfp4"
+    assert bench.traffic_key(make_workload("long_mxfp4", fmt="mxfp4_rg")) == "long_mxfp4/mxfp4_rg"
