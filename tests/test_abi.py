@@ -69,3 +69,37 @@ def test_host_argument_checks(lib):
     assert lib.dsa_score_paged(2, 32, 32, 32, 4352 + 8, 1, 16, 1, 1, 16, 16, 1, 1, 1, None, 0, 4, None, 256,
                                10**9, None, None) == -1                         # MXFP4 stride not a multiple of 16
     assert lib.dsa_topk(None, 10, None, 1, 20, 4, None, None, 0, None) == -1  # ld < width
+
+
+def test_more_host_argument_checks(lib):
+    """The documented error codes of the remaining calls, all decided on the host."""
+    A = 1 << 20   # a 256-byte-aligned stand-in address (never dereferenced: every call below fails its checks)
+    # dsa_decode_layout_dcp: rank outside the world, interleave < 1, world < 1
+    assert lib.dsa_decode_layout_dcp(A, 1, A, 1, 1, 2, 2, 64, A, A, None) == -1
+    assert lib.dsa_decode_layout_dcp(A, 1, A, 1, 1, 0, 2, 0, A, A, None) == -1
+    assert lib.dsa_decode_layout_dcp(A, 1, A, 1, 1, 0, 0, 64, A, A, None) == -1
+    # dsa_topk_merge: short leading dimension, bad rank with out_local, unaligned workspace, world < 1
+    assert lib.dsa_topk_merge(A, 63, A, 64, 2, 2, 32, 16, 32, A, 0, None, A, 10**9, None) == -1
+    assert lib.dsa_topk_merge(A, 64, A, 64, 2, 2, 32, 16, 32, A, 2, A, A, 10**9, None) == -1
+    assert lib.dsa_topk_merge(A, 64, A, 64, 2, 2, 32, 16, 32, A, 0, None, A + 16, 10**9, None) == -1
+    assert lib.dsa_topk_merge(A, 64, A, 64, 2, 0, 32, 16, 32, A, 0, None, A, 10**9, None) == -1
+    assert lib.dsa_topk_merge(A, 64, A, 64, 2, 2, 32, 16, 32, A, 0, None, A, 16, None) == -1   # workspace too small
+    # dsa_query_norm: unknown variant, short or odd row stride, unaligned rows
+    assert lib.dsa_query_norm(A, 1536, A, 1e-6, 4, A, 1536, 2, None) == -1
+    assert lib.dsa_query_norm(A, 1500, A, 1e-6, 4, A, 1536, 0, None) == -1
+    assert lib.dsa_query_norm(A, 1540, A, 1e-6, 4, A, 1536, 0, None) == -1
+    assert lib.dsa_query_norm(A + 2, 1536, A, 1e-6, 4, A, 1536, 0, None) == -1
+    assert lib.dsa_query_norm(None, 1536, None, 1e-6, 0, None, 1536, 0, None) == 0    # empty batch
+    # dsa_score_paged: unaligned query rows or workspace, short block-table stride, short logits
+    # leading dimension, a workspace too small, missing cache with pages
+    base = [0, A, A, A, 8448, 1, A, 4, 4, A, A, 1, 1, 1, None, 0, 16, A, A, 10**9, None, None]   # never called as is
+    for i, v in ((1, A + 8), (18, A + 128), (7, 3), (19, 64)):
+        bad = list(base)
+        bad[i] = v
+        assert lib.dsa_score_paged(*bad) == -1, i
+    bad = list(base)
+    bad[14], bad[15] = A, 100                             # logits with ld < max_pages * 64
+    assert lib.dsa_score_paged(*bad) == -1
+    bad = list(base)
+    bad[3] = None                                         # pages but no cache
+    assert lib.dsa_score_paged(*bad) == -1
