@@ -103,3 +103,38 @@ def test_more_host_argument_checks(lib):
     bad = list(base)
     bad[3] = None                                         # pages but no cache
     assert lib.dsa_score_paged(*bad) == -1
+
+
+def test_prepare_step_returns_each_part_s_error(lib):
+    """The fused preparation reports the argument error of whichever part
+    (quantize, insert, layout) is wrong, before any launch."""
+    A = 1 << 20
+    ok_q = [0, A, 4096, A, 32, 1, A, A]                       # fmt, q, stride, wv, stride, rows, q_out, w_out
+    ok_k = [A, 128, A, A, 1e-6, A, 1, A, 8448, 1]             # k, stride, gamma, beta, eps, slots, n, cache, stride, pages
+    ok_l = [A, 1, A, 1, 1, A, A]                              # seq, num_seq, qlen, R, num_rows, starts, row_ends
+    tail = [None, None]                                       # status, stream
+
+    def call(q, k, l):
+        return lib.dsa_prepare_step(*q, *k, *l, *tail)
+
+    bad_q = list(ok_q)
+    bad_q[0] = 9                                              # unknown format
+    assert call(bad_q, ok_k, ok_l) == -2
+    bad_q = list(ok_q)
+    bad_q[2] = 4000                                           # query row stride < 4096
+    assert call(bad_q, ok_k, ok_l) == -1
+    bad_k = list(ok_k)
+    bad_k[8] = 4352                                           # FP8 page stride < 8448
+    assert call(ok_q, bad_k, ok_l) == -1
+    bad_l = list(ok_l)
+    bad_l[1] = 0                                              # fewer seq_lens than requests
+    assert call(ok_q, ok_k, bad_l) == -1
+
+
+def test_the_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No fallback: a missing libdsa.so raises instead of computing anything."""
+    from sparse_attention_indexer_score_gb300 import dsa
+    monkeypatch.setattr(dsa, "_lib", None)
+    monkeypatch.setattr(dsa, "LIB_PATH", str(tmp_path / "libdsa.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        dsa.lib()
