@@ -84,3 +84,21 @@ def test_values_are_bf16_patterns_of_the_stated_draws():
     big = np.abs(bf16_bits_to_f32(make_workload("mxfp4_decode").q_bits)).ravel()
     share = float((big > 6.0).mean())   # |N(0,1)| > 6 is ~2e-9; x20 outliers exceed 6 about 77 % of the time
     assert 0.005 < share < 0.01
+
+
+@pytest.mark.parametrize("name,unique,scored,rows", [
+    ("fp8_decode", 393_216, 393_216, 64),            # 64 x mean(U[4096, 8192])
+    ("mxfp4_decode", 1_572_864, 1_572_864, 64),      # 64 x mean(U[16384, 32768])
+    ("spec_verify", 4_456_448, 11_141_120, 324),     # 128 x mean(U[4096, 65536]); 2.5 rows a request + 4 padding
+    ("long_mxfp4", 1_048_576, 1_048_576, 8),         # 8 x 131072
+])
+def test_sizes_are_those_of_the_stated_configurations(name, unique, scored, rows):
+    """Keys read (the requests' lengths), keys scored (each row to its own
+    causal bound) and rows come out within 5 % of the configurations'
+    expected sizes."""
+    wl = make_workload(name)
+    got_scored = sum(int(wl.seq_lens[q]) - int(wl.query_lens[q]) + i + 1
+                     for q in range(wl.R) for i in range(int(wl.query_lens[q])))
+    assert abs(int(wl.seq_lens.sum()) / unique - 1) < 0.05
+    assert abs(got_scored / scored - 1) < 0.05
+    assert abs(wl.num_rows / rows - 1) < 0.05
