@@ -54,9 +54,10 @@ extern "C" {
  *  DSA_FMT_FP8     E4M3 keys, one power-of-two FP32 scale per token (132 B/token);
  *                  E4M3 queries with the per-head scale folded into the weights.
  *  DSA_FMT_FP8_MX  as DSA_FMT_FP8, but the key scale is stored as its exponent
- *                  in four equal UE8M0 bytes (the "mx" scales).  The scorer treats
- *                  byte b as the scale of columns 32b..32b+31, which for the
- *                  four equal bytes the writer stores is the token's one scale.
+ *                  in four UE8M0 bytes (the "mx" scales).  The scorer applies
+ *                  byte b to columns 32b..32b+31 (MX block scales, inside a
+ *                  block-scaled MMA), so caches with unequal bytes score as
+ *                  such; the writer stores the token's one exponent four times.
  *  DSA_FMT_MXFP4   E2M1 keys and queries, one UE8M0 scale per 32 columns
  *                  (68 B/token); the head weights carry only the 1/64 factor.
  *  DSA_FMT_MXFP4_RG  the codes and scales of DSA_FMT_MXFP4, placed group-major
@@ -369,20 +370,24 @@ int dsa_topk_merge(const float* scores, int64_t scores_ld, const int32_t* idx,
  * cudaMalloc, or a plugin host that passes a kernel its inputs and outputs but
  * no allocator.  It computes what dsa_topk computes, with the same arguments
  * minus the workspace.  Its scratch is a file-scope device array of
- * DSA_TOPK_NOALLOC_MAX_ROWS rows (512 KB), held by every GPU that loads
- * the library until the process exits.
+ * DSA_TOPK_NOALLOC_SCRATCH_BYTES (about 5 MB: for each of the
+ * DSA_TOPK_NOALLOC_MAX_ROWS rows two 8 KB histograms, 16 bytes of counters and
+ * 64 KB of candidates), held by every GPU that loads the library until the
+ * process exits.
  *
  *   - rows > DSA_TOPK_NOALLOC_MAX_ROWS returns DSA_ERR_UNSUPPORTED (split the rows
  *     over several calls).
- *   - The first call on a device looks up the array's device address on the
- *     current device (cudaGetSymbolAddress); make that first call before any
- *     stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress, a host-side query).  The first call on a device
+ *     also loads the library's device code there: make that first call before
+ *     any stream capture.
  *   - Every call shares the one array: it clears the parts that must start at
  *     zero on its stream, but calls that overlap on the GPU (other streams or
  *     other threads) race and must be serialised by the caller.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
  */
 #define DSA_TOPK_NOALLOC_MAX_ROWS 64
+#define DSA_TOPK_NOALLOC_SCRATCH_BYTES 5243904
 int dsa_topk_noalloc(const float* logits, int64_t ld, const int32_t* row_ends,
                      int64_t rows, int64_t width, int64_t k, int32_t* out, void* stream);
 

@@ -101,13 +101,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-// Wait for a phase to complete, with a time limit only (used on the exit
-// path to drain copies in flight).
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
-    const unsigned long long t0 = globaltimer();
+// Wait for a phase to complete until `deadline` (globaltimer ns): used on the
+// exit path, so that copies in flight land before the CTA exits.  One deadline
+// serves a whole drain.  Past it the timeout bit of the status word is set
+// (the call's results and the CTA's shared memory are then invalid) and the
+// wait returns false.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, unsigned long long deadline,
+                                           int32_t* status) {
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > kWaitLimitNs) return;
+        if (globaltimer() > deadline) {
+            if (status) atomicOr(status, DSA_STATUS_TIMEOUT);
+            return false;
+        }
     }
+    return true;
 }
 
 // Shared-memory counter with release / acquire ordering (a thread's earlier
@@ -219,6 +226,17 @@ __device__ __forceinline__ void tc_mma_mxf4(uint32_t d, uint64_t a, uint64_t b, 
     asm volatile(
         "{\n\t.reg .pred p;\n\t setp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], "
+        "p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+// E4M3 operands with one UE8M0 scale per row per instruction (K = 32): byte
+// `id` of each row's scale word, chosen by the instruction descriptor's sf ids.
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], "
         "p;\n\t}" ::"r"(d),
         "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
         : "memory");

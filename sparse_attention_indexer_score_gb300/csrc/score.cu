@@ -27,8 +27,9 @@
 //              scales (warp 0 copies the first page's codes), so two threads
 //              feed the copy engine.
 //
-// Formats: FP8 and FP8-MX use kind::f8f6f4 (E4M3 x E4M3) and multiply the
-// per-key scale in the epilogue.  MXFP4 keeps its codes packed and uses
+// Formats: FP8 uses kind::f8f6f4 (E4M3 x E4M3) and multiplies the per-key
+// FP32 scale in the epilogue.  FP8-MX uses kind::mxf8f6f4 with one UE8M0 key
+// scale per 32 columns (scale byte kk in instruction kk).  MXFP4 keeps its codes packed and uses
 // kind::mxf4 (K = 64, two UE8M0 scales per row from TMEM, scale bytes 2m and
 // 2m + 1 in instruction m).  Token-major pages are 64 rows of 64 bytes, which
 // one TMA box lands in the 64-byte-swizzled K-major layout; as packed stages
@@ -525,8 +526,12 @@ __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, 
         if (ok) pr.finish(p);
         // Drain: every copy issued must have landed before the CTA exits.
         const int it = pr.it, i_seg = pr.i_seg, lg = pr.lg;
-        for (int i = max(0, it - (1 << lg)); i < it; ++i) mbar_drain(pr.full + (i & ((1 << lg) - 1)), (i >> lg) & 1);
-        for (int i = max(0, i_seg - 2); i < i_seg; ++i) mbar_drain(pr.qfull + (i & 1), (i >> 1) & 1);
+        const unsigned long long deadline = globaltimer() + kWaitLimitNs;
+        bool drained = true;
+        for (int i = max(0, it - (1 << lg)); i < it && drained; ++i)
+            drained = mbar_drain(pr.full + (i & ((1 << lg) - 1)), (i >> lg) & 1, deadline, p.status);
+        for (int i = max(0, i_seg - 2); i < i_seg && drained; ++i)
+            drained = mbar_drain(pr.qfull + (i & 1), (i >> 1) & 1, deadline, p.status);
     }
     __syncwarp();
 }
@@ -576,14 +581,15 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                                          uint64_t* done_bar, volatile int* abort) {
     const int lane = threadIdx.x & 31;
     const int w = (threadIdx.x >> 5) - 1;
-    // FP8 keys carry one scale per key: an FP32 power of two, or (FP8-MX) one
-    // UE8M0 exponent repeated in the four bytes of the scale word, so the
-    // product with the (unscaled) FP8 query is 2^e * sum q8 k8 either way; both
-    // take the plain FP8 MMA and apply the key scale in the epilogue.  Only
-    // MXFP4 uses the block-scaled MMA.
-    const bool key_scale = !fmt_fp4(p.fmt);
-    const bool mx_byte = (p.fmt == DSA_FMT_FP8_MX);
+    // FP8 keys with an FP32 scale take the plain FP8 MMA and the key scale in
+    // the epilogue.  FP8-MX keys carry four UE8M0 bytes, byte b the scale of
+    // columns 32b..32b+31: the block-scaled FP8 MMA applies byte kk in its
+    // instruction kk (K = 32), the query's scales being 1 (its scale is folded
+    // into the head weights).  MXFP4 uses the block-scaled FP4 MMA.
+    const bool key_scale = (p.fmt == DSA_FMT_FP8);
+    const bool fp8mx = (p.fmt == DSA_FMT_FP8_MX);
     const bool fp4 = fmt_fp4(p.fmt);
+    const bool block_scaled = !key_scale;
     const bool rg = (p.fmt == DSA_FMT_MXFP4_RG);
     const int lg = ring_stages_log2(p.fmt);
     const int stage_bytes = ring_stage_bytes(p.fmt);
@@ -612,14 +618,14 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             nrows = p.segs[tag.y].z;
             qb = cur & 1;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(qfull + qb, (cur >> 1) & 1, abort, p.status))) break;
-            if (fp4) {
+            if (block_scaled) {
                 // Query block scales: line L of the atom holds the words of MMA
                 // rows L, 32 + L, 64 + L, 96 + L (row r * 32 + h = head h of query row r).
                 const uint8_t* raw = smem + OFF_QSF + qb * kQsfBytes;
                 // word of head `lane` of row r: token-major rows hold it as is; row-group
-                // rows hold block g's byte at g * 64 + head
+                // rows hold block g's byte at g * 64 + head; FP8 queries are unscaled (2^0)
                 auto word = [&](int r) -> uint32_t {
-                    if (r >= nrows) return 0x7F7F7F7Fu;
+                    if (r >= nrows || fp8mx) return 0x7F7F7F7Fu;
                     if (!rg) return reinterpret_cast<const uint32_t*>(raw + r * kQsfRow)[lane];
                     const uint8_t* b = raw + r * kQsfRowRg + lane;
                     return static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[kRgQuerySlots]) << 8) |
@@ -662,12 +668,11 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             w3 = rs[96 + lane];
         }
         if (key_scale) {
-            // FP8-MX: byte 0 of the word is e + 127, and 2^e has exactly those exponent bits
             float* ks = reinterpret_cast<float*>(smem + OFF_KS + a * 512);
-            ks[lane] = __uint_as_float(mx_byte ? (w0 & 0xFFu) << 23 : w0);
-            ks[32 + lane] = __uint_as_float(mx_byte ? (w1 & 0xFFu) << 23 : w1);
-            ks[64 + lane] = __uint_as_float(mx_byte ? (w2 & 0xFFu) << 23 : w2);
-            ks[96 + lane] = __uint_as_float(mx_byte ? (w3 & 0xFFu) << 23 : w3);
+            ks[lane] = __uint_as_float(w0);
+            ks[32 + lane] = __uint_as_float(w1);
+            ks[64 + lane] = __uint_as_float(w2);
+            ks[96 + lane] = __uint_as_float(w3);
         } else {
             reinterpret_cast<uint4*>(smem + OFF_SFA + s * 512)[lane] = make_uint4(w0, w1, w2, w3);
             fence_proxy_async_smem();
@@ -683,6 +688,15 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                 const uint32_t id = idesc_f8f6f4(kMmaE4M3, kMmaE4M3, 128, n);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) tc_mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, id, kk > 0);
+            } else if (fp8mx) {
+                const uint32_t sfa = tmem + TM_SFA + s * 4;
+                tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
+                const uint32_t sfb = tmem + TM_SFB + (qb * kMmaWarps + w) * 4;
+                const uint64_t ad = desc_sw128(ka), bd = desc_sw128(kb);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_mxf8(d, ad + 2 * kk, bd + 2 * kk, idesc_mx(kMmaE4M3, kMmaE4M3, 128, n, kk, kk), sfa, sfb,
+                                kk > 0);
             } else if (rg) {
                 const uint32_t sfa = tmem + TM_SFA + s * 4;
                 tc_cp_32x128b_warpx4(sfa, desc_rows16(smem_u32(smem + OFF_SFA + s * 512)));
@@ -713,7 +727,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
     }
     if (lane == 0) {
         tc_commit(done_bar);
-        mbar_drain(done_bar, 0);
+        mbar_drain(done_bar, 0, globaltimer() + kWaitLimitNs, p.status);
     }
     __syncwarp();
 }
@@ -791,7 +805,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
     const int m = quarter * 32 + lane;       // key of the tile this thread owns
     float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - kFirstEpiWarp) * (kSegRows * kHeads);
     const int2* ainfo = reinterpret_cast<const int2*>(smem + OFF_AINFO);
-    const bool f32scale = !fmt_fp4(p.fmt);   // FP8 and FP8-MX: one scale per key
+    const bool f32scale = (p.fmt == DSA_FMT_FP8);   // FP32 key scale (FP8-MX scales act inside the MMA)
     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC;
     uint32_t* gh = reinterpret_cast<uint32_t*>(smem + OFF_HIST) + group * kGroupHistWords;
     const int e = threadIdx.x - 32 * kFirstEpiWarp - group * 128;   // thread index within the group
@@ -1076,11 +1090,14 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
                    status) != cudaSuccess)
         return DSA_ERR_CUDA;
 
-    static bool attr_set = false;
-    if (!attr_set) {
+    // The kernel's shared-memory limit is an attribute of each device's copy of it.
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
+    if (!attr_set[dev]) {
         if (cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem) != cudaSuccess)
             return DSA_ERR_CUDA;
-        attr_set = true;
+        attr_set[dev] = true;
     }
     ScoreArgs a;
     a.fmt = fmt;

@@ -3,7 +3,7 @@
 import numpy as np
 import pytest
 
-from dsa_case import bf16_tensor, check_logits, check_topk, gpu_run, oracle_run
+from dsa_case import bf16_tensor, check_logits, check_topk, gpu_run, oracle_rows, oracle_run
 from oracle import indexer as O
 from synth import bf16_bits_to_f32, make_workload
 
@@ -211,22 +211,93 @@ def test_score_cache_bytes_match_oracle(cuda_lib, fmt):
                               o["cache"][p_or * stride:p_or * stride + O.page_bytes(fmt)]), p_gpu
 
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp4_rg"])
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("case", [1, 2, 3, 5])
-def test_score_mxfp4_page_stride(cuda_lib, fmt, case):
-    """MXFP4 in either placement in a pool whose physical page stride (4400
-    bytes) is above the 4352-byte section and not a multiple of 32."""
+def test_score_page_stride(cuda_lib, fmt, case):
+    """Every format in a pool whose physical page stride is 48 bytes above the
+    page section (8496 for FP8, 4400 for MXFP4: merged caches, page
+    "amd.ops.fp4_indexer", cache_views), not a multiple of 32."""
     spec = dict(SMALL[case])
     wl = make_workload("tiny_fp8", fmt=fmt, seed=300 + case, topk=[16, 64, 100, 5, 2, 512][case], **spec)
-    g = gpu_run(wl, page_stride=4400)
-    o = oracle_run(wl, page_stride=4400)
+    section = O.page_bytes(fmt)
+    stride = section + 48
+    g = gpu_run(wl, page_stride=stride)
+    o = oracle_run(wl, page_stride=stride)
     assert g["status"] == 0
     cache = g["cache"].cpu().numpy()
     for p_gpu, p_or in o["remap"].items():
-        assert np.array_equal(cache[p_gpu * 4400:p_gpu * 4400 + 4352], o["cache"][p_or * 4400:p_or * 4400 + 4352])
+        assert np.array_equal(cache[p_gpu * stride:p_gpu * stride + section],
+                              o["cache"][p_or * stride:p_or * stride + section])
     rows = range(wl.num_rows)
     check_logits(g["logits"], o["scores"], o["row_ends"], rows)
     check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, rows)
+
+
+def _fp8_code_bytes(rng, shape):
+    """E4M3 codes of magnitude 2^-2 .. 3.75: random sign, exponent field 5..8,
+    random mantissa (no NaN code)."""
+    sign = rng.integers(0, 2, shape, dtype=np.uint8) << 7
+    exp = rng.integers(5, 9, shape, dtype=np.uint8) << 3
+    man = rng.integers(0, 8, shape, dtype=np.uint8)
+    return (sign | exp | man).astype(np.uint8)
+
+
+@pytest.mark.parametrize("page_stride", [8448, 8448 + 64])
+def test_fp8_mx_unequal_block_scales(cuda_lib, page_stride):
+    """FP8-MX keys whose four UE8M0 bytes differ: byte b scales columns
+    32b..32b+31 (page "cutedsl.dsa.index", module docstring: the MX scales of
+    the logits kernels).  Cache, query rows and weights are seeded bytes
+    written on the host, not by the library's writer; the oracle decodes the
+    same bytes per 32-column block."""
+    import torch
+    rng = np.random.default_rng(77 + page_stride)
+    qlen = np.array([1, 3, 4, 2, 1, 4], np.int32)
+    seq = np.array([1, 700, 129, 64, 1000, 300], np.int32)
+    R = len(qlen)
+    npg = (seq + 63) // 64
+    num_pages = int(npg.sum()) + 3
+    max_pages = int(npg.max())
+    perm = rng.permutation(num_pages).astype(np.int32)
+    bt = np.full((R, max_pages), -1, np.int32)
+    off = 0
+    for q in range(R):
+        bt[q, :npg[q]] = perm[off:off + npg[q]]
+        off += npg[q]
+    cache = np.zeros(num_pages * page_stride, np.uint8)
+    for p in range(num_pages):
+        base = p * page_stride
+        cache[base:base + 8192] = _fp8_code_bytes(rng, 8192)
+        cache[base + 8192:base + 8448] = rng.integers(124, 131, 256).astype(np.uint8)   # 2^-3 .. 2^3, unequal
+    rows = int(qlen.sum()) + 2                                                         # two padding rows
+    q_rows = _fp8_code_bytes(rng, (rows, 4096))
+    # positive head weights: the weighted head sum does not cancel, so FP32
+    # accumulation stays far inside the tolerance whatever the block scales
+    w = ((np.abs(rng.standard_normal((rows, 32))).astype(np.float32).view(np.uint32) >> 16) << 16).view(np.float32)
+    starts, row_ends = O.decode_layout(seq, qlen, rows)
+    k = 96
+    dev = "cuda"
+    wt = torch.from_numpy(w).to(torch.bfloat16).to(dev)
+    logits, top = cuda_lib.score_paged("fp8_mx", torch.from_numpy(q_rows).to(dev), wt,
+                                       torch.from_numpy(cache).to(dev), page_stride, num_pages,
+                                       torch.from_numpy(bt).to(dev), torch.from_numpy(starts).to(dev),
+                                       torch.from_numpy(row_ends).to(dev), int(qlen.max()), k=k, want_logits=True)
+    torch.cuda.synchronize()
+    want = O.score_paged("fp8_mx", q_rows, w, cache, page_stride, bt, starts, row_ends)
+    check_logits(logits.cpu().numpy(), want, row_ends, range(rows))
+    check_topk(top.cpu().numpy(), want, row_ends, k, range(rows))
+    # the writer's form: the four scale bytes of each key equal (byte 0 copied to bytes 1-3)
+    eq = cache.copy()
+    for p in range(num_pages):
+        base = p * page_stride + 8192
+        sb = eq[base:base + 256].reshape(64, 4)
+        sb[:, 1:] = sb[:, :1]
+    want_eq = O.score_paged("fp8_mx", q_rows, w, eq, page_stride, bt, starts, row_ends)
+    logits_eq, _ = cuda_lib.score_paged("fp8_mx", torch.from_numpy(q_rows).to(dev), wt,
+                                        torch.from_numpy(eq).to(dev), page_stride, num_pages,
+                                        torch.from_numpy(bt).to(dev), torch.from_numpy(starts).to(dev),
+                                        torch.from_numpy(row_ends).to(dev), int(qlen.max()), want_logits=True)
+    torch.cuda.synchronize()
+    check_logits(logits_eq.cpu().numpy(), want_eq, row_ends, range(rows))
 
 
 def test_topk_standalone_exact(cuda_lib):
@@ -293,29 +364,27 @@ def test_empty_and_degenerate(cuda_lib):
 
 
 @pytest.mark.parametrize("name", ["tiny_fp8", "fp8_decode", "mxfp4_decode", "spec_verify", "long_mxfp4",
-                                  "long_mxfp4/mxfp4_rg"])
-def test_full_size_sampled_rows(cuda_lib, name):
+                                  "long_mxfp4/mxfp4_rg", "fp8_decode@8512"])
+def test_full_size_all_rows(cuda_lib, name):
     """The named decode-step workloads at full size, in the launch configuration
-    the bench times (``name/format`` overrides the cache format); the oracle
-    checks a sample of rows (all for the tiny one)."""
+    the bench times (``name/format`` overrides the cache format, ``name@stride``
+    the physical page stride), every row against the oracle: logits element by
+    element, top-k sets, row bounds and quantised query rows."""
+    name, _, stride = name.partition("@")
     name, _, fmt = name.partition("/")
-    wl = make_workload(name, **({"fmt": fmt} if fmt else {}))
-    g = gpu_run(wl, want_logits=True)
+    overrides = {"fmt": fmt} if fmt else {}
+    page_stride = int(stride) if stride else None
+    wl = make_workload(name, **overrides)
+    g = gpu_run(wl, want_logits=True, page_stride=page_stride)
     assert g["status"] == 0
-    rng = np.random.default_rng(0)
-    real = [r for r in range(wl.num_rows) if wl.row_request[r] >= 0]
-    if name == "tiny_fp8":
-        rows = list(range(wl.num_rows))
-    else:
-        rows = sorted(set(rng.choice(real, size=min(3, len(real)), replace=False).tolist() + [real[-1]]))
-        if name == "spec_verify":
-            rows += [wl.num_rows - 1]     # a padding row
-    o = oracle_run(wl, rows=rows)
-    assert np.array_equal(g["row_ends"], o["row_ends"])
+    rows = list(range(wl.num_rows))
+    scores, top, row_ends, starts, q_rows = oracle_rows(name, overrides, rows, page_stride=page_stride)
+    assert np.array_equal(g["row_ends"], row_ends) and np.array_equal(g["starts"], starts)
     used = _used(wl.fmt)
-    assert np.array_equal(g["q_rows"][:, :used], o["q_rows"][:, :used])
-    check_logits(g["logits"], o["scores"], o["row_ends"], rows)
-    check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, rows)
+    assert np.array_equal(g["q_rows"][:, :used], q_rows[:, :used])
+    for r in rows:
+        check_logits(g["logits"][r:r + 1], scores[r][None], row_ends[r:r + 1], [0])
+        check_topk(g["topk"][r:r + 1], scores[r][None], row_ends[r:r + 1], wl.topk, [0])
 
 
 def test_graphed_step_matches_eager(cuda_lib):
