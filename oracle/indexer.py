@@ -249,33 +249,23 @@ def insert_key(fmt: str, cache: np.ndarray, page_stride: int, num_pages: int,
     normed = layer_norm_bf16(x, gamma, beta, eps)
     codes, scale_bytes = quantize_key(fmt, normed)
     flat = cache.reshape(-1)
-    bad = 0
+    inside = slots < num_pages * PAGE
+    bad = int(np.count_nonzero((slots >= 0) & ~inside))
+    # keys written in order: where a slot repeats, the last key's bytes stay
+    order = np.arange(slots.size)[(slots >= 0) & inside]
+    _, last = np.unique(slots[order][::-1], return_index=True)
+    keep = order[::-1][last]
+    page, off = np.divmod(slots[keep], PAGE)
+    base = page * page_stride
     if fmt == "mxfp4_rg":
-        for i, slot in enumerate(slots):
-            if slot < 0:
-                continue
-            if slot >= num_pages * PAGE:
-                bad += 1
-                continue
-            page, off = divmod(int(slot), PAGE)
-            base = page * page_stride
-            for g in range(4):
-                a = base + g * RG_GROUP_BYTES + off * 16
-                flat[a: a + 16] = codes[i][g * 16:(g + 1) * 16]
-                flat[base + FP4_KEY_BYTES + g * RG_SCALE_GROUP + off] = scale_bytes[i][g]
+        for g in range(4):
+            flat[(base + g * RG_GROUP_BYTES + off * 16)[:, None] + np.arange(16)] = codes[keep, g * 16:(g + 1) * 16]
+            flat[base + FP4_KEY_BYTES + g * RG_SCALE_GROUP + off] = scale_bytes[keep, g]
         return bad
     code_bytes = DIM if not _fp4(fmt) else DIM // 2
     scale_base = PAGE * code_bytes
-    for i, slot in enumerate(slots):
-        if slot < 0:
-            continue
-        if slot >= num_pages * PAGE:
-            bad += 1
-            continue
-        page, off = divmod(int(slot), PAGE)
-        base = page * page_stride
-        flat[base + off * code_bytes: base + (off + 1) * code_bytes] = codes[i]
-        flat[base + scale_base + off * 4: base + scale_base + off * 4 + 4] = scale_bytes[i]
+    flat[(base + off * code_bytes)[:, None] + np.arange(code_bytes)] = codes[keep]
+    flat[(base + scale_base + off * 4)[:, None] + np.arange(4)] = scale_bytes[keep]
     return bad
 
 
@@ -363,12 +353,31 @@ def decode_keys(fmt: str, cache: np.ndarray, page_stride: int, pages, n: int) ->
     return (e2m1_decode(codes).reshape(n, 4, 32) * np.ldexp(1.0, e)[..., None]).reshape(n, DIM)
 
 
-def score_row(fmt: str, q_row, w_row, keys: np.ndarray) -> np.ndarray:
-    """score[t] = sum_h w_h * ReLU(q_h . k_t) in float64 (page *cutedsl.dsa.index*,
-    module docstring; *amd.ops.fp4_indexer*, ``score_paged``)."""
-    Q = decode_query(fmt, q_row)
-    dots = keys @ Q.T                                   # [n, 32], exact
+def decode_queries(payload_row, scales_row) -> np.ndarray:
+    """float64 [heads, 128] values of one row of ``quantize_queries``' output:
+    payload [heads, 64] (E2M1 pairs) and the row's 256 scale bytes, block g of
+    head h at g * 64 + h (page *amd.ops.fp4_indexer*, ``quantize_queries``; the
+    group-major order is a reading)."""
+    payload_row = np.asarray(payload_row, dtype=np.uint8)
+    heads = payload_row.shape[0]
+    codes = unpack_e2m1(payload_row)                                        # [heads, 128]
+    sc = np.asarray(scales_row, dtype=np.uint8).reshape(4, RG_QUERY_HEAD_SLOTS)
+    e = sc[:, :heads].T.astype(np.int64) - 127                              # [heads, 4]
+    return (e2m1_decode(codes).reshape(heads, 4, 32) * np.ldexp(1.0, e)[..., None]).reshape(heads, DIM)
+
+
+def relu_weighted(Q: np.ndarray, w_row, keys: np.ndarray) -> np.ndarray:
+    """score[t] = sum_h w_h * ReLU(q_h . k_t) in float64 for decoded queries Q
+    [heads, 128] and keys [n, 128] (page *cutedsl.dsa.index*, module docstring;
+    *amd.ops.fp4_indexer*, ``score_paged``)."""
+    dots = keys @ Q.T                                   # [n, heads], exact
     return np.maximum(dots, 0.0) @ np.asarray(w_row, dtype=np.float64)
+
+
+def score_row(fmt: str, q_row, w_row, keys: np.ndarray) -> np.ndarray:
+    """score[t] = sum_h w_h * ReLU(q_h . k_t) in float64 for one 32-head query
+    row of ``quantize_query``."""
+    return relu_weighted(decode_query(fmt, q_row), w_row, keys)
 
 
 def score_paged(fmt: str, q_rows, w, cache, page_stride: int, block_table,
@@ -396,6 +405,41 @@ def score_paged(fmt: str, q_rows, w, cache, page_stride: int, block_table,
         for r in rs:
             e = int(row_ends[r])
             out[r, :e] = score_row(fmt, q_rows[r], w[r], keys[:e])
+    return out
+
+
+def score_paged_heads(fmt: str, payload, scales, w, cache, page_stride: int, block_table,
+                      starts, row_ends, rows_subset=None):
+    """Logits of MXFP4 queries with 16, 32 or 64 heads against an MXFP4 cache in
+    either placement (page *amd.ops.fp4_indexer*, ``score_paged``: queries
+    quantised by ``quantize_queries``, weights [rows, heads] carrying the head
+    factors but no group scales).  payload uint8 [rows, heads, 64]; scales
+    uint8 [rows, 1, 4, 16, 4] (or [rows, 256]); w [rows, heads].  Rows,
+    bounds and -inf fill as ``score_paged``."""
+    if not _fp4(fmt):
+        raise ValueError("queries of quantize_queries score against MXFP4 caches")
+    payload = np.asarray(payload, dtype=np.uint8)
+    if payload.ndim != 3 or payload.shape[1] not in RG_QUERY_HEADS or payload.shape[2] != DIM // 2:
+        raise ValueError("payload must be [rows, heads, 64] with heads 16, 32 or 64")
+    scales = np.asarray(scales, dtype=np.uint8).reshape(payload.shape[0], 4 * RG_QUERY_HEAD_SLOTS)
+    w = np.asarray(w, dtype=np.float64)
+    block_table = np.asarray(block_table)
+    starts = np.asarray(starts, dtype=np.int64)
+    row_ends = np.asarray(row_ends, dtype=np.int64)
+    rows = row_ends.shape[0]
+    width = block_table.shape[1] * PAGE
+    out = np.full((rows, width), -np.inf, dtype=np.float64)
+    wanted = None if rows_subset is None else set(int(r) for r in rows_subset)
+    for q in range(starts.shape[0] - 1):
+        rs = [r for r in range(int(starts[q]), int(starts[q + 1]))
+              if r < rows and (wanted is None or r in wanted) and row_ends[r] > 0]
+        if not rs:
+            continue
+        n = int(max(row_ends[r] for r in rs))
+        keys = decode_keys(fmt, cache, page_stride, block_table[q], n)
+        for r in rs:
+            e = int(row_ends[r])
+            out[r, :e] = relu_weighted(decode_queries(payload[r], scales[r]), w[r], keys[:e])
     return out
 
 

@@ -83,6 +83,45 @@ def oracle_run(wl: Workload, rows=None, page_stride=None):
                 remap=remap, cache=cache)
 
 
+def _oracle_chunk(job):
+    """Worker of ``oracle_rows``: the oracle's scores and top-k of some rows."""
+    from synth import make_workload
+    name, overrides, rows, page_stride = job
+    o = oracle_run(make_workload(name, **overrides), rows=rows, page_stride=page_stride)
+    rows = list(rows)
+    return rows, o["scores"][rows], o["topk"][rows], o["row_ends"], o["starts"], o["q_rows"]
+
+
+def oracle_rows(name, overrides, rows, page_stride=None, workers=None):
+    """``oracle_run`` of a named workload over ``rows``, the requests split
+    over spawned worker processes (each rebuilds the workload from its seed).
+    Returns (scores {row: float64 [width]}, topk {row: int32 [k]}, row_ends,
+    starts, q_rows)."""
+    import multiprocessing as mp
+    import os
+    from synth import make_workload
+    wl = make_workload(name, **overrides)
+    by_req = {}
+    for r in rows:
+        by_req.setdefault(int(wl.row_request[r]), []).append(int(r))
+    groups = list(by_req.values())
+    workers = workers or max(1, min(len(groups), (os.cpu_count() or 2) - 1, 16))
+    chunks = [[] for _ in range(workers)]
+    for i, g in enumerate(sorted(groups, key=lambda g: -int(wl.seq_lens[wl.row_request[g[0]]]) if
+                                 wl.row_request[g[0]] >= 0 else 0)):
+        chunks[i % workers] += g
+    jobs = [(name, overrides, sorted(c), page_stride) for c in chunks if c]
+    ctx = mp.get_context("spawn")
+    scores, top = {}, {}
+    row_ends = starts = q_rows = None
+    with ctx.Pool(len(jobs)) as pool:
+        for rs, sc, tk, re_, st, qr in pool.imap_unordered(_oracle_chunk, jobs):
+            for i, r in enumerate(rs):
+                scores[r], top[r] = sc[i], tk[i]
+            row_ends, starts, q_rows = re_, st, qr
+    return scores, top, row_ends, starts, q_rows
+
+
 def check_logits(got: np.ndarray, want: np.ndarray, row_ends, rows):
     """|got - want| <= max(1e-3 |want|, 1e-4) on every valid position; -inf past the bound."""
     for r in rows:

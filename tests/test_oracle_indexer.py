@@ -132,6 +132,21 @@ def test_insert_padding_and_out_of_range_slots():
     assert bad == 2 and not cache.any()
 
 
+@pytest.mark.parametrize("fmt", ["fp8", "fp8_mx", "mxfp4", "mxfp4_rg"])
+def test_insert_repeated_slot_keeps_the_last_key(fmt):
+    """Keys are written in order: a slot named twice holds the later key's
+    bytes, as if that key alone had been inserted there."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((5, 128)).astype(np.float32)
+    g, b = np.ones(128, np.float32), np.zeros(128, np.float32)
+    stride = O.page_bytes(fmt)
+    both = np.zeros(2 * stride, np.uint8)
+    O.insert_key(fmt, both, stride, 2, x, g, b, 1e-6, np.array([70, 3, 70, 9, 3], np.int64))
+    alone = np.zeros(2 * stride, np.uint8)
+    O.insert_key(fmt, alone, stride, 2, x[2:], g, b, 1e-6, np.array([70, 9, 3], np.int64))
+    assert np.array_equal(both, alone)
+
+
 def test_key_scale_power_of_two_equivariance():
     rng = np.random.default_rng(5)
     normed = _bf16_values(rng, (64, 128))
