@@ -626,26 +626,26 @@ extern "C" const char* dsa_version(void) { return "dsa-gb300 0.1.0"; }
 namespace dsa {
 
 constexpr size_t noalloc_align(size_t x) { return (x + 255) & ~size_t(255); }
+// Two 2048-bin histograms per row (level 1 and level 2: 8 KB each), 16 bytes
+// of counters per row and 8192 candidates of 8 bytes per split row (64 KB):
+// with 64 rows 512 KB + 512 KB + 1 KB + 4 MB.
 constexpr size_t kNoAllocBytes = 2 * noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kHistBins * sizeof(unsigned)) +
                                  noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * 4 * sizeof(int)) +
                                  noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kCandCap * sizeof(uint2));
+static_assert(kNoAllocBytes == DSA_TOPK_NOALLOC_SCRATCH_BYTES, "the header states the array's size");
 
 static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocBytes];
 
-// Device address of g_topk_scratch on the current device, looked up once per
-// device (in host code the array's name is only a stand-in, not an address).
+// Device address of g_topk_scratch on the current device.  In host code the
+// array's name is only a stand-in, not an address.  The lookup is made on
+// every call: it is a host-side query that allocates nothing, and a cached
+// address would go stale if the device's context were reset (the module is
+// then loaded again, possibly elsewhere).  The first lookup on a device loads
+// the library's device code there.
 static int noalloc_scratch(uint8_t** ptr) {
-    static std::mutex mu;
-    static uint8_t* addr[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || !p) return DSA_ERR_CUDA;
-        addr[dev] = static_cast<uint8_t*>(p);
-    }
-    *ptr = addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || !p) return DSA_ERR_CUDA;
+    *ptr = static_cast<uint8_t*>(p);
     return DSA_OK;
 }
 
