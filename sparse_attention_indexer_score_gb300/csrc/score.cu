@@ -733,18 +733,30 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
 }
 
 // Scores of one query row for the 32 keys of this warp (one per lane) from
-// the 32 head columns v of its accumulator.
+// the 32 head columns v of its accumulator: sum_h w_h * max(acc_h, 0), four
+// partial sums by head mod 4, combined as ((s0 + s1) + (s2 + s3)).  The ReLU
+// is an integer max on the FP32 bits (negative values, -0 included, have the
+// sign bit set and are negative as signed integers); the multiply-adds run two
+// at a time (fma.rn.f32x2, each lane rounded as fmaf).
 __device__ __forceinline__ float head_sum(const uint32_t* v, const float* wr, float ksm) {
-    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    unsigned long long s01 = 0ull, s23 = 0ull;   // (s0, s1), (s2, s3) as f32x2, +0.0
 #pragma unroll
     for (int h4 = 0; h4 < 8; ++h4) {
         const float4 w4 = reinterpret_cast<const float4*>(wr)[h4];
-        s[0] = fmaf(w4.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.0f), s[0]);
-        s[1] = fmaf(w4.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f), s[1]);
-        s[2] = fmaf(w4.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f), s[2]);
-        s[3] = fmaf(w4.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.0f), s[3]);
+        const int r0 = max(static_cast<int>(v[4 * h4 + 0]), 0), r1 = max(static_cast<int>(v[4 * h4 + 1]), 0);
+        const int r2 = max(static_cast<int>(v[4 * h4 + 2]), 0), r3 = max(static_cast<int>(v[4 * h4 + 3]), 0);
+        asm("{\n\t.reg .b64 a, b;\n\tmov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+            "fma.rn.f32x2 %0, a, b, %0;\n\t}"
+            : "+l"(s01)
+            : "f"(w4.x), "f"(w4.y), "r"(r0), "r"(r1));
+        asm("{\n\t.reg .b64 a, b;\n\tmov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+            "fma.rn.f32x2 %0, a, b, %0;\n\t}"
+            : "+l"(s23)
+            : "f"(w4.z), "f"(w4.w), "r"(r2), "r"(r3));
     }
-    return ((s[0] + s[1]) + (s[2] + s[3])) * ksm;
+    const float s0 = __uint_as_float(static_cast<uint32_t>(s01)), s1 = __uint_as_float(static_cast<uint32_t>(s01 >> 32));
+    const float s2 = __uint_as_float(static_cast<uint32_t>(s23)), s3 = __uint_as_float(static_cast<uint32_t>(s23 >> 32));
+    return ((s0 + s1) + (s2 + s3)) * ksm;
 }
 
 // Logit store and histogram count of one row's 32 scores (one per lane);
