@@ -2,20 +2,24 @@
 
 One step = the whole hot path over one batch of seeded synthetic inputs:
 prepare_step (quantize_query + insert_key + decode_layout in one launch) ->
-score_paged (+ fused top-k).  The default workload is ``fp8_decode`` (64 requests x 1 row, 4096..8192 keys,
-FP8 keys with FP32 scales at 132 B/token, top-2048).
+score_paged (+ fused top-k).  The headline workload is ``spec_verify`` (128
+requests x 1..4 verify rows, 4096..65536 keys, FP8 keys with UE8M0 scales,
+top-2048), the largest one that the step runs on one GPU; ``fp8_decode``,
+``mxfp4_decode`` and ``long_mxfp4`` follow, each with an object of the same
+keys under ``configs``.
 
 Prints one JSON line.  ``value`` is scored keys per second (sum of the row
-bounds over the timed steps / device time) with inputs resident in HBM.  The
-K timed steps run as one captured CUDA graph; the key cache is replicated
-until the replicas exceed three times the L2 size and the steps use them in
-turn, so every step reads its keys from HBM.  ``e2e`` is the same metric
-through the public API with every step copying its inputs in from pinned host
-memory and its top-k back (``StepPipeline``; ``e2e_graphed`` and
-``e2e_eager`` run the step one at a time).  ``--fmt`` runs a workload in
-another cache format (e.g. ``mxfp4_rg``); ``--op`` times QueryNorm or the
-DCP top-k merge instead of the step.  ``--impl reference`` times the CPU
-oracle instead.
+bounds of a step / device time of a step) with inputs resident in HBM.  The K
+timed steps run as one captured CUDA graph, replayed until at least 100 ms
+have been timed, each replay between CUDA events; the median replay gives the
+step time.  The key cache is replicated until the replicas exceed three times
+the L2 size and the steps use them in turn, so every step reads its keys from
+HBM.  ``e2e`` is the same metric through the public API with every step
+copying its inputs in from pinned host memory and its top-k back
+(``StepPipeline``; ``e2e_graphed`` and ``e2e_eager`` run the step one at a
+time).  ``--fmt`` runs workloads in another cache format (e.g. ``mxfp4_rg``);
+``--op`` times QueryNorm or the DCP top-k merge instead of the step.
+``--impl reference`` times the CPU oracle on the headline workload instead.
 
 Multi-GPU (``torchrun``): every rank runs its own replica of the workload
 (the step has no exchange); the timing is the max over ranks and ``value``
@@ -147,7 +151,7 @@ def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         d = json.load(open(path))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops_sustained"]),
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1700.0, "source": "fallback"}
 
@@ -161,14 +165,49 @@ FLOPS_PER_SCORED_KEY = 2 * 32 * 128   # one row's 32 head dot products of 128 co
 
 def tensor_side(scored_keys: int, kernel_ms: float, fmt: str, peaks: dict) -> dict:
     """The score kernel against the tensor-core roof: algorithmic FLOPs per
-    launch over its event time, against the measured sustained bf16 rate times
-    the nominal ratio of the MMA's operand type."""
+    launch over its event time, against the rate of the kernel's MMA kind
+    measured on this GPU by the library's probe (``mma_tflops``), else the
+    measured burst bf16 rate (the kernel is timed alone) times the nominal
+    ratio of the MMA's operand type."""
     flops = FLOPS_PER_SCORED_KEY * scored_keys
     achieved = flops / (kernel_ms / 1e3) / 1e12
-    peak = peaks["bf16_tflops"] * TENSOR_RATIO[fmt]
+    kind = "mxf4" if fmt in FP4_FORMATS else "fp8"
+    probe = peaks.get("mma_tflops", {}).get(kind)
+    if probe:
+        peak, source = probe, (f"measured on this GPU: dense tcgen05 {kind} MMA rate "
+                               "(128 x 128 tiles, operands in shared memory)")
+    else:
+        peak = peaks["bf16_tflops"] * TENSOR_RATIO[fmt]
+        source = f"{peaks['source']} burst bf16 x {TENSOR_RATIO[fmt]:g} (nominal {fmt} / bf16)"
     return {"flops_per_launch": flops, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak,
-            "peak_source": f"{peaks['source']} sustained bf16 x {TENSOR_RATIO[fmt]:g} (nominal {fmt} / bf16)"}
+            "frac": achieved / peak, "peak_source": source}
+
+
+def measure_mma_tflops(iters: int = 1 << 16, reps: int = 5) -> dict:
+    """Dense tensor-core rates of the scorer's MMA kinds on this GPU, from the
+    library's probe (one CTA per SM issuing back-to-back 128 x 128 x K MMAs),
+    timed with CUDA events on the stream: the best of ``reps`` launches."""
+    import torch
+    from sparse_attention_indexer_score_gb300 import dsa
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {}
+    for kind in ("fp8", "mxf4"):
+        dsa.probe_mma(kind, iters, status)
+        best = None
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dsa.probe_mma(kind, iters, status)
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        if int(status.item()) != 0:
+            raise RuntimeError("the MMA probe's final wait gave up")
+        out[kind] = 2 * 128 * 128 * dsa.MMA_K[kind] * iters * sms / (best / 1e3) / 1e12
+    return out
 
 
 def score_source_hash() -> str:
@@ -265,6 +304,7 @@ def oracle_one_core(wl, budget_s: float):
 
 def run_reference(args, wl):
     """The oracle on the host cores: each step a bounded sample of the workload."""
+    from oracle import indexer as O
     cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
     per_step = max(0.5, min(8.0, 60.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -277,11 +317,13 @@ def run_reference(args, wl):
         keys += k
         secs += s
     value = keys / secs if secs > 0 else 0.0
+    _, row_ends = O.decode_layout(wl.seq_lens, wl.query_lens, wl.num_rows)
+    ab = algorithmic_bytes(wl, row_ends)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(wl), "sample": desc},
+        "config": workload_config(wl, ab, args.gpus),
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"per step about {per_step:.1f} s of oracle work: {desc}"},
@@ -308,19 +350,20 @@ def whole_job_rate(units_per_step_per_rank: float, steps: int, world: int, total
 
 
 # ----------------------------------------------------------------- GPU
-def run_ours(args, wl, rank, world, local_rank):
+TIMED_MS_MIN = 100.0   # every workload's timed region lasts at least this long
+
+
+def measure_workload(args, wl, world, local_rank, e2e_modes=("pipelined", "graphed", "eager")):
+    """Times one workload on this rank's GPU.  Returns the rank-local raw
+    numbers (times in ms) and the workload's config object."""
     import torch
-    import torch.distributed as dist
 
     sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from sparse_attention_indexer_score_gb300 import build as _b
-    _b.build()
     from sparse_attention_indexer_score_gb300 import dsa
     from sparse_attention_indexer_score_gb300.step import DecodeIndexer, GraphedStep, StepPipeline
     from dsa_case import bf16_tensor
 
     dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
     ix = DecodeIndexer(wl.fmt, wl.num_pages, torch.from_numpy(wl.block_table), torch.from_numpy(wl.gamma),
                        torch.from_numpy(wl.beta), wl.eps, wl.num_rows, wl.topk, dev)
     kb, sl = wl.prefill_all()
@@ -355,14 +398,10 @@ def run_ours(args, wl, rank, world, local_rank):
     row_ends = out.row_ends.cpu().numpy()
     ab = algorithmic_bytes(wl, row_ends)
 
-    # One CUDA graph per replica for the timed steps; a second set with the
-    # library's events around the scoring kernel for the roofline timing.
-    graphs, kgraphs, kev = [], [], []
+    # One CUDA graph per replica with the library's events around the scoring
+    # kernel (the roofline timing of that kernel alone).
+    kgraphs, kev = [], []
     for r in range(n_rep):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            step(d, r)
-        graphs.append(g)
         a, b = dsa.TimingEvent(), dsa.TimingEvent()
         kg = torch.cuda.CUDAGraph()
         dsa.set_score_timing(a, b)
@@ -371,45 +410,59 @@ def run_ours(args, wl, rank, world, local_rank):
         dsa.set_score_timing(None, None)
         kgraphs.append(kg)
         kev.append((a, b))
-    for i in range(args.warmup * n_rep):
-        graphs[i % n_rep].replay()
     # The timed steps: one CUDA graph holding all K steps (step i reads replica
     # i mod n), so the GPU runs them back to back as a serving loop issues
-    # them, with the PDL edges between steps kept.  One untimed replay uploads
-    # it first.
+    # them, with the PDL edges between steps kept.
     timed = torch.cuda.CUDAGraph()
     with torch.cuda.graph(timed):
         for i in range(args.steps):
             step(d, i % n_rep)
-    timed.replay()
+    for _ in range(args.warmup):    # W untimed warm-up replays (W x K steps)
+        timed.replay()
     torch.cuda.synchronize()
+    t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_a.record()
+    timed.replay()
+    t_b.record()
+    torch.cuda.synchronize()
+    est = max(t_a.elapsed_time(t_b), 1e-3)
+    replays = max(1, min(10000, int(-(-TIMED_MS_MIN // est))))
     if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([replays], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        replays = int(t.item())
         dist.barrier()
 
-    # headline: K steps, device time of the whole replay
-    t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # headline: `replays` replays of exactly K steps each, each bracketed by
+    # CUDA events on the stream; the median replay is the K-step time
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
     with ClockSampler(local_rank) as clocks:
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         clocks.mark_start()
-        t_a.record()
-        timed.replay()
-        t_b.record()
+        for a, b in evs:
+            a.record()
+            timed.replay()
+            b.record()
         torch.cuda.synchronize()
         clocks.mark_end()
         if world > 1:
             dist.barrier()
     clk = clocks.summary()
-    step_ms = t_a.elapsed_time(t_b)
+    rep_ms = sorted(a.elapsed_time(b) for a, b in evs)
+    step_ms = statistics.median(rep_ms)
 
-    # the scoring kernel alone
+    # the scoring kernel alone, one step per replay, about as long
+    n_k = max(args.steps, int(TIMED_MS_MIN // max(est / args.steps, 1e-3)))
+    n_k = min(n_k, 20000)
     kernel_ms = 0.0
-    for i in range(args.steps):
+    for i in range(n_k):
         kgraphs[i % n_rep].replay()
         a, b = kev[i % n_rep]
         kernel_ms += a.elapsed_ms(b)
-    kernel_ms /= args.steps
+    kernel_ms /= n_k
 
     # End to end through the public API from pinned host buffers, every step
     # copying its inputs in and its top-k back: the serving loop's pipeline
@@ -420,7 +473,7 @@ def run_ours(args, wl, rank, world, local_rank):
     h_top = torch.empty((wl.num_rows, wl.topk), dtype=torch.int32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = h_top.numel() * 4
-    e2e_steps = min(args.steps, 200)
+    e2e_steps = max(args.steps, min(2000, int(TIMED_MS_MIN // max(est / args.steps, 1e-3))))
 
     def timed_e2e(run_step):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
@@ -430,82 +483,153 @@ def run_ours(args, wl, rank, world, local_rank):
             run_step(i)
             b.record()
         torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in ev) * args.steps / e2e_steps
+        return sum(a.elapsed_time(b) for a, b in ev) / e2e_steps
 
     like = dict(q=host["q"], wv=host["wv"], keys=host["keys"], slots=host["slots"], seq_lens=host["seq"],
                 query_lens=host["qlen"])
-    gsteps = []
-    for r in range(n_rep):
-        ix.cache = caches[r]
-        gsteps.append(GraphedStep(ix, like, max_q))      # staging buffers filled from `like`
-    h2d_graph, d2h_graph = gsteps[0].staging_bytes, gsteps[0].host_topk.numel() * 4
-    e2e_graphed_ms = timed_e2e(lambda i: gsteps[i % n_rep].replay())
+    res = {"step_ms": step_ms / args.steps, "kernel_ms": kernel_ms, "replays": replays,
+           "replay_ms": [rep_ms[0], rep_ms[-1]], "clocks": clk}
+    gs0 = GraphedStep(ix, like, max_q)
+    h2d_graph, d2h_graph = gs0.staging_bytes, gs0.host_topk.numel() * 4
+    del gs0
+    if "graphed" in e2e_modes:
+        gsteps = []
+        for r in range(n_rep):
+            ix.cache = caches[r]
+            gsteps.append(GraphedStep(ix, like, max_q))      # staging buffers filled from `like`
+        res["e2e_graphed_ms"] = timed_e2e(lambda i: gsteps[i % n_rep].replay())
+        del gsteps
     pipe = StepPipeline(ix, like, max_q, caches=caches)
-    pipe.run(2 * n_rep)                                   # warm-up
+    pipe.run(2 * n_rep)                                       # warm-up
     torch.cuda.synchronize()
     p_start, p_end = pipe.run(e2e_steps)
     torch.cuda.synchronize()
-    e2e_ms = p_start.elapsed_time(p_end) * args.steps / e2e_steps
+    res["e2e_ms"] = p_start.elapsed_time(p_end) / e2e_steps
+    del pipe
+    if "eager" in e2e_modes:
+        def eager_step(i):
+            for k in d:
+                d[k].copy_(pinned[k], non_blocking=True)
+            step(d, i % n_rep)
+            h_top.copy_(topk_out, non_blocking=True)
+        res["e2e_eager_ms"] = timed_e2e(eager_step)
+    res.update(ab=ab, n_rep=n_rep, cache_bytes=cache_bytes, l2=l2, h2d=h2d, d2h=d2h, h2d_graph=h2d_graph,
+               d2h_graph=d2h_graph, e2e_steps=e2e_steps, kernel_launches=n_k)
+    del kgraphs, timed, caches, ix
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
-    def eager_step(i):
-        for k in d:
-            d[k].copy_(pinned[k], non_blocking=True)
-        step(d, i % n_rep)
-        h_top.copy_(topk_out, non_blocking=True)
-    e2e_eager_ms = timed_e2e(eager_step)
 
-    step_ms, e2e_ms, e2e_graphed_ms, e2e_eager_ms, kernel_ms = max_over_ranks(
-        [step_ms, e2e_ms, e2e_graphed_ms, e2e_eager_ms, kernel_ms], dev)
-    if rank != 0:
-        return
-    value = whole_job_rate(ab["scored"], args.steps, world, step_ms)
-    peaks = measured_peaks()
+def workload_config(wl, ab, gpus) -> dict:
+    """The config object of a workload (the same in both arms)."""
+    return {"workload": workload_desc(wl), "rows": wl.num_rows, "requests": wl.R,
+            "scored_keys_per_step": ab["scored"], "unique_keys_per_step": ab["keys_unique"],
+            "cache_bytes_per_step": ab["cache"], "parallelism": f"replicas x{gpus}"}
+
+
+def cpu_leg(wl, seconds: float, one_core_seconds: float) -> dict:
+    keys, secs, desc = oracle_sample(wl, seconds)
+    out = {"value": keys / secs if secs else None, "unit": UNIT,
+           "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", 1)), "kind": "oracle",
+           "sample": f"{desc}; {secs:.1f} s"}
+    one = oracle_one_core(wl, one_core_seconds)
+    if one is not None:
+        k1, s1, d1 = one
+        out["one_core"] = {"value": k1 / s1 if s1 else None, "unit": UNIT, "cores": 1,
+                           "sample": f"{d1}; {s1:.1f} s"}
+    return out
+
+
+def workload_record(args, wl, res, world, peaks) -> dict:
+    """The JSON object of one measured workload (all ranks' max already taken)."""
+    ab = res["ab"]
+    step_ms = res["step_ms"]
+    kernel_ms = res["kernel_ms"]
+    value = whole_job_rate(ab["scored"], 1, world, step_ms)
     achieved = ab["score_kernel"] / (kernel_ms / 1e3) / 1e9
     traffic = ncu_traffic(traffic_key(wl), ab["score_kernel"])
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp4_e2m1" if wl.fmt in FP4_FORMATS else "fp8_e4m3",
-        "data": "synthetic",
-        "config": {"workload": workload_desc(wl), "rows": wl.num_rows, "requests": wl.R,
-                   "scored_keys_per_step": ab["scored"], "unique_keys_per_step": ab["keys_unique"],
-                   "cache_bytes_per_step": ab["cache"],
-                   "l2": (f"inputs larger than L2: {n_rep} replicas of the key cache "
-                          f"({n_rep * cache_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB) used in turn, no flush"),
-                   "launch": "the K timed steps captured as one CUDA graph (PDL edges kept), replayed once",
-                   "parallelism": f"replicas x{world}"},
-        "cache_gbs": ab["cache"] * args.steps * world / (step_ms / 1e3) / 1e9,
+    rec = {
+        "value": value, "unit": UNIT, "ms_per_step": step_ms,
+        "dtype": "fp4_e2m1" if wl.fmt in FP4_FORMATS else "fp8_e4m3",
+        "config": workload_config(wl, ab, args.gpus),
+        "cache_gbs": ab["cache"] * world / (step_ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": "score_kernel", "kernel_us": kernel_ms * 1e3,
-                     "peak_source": f"{peaks['source']} HBM copy bandwidth",
-                     "step_frac": (ab["step"] / (step_ms / args.steps / 1e3) / 1e9) / peaks["hbm_gbs"],
+                     "bytes_per_launch": ab["score_kernel"],
+                     "peak_source": f"{peaks['source']} HBM copy bandwidth (of measured)",
+                     "step_frac": (ab["step"] / (step_ms / 1e3) / 1e9) / peaks["hbm_gbs"],
+                     "step_bytes": ab["step"],
                      "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "tensor": tensor_side(ab["scored"], kernel_ms, wl.fmt, peaks)},
-        "e2e": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": h2d_graph, "d2h_bytes_per_step": d2h_graph,
+        "e2e": {"value": whole_job_rate(ab["scored"], 1, world, res["e2e_ms"]), "unit": UNIT,
+                "h2d_bytes_per_step": res["h2d_graph"], "d2h_bytes_per_step": res["d2h_graph"],
                 "how": ("StepPipeline: each step copies its inputs in from a pinned staging buffer and its "
                         "top-k back, overlapped with the neighbouring steps' compute on two copy streams; "
-                        "device time from the first copy in to the last copy out")},
-        "e2e_graphed": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_graphed_ms), "unit": UNIT,
-                        "h2d_bytes_per_step": h2d_graph, "d2h_bytes_per_step": d2h_graph,
-                        "how": "GraphedStep replayed one step at a time: copy in, step, copy back, serialised"},
-        "e2e_eager": {"value": whole_job_rate(ab["scored"], args.steps, world, e2e_eager_ms), "unit": UNIT,
-                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                      "how": "eager public-API calls per step, the same host copies in the timed region"},
-        "gpu_launches": STEP_KERNELS * args.steps,
-        "clocks": clk,
+                        f"device time from the first copy in to the last copy out over {res['e2e_steps']} steps")},
+        "timing": {"l2": (f"inputs larger than L2: {res['n_rep']} replicas of the key cache "
+                          f"({res['n_rep'] * res['cache_bytes'] / 1e6:.0f} MB, L2 {res['l2'] / 1e6:.0f} MB) "
+                          "used in turn, no flush"),
+                   "launch": (f"the K = {args.steps} timed steps captured as one CUDA graph (PDL edges kept); "
+                              f"{res['replays']} replays of it, each between CUDA events, median replay reported"),
+                   "replay_ms_min_max": res["replay_ms"], "replays": res["replays"],
+                   "kernel_launches_timed": res["kernel_launches"]},
+        "clocks": res["clocks"],
     }
-    if not args.no_cpu_baseline:
-        keys, secs, desc = oracle_sample(wl, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": keys / secs if secs else None, "unit": UNIT,
-                                "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", 1)), "kind": "oracle",
-                                "sample": f"{desc}; {secs:.1f} s"}
-        one = oracle_one_core(wl, min(args.cpu_seconds, 1.0))
-        if one is not None:
-            k1, s1, d1 = one
-            line["cpu_baseline"]["one_core"] = {"value": k1 / s1 if s1 else None, "unit": UNIT, "cores": 1,
-                                                "sample": f"{d1}; {s1:.1f} s"}
+    if "e2e_graphed_ms" in res:
+        rec["e2e_graphed"] = {"value": whole_job_rate(ab["scored"], 1, world, res["e2e_graphed_ms"]), "unit": UNIT,
+                              "h2d_bytes_per_step": res["h2d_graph"], "d2h_bytes_per_step": res["d2h_graph"],
+                              "how": "GraphedStep replayed one step at a time: copy in, step, copy back, serialised"}
+    if "e2e_eager_ms" in res:
+        rec["e2e_eager"] = {"value": whole_job_rate(ab["scored"], 1, world, res["e2e_eager_ms"]), "unit": UNIT,
+                            "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                            "how": "eager public-API calls per step, the same host copies in the timed region"}
+    return rec
+
+
+def run_ours(args, names, rank, world, local_rank):
+    import torch
+
+    from sparse_attention_indexer_score_gb300 import build as _b
+    _b.build()
+    from synth import make_workload
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks = measured_peaks()
+    peaks["mma_tflops"] = measure_mma_tflops()
+    records = {}
+    for i, name in enumerate(names):
+        wl = make_workload(name, **({"fmt": args.fmt} if args.fmt else {}))
+        modes = ("pipelined", "graphed", "eager") if i == 0 else ("pipelined",)
+        res = measure_workload(args, wl, world, local_rank, modes)
+        keys = ["step_ms", "kernel_ms", "e2e_ms", "e2e_graphed_ms", "e2e_eager_ms"]
+        vals = max_over_ranks([res.get(k, 0.0) for k in keys], dev)
+        for k, v in zip(keys, vals):
+            if k in res:
+                res[k] = v
+        if rank == 0:
+            rec = workload_record(args, wl, res, world, peaks)
+            if not args.no_cpu_baseline:
+                rec["cpu_baseline"] = cpu_leg(wl, args.cpu_seconds if i == 0 else args.cpu_seconds / 2,
+                                              1.0 if i == 0 else 0.5)
+            records[name if not args.fmt else f"{name}/{args.fmt}"] = (rec, res)
+    if rank != 0:
+        return
+    head_name = next(iter(records))
+    head, hres = records[head_name]
+    line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+            "config": head["config"]}
+    for k in ("cache_gbs", "roofline", "e2e", "e2e_graphed", "e2e_eager", "timing", "clocks", "cpu_baseline"):
+        if k in head:
+            line[k] = head[k]
+    line["gpu_launches"] = STEP_KERNELS * args.steps * hres["replays"]
+    line["mma_peaks_tflops"] = {k: round(v, 1) for k, v in peaks["mma_tflops"].items()}
+    if len(records) > 1:
+        line["configs"] = {n: r for n, (r, _) in list(records.items())[1:]}
     print(json.dumps(line))
 
 
@@ -589,19 +713,25 @@ def run_topk_merge(args):
         "gpu_launches": 3 * args.steps}))
 
 
+DEFAULT_CONFIGS = "spec_verify,fp8_decode,mxfp4_decode,long_mxfp4"
+
+
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", default="fp8_decode")
-    p.add_argument("--fmt", default=None, help="override the workload's cache format (e.g. mxfp4_rg)")
-    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--configs", default=DEFAULT_CONFIGS,
+                   help="comma-separated workloads; the first is the headline, the others get objects "
+                        "of their own under 'configs'")
+    p.add_argument("--config", default=None, help="one workload alone (same as --configs NAME)")
+    p.add_argument("--fmt", default=None, help="override the workloads' cache format (e.g. mxfp4_rg)")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--op", choices=["step", "query_norm", "topk_merge"], default="step",
+    p.add_argument("--op", choices=["step", "query_norm", "topk_merge", "mma_peak"], default="step",
                    help="step: the decode step (the headline); query_norm: the q_a RMSNorm alone; "
-                        "topk_merge: the DCP top-k merge alone")
+                        "topk_merge: the DCP top-k merge alone; mma_peak: the tensor-core rate probe")
     p.add_argument("--norm-rows", type=int, default=16384)
     args = p.parse_args()
     if args.warmup < 3:
@@ -612,14 +742,22 @@ def main():
     if args.op == "topk_merge":
         run_topk_merge(args)
         return
+    if args.op == "mma_peak":
+        from sparse_attention_indexer_score_gb300 import build as _b
+        _b.build()
+        r = measure_mma_tflops()
+        print(json.dumps({"metric": "dense tcgen05 MMA rate (128 x 128 tiles, operands in shared memory)",
+                          "value": r["fp8"], "unit": "TFLOP/s", "n_gpus": 1, "dtype": "fp8_e4m3",
+                          "data": "synthetic", "mxf4_tflops": r["mxf4"], "higher_is_better": True}))
+        return
+    names = [args.config] if args.config else [n for n in args.configs.split(",") if n]
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
-    from synth import make_workload
-    wl = make_workload(args.config, **({"fmt": args.fmt} if args.fmt else {}))
     if args.impl == "reference":
         if rank == 0:
-            run_reference(args, wl)
+            from synth import make_workload
+            run_reference(args, make_workload(names[0], **({"fmt": args.fmt} if args.fmt else {})))
         return
     if world > 1:
         import torch
@@ -627,7 +765,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        run_ours(args, wl, rank, world, local_rank)
+        run_ours(args, names, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -312,6 +312,38 @@ int dsa_score_paged(int fmt, const void* q_rows, const void* w,
                     int32_t* status, void* stream);
 
 /*
+ * dsa_score_paged_heads - dsa_score_paged for MXFP4 queries of 16, 32 or 64
+ * heads in the quantize_queries form.
+ *
+ * Page "amd.ops.fp4_indexer": score_paged quantises [rows, heads, 128] queries
+ * with quantize_queries (heads 16, 32 or 64) and scores them against the
+ * MXFP4 cache; its weights carry the head factors but no group scales.
+ *
+ *   fmt           DSA_FMT_MXFP4 or DSA_FMT_MXFP4_RG (the cache's placement);
+ *                 other formats return DSA_ERR_UNSUPPORTED.
+ *   heads         16, 32 or 64 (else DSA_ERR_UNSUPPORTED).
+ *   payload       uint8 [rows][heads][64] from dsa_quantize_queries_rg, 16-byte
+ *                 aligned: head h's E2M1 pairs.
+ *   q_scales      uint8 [rows][256] from dsa_quantize_queries_rg (block g of
+ *                 head h at g * 64 + h), 16-byte aligned.
+ *   w             BF16 [rows][heads] head weights.
+ *   every other argument as dsa_score_paged, whose workspace size it uses.
+ *
+ * score[r][t] = sum_h w[r][h] * ReLU(q_h . k_t) over the query's heads.  A
+ * request's rows are scored in groups of min(4, 128 / heads) rows per key
+ * read.
+ */
+int dsa_score_paged_heads(int fmt, int64_t heads, const void* payload, const void* q_scales, const void* w,
+                          const void* cache, int64_t page_stride, int64_t num_pages,
+                          const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                          const int32_t* starts, const int32_t* row_ends,
+                          int64_t num_requests, int64_t rows, int64_t max_query_len,
+                          float* logits, int64_t logits_ld,
+                          int64_t k, int32_t* topk,
+                          void* workspace, size_t workspace_bytes,
+                          int32_t* status, void* stream);
+
+/*
  * dsa_topk_workspace_size - bytes of scratch dsa_topk needs (zero-filled before
  * first use, left zero-filled by every completed call).
  */
@@ -408,6 +440,22 @@ void dsa_set_score_timing(void* before, void* after);
 int dsa_timing_event_create(void** event);
 int dsa_timing_event_destroy(void* event);
 int dsa_timing_elapsed_ms(void* start, void* end, float* ms);
+
+/*
+ * dsa_probe_mma - measurement helper: the dense tensor-core rate of the MMA
+ * kinds the scorer uses, on this GPU.  The pages have no counterpart; it
+ * exists so that the scorer's tensor-side roofline has a measured peak.
+ *
+ * Launches one CTA per SM; each issues `iters` tcgen05.mma instructions of
+ * M = 128, N = 128 back to back on operands held in shared memory, into one
+ * accumulator in tensor memory: kind 0 = kind::f8f6f4 E4M3 x E4M3 (K = 32),
+ * kind 1 = kind::mxf4 packed E2M1 with UE8M0 block scales (K = 64).  Time the
+ * launch on `stream` with CUDA events: FLOPs = 2 * 128 * 128 * K * iters * SMs.
+ *   status  optional int32 device word: DSA_STATUS_TIMEOUT if the final wait
+ *           for the MMAs gave up (then the timing is invalid).
+ * Returns DSA_ERR_INVALID for another kind or iters outside [1, 2^22].
+ */
+int dsa_probe_mma(int kind, int64_t iters, int32_t* status, void* stream);
 
 /* dsa_version - library version string. */
 const char* dsa_version(void);

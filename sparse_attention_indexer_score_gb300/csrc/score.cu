@@ -11,21 +11,22 @@
 //   D[128 keys][32 * rows] = K[128 x 128] . Q[32 * rows x 128]^T   (FP32 in TMEM)
 //
 // Warp roles of the persistent CTA (one per SM):
-//   warp 0     TMA producer: block-table gather of key pages (+ their scales)
-//              into a shared-memory ring (8 stages of 16 KB for FP8, 16 of
-//              8 KB for packed MXFP4); query rows per segment.
+//   warp 0     planner: resolves 32 tiles' segments and block-table pages at a
+//              time, loads each segment's query rows (TMA), tags each ring
+//              stage (8 stages of 16 KB for FP8, 16 of 8 KB for packed MXFP4)
+//              and hands the tile's page ids to its copy warp.
 //   warps 1-2  tcgen05 issuers of alternate tiles: scale factors into TMEM,
 //              the tile's MMAs (FP8: 4 with K = 32; MXFP4: 2 with K = 64) into
-//              one of three TMEM accumulators.  One issuer's per-tile chain of
-//              waits, tag and scale handling and MMA issue is longer than a
-//              tile's copy time.
+//              one of three TMEM accumulators.
 //   warps 3-10 epilogue, two groups of four: tcgen05.ld of the accumulator
 //              (thread = key), ReLU-weighted head sum, FP32 key scale, logits
 //              store, and a shared-memory histogram of the scores for the
 //              top-k pass.
-//   warp 11    second copy issuer: each tile's second page and both pages'
-//              scales (warp 0 copies the first page's codes), so two threads
-//              feed the copy engine.
+//   warps 11-14  copy warps: warp 11 + c issues every TMA copy (both pages'
+//              codes and scales) of the tiles at positions c, c + 4, ...  One
+//              copy-issuing thread moves about one page per few hundred
+//              nanoseconds whatever the page size, so four of them keep the
+//              HBM gather going.
 //
 // Formats: FP8 uses kind::f8f6f4 (E4M3 x E4M3) and multiplies the per-key
 // FP32 scale in the epilogue.  FP8-MX uses kind::mxf8f6f4 with one UE8M0 key
@@ -50,16 +51,18 @@ constexpr int kPageSmem = 64 * 128;           // one FP8 page's codes in shared 
 // Transaction bytes of one TMA copy: an MXFP4 page's codes 4096, an MXFP4
 // query row 2048 (packed, as in shared memory).
 constexpr uint32_t kFp8PageTx = 64 * 128, kFp4PageTx = 64 * 64;
-constexpr uint32_t kFp8QRowTx = kQRowBytes, kFp4QRowTx = kQRowBytes / 2;
+constexpr uint32_t kFp8QRowTx = kQRowBytes;
 // Row-group MXFP4 in shared memory: a tile's column group g at g * 2048 (the
 // two pages' 1024-byte boxes in key order); query chunk c (16 bytes = 32
 // columns of every head) at c * 2048, query row r's 32 heads at + r * 512.
 constexpr int kRgTileGroup = 2 * kRgGroupBytes;
 constexpr int kRgQChunk = 2048;
-constexpr int kSegRows = 4;                   // query rows per segment
+constexpr int kSegRows = 4;                   // most query rows per segment (min(4, 128 / heads))
 // Raw query scale bytes staged per row: 32 heads x 4 (token-major MXFP4) or
 // the row's 4 x 64 row-group slots.
 constexpr int kQsfRow = 128, kQsfRowRg = 4 * kRgQuerySlots;
+// A segment's queries: rows x heads x 128 B (FP8, 32 heads) or 64 B (MXFP4);
+// heads x segment rows <= 128 (the MMA's N), so one buffer holds 16 KB at most.
 constexpr int kQBufBytes = kSegRows * kQRowBytes;
 // Two epilogue groups of four warps (one per TMEM lane quarter) drain
 // alternate tiles, so two accumulators are read out at once.
@@ -70,21 +73,24 @@ constexpr int kEpiWarps = 4 * kEpiGroups;
 // group w drains.
 constexpr int kMmaWarps = 2;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
-constexpr int kPageWarp = kFirstEpiWarp + kEpiWarps;   // copies each tile's second page and both scale boxes
-constexpr int kScoreThreads = 32 * (kPageWarp + 1);
-// Page ids handed from warp 0 to the page warp: a ring of kPageRing entries
+// Copy warps: warp kFirstCopyWarp + c issues every copy (both pages' codes and
+// scales) of the tiles at sequence positions c, c + kCopyWarps, ...  A
+// thread that issues TMA copies moves about one page per few hundred
+// nanoseconds whatever the page size, so the copy rate an SM needs takes
+// several issuing threads.
+constexpr int kFirstCopyWarp = kFirstEpiWarp + kEpiWarps;
+constexpr int kCopyWarps = 4;
+constexpr int kScoreThreads = 32 * (kFirstCopyWarp + kCopyWarps);
+// Page ids handed from warp 0 to the copy warps: a ring of kPageRing entries
 // {first page, second page} (>= 0 page, kNoPage none, kEndMark end of sequence).
 constexpr int kPageRing = 64, kNoPage = -1, kEndMark = -2;
+static_assert(kStages % kCopyWarps == 0 && kMaxStages % kCopyWarps == 0, "copy warp c owns the stages of its residue");
 static_assert(kMmaWarps == kEpiGroups && kStages % kMmaWarps == 0 && kMaxStages % kMmaWarps == 0,
               "issuer w owns stages and group w");
 constexpr int kAcc = 3;                       // TMEM accumulators in flight (MMA latency is hidden behind 2)
 constexpr int kPlanSmemSegs = 4096;           // segments whose tile prefix the plan keeps on chip
-// Tile assignment: every CTA owns an equal contiguous range of the first
-// three quarters of the tiles (segment locality); the last quarter is a pool
-// claimed in chunks of kChunkTiles by whichever CTA runs out of work first,
-// which absorbs the speed differences between SMs.
-constexpr int kPoolDiv = 4;
-constexpr int kChunkTiles = 4;
+// Tile assignment: every CTA owns one contiguous range of tiles (segment
+// locality), the ranges splitting the tiles' estimated cost evenly.
 
 constexpr int OFF_TILES = 0;
 constexpr int OFF_QBUF = OFF_TILES + kStages * kTileBytes;
@@ -100,22 +106,23 @@ constexpr int OFF_W = OFF_KS + kAcc * 128 * 4;            // float[kEpiWarps][4 
 // global memory when the segment changes and at least every kHistFlushTiles
 // tiles (so that no count passes 2^16 - 1).
 constexpr int kHistFlushTiles = 256;
-constexpr int OFF_HIST = OFF_W + kEpiWarps * kSegRows * kHeads * 4;
+constexpr int OFF_HIST = OFF_W + kEpiWarps * 128 * 4;   // per warp: segment rows x heads <= 128 weights
 constexpr int kGroupHistWords = kSegRows * kHistBins / 2;
 // int4[kMaxStages]: {tile in segment, segment, segment ordinal in this CTA's sequence}
 constexpr int OFF_SINFO = OFF_HIST + kEpiGroups * kGroupHistWords * 4;
 constexpr int OFF_AINFO = OFF_SINFO + kMaxStages * 16;       // int2[kAcc]: {tile in segment, segment} per accumulator
-constexpr int OFF_PRING = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;   // int2[kPageRing]
-constexpr int OFF_BAR = OFF_PRING + kPageRing * 8;
+constexpr int OFF_PRING = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;   // int4[2 * kPageRing]
+constexpr int OFF_BAR = OFF_PRING + kPageRing * 32;
 // full, empty, qfull, tfull (per accumulator and epilogue group), done.  A
 // group's accumulator barrier is used by the sequence positions it, it + 6, ...
 // of that group alone: one barrier per accumulator, filled by both issuers,
 // could show a group a phase of the other group's fill (the two issuers'
 // MMAs complete in no common order) and its parity wait would take it.
 constexpr int kNumBars = 2 * kMaxStages + 2 + kAcc * kEpiGroups + 1;
-// TMEM address, abort flag, released[kAcc] at +16, page ring published / consumed at +32 / +36
+// TMEM address, abort flag, released[kAcc] at +16, page ring published at +32,
+// consumed[kCopyWarps] (entries each copy warp has taken) at +48
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
-constexpr int kScoreSmem = OFF_MISC + 48 + 1024;       // + slack to align the base to 1024
+constexpr int kScoreSmem = OFF_MISC + 48 + 4 * kCopyWarps + 1024;   // + slack to align the base to 1024
 static_assert(kScoreSmem <= 227 * 1024, "scoring CTA exceeds the shared memory of an SM");
 
 // TMEM columns: kAcc accumulators of up to 128 columns, then scale factors.
@@ -142,7 +149,6 @@ struct ScoreArgs {
     int64_t bt_stride;
     const uint8_t* q_rows;
     const __nv_bfloat16* w;
-    int* claim;          // chunk counter of the shared tail pool (zeroed by the plan)
     const int4* segs;
     const int* seg_prefix;
     const int* eff_end;
@@ -152,6 +158,11 @@ struct ScoreArgs {
     int hist_k;          // rows whose bound exceeds hist_k get a histogram; -1: none
     unsigned* hist;
     int32_t* status;
+    int heads;                 // query heads: 32, or (MXFP4 queries of quantize_queries) 16 or 64
+    const uint8_t* q_scales;   // MXFP4 query scales of row r at q_scales + r * qs_stride
+    int64_t qs_stride;
+    int qs_group_major;        // scale of block g of head h at g * 64 + h (else at h * 4 + g)
+    int64_t w_stride;          // BF16 head weights of row r at w + r * w_stride
 };
 
 // Segment s with prefix[s] <= t < prefix[s + 1] (prefix[S] > t).
@@ -168,6 +179,7 @@ __device__ __forceinline__ int find_segment(const int* prefix, int S, int t) {
 // One CTA: validates request starts and row bounds, splits requests into
 // segments of up to 4 rows and lays their 128-key tiles out in one index space.
 constexpr int kPlanThreads = 256;
+constexpr int kTileCostBase = 4;   // a tile's estimated cost: this + its segment's rows
 constexpr int kPlanSmemRows = 4096;   // row bounds the plan keeps on chip
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ starts,
@@ -175,7 +187,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             int max_keys, int* __restrict__ info,
                                                             int4* __restrict__ segs, int* __restrict__ seg_prefix,
                                                             int* __restrict__ eff_end, int4* __restrict__ cta, int G,
-                                                            int32_t* status) {
+                                                            int seg_rows, int32_t* status) {
     // The scoring CTAs (persistent, one per SM, most of its registers) are let
     // in only once the work before this kernel has finished, so that they do
     // not crowd out a still-running predecessor; their prologue then overlaps
@@ -208,13 +220,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
             s0 = min(max(a, 0), rows);
             s1 = min(max(b, s0), rows);
         }
-        const int nseg = (s1 - s0 + kSegRows - 1) / kSegRows;
+        const int nseg = (s1 - s0 + seg_rows - 1) / seg_rows;
         const int inc = block_inclusive_scan(nseg, warp_tmp, &chunk_total);
         const int sbase = carry + inc - nseg;
         for (int i = 0; i < nseg; ++i) {
             if (sbase + i > rows) { bad = true; break; }   // overlapping requests: capacity is rows + 1
-            const int row0 = s0 + i * kSegRows;
-            const int nr = min(kSegRows, s1 - row0);
+            const int row0 = s0 + i * seg_rows;
+            const int nr = min(seg_rows, s1 - row0);
             int maxend = 0;
             for (int r = row0; r < row0 + nr; ++r) {
                 int e = rows_fit ? se[r] : row_ends[r];
@@ -231,11 +243,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     }
     if (bad && status) atomicOr(status, DSA_STATUS_BAD_GEOMETRY);
     const int S = min(carry, rows + 1);
+    // Tile prefix and, when the segments fit on chip, the prefix of the tiles'
+    // estimated cost (kTileCostBase + the segment's rows per tile; `se` is free now).
+    const bool weighted = S <= kPlanSmemSegs && S <= kPlanSmemRows;
     carry = 0;
+    int wcarry = 0;
     for (int base = 0; base < S; base += blockDim.x) {
         const int i = base + threadIdx.x;
-        int tiles = 0;
-        if (i < S) tiles = i < kPlanSmemSegs ? sp[i] : (segs[i].w + kTileRows - 1) / kTileRows;
+        int tiles = 0, cost = 0;
+        if (i < S) {
+            tiles = i < kPlanSmemSegs ? sp[i] : (segs[i].w + kTileRows - 1) / kTileRows;
+            if (weighted) cost = tiles * (kTileCostBase + segs[i].z);
+        }
         const int inc = block_inclusive_scan(tiles, warp_tmp, &chunk_total);
         if (i < S) {
             seg_prefix[i] = carry + inc - tiles;
@@ -243,23 +262,41 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         }
         carry += chunk_total;
         __syncthreads();
+        if (weighted) {
+            const int winc = block_inclusive_scan(cost, warp_tmp, &chunk_total);
+            if (i < S) se[i] = wcarry + winc - cost;
+            wcarry += chunk_total;
+            __syncthreads();
+        }
     }
     const int T = carry;
-    const int Ts = T - (T / kPoolDiv) / kChunkTiles * kChunkTiles;   // tiles of the static ranges
     if (threadIdx.x == 0) {
         seg_prefix[S] = T;
         if (S <= kPlanSmemSegs) sp[S] = T;
+        if (weighted) se[S] = wcarry;
         info[0] = S;
         info[1] = T;
-        info[2] = 0;   // pool chunks claimed
-        info[3] = Ts;
     }
     __syncthreads();
     // Static tile range and first segment of every scoring CTA, so that a CTA
-    // starts from one load instead of a search through global memory.
+    // starts from one load instead of a search through global memory.  The
+    // ranges split the estimated cost evenly (a tile of a segment of n rows
+    // costs kTileCostBase + n: its copy and MMA, and n rows of epilogue), else
+    // the tiles.
+    auto tile_at = [&](int c) -> int {   // first tile of CTA c
+        if (!weighted || wcarry == 0) return static_cast<int>(static_cast<int64_t>(c) * T / G);
+        const int64_t B = static_cast<int64_t>(c) * wcarry / G;
+        int lo = 0, hi = S;   // the last segment with se[lo] <= B
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (se[mid] <= B) lo = mid; else hi = mid;
+        }
+        const int per = kTileCostBase + segs[lo].z;
+        return min(sp[lo + 1], sp[lo] + static_cast<int>((B - se[lo]) / per));
+    };
     for (int c = threadIdx.x; c < G; c += blockDim.x) {
-        const int t0 = static_cast<int>(static_cast<int64_t>(c) * Ts / G);
-        const int t1 = static_cast<int>(static_cast<int64_t>(c + 1) * Ts / G);
+        const int t0 = c == 0 ? 0 : tile_at(c);
+        const int t1 = c + 1 == G ? T : tile_at(c + 1);
         int seg = -1;
         if (S <= kPlanSmemSegs && S > 0) {
             int lo = 0, hi = S;
@@ -280,23 +317,52 @@ struct TilePlan {
     int j;     // tile index within the segment
     int pid0;  // physical page of keys 0..63 (-1: none)
     int pid1;  // physical page of keys 64..127 (-1: none)
+    int row0;  // the segment's first query row
+    int nrows; // the segment's rows
 };
 
-__device__ __forceinline__ TilePlan plan_tile(const ScoreArgs& p, int t, int t1, int seg, int S) {
-    TilePlan tp{-1, 0, -1, -1};
-    if (t >= t1) return tp;
-    if (t >= p.seg_prefix[seg + 1]) {
-        // binary search in (seg, S): the tile lies past the starting segment
-        int lo = seg + 1, hi = S;
+// Plans of the tiles base + lane (lanes below n; the others get no pages) of
+// one warp, whose tiles lie in segments seg, seg + 1, ...: lane k loads the
+// tile prefix and record of segment seg + k (one round trip for the warp),
+// every lane finds its tile's segment among those 32 by a search over
+// shuffled registers, then loads its two block-table entries.  Tiles past
+// segment seg + 31 (batches crossing more than 31 segments) search the global
+// prefix instead.
+__device__ __forceinline__ TilePlan plan_batch(const ScoreArgs& p, int base, int n, int seg, int S) {
+    const int lane = threadIdx.x & 31;
+    const int t = base + lane;
+    const int sk = min(seg + lane, S);
+    const int q = p.seg_prefix[sk];                                  // first tile of segment seg + lane
+    const int4 rec = sk < S ? p.segs[sk] : make_int4(0, 0, 0, 0);
+    int cnt = 0;   // the last k <= 31 with prefix[seg + k] <= t (prefix sorted, prefix[seg] <= t)
+#pragma unroll
+    for (int step = 16; step >= 1; step >>= 1) {
+        const int v = __shfl_sync(0xFFFFFFFFu, q, cnt + step);
+        if (cnt + step <= 31 && v <= t) cnt += step;
+    }
+    TilePlan tp{-1, 0, -1, -1, 0, 0};
+    int first = __shfl_sync(0xFFFFFFFFu, q, cnt);
+    int4 si;
+    si.x = __shfl_sync(0xFFFFFFFFu, rec.x, cnt);
+    si.y = __shfl_sync(0xFFFFFFFFu, rec.y, cnt);
+    si.z = __shfl_sync(0xFFFFFFFFu, rec.z, cnt);
+    si.w = __shfl_sync(0xFFFFFFFFu, rec.w, cnt);
+    int sg = seg + cnt;
+    if (lane >= n) return tp;
+    if (cnt == 31 && sg + 1 < S && p.seg_prefix[sg + 1] <= t) {
+        int lo = sg + 1, hi = S;   // the tile lies past the 32 segments loaded above
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (p.seg_prefix[mid] <= t) lo = mid; else hi = mid;
         }
-        seg = lo;
+        sg = lo;
+        first = p.seg_prefix[sg];
+        si = p.segs[sg];
     }
-    tp.seg = seg;
-    const int4 si = p.segs[seg];
-    const int j = t - p.seg_prefix[seg];
+    tp.seg = sg;
+    tp.row0 = si.y;
+    tp.nrows = si.z;
+    const int j = t - first;
     tp.j = j;
     const int npages = (si.w + kPage - 1) / kPage;
     const int32_t* row = p.block_table + static_cast<int64_t>(si.x) * p.bt_stride;
@@ -311,21 +377,6 @@ __device__ __forceinline__ TilePlan plan_tile(const ScoreArgs& p, int t, int t1,
     }
     if (bad && p.status) atomicOr(p.status, DSA_STATUS_BAD_PAGE);
     return tp;
-}
-
-// Segment of tile t (the last s with prefix[s] <= t) by a 32-way search of
-// the whole warp: each round keeps one of 32 sub-ranges of [lo, hi).
-__device__ __forceinline__ int warp_find_segment(const int* prefix, int S, int t) {
-    const int lane = threadIdx.x & 31;
-    int lo = 0, hi = S;
-    while (hi - lo > 1) {
-        const int step = (hi - lo + 31) >> 5;
-        const int i = lo + lane * step;
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, i < hi && prefix[i] <= t);   // lanes 0..L (prefix sorted)
-        lo += (31 - __clz(m)) * step;
-        hi = min(hi, lo + step);
-    }
-    return lo;
 }
 
 // Bounded wait until a release counter reaches `need` (wrap-safe compare);
@@ -365,10 +416,10 @@ __device__ __forceinline__ void issue_scales(const CUtensorMap* smap, uint8_t* s
     tma_load_2d(smem + OFF_RAWSC + s * 512 + h * 256, smap, 0, pid, bar);
 }
 
-// Issues the loads of one tile (lane 0 of the producer warp): the segment's
-// query rows when the segment changes, then the first page's codes into the
-// next ring stage, tagged with {tile in segment, segment, segment ordinal};
-// the page ids go to the page warp, which copies the rest of the tile.
+// Prepares one tile (lane 0 of the producer warp): the segment's query rows
+// when the segment changes, then the next ring stage, tagged with {tile in
+// segment, segment, segment ordinal}; the page ids go to the tile's copy
+// warp, which copies its pages.
 //
 // Query buffer b holds the segments of ordinals b, b + 2, ...  Before it is
 // refilled, the MMAs of the segment it held must be done: every issuer's last
@@ -388,16 +439,22 @@ struct Producer {
     bool rg;             // row-group placement: packed boxes per column group
     int lg;              // log2 of the ring's stage count
     int stage_bytes;     // shared memory of a stage's codes
-    int2* page_ring;     // {first, second} page ids for the page warp
+    int4* page_ring;     // per position: {first page, second page, tile in segment, segment}, {ordinal}
     uint32_t* published; // entries written (release)
-    const uint32_t* consumed;   // entries the page warp has taken (acquire)
+    const uint32_t* consumed;   // [kCopyWarps]: entries each copy warp has taken (acquire)
     int cur = -1, i_seg = 0, it = 0;
 
-    // Hands position it's page ids to the page warp (ring of kPageRing).
-    __device__ __forceinline__ bool publish(const ScoreArgs& p, int2 v) {
-        if (it >= kPageRing && !count_wait(consumed, static_cast<uint32_t>(it - kPageRing + 1), abort, p.status))
-            return false;
-        page_ring[it & (kPageRing - 1)] = v;
+    // Hands position it's page ids to its copy warp (ring of kPageRing); the
+    // entry's previous occupant, position it - kPageRing, must have been taken.
+    __device__ __forceinline__ bool publish(const ScoreArgs& p, int4 v, int ord) {
+        if (it >= kPageRing) {
+            const int old = it - kPageRing;
+            if (!count_wait(consumed + (old % kCopyWarps), static_cast<uint32_t>(old / kCopyWarps + 1), abort,
+                            p.status))
+                return false;
+        }
+        page_ring[2 * (it & (kPageRing - 1))] = v;
+        page_ring[2 * (it & (kPageRing - 1)) + 1] = make_int4(ord, 0, 0, 0);
         smem_add_release(published, 1u);
         return true;
     }
@@ -414,10 +471,10 @@ struct Producer {
         }
     }
 
-    __device__ __forceinline__ bool issue(const ScoreArgs& p, int sg, int j, int p0, int p1) {
+    __device__ __forceinline__ bool issue(const ScoreArgs& p, int sg, int j, int p0, int p1, int row0, int nrows) {
         if (sg != cur) {
             cur = sg;
-            const int4 si = p.segs[sg];
+            const int2 si = make_int2(row0, nrows);
             const int qb = i_seg & 1;
             for (int w = 0; w < kMmaWarps; ++w) {
                 // release of tile l: round l >> lg of its stage's empty barrier; while
@@ -428,51 +485,46 @@ struct Producer {
                     return false;
                 set_last_tile(qb, w, -1);
             }
-            const uint32_t qsf = rg ? kQsfRowRg : kQsfRow;
-            const uint32_t bytes = si.z * (fp4 ? kFp4QRowTx + qsf : kFp8QRowTx);
+            const uint32_t qsf = p.qs_group_major ? kQsfRowRg : kQsfRow;
+            const uint32_t qrow = fp4 ? 64u * p.heads : kFp8QRowTx;   // packed MXFP4: heads x 64 B
+            const uint32_t bytes = si.y * (fp4 ? qrow + qsf : qrow);
             mbar_arrive_expect_tx(qfull + qb, bytes);
             uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
-            for (int r = 0; r < si.z; ++r) {
+            for (int r = 0; r < si.y; ++r) {
                 if (rg) {
-                    // packed: 16-byte column chunk c of the 32 heads at c * 2048 + r * 512
+                    // packed: 16-byte column chunk c of every head at c * 2048 + (r * heads + h) * 16
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        tma_load_3d(qdst + c * kRgQChunk + r * 512, qmap, 16 * c, 0, si.y + r, qfull + qb);
+                        tma_load_3d(qdst + c * kRgQChunk + r * 16 * p.heads, qmap, 16 * c, 0, si.x + r, qfull + qb);
                 } else {
-                    // FP8 rows of 4096 bytes, packed MXFP4 rows of 2048 (32 heads x 64 B)
-                    tma_load_3d(qdst + r * (fp4 ? kFp4QRowTx : kQRowBytes), qmap, 0, 0, si.y + r, qfull + qb);
+                    // FP8 rows of 4096 bytes, packed MXFP4 rows of heads x 64 B
+                    tma_load_3d(qdst + r * qrow, qmap, 0, 0, si.x + r, qfull + qb);
                 }
                 if (fp4)
                     bulk_load(smem + OFF_QSF + qb * kQsfBytes + r * qsf,
-                              p.q_rows + static_cast<int64_t>(si.y + r) * kQRowBytes + kFp4Scales, qsf, qfull + qb);
+                              p.q_scales + static_cast<int64_t>(si.x + r) * p.qs_stride, qsf, qfull + qb);
             }
             ++i_seg;
         }
         const int s = it & ((1 << lg) - 1);
         if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
-        reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(j, sg, i_seg - 1, 0);
         set_last_tile((i_seg - 1) & 1, it % kMmaWarps, it);
-        // the stage's full barrier takes two arrivals: this warp's (the first page's codes) and
-        // the page warp's (the second page's codes, both pages' scales)
-        if (!publish(p, make_int2(p0 >= 0 ? p0 : kNoPage, p1 >= 0 ? p1 : kNoPage))) return false;
-        if (p0 < 0) {
-            mbar_arrive(full + s);   // no valid page: scores of these keys are unspecified
-        } else {
-            mbar_arrive_expect_tx(full + s, fp4 ? kFp4PageTx : kFp8PageTx);
-            issue_codes(kmap, smem, full + s, s, stage_bytes, fp4, rg, 0, p0);
-        }
+        // the copy warp writes the stage's tag and arms its full barrier for the
+        // tile's bytes (a tile without valid pages: scores of its keys are unspecified)
+        if (!publish(p, make_int4(p0 >= 0 ? p0 : kNoPage, p1 >= 0 ? p1 : kNoPage, j, sg), i_seg - 1)) return false;
         ++it;
         return true;
     }
 
-    // End of this CTA's sequence: one stage tagged -1, with no copies, per issuer.
+    // End of this CTA's sequence: one stage tagged -1, with no copies, per copy
+    // warp (each copy warp stops at its end mark; each issuer at the first one
+    // of its positions).
+    static_assert(kCopyWarps >= kMmaWarps, "every issuer meets an end tag");
     __device__ __forceinline__ bool finish(const ScoreArgs& p) {
-        for (int w = 0; w < kMmaWarps; ++w) {
+        for (int w = 0; w < kCopyWarps; ++w) {
             const int s = it & ((1 << lg) - 1);
             if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
-            reinterpret_cast<int4*>(smem + OFF_SINFO)[s] = make_int4(-1, -1, -1, 0);
-            if (!publish(p, make_int2(kEndMark, kEndMark))) return false;
-            mbar_arrive(full + s);
+            if (!publish(p, make_int4(kEndMark, kEndMark, -1, -1), -1)) return false;
             ++it;
         }
         return true;
@@ -482,44 +534,26 @@ struct Producer {
 // Warp 0.  Its 32 lanes resolve the segments and block-table entries of 32
 // tiles at once (the next batch's loads are in flight while lane 0 issues the
 // current batch's tiles), so block-table latency is paid once per batch.
-// After its own range the warp claims chunks of the pool until none is left.
-__device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, int t0, int t1, int seg, int S,
-                                              int Ts, int T) {
+__device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, int t0, int t1, int seg, int S) {
     const int lane = threadIdx.x & 31;
     bool ok = true;
     if (t0 < t1) {
-        TilePlan nxt = plan_tile(p, t0 + lane, t1, seg, S);
+        TilePlan nxt = plan_batch(p, t0, min(32, t1 - t0), seg, S);
         for (int base = t0; base < t1 && ok; base += 32) {
             const TilePlan mine = nxt;
             const int last = min(31, t1 - 1 - base);
             const int seg_end = __shfl_sync(0xFFFFFFFFu, mine.seg, last);
-            if (base + 32 < t1) nxt = plan_tile(p, base + 32 + lane, t1, seg_end, S);
+            if (base + 32 < t1) nxt = plan_batch(p, base + 32, min(32, t1 - base - 32), seg_end, S);
             for (int i = 0; i <= last && ok; ++i) {
                 const int sg = __shfl_sync(0xFFFFFFFFu, mine.seg, i);
                 const int j = __shfl_sync(0xFFFFFFFFu, mine.j, i);
                 const int p0 = __shfl_sync(0xFFFFFFFFu, mine.pid0, i);
                 const int p1 = __shfl_sync(0xFFFFFFFFu, mine.pid1, i);
-                if (lane == 0) ok = pr.issue(p, sg, j, p0, p1);
+                const int r0 = __shfl_sync(0xFFFFFFFFu, mine.row0, i);
+                const int nr = __shfl_sync(0xFFFFFFFFu, mine.nrows, i);
+                if (lane == 0) ok = pr.issue(p, sg, j, p0, p1, r0, nr);
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             }
-        }
-    }
-    while (ok && Ts < T) {
-        int id = 0;
-        if (lane == 0) id = atomicAdd(p.claim, 1);
-        id = __shfl_sync(0xFFFFFFFFu, id, 0);
-        const int64_t base = Ts + static_cast<int64_t>(id) * kChunkTiles;
-        if (base >= T) break;
-        const int b = static_cast<int>(base);
-        const int end = min(T, b + kChunkTiles);
-        const TilePlan mine = plan_tile(p, b + lane, end, warp_find_segment(p.seg_prefix, S, b), S);
-        for (int i = 0; i < end - b && ok; ++i) {
-            const int sg = __shfl_sync(0xFFFFFFFFu, mine.seg, i);
-            const int j = __shfl_sync(0xFFFFFFFFu, mine.j, i);
-            const int p0 = __shfl_sync(0xFFFFFFFFu, mine.pid0, i);
-            const int p1 = __shfl_sync(0xFFFFFFFFu, mine.pid1, i);
-            if (lane == 0) ok = pr.issue(p, sg, j, p0, p1);
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         }
     }
     if (lane == 0) {
@@ -536,28 +570,40 @@ __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, 
     __syncwarp();
 }
 
-// Warp kPageWarp.  Follows warp 0's positions through the page ring and
-// copies each tile's second page and both pages' scales into the same stage,
-// arming the stage's full barrier for its own bytes (it waits for the same
-// free-stage phase as warp 0; the stage cannot move on before this warp's
-// arrival).
-__device__ __forceinline__ void page_role(const ScoreArgs& p, const CUtensorMap* kmap, const CUtensorMap* smap,
+// Copy warp c (warp kFirstCopyWarp + c).  Follows warp 0's positions c, c +
+// kCopyWarps, ... through the page ring and copies each tile's two pages (codes
+// and scales) into its stage, arming the stage's full barrier for those bytes
+// (it waits for the same free-stage phase as warp 0; the stage cannot move on
+// before this warp's arrival).
+__device__ __forceinline__ void copy_role(const ScoreArgs& p, const CUtensorMap* kmap, const CUtensorMap* smap,
                                           uint8_t* smem, uint64_t* full, uint64_t* empty, const uint32_t* published,
-                                          uint32_t* consumed, volatile int* abort) {
+                                          uint32_t* consumed, volatile int* abort, int c) {
     if ((threadIdx.x & 31) != 0) return;
     const bool fp4 = fmt_fp4(p.fmt), rg = (p.fmt == DSA_FMT_MXFP4_RG);
     const int lg = ring_stages_log2(p.fmt), stage_bytes = ring_stage_bytes(p.fmt);
-    const int2* ring = reinterpret_cast<const int2*>(smem + OFF_PRING);
-    int ends = 0;
-    for (int j = 0; ends < kMmaWarps; ++j) {
+    const uint32_t page_tx = (fp4 ? kFp4PageTx : kFp8PageTx) + 256u;
+    const int4* ring = reinterpret_cast<const int4*>(smem + OFF_PRING);
+    int4* sinfo = reinterpret_cast<int4*>(smem + OFF_SINFO);
+    for (int j = c;; j += kCopyWarps) {
         if (!count_wait(published, static_cast<uint32_t>(j + 1), abort, p.status)) break;
-        const int2 v = ring[j & (kPageRing - 1)];
+        const int4 v = ring[2 * (j & (kPageRing - 1))];
+        const int ord = ring[2 * (j & (kPageRing - 1)) + 1].x;
+        smem_add_release(consumed + c, 1u);
         const int s = j & ((1 << lg) - 1);
         if (!mbar_wait(empty + s, ((j >> lg) & 1) ^ 1, abort, p.status)) break;
-        const uint32_t bytes = (v.x >= 0 ? 256u : 0u) + (v.y >= 0 ? (fp4 ? kFp4PageTx : kFp8PageTx) + 256u : 0u);
+        // the stage's tag: {tile in segment, segment, segment ordinal}; -1 ends an issuer's sequence
+        sinfo[s] = v.x == kEndMark ? make_int4(-1, -1, -1, 0) : make_int4(v.z, v.w, ord, 0);
+        if (v.x == kEndMark) {
+            mbar_arrive(full + s);
+            break;
+        }
+        const uint32_t bytes = (v.x >= 0 ? page_tx : 0u) + (v.y >= 0 ? page_tx : 0u);
         if (bytes) {
             mbar_arrive_expect_tx(full + s, bytes);
-            if (v.x >= 0) issue_scales(smap, smem, full + s, s, 0, v.x);
+            if (v.x >= 0) {
+                issue_codes(kmap, smem, full + s, s, stage_bytes, fp4, rg, 0, v.x);
+                issue_scales(smap, smem, full + s, s, 0, v.x);
+            }
             if (v.y >= 0) {
                 issue_codes(kmap, smem, full + s, s, stage_bytes, fp4, rg, 1, v.y);
                 issue_scales(smap, smem, full + s, s, 1, v.y);
@@ -565,8 +611,6 @@ __device__ __forceinline__ void page_role(const ScoreArgs& p, const CUtensorMap*
         } else {
             mbar_arrive(full + s);
         }
-        smem_add_release(consumed, 1u);
-        if (v.x == kEndMark) ++ends;
     }
 }
 
@@ -620,24 +664,25 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(qfull + qb, (cur >> 1) & 1, abort, p.status))) break;
             if (block_scaled) {
                 // Query block scales: line L of the atom holds the words of MMA
-                // rows L, 32 + L, 64 + L, 96 + L (row r * 32 + h = head h of query row r).
+                // rows L, 32 + L, 64 + L, 96 + L (row n = r * heads + h: head h of query row r).
                 const uint8_t* raw = smem + OFF_QSF + qb * kQsfBytes;
-                // word of head `lane` of row r: token-major rows hold it as is; row-group
+                // the word of MMA row n: head-major rows hold it as is; group-major
                 // rows hold block g's byte at g * 64 + head; FP8 queries are unscaled (2^0)
-                auto word = [&](int r) -> uint32_t {
+                auto word = [&](int n) -> uint32_t {
+                    const int r = n / p.heads, h = n - r * p.heads;
                     if (r >= nrows || fp8mx) return 0x7F7F7F7Fu;
-                    if (!rg) return reinterpret_cast<const uint32_t*>(raw + r * kQsfRow)[lane];
-                    const uint8_t* b = raw + r * kQsfRowRg + lane;
+                    if (!p.qs_group_major) return reinterpret_cast<const uint32_t*>(raw + r * kQsfRow)[h];
+                    const uint8_t* b = raw + r * kQsfRowRg + h;
                     return static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[kRgQuerySlots]) << 8) |
                            (static_cast<uint32_t>(b[2 * kRgQuerySlots]) << 16) |
                            (static_cast<uint32_t>(b[3 * kRgQuerySlots]) << 24);
                 };
                 uint8_t* atom = smem + OFF_SFB + (qb * kMmaWarps + w) * 512;
                 uint4 line;
-                line.x = word(0);
-                line.y = word(1);
-                line.z = word(2);
-                line.w = word(3);
+                line.x = word(lane);
+                line.y = word(32 + lane);
+                line.z = word(64 + lane);
+                line.w = word(96 + lane);
                 reinterpret_cast<uint4*>(atom)[lane] = line;
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -682,7 +727,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             const uint32_t d = tmem + TM_ACC + a * 128;
             const uint32_t ka = smem_u32(smem + OFF_TILES + s * stage_bytes);
             const uint32_t kb = smem_u32(smem + OFF_QBUF + qb * kQBufBytes);
-            const uint32_t n = 32u * nrows;
+            const uint32_t n = static_cast<uint32_t>(p.heads * nrows);
             if (key_scale) {
                 const uint64_t ad = desc_sw128(ka), bd = desc_sw128(kb);
                 const uint32_t id = idesc_f8f6f4(kMmaE4M3, kMmaE4M3, 128, n);
@@ -733,15 +778,16 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
 }
 
 // Scores of one query row for the 32 keys of this warp (one per lane) from
-// the 32 head columns v of its accumulator: sum_h w_h * max(acc_h, 0), four
+// the H head columns v of its accumulator: sum_h w_h * max(acc_h, 0), four
 // partial sums by head mod 4, combined as ((s0 + s1) + (s2 + s3)).  The ReLU
 // is an integer max on the FP32 bits (negative values, -0 included, have the
 // sign bit set and are negative as signed integers); the multiply-adds run two
 // at a time (fma.rn.f32x2, each lane rounded as fmaf).
+template <int H>
 __device__ __forceinline__ float head_sum(const uint32_t* v, const float* wr, float ksm) {
     unsigned long long s01 = 0ull, s23 = 0ull;   // (s0, s1), (s2, s3) as f32x2, +0.0
 #pragma unroll
-    for (int h4 = 0; h4 < 8; ++h4) {
+    for (int h4 = 0; h4 < H / 4; ++h4) {
         const float4 w4 = reinterpret_cast<const float4*>(wr)[h4];
         const int r0 = max(static_cast<int>(v[4 * h4 + 0]), 0), r1 = max(static_cast<int>(v[4 * h4 + 1]), 0);
         const int r2 = max(static_cast<int>(v[4 * h4 + 2]), 0), r3 = max(static_cast<int>(v[4 * h4 + 3]), 0);
@@ -809,13 +855,15 @@ __device__ __forceinline__ void flush_group_hist(const ScoreArgs& p, uint32_t* g
 // Warps kFirstEpiWarp .. + kEpiWarps.  Group g drains the accumulators of
 // sequence positions g, g + kEpiGroups, ...; every warp works on its own
 // (per-warp head weights, row bounds in registers, one release count per tile).
+// H query heads: row r of a segment owns accumulator columns r * H .. r * H + H - 1.
+template <int H>
 __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* tfull,
                                               uint32_t* released, volatile int* abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int group = (warp - kFirstEpiWarp) >> 2;
     const int quarter = warp & 3;            // TMEM lanes this warp may access
     const int m = quarter * 32 + lane;       // key of the tile this thread owns
-    float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - kFirstEpiWarp) * (kSegRows * kHeads);
+    float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - kFirstEpiWarp) * 128;
     const int2* ainfo = reinterpret_cast<const int2*>(smem + OFF_AINFO);
     const bool f32scale = (p.fmt == DSA_FMT_FP8);   // FP32 key scale (FP8-MX scales act inside the MMA)
     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC;
@@ -847,8 +895,8 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
             const int4 si = p.segs[cur];
             row0 = si.y;
             nrows = si.z;
-            for (int r = 0; r < nrows; ++r)
-                wsm[r * kHeads + lane] = __bfloat162float(p.w[static_cast<int64_t>(row0 + r) * kHeads + lane]);
+            for (int i = lane; i < nrows * H; i += 32)
+                wsm[i] = __bfloat162float(p.w[static_cast<int64_t>(row0 + i / H) * p.w_stride + i % H]);
             end_l = lane < nrows ? p.eff_end[row0 + lane] : 0;
             hist_m = __ballot_sync(0xFFFFFFFFu, lane < nrows && p.hist_k >= 0 && end_l > p.hist_k);
             __syncwarp();
@@ -856,25 +904,31 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
         const float ksm = f32scale ? reinterpret_cast<const float*>(smem + OFF_KS + a * 512)[m] : 1.0f;
         const int tpos = tag.x * kTileRows + m;
         const uint32_t acc = tbase + a * 128;
+        // 64-column loads of 64 / H rows; a remainder of fewer rows in 32-column loads
+        constexpr int kRpl = 64 / H;
         int r = 0;
-        for (; r + 2 <= nrows; r += 2) {
+        for (; r + kRpl <= nrows; r += kRpl) {
             uint32_t v[64];
-            tc_ld_32x32b_x64(acc + r * 32, v);
+            tc_ld_32x32b_x64(acc + r * H, v);
             tc_wait_ld_regs<64>(v);
-            const float s0 = head_sum(v, wsm + r * kHeads, ksm);
-            const float s1 = head_sum(v + 32, wsm + (r + 1) * kHeads, ksm);
-            emit_row(p, row0 + r, tpos, s0, __shfl_sync(0xFFFFFFFFu, end_l, r), (hist_m >> r) & 1,
-                     gh + r * (kHistBins / 2));
-            emit_row(p, row0 + r + 1, tpos, s1, __shfl_sync(0xFFFFFFFFu, end_l, r + 1), (hist_m >> (r + 1)) & 1,
-                     gh + (r + 1) * (kHistBins / 2));
+#pragma unroll
+            for (int i = 0; i < kRpl; ++i)
+                emit_row(p, row0 + r + i, tpos, head_sum<H>(v + i * H, wsm + (r + i) * H, ksm),
+                         __shfl_sync(0xFFFFFFFFu, end_l, r + i), (hist_m >> (r + i)) & 1,
+                         gh + (r + i) * (kHistBins / 2));
         }
-        if (r < nrows) {
-            uint32_t v[32];
-            tc_ld_32x32b_x32(acc + r * 32, v);
-            tc_wait_ld_regs<32>(v);
-            const float s0 = head_sum(v, wsm + r * kHeads, ksm);
-            emit_row(p, row0 + r, tpos, s0, __shfl_sync(0xFFFFFFFFu, end_l, r), (hist_m >> r) & 1,
-                     gh + r * (kHistBins / 2));
+        if constexpr (H < 64) {
+            for (; r < nrows; r += 32 / H) {
+                uint32_t v[32];
+                tc_ld_32x32b_x32(acc + r * H, v);   // within the accumulator's 128 columns
+                tc_wait_ld_regs<32>(v);
+#pragma unroll
+                for (int i = 0; i < 32 / H; ++i)
+                    if (r + i < nrows)
+                        emit_row(p, row0 + r + i, tpos, head_sum<H>(v + i * H, wsm + (r + i) * H, ksm),
+                                 __shfl_sync(0xFFFFFFFFu, end_l, r + i), (hist_m >> (r + i)) & 1,
+                                 gh + (r + i) * (kHistBins / 2));
+            }
         }
         tc_fence_before();
         __syncwarp();
@@ -898,19 +952,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     uint32_t* released = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 16);   // per accumulator
     uint32_t* published = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 32);
-    uint32_t* consumed = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 36);
+    uint32_t* consumed = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 48);   // per copy warp
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMaxStages; ++s) {
-            mbar_init(full + s, 2);   // warp 0 (first page's codes) and the page warp (the rest)
+            mbar_init(full + s, 1);   // the tile's copy warp (its tag and bytes)
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) mbar_init(qfull + b, 1);
         for (int b = 0; b < kAcc * kEpiGroups; ++b) mbar_init(tfull + b, 2);
         for (int b = 0; b < kAcc; ++b) released[b] = 0u;
         *published = 0u;
-        *consumed = 0u;
+        for (int c = 0; c < kCopyWarps; ++c) consumed[c] = 0u;
         mbar_init(done_bar, kMmaWarps);
         *abort = 0;
         mbar_fence_init();
@@ -931,7 +985,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
     if (warp == 0) {
         const int4 range = args.cta[blockIdx.x];   // {first tile, end tile, first segment, segments}
-        const int T = args.claim[-1], Ts = args.claim[1];
         const int t0 = range.x, t1 = range.y, S = range.w;
         const int seg = (t0 < t1 && range.z < 0) ? find_segment(args.seg_prefix, S, t0) : range.z;
         Producer pr{&kmap,
@@ -946,16 +999,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     args.fmt == DSA_FMT_MXFP4_RG,
                     ring_stages_log2(args.fmt),
                     ring_stage_bytes(args.fmt),
-                    reinterpret_cast<int2*>(smem + OFF_PRING),
+                    reinterpret_cast<int4*>(smem + OFF_PRING),
                     published,
                     consumed};
-        producer_role(pr, args, t0, t1, seg, S, Ts, T);
+        producer_role(pr, args, t0, t1, seg, S);
     } else if (warp < kFirstEpiWarp) {
         mma_role(args, smem, tmem, full, empty, qfull, tfull, released, done_bar, abort);
-    } else if (warp < kPageWarp) {
-        epilogue_role(args, smem, tmem, tfull, released, abort);
+    } else if (warp < kFirstCopyWarp) {
+        if (args.heads == 16) epilogue_role<16>(args, smem, tmem, tfull, released, abort);
+        else if (args.heads == 64) epilogue_role<64>(args, smem, tmem, tfull, released, abort);
+        else epilogue_role<32>(args, smem, tmem, tfull, released, abort);
     } else {
-        page_role(args, &kmap, &smap, smem, full, empty, published, consumed, abort);
+        copy_role(args, &kmap, &smap, smem, full, empty, published, consumed, abort, warp - kFirstCopyWarp);
     }
     tc_fence_before();
     __syncthreads();
@@ -1008,12 +1063,28 @@ extern "C" size_t dsa_workspace_size(int fmt, int64_t rows, int64_t num_requests
     return workspace_layout(rows, max_pages * kPage, true, true).total;
 }
 
-extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const void* cache, int64_t page_stride,
-                               int64_t num_pages, const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
-                               const int32_t* starts, const int32_t* row_ends, int64_t num_requests, int64_t rows,
-                               int64_t max_query_len, float* logits, int64_t logits_ld, int64_t k, int32_t* topk,
-                               void* workspace, size_t workspace_bytes, int32_t* status, void* stream_) {
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+namespace dsa {
+
+// Query operands of one scoring call: `heads` heads per row, payload row r at
+// q + r * q_stride (FP8: 32 x 128 codes; MXFP4: heads x 64 packed bytes), MXFP4
+// scales of row r at q_scales + r * qs_stride (group-major or head-major),
+// BF16 weights of row r at w + r * w_stride.
+struct QueryOperands {
+    int heads;
+    const void* q;
+    int64_t q_stride;
+    const void* q_scales;
+    int64_t qs_stride;
+    bool qs_group_major;
+    const void* w;
+    int64_t w_stride;
+};
+
+static int score_paged_impl(int fmt, const QueryOperands& qo, const void* cache, int64_t page_stride,
+                            int64_t num_pages, const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                            const int32_t* starts, const int32_t* row_ends, int64_t num_requests, int64_t rows,
+                            int64_t max_query_len, float* logits, int64_t logits_ld, int64_t k, int32_t* topk,
+                            void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t stream) {
     if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4_RG) return DSA_ERR_UNSUPPORTED;
     if (rows < 0 || num_requests < 0 || max_pages < 0 || num_pages < 0 || k < 0 || max_query_len < 0)
         return DSA_ERR_INVALID;
@@ -1023,13 +1094,15 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     const int64_t width = max_pages * kPage;
     if (rows > (1 << 30) || num_requests > (1 << 30) || width > (int64_t(1) << 30) || num_pages > 0x7FFFFFFF)
         return DSA_ERR_UNSUPPORTED;
-    if (!q_rows || !w || !starts || !row_ends || !workspace) return DSA_ERR_INVALID;
+    const void* q_rows = qo.q;
+    const void* w = qo.w;
+    if (!q_rows || !w || !starts || !row_ends || !workspace || (fp4 && !qo.q_scales)) return DSA_ERR_INVALID;
     if (num_pages > 0 && !cache) return DSA_ERR_INVALID;
     if (max_pages > 0 && num_requests > 0 && (!block_table || bt_stride < max_pages)) return DSA_ERR_INVALID;
     const int64_t min_stride = fp4 ? DSA_FP4_PAGE_BYTES : DSA_FP8_PAGE_BYTES;
     if (page_stride < min_stride || page_stride % 16) return DSA_ERR_INVALID;
-    if (!aligned(cache, 16) || !aligned(q_rows, 16) || !aligned(workspace, 256) ||
-        !aligned(w, 2))
+    if (!aligned(cache, 16) || !aligned(q_rows, 16) || !aligned(workspace, 256) || !aligned(w, 2) ||
+        (fp4 && !aligned(qo.q_scales, 16)) || qo.q_stride % 16 || qo.qs_stride % 16)
         return DSA_ERR_INVALID;
     if (logits && (logits_ld < width || !aligned(logits, 4))) return DSA_ERR_INVALID;
     const bool want_topk = (k > 0 && topk != nullptr);
@@ -1039,6 +1112,8 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     float* out_logits = logits ? logits : reinterpret_cast<float*>(ws + L.logits);
     const int64_t ld = logits ? logits_ld : width;
+    const int heads = qo.heads;
+    const int seg_rows = heads > 32 ? 128 / heads : kSegRows;
 
     // Tensor maps: key pages, key scales, query rows.
     CUtensorMap kmap, smap, qmap;
@@ -1074,18 +1149,18 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
             return DSA_ERR_CUDA;
     }
     if (rg) {
-        // {64 code bytes, 32 heads, rows}: one box = one 16-byte column chunk of a row's heads
-        const cuuint64_t dims[3] = {64, 32, static_cast<cuuint64_t>(rows)};
-        const cuuint64_t strides[2] = {64, kQRowBytes};
-        const cuuint32_t box[3] = {16, 32, 1};
+        // {64 code bytes, heads, rows}: one box = one 16-byte column chunk of a row's heads
+        const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(qo.q_stride)};
+        const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(heads), 1};
         if (encode_tiled(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q_rows), dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
             return DSA_ERR_CUDA;
     } else {
         const cuuint64_t row = fp4 ? 64 : 128;
-        const cuuint64_t dims[3] = {row, 32, static_cast<cuuint64_t>(rows)};
-        const cuuint64_t strides[2] = {row, kQRowBytes};
-        const cuuint32_t box[3] = {static_cast<cuuint32_t>(row), 32, 1};
+        const cuuint64_t dims[3] = {row, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[2] = {row, static_cast<cuuint64_t>(qo.q_stride)};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(row), static_cast<cuuint32_t>(heads), 1};
         if (encode_tiled(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q_rows), dims, strides, box,
                          fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return DSA_ERR_CUDA;
@@ -1099,7 +1174,7 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     const int grid = device_sm_count() < kMaxScoreCtas ? device_sm_count() : kMaxScoreCtas;
     if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, starts, row_ends, static_cast<int>(num_requests),
                    static_cast<int>(rows), static_cast<int>(width), info, segs, seg_prefix, eff_end, cta, grid,
-                   status) != cudaSuccess)
+                   seg_rows, status) != cudaSuccess)
         return DSA_ERR_CUDA;
 
     // The kernel's shared-memory limit is an attribute of each device's copy of it.
@@ -1118,7 +1193,6 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     a.bt_stride = bt_stride;
     a.q_rows = static_cast<const uint8_t*>(q_rows);
     a.w = static_cast<const __nv_bfloat16*>(w);
-    a.claim = info + 2;   // info: {segments, tiles, pool chunks claimed, static tiles}
     a.segs = segs;
     a.seg_prefix = seg_prefix;
     a.eff_end = eff_end;
@@ -1128,6 +1202,11 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     a.hist_k = want_topk ? static_cast<int>(k) : -1;
     a.hist = reinterpret_cast<unsigned*>(ws + L.hist);
     a.status = status;
+    a.heads = heads;
+    a.q_scales = static_cast<const uint8_t*>(qo.q_scales);
+    a.qs_stride = qo.qs_stride;
+    a.qs_group_major = qo.qs_group_major ? 1 : 0;
+    a.w_stride = qo.w_stride;
     if (g_time_before && g_time_after)   // external: kept as a record node under stream capture
         cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_time_before), stream, cudaEventRecordExternal);
     if (launch_pdl(score_kernel, dim3(grid), dim3(kScoreThreads), kScoreSmem, stream, kmap, smap, qmap,
@@ -1138,4 +1217,37 @@ extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const
     if (!want_topk && !logits) return DSA_OK;
     return launch_select(out_logits, logits, ld, width, eff_end, rows, want_topk ? k : 0, want_topk ? topk : nullptr,
                          ws, L, stream, true);
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" int dsa_score_paged(int fmt, const void* q_rows, const void* w, const void* cache, int64_t page_stride,
+                               int64_t num_pages, const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                               const int32_t* starts, const int32_t* row_ends, int64_t num_requests, int64_t rows,
+                               int64_t max_query_len, float* logits, int64_t logits_ld, int64_t k, int32_t* topk,
+                               void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+    // 4096-byte query rows of 32 heads; MXFP4 rows carry their scales at byte 2048
+    // (head-major, or group-major in the row-group format)
+    QueryOperands qo{kHeads, q_rows, kQRowBytes,
+                     q_rows ? static_cast<const uint8_t*>(q_rows) + kFp4Scales : nullptr, kQRowBytes,
+                     fmt == DSA_FMT_MXFP4_RG, w, kHeads};
+    return score_paged_impl(fmt, qo, cache, page_stride, num_pages, block_table, bt_stride, max_pages, starts,
+                            row_ends, num_requests, rows, max_query_len, logits, logits_ld, k, topk, workspace,
+                            workspace_bytes, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dsa_score_paged_heads(int fmt, int64_t heads, const void* payload, const void* q_scales, const void* w,
+                                     const void* cache, int64_t page_stride, int64_t num_pages,
+                                     const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                                     const int32_t* starts, const int32_t* row_ends, int64_t num_requests,
+                                     int64_t rows, int64_t max_query_len, float* logits, int64_t logits_ld, int64_t k,
+                                     int32_t* topk, void* workspace, size_t workspace_bytes, int32_t* status,
+                                     void* stream) {
+    if (!fmt_fp4(fmt) || (heads != 16 && heads != 32 && heads != 64)) return DSA_ERR_UNSUPPORTED;
+    QueryOperands qo{static_cast<int>(heads), payload, heads * 64, q_scales, 4 * kRgQuerySlots, true, w, heads};
+    return score_paged_impl(fmt, qo, cache, page_stride, num_pages, block_table, bt_stride, max_pages, starts,
+                            row_ends, num_requests, rows, max_query_len, logits, logits_ld, k, topk, workspace,
+                            workspace_bytes, status, static_cast<cudaStream_t>(stream));
 }

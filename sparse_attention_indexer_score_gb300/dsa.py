@@ -44,6 +44,8 @@ _SIGS = {
     "dsa_workspace_size": (_c.c_size_t, [_c.c_int, _I64, _I64, _I64, _I64]),
     "dsa_score_paged": (_c.c_int, [_c.c_int, _P, _P, _P, _I64, _I64, _P, _I64, _I64, _P, _P, _I64, _I64, _I64,
                                    _P, _I64, _I64, _P, _P, _c.c_size_t, _P, _P]),
+    "dsa_score_paged_heads": (_c.c_int, [_c.c_int, _I64, _P, _P, _P, _P, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
+                                         _I64, _I64, _P, _I64, _I64, _P, _P, _c.c_size_t, _P, _P]),
     "dsa_topk_workspace_size": (_c.c_size_t, [_I64, _I64]),
     "dsa_topk": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _P, _P, _c.c_size_t, _P]),
     "dsa_topk_noalloc": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _P, _P]),
@@ -52,6 +54,7 @@ _SIGS = {
     "dsa_timing_event_destroy": (_c.c_int, [_P]),
     "dsa_timing_elapsed_ms": (_c.c_int, [_P, _P, _c.POINTER(_c.c_float)]),
     "dsa_version": (_c.c_char_p, []),
+    "dsa_probe_mma": (_c.c_int, [_c.c_int, _I64, _P, _P]),
 }
 
 
@@ -306,6 +309,41 @@ def score_paged(fmt: str, q_rows: torch.Tensor, w: torch.Tensor, cache: torch.Te
     return logits, topk_out
 
 
+def score_paged_heads(fmt: str, payload: torch.Tensor, scales: torch.Tensor, w: torch.Tensor, cache: torch.Tensor,
+                      page_stride: int, num_pages: int, block_table: torch.Tensor, starts: torch.Tensor,
+                      row_ends: torch.Tensor, max_query_len: int, k: int = 0, want_logits: bool = False,
+                      workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """Paged logits (+ top-k) of MXFP4 queries of 16, 32 or 64 heads:
+    payload uint8 [rows, heads, 64] and scales uint8 [rows, 1, 4, 16, 4] from
+    ``quantize_queries_rg``, w BF16 [rows, heads].  Returns (logits or None,
+    top-k or None) as ``score_paged``."""
+    if payload.dtype != torch.uint8 or payload.dim() != 3 or payload.shape[2] != 64 or not payload.is_contiguous():
+        raise ValueError("payload must be contiguous uint8 [rows, heads, 64]")
+    rows, heads = payload.shape[0], payload.shape[1]
+    if scales.dtype != torch.uint8 or scales.numel() != rows * 256 or not scales.is_contiguous():
+        raise ValueError("scales must be contiguous uint8 [rows, 1, 4, 16, 4]")
+    if w.dtype != torch.bfloat16 or tuple(w.shape) != (rows, heads) or not w.is_contiguous():
+        raise ValueError("w must be contiguous BF16 [rows, heads]")
+    if row_ends.numel() != rows:
+        raise ValueError("row_ends must hold one bound per query row")
+    R = starts.numel() - 1
+    max_pages = block_table.shape[1] if block_table.dim() == 2 else 0
+    width = max_pages * 64
+    dev = payload.device
+    logits = torch.empty((rows, width), dtype=torch.float32, device=dev) if want_logits else None
+    top = torch.empty((rows, k), dtype=torch.int32, device=dev) if k > 0 else None
+    if workspace is None:
+        workspace = new_workspace(workspace_size(fmt, rows, R, max_pages, k), dev)
+    rc = lib().dsa_score_paged_heads(
+        _fmt(fmt), heads, _ptr(payload), _ptr(scales), _ptr(w), _ptr(cache), int(page_stride), int(num_pages),
+        _ptr(block_table), block_table.stride(0) if block_table.dim() == 2 else 0, max_pages,
+        _ptr(starts), _ptr(row_ends), R, rows, int(max_query_len),
+        _ptr(logits), logits.stride(0) if logits is not None else 0,
+        int(k), _ptr(top), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+    _check(rc, "dsa_score_paged_heads")
+    return logits, top
+
+
 def topk(logits: torch.Tensor, row_ends: torch.Tensor, k: int, width: Optional[int] = None,
          workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Top-k positions of each row of FP32 logits [rows, >= width] (valid below row_ends)."""
@@ -370,6 +408,20 @@ def set_score_timing(before: Optional[TimingEvent], after: Optional[TimingEvent]
         lib().dsa_set_score_timing(None, None)
     else:
         lib().dsa_set_score_timing(before.handle, after.handle)
+
+
+MMA_KINDS = {"fp8": 0, "mxf4": 1}
+MMA_K = {"fp8": 32, "mxf4": 64}
+
+
+def probe_mma(kind: str, iters: int, status: Optional[torch.Tensor] = None,
+              device: Optional[torch.device] = None) -> None:
+    """Launches the tensor-core rate probe (``dsa_probe_mma``) on the current
+    stream: one CTA per SM, ``iters`` MMAs of 128 x 128 x K each."""
+    if kind not in MMA_KINDS:
+        raise ValueError(f"kind must be one of {sorted(MMA_KINDS)}")
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    _check(lib().dsa_probe_mma(MMA_KINDS[kind], int(iters), _ptr(status), _stream(dev)), "dsa_probe_mma")
 
 
 def version() -> str:

@@ -487,3 +487,41 @@ def test_step_pipeline_matches_eager(cuda_lib):
             for r in range(wl.num_rows):
                 assert sorted(got[r].tolist()) == sorted(want[r].tolist()), (rnd, i, r)
     assert ix.status_bits() == 0
+
+
+@pytest.mark.parametrize("heads", [16, 32, 64])
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp4_rg"])
+@pytest.mark.parametrize("case", [2, 3, 5])
+def test_score_heads_parity(cuda_lib, fmt, heads, case):
+    """Page "amd.ops.fp4_indexer", score_paged: queries of 16, 32 or 64 heads,
+    quantised by quantize_queries on each side, scored against the MXFP4 cache
+    in either placement; logits and top-k against the oracle."""
+    import torch
+    spec = dict(SMALL[case])
+    wl = make_workload("tiny_fp8", fmt=fmt, seed=500 + case + heads, topk=[16, 64, 100, 5, 2, 512][case], **spec)
+    rng = np.random.default_rng(900 + heads + case)
+    x = rng.standard_normal((wl.num_rows, heads, 128)).astype(np.float32)
+    qb = ((x.view(np.uint32).astype(np.uint64) + 0x7FFF + ((x.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+    wf = rng.standard_normal((wl.num_rows, heads)).astype(np.float32)
+    wb = ((wf.view(np.uint32).astype(np.uint64) + 0x7FFF + ((wf.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+    g = gpu_run(wl)                                     # the GPU cache (prefill + step keys) and row bounds
+    o = oracle_run(wl)                                  # the oracle's own cache of the same keys
+    payload, scales = cuda_lib.quantize_queries_rg(bf16_tensor(qb, "cuda"))
+    w = bf16_tensor(wb, "cuda")
+    dev = "cuda"
+    logits, top = cuda_lib.score_paged_heads(fmt, payload, scales, w, g["cache"], g["page_stride"], wl.num_pages,
+                                             torch.from_numpy(wl.block_table).to(dev),
+                                             torch.from_numpy(g["starts"]).to(dev),
+                                             torch.from_numpy(g["row_ends"]).to(dev),
+                                             int(wl.query_lens.max(initial=0)), k=wl.topk, want_logits=True)
+    torch.cuda.synchronize()
+    want_p, want_s = O.quantize_queries(bf16_bits_to_f32(qb))
+    bt = np.full_like(wl.block_table, -1)
+    for qq in range(wl.R):
+        n = (int(wl.seq_lens[qq]) + 63) // 64
+        bt[qq, :n] = [o["remap"][int(pg)] for pg in wl.block_table[qq, :n]]
+    want = O.score_paged_heads(fmt, want_p, want_s, bf16_bits_to_f32(wb), o["cache"], O.page_bytes(fmt), bt,
+                               o["starts"], o["row_ends"])
+    rows = range(wl.num_rows)
+    check_logits(logits.cpu().numpy(), want, o["row_ends"], rows)
+    check_topk(top.cpu().numpy(), want, o["row_ends"], wl.topk, rows)
