@@ -84,6 +84,10 @@ constexpr int kScoreThreads = 32 * (kFirstCopyWarp + kCopyWarps);
 // Page ids handed from warp 0 to the copy warps: a ring of kPageRing entries
 // {first page, second page} (>= 0 page, kNoPage none, kEndMark end of sequence).
 constexpr int kPageRing = 64, kNoPage = -1, kEndMark = -2;
+// The planner stays at most kLead positions ahead of the copy warps (the
+// ring entry it overwrites, kPageRing positions back, is older still).
+constexpr int kLead = 56;
+static_assert(kLead < kPageRing, "the ring holds the planner's lead");
 static_assert(kStages % kCopyWarps == 0 && kMaxStages % kCopyWarps == 0, "copy warp c owns the stages of its residue");
 static_assert(kMmaWarps == kEpiGroups && kStages % kMmaWarps == 0 && kMaxStages % kMmaWarps == 0,
               "issuer w owns stages and group w");
@@ -109,9 +113,11 @@ constexpr int kHistFlushTiles = 256;
 constexpr int OFF_HIST = OFF_W + kEpiWarps * 128 * 4;   // per warp: segment rows x heads <= 128 weights
 constexpr int kGroupHistWords = kSegRows * kHistBins / 2;
 // int4[kMaxStages]: {tile in segment, segment, segment ordinal in this CTA's sequence}
+// int4[2 * kMaxStages]: per stage {tile in segment, segment, segment ordinal, 0}, {first row, rows, 0, 0}
 constexpr int OFF_SINFO = OFF_HIST + kEpiGroups * kGroupHistWords * 4;
-constexpr int OFF_AINFO = OFF_SINFO + kMaxStages * 16;       // int2[kAcc]: {tile in segment, segment} per accumulator
-constexpr int OFF_PRING = OFF_AINFO + ((kAcc * 8 + 15) / 16) * 16;   // int4[2 * kPageRing]
+// int4[kAcc]: {tile in segment, segment, first row, rows} per accumulator
+constexpr int OFF_AINFO = OFF_SINFO + kMaxStages * 32;
+constexpr int OFF_PRING = OFF_AINFO + kAcc * 16;   // int4[2 * kPageRing]
 constexpr int OFF_BAR = OFF_PRING + kPageRing * 32;
 // full, empty, qfull, tfull (per accumulator and epilogue group), done.  A
 // group's accumulator barrier is used by the sequence positions it, it + 6, ...
@@ -120,9 +126,10 @@ constexpr int OFF_BAR = OFF_PRING + kPageRing * 32;
 // MMAs complete in no common order) and its parity wait would take it.
 constexpr int kNumBars = 2 * kMaxStages + 2 + kAcc * kEpiGroups + 1;
 // TMEM address, abort flag, released[kAcc] at +16, page ring published at +32,
-// consumed[kCopyWarps] (entries each copy warp has taken) at +48
+// consumed[kCopyWarps] (entries each copy warp has taken) at +48, then
+// armed[kCopyWarps] (positions each copy warp has passed the free-stage wait for)
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
-constexpr int kScoreSmem = OFF_MISC + 48 + 4 * kCopyWarps + 1024;   // + slack to align the base to 1024
+constexpr int kScoreSmem = OFF_MISC + 48 + 8 * kCopyWarps + 1024;   // + slack to align the base to 1024
 static_assert(kScoreSmem <= 227 * 1024, "scoring CTA exceeds the shared memory of an SM");
 
 // TMEM columns: kAcc accumulators of up to 128 columns, then scale factors.
@@ -163,6 +170,7 @@ struct ScoreArgs {
     int64_t qs_stride;
     int qs_group_major;        // scale of block g of head h at g * 64 + h (else at h * 4 + g)
     int64_t w_stride;          // BF16 head weights of row r at w + r * w_stride
+    int rows;                  // query rows of the call
 };
 
 // Segment s with prefix[s] <= t < prefix[s + 1] (prefix[S] > t).
@@ -399,33 +407,40 @@ __device__ __forceinline__ bool count_wait(const uint32_t* c, uint32_t need, vol
 
 // Copies the codes of page h (0 or 1) of a tile, id pid, into stage s (FP8:
 // one 128-byte-swizzled box; MXFP4: one 64-byte-swizzled box; row-group: one
-// box per column group, group g at g * 2048 + h * 1024).
+// box per column group, group g at g * 2048 + h * 1024).  Key pages are read
+// once per step, so they are loaded with an evict-first L2 policy: the step's
+// logits, histograms and block tables stay in L2 for the kernels after it.
 __device__ __forceinline__ void issue_codes(const CUtensorMap* kmap, uint8_t* smem, uint64_t* bar, int s,
-                                            int stage_bytes, bool fp4, bool rg, int h, int pid) {
+                                            int stage_bytes, bool fp4, bool rg, int h, int pid, uint64_t pol) {
     uint8_t* dst = smem + OFF_TILES + s * stage_bytes;
     if (rg) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) tma_load_4d(dst + g * kRgTileGroup + h * kRgGroupBytes, kmap, 0, 0, g, pid, bar);
+        for (int g = 0; g < 4; ++g)
+            tma_load_4d_hint(dst + g * kRgTileGroup + h * kRgGroupBytes, kmap, 0, 0, g, pid, bar, pol);
     } else {
-        tma_load_3d(dst + h * (fp4 ? kFp4KeyBytes : kPageSmem), kmap, 0, 0, pid, bar);
+        tma_load_3d_hint(dst + h * (fp4 ? kFp4KeyBytes : kPageSmem), kmap, 0, 0, pid, bar, pol);
     }
 }
 // Copies the 256 scale bytes of page h of a tile into stage s.
 __device__ __forceinline__ void issue_scales(const CUtensorMap* smap, uint8_t* smem, uint64_t* bar, int s, int h,
-                                             int pid) {
-    tma_load_2d(smem + OFF_RAWSC + s * 512 + h * 256, smap, 0, pid, bar);
+                                             int pid, uint64_t pol) {
+    tma_load_2d_hint(smem + OFF_RAWSC + s * 512 + h * 256, smap, 0, pid, bar, pol);
 }
 
-// Prepares one tile (lane 0 of the producer warp): the segment's query rows
-// when the segment changes, then the next ring stage, tagged with {tile in
-// segment, segment, segment ordinal}; the page ids go to the tile's copy
-// warp, which copies its pages.
+// Warp 0 lays out this CTA's sequence of tiles (positions 0, 1, ...): each
+// position's ring entry {first page, second page, tile in segment, segment},
+// {segment ordinal} is written by lane 0, and a batch of entries is made
+// visible to the copy warps with one release.  On a segment change it loads
+// the segment's query rows into query buffer (ordinal & 1).
 //
 // Query buffer b holds the segments of ordinals b, b + 2, ...  Before it is
 // refilled, the MMAs of the segment it held must be done: every issuer's last
 // tile of that segment has released its ring stage (an issuer's MMAs complete
-// in order), which the producer waits for unless it has already waited for
-// that release when it refilled the stage.
+// in order).  The planner runs ahead of the stages (up to the ring's length),
+// so a release is recognised either on the stage's empty barrier (the phase
+// of that position's use) or, once the stage has been taken again, by the
+// copy warp that owns the position kStages later having passed its wait for
+// it (armed counts; kStages is a multiple of the copy warps).
 struct Producer {
     const CUtensorMap* kmap;
     const CUtensorMap* smap;
@@ -439,24 +454,58 @@ struct Producer {
     bool rg;             // row-group placement: packed boxes per column group
     int lg;              // log2 of the ring's stage count
     int stage_bytes;     // shared memory of a stage's codes
-    int4* page_ring;     // per position: {first page, second page, tile in segment, segment}, {ordinal}
-    uint32_t* published; // entries written (release)
+    int4* page_ring;     // per position: {first page, second page, tile in segment, segment}, {ordinal, first row, rows}
+    uint32_t* published; // entries made visible (release)
     const uint32_t* consumed;   // [kCopyWarps]: entries each copy warp has taken (acquire)
-    int cur = -1, i_seg = 0, it = 0;
+    const uint32_t* armed;      // [kCopyWarps]: positions each copy warp has passed the free-stage wait for
+    int cur = -1, i_seg = 0, it = 0, pub = 0;
 
-    // Hands position it's page ids to its copy warp (ring of kPageRing); the
-    // entry's previous occupant, position it - kPageRing, must have been taken.
-    __device__ __forceinline__ bool publish(const ScoreArgs& p, int4 v, int ord) {
-        if (it >= kPageRing) {
-            const int old = it - kPageRing;
-            if (!count_wait(consumed + (old % kCopyWarps), static_cast<uint32_t>(old / kCopyWarps + 1), abort,
-                            p.status))
-                return false;
+    // Makes the entries written so far visible to the copy warps.
+    __device__ __forceinline__ void flush() {
+        if (it > pub) {
+            smem_add_release(published, static_cast<uint32_t>(it - pub));
+            pub = it;
         }
-        page_ring[2 * (it & (kPageRing - 1))] = v;
-        page_ring[2 * (it & (kPageRing - 1)) + 1] = make_int4(ord, 0, 0, 0);
-        smem_add_release(published, 1u);
-        return true;
+    }
+    // Room for position it: the copy warps have taken position it - kLead and
+    // the ring entry it overwrites, it - kPageRing.
+    __device__ __forceinline__ bool taken(const ScoreArgs& p, int old) {
+        if (old < 0) return true;
+        if (static_cast<int>(smem_ld_acquire(consumed + (old % kCopyWarps)) - (old / kCopyWarps + 1)) >= 0)
+            return true;
+        flush();   // the copy warps must see the pending entries to make room
+        return count_wait(consumed + (old % kCopyWarps), static_cast<uint32_t>(old / kCopyWarps + 1), abort,
+                          p.status);
+    }
+    __device__ __forceinline__ bool room(const ScoreArgs& p) {
+        return taken(p, it - kLead) && taken(p, it - kPageRing);
+    }
+    // Bounded wait for the release of position l's stage use (its MMAs are done).
+    // The stage's empty barrier completes one phase per use; its parity names
+    // l's phase only while the stage is in l's use: after the copy warp owning
+    // l has taken the stage for l (armed covers l) and before it takes it again
+    // for l + stages (armed covers that, and l's release came before).
+    __device__ __forceinline__ bool released(const ScoreArgs& p, int l) {
+        const int stages = 1 << lg;
+        const int c = l % kCopyWarps;
+        const uint32_t started = static_cast<uint32_t>((l - c) / kCopyWarps + 1);
+        const uint32_t need = static_cast<uint32_t>((l + stages - c) / kCopyWarps + 1);
+        uint64_t* bar = empty + (l & (stages - 1));
+        const uint32_t parity = (l >> lg) & 1;
+        const unsigned long long t0 = globaltimer();
+        for (uint32_t i = 0;; ++i) {
+            const uint32_t a = smem_ld_acquire(armed + c);
+            if (static_cast<int>(a - need) >= 0) return true;
+            if (static_cast<int>(a - started) >= 0 && mbar_test_wait(bar, parity)) return true;
+            if ((i & 63) == 63) {
+                if (*abort) return false;
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    *abort = 1;
+                    if (p.status) atomicOr(p.status, DSA_STATUS_TIMEOUT);
+                    return false;
+                }
+            }
+        }
     }
     int last00 = -1, last01 = -1, last10 = -1, last11 = -1;   // last tile of query buffer b for issuer w
 
@@ -471,18 +520,17 @@ struct Producer {
         }
     }
 
-    __device__ __forceinline__ bool issue(const ScoreArgs& p, int sg, int j, int p0, int p1, int row0, int nrows) {
+    // Lane 0: writes position it's entry (loading the segment's queries first
+    // when the segment changes); the entry becomes visible at the next flush.
+    __device__ __forceinline__ bool add(const ScoreArgs& p, int sg, int j, int p0, int p1, int row0, int nrows) {
         if (sg != cur) {
             cur = sg;
             const int2 si = make_int2(row0, nrows);
             const int qb = i_seg & 1;
+            flush();   // the tiles before the change can be copied while this waits
             for (int w = 0; w < kMmaWarps; ++w) {
-                // release of tile l: round l >> lg of its stage's empty barrier; while
-                // it - l <= stages the stage's next use is not yet issued
                 const int l = last_tile(qb, w);
-                if (l >= 0 && it - l <= (1 << lg) &&
-                    !mbar_wait(empty + (l & ((1 << lg) - 1)), (l >> lg) & 1, abort, p.status))
-                    return false;
+                if (l >= 0 && !released(p, l)) return false;
                 set_last_tile(qb, w, -1);
             }
             const uint32_t qsf = p.qs_group_major ? kQsfRowRg : kQsfRow;
@@ -506,13 +554,14 @@ struct Producer {
             }
             ++i_seg;
         }
-        const int s = it & ((1 << lg) - 1);
-        if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
+        if (!room(p)) return false;
         set_last_tile((i_seg - 1) & 1, it % kMmaWarps, it);
         // the copy warp writes the stage's tag and arms its full barrier for the
         // tile's bytes (a tile without valid pages: scores of its keys are unspecified)
-        if (!publish(p, make_int4(p0 >= 0 ? p0 : kNoPage, p1 >= 0 ? p1 : kNoPage, j, sg), i_seg - 1)) return false;
+        page_ring[2 * (it & (kPageRing - 1))] = make_int4(p0 >= 0 ? p0 : kNoPage, p1 >= 0 ? p1 : kNoPage, j, sg);
+        page_ring[2 * (it & (kPageRing - 1)) + 1] = make_int4(i_seg - 1, row0, nrows, 0);
         ++it;
+        if (it - pub >= kCopyWarps) flush();   // one release per kCopyWarps entries
         return true;
     }
 
@@ -522,11 +571,12 @@ struct Producer {
     static_assert(kCopyWarps >= kMmaWarps, "every issuer meets an end tag");
     __device__ __forceinline__ bool finish(const ScoreArgs& p) {
         for (int w = 0; w < kCopyWarps; ++w) {
-            const int s = it & ((1 << lg) - 1);
-            if (!mbar_wait(empty + s, ((it >> lg) & 1) ^ 1, abort, p.status)) return false;
-            if (!publish(p, make_int4(kEndMark, kEndMark, -1, -1), -1)) return false;
+            if (!room(p)) return false;
+            page_ring[2 * (it & (kPageRing - 1))] = make_int4(kEndMark, kEndMark, -1, -1);
+            page_ring[2 * (it & (kPageRing - 1)) + 1] = make_int4(-1, 0, 0, 0);
             ++it;
         }
+        flush();
         return true;
     }
 };
@@ -551,19 +601,19 @@ __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, 
                 const int p1 = __shfl_sync(0xFFFFFFFFu, mine.pid1, i);
                 const int r0 = __shfl_sync(0xFFFFFFFFu, mine.row0, i);
                 const int nr = __shfl_sync(0xFFFFFFFFu, mine.nrows, i);
-                if (lane == 0) ok = pr.issue(p, sg, j, p0, p1, r0, nr);
+                if (lane == 0) ok = pr.add(p, sg, j, p0, p1, r0, nr);
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             }
+            if (lane == 0) pr.flush();   // one release per batch
         }
     }
     if (lane == 0) {
         if (ok) pr.finish(p);
-        // Drain: every copy issued must have landed before the CTA exits.
-        const int it = pr.it, i_seg = pr.i_seg, lg = pr.lg;
+        // Drain: the query rows this warp loaded must have landed before the CTA
+        // exits (no later load reuses a buffer, so the last phases are unambiguous).
+        const int i_seg = pr.i_seg;
         const unsigned long long deadline = globaltimer() + kWaitLimitNs;
         bool drained = true;
-        for (int i = max(0, it - (1 << lg)); i < it && drained; ++i)
-            drained = mbar_drain(pr.full + (i & ((1 << lg) - 1)), (i >> lg) & 1, deadline, p.status);
         for (int i = max(0, i_seg - 2); i < i_seg && drained; ++i)
             drained = mbar_drain(pr.qfull + (i & 1), (i >> 1) & 1, deadline, p.status);
     }
@@ -571,47 +621,59 @@ __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, 
 }
 
 // Copy warp c (warp kFirstCopyWarp + c).  Follows warp 0's positions c, c +
-// kCopyWarps, ... through the page ring and copies each tile's two pages (codes
-// and scales) into its stage, arming the stage's full barrier for those bytes
-// (it waits for the same free-stage phase as warp 0; the stage cannot move on
-// before this warp's arrival).
+// kCopyWarps, ... through the page ring: waits for the position's stage to be
+// free (and counts that in armed[c]), writes the stage's tag, and copies the
+// tile's two pages (codes and scales) into it, arming the stage's full
+// barrier for those bytes.  Its stages are its own (the ring's stage count is
+// a multiple of the copy warps), so on the way out it drains the copies of its
+// last uses of them without ambiguity.
 __device__ __forceinline__ void copy_role(const ScoreArgs& p, const CUtensorMap* kmap, const CUtensorMap* smap,
                                           uint8_t* smem, uint64_t* full, uint64_t* empty, const uint32_t* published,
-                                          uint32_t* consumed, volatile int* abort, int c) {
+                                          uint32_t* consumed, uint32_t* armed, volatile int* abort, int c) {
     if ((threadIdx.x & 31) != 0) return;
     const bool fp4 = fmt_fp4(p.fmt), rg = (p.fmt == DSA_FMT_MXFP4_RG);
     const int lg = ring_stages_log2(p.fmt), stage_bytes = ring_stage_bytes(p.fmt);
     const uint32_t page_tx = (fp4 ? kFp4PageTx : kFp8PageTx) + 256u;
+    const uint64_t pol = l2_evict_first_policy();
     const int4* ring = reinterpret_cast<const int4*>(smem + OFF_PRING);
     int4* sinfo = reinterpret_cast<int4*>(smem + OFF_SINFO);
+    int last_j = -1;   // the last position whose full barrier this warp arrived on
     for (int j = c;; j += kCopyWarps) {
         if (!count_wait(published, static_cast<uint32_t>(j + 1), abort, p.status)) break;
         const int4 v = ring[2 * (j & (kPageRing - 1))];
-        const int ord = ring[2 * (j & (kPageRing - 1)) + 1].x;
+        const int4 vs = ring[2 * (j & (kPageRing - 1)) + 1];   // {ordinal, first row, rows}
         smem_add_release(consumed + c, 1u);
         const int s = j & ((1 << lg) - 1);
         if (!mbar_wait(empty + s, ((j >> lg) & 1) ^ 1, abort, p.status)) break;
+        smem_add_release(armed + c, 1u);   // position j - stages is released
         // the stage's tag: {tile in segment, segment, segment ordinal}; -1 ends an issuer's sequence
-        sinfo[s] = v.x == kEndMark ? make_int4(-1, -1, -1, 0) : make_int4(v.z, v.w, ord, 0);
+        sinfo[2 * s] = v.x == kEndMark ? make_int4(-1, -1, -1, 0) : make_int4(v.z, v.w, vs.x, 0);
+        sinfo[2 * s + 1] = make_int4(vs.y, vs.z, 0, 0);
         if (v.x == kEndMark) {
             mbar_arrive(full + s);
+            last_j = j;
             break;
         }
         const uint32_t bytes = (v.x >= 0 ? page_tx : 0u) + (v.y >= 0 ? page_tx : 0u);
         if (bytes) {
             mbar_arrive_expect_tx(full + s, bytes);
             if (v.x >= 0) {
-                issue_codes(kmap, smem, full + s, s, stage_bytes, fp4, rg, 0, v.x);
-                issue_scales(smap, smem, full + s, s, 0, v.x);
+                issue_codes(kmap, smem, full + s, s, stage_bytes, fp4, rg, 0, v.x, pol);
+                issue_scales(smap, smem, full + s, s, 0, v.x, pol);
             }
             if (v.y >= 0) {
-                issue_codes(kmap, smem, full + s, s, stage_bytes, fp4, rg, 1, v.y);
-                issue_scales(smap, smem, full + s, s, 1, v.y);
+                issue_codes(kmap, smem, full + s, s, stage_bytes, fp4, rg, 1, v.y, pol);
+                issue_scales(smap, smem, full + s, s, 1, v.y, pol);
             }
         } else {
             mbar_arrive(full + s);
         }
+        last_j = j;
     }
+    // every copy issued must have landed before the CTA exits
+    const unsigned long long deadline = globaltimer() + kWaitLimitNs;
+    for (int jj = last_j; jj >= 0 && jj > last_j - (1 << lg); jj -= kCopyWarps)
+        if (!mbar_drain(full + (jj & ((1 << lg) - 1)), (jj >> lg) & 1, deadline, p.status)) break;
 }
 
 // Warps 1 .. kMmaWarps.  Issuer w follows the stage tags of sequence
@@ -638,19 +700,20 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
     const int lg = ring_stages_log2(p.fmt);
     const int stage_bytes = ring_stage_bytes(p.fmt);
     const int4* sinfo = reinterpret_cast<const int4*>(smem + OFF_SINFO);
-    int2* ainfo = reinterpret_cast<int2*>(smem + OFF_AINFO);
+    int4* ainfo = reinterpret_cast<int4*>(smem + OFF_AINFO);
     int cur = -1, qb = 0, nrows = 0;
     for (int it = w;; it += kMmaWarps) {
         const int s = it & ((1 << lg) - 1);
         const int a = it % kAcc;
         const uint32_t need = 4u * static_cast<uint32_t>(it / kAcc);   // releases of its earlier uses
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(full + s, (it >> lg) & 1, abort, p.status))) break;
-        const int4 tag = sinfo[s];
+        const int4 tag = sinfo[2 * s];
+        const int4 rowinfo = sinfo[2 * s + 1];   // the segment's {first row, rows}
         if (tag.y < 0) {
             // this issuer's epilogue group takes the end tag
             if (!__all_sync(0xFFFFFFFFu, count_wait(released + a, need, abort, p.status))) break;
             if (lane == 0) {
-                ainfo[a] = make_int2(tag.x, tag.y);
+                ainfo[a] = make_int4(tag.x, tag.y, 0, 0);
                 mbar_arrive(tfull + a * kEpiGroups + w);
                 mbar_arrive(tfull + a * kEpiGroups + w);
             }
@@ -659,7 +722,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
         }
         if (tag.z != cur) {
             cur = tag.z;
-            nrows = p.segs[tag.y].z;
+            nrows = rowinfo.y;
             qb = cur & 1;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(qfull + qb, (cur >> 1) & 1, abort, p.status))) break;
             if (block_scaled) {
@@ -763,7 +826,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                     tc_mma_mxf4(d, ad + 2 * m, bd + 2 * m, idesc_mx(kMmaMxf4E2M1, kMmaMxf4E2M1, 128, n, 2 * m, 2 * m),
                                 sfa, sfb, m > 0);
             }
-            ainfo[a] = make_int2(tag.x, tag.y);
+            ainfo[a] = make_int4(tag.x, tag.y, rowinfo.x, rowinfo.y);
             tc_commit(empty + s);
             tc_commit(tfull + a * kEpiGroups + w);
             mbar_arrive(tfull + a * kEpiGroups + w);   // releases the key scales and the tag written above
@@ -864,7 +927,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
     const int quarter = warp & 3;            // TMEM lanes this warp may access
     const int m = quarter * 32 + lane;       // key of the tile this thread owns
     float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - kFirstEpiWarp) * 128;
-    const int2* ainfo = reinterpret_cast<const int2*>(smem + OFF_AINFO);
+    const int4* ainfo = reinterpret_cast<const int4*>(smem + OFF_AINFO);
     const bool f32scale = (p.fmt == DSA_FMT_FP8);   // FP32 key scale (FP8-MX scales act inside the MMA)
     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC;
     uint32_t* gh = reinterpret_cast<uint32_t*>(smem + OFF_HIST) + group * kGroupHistWords;
@@ -872,6 +935,13 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
     int cur = -1, row0 = 0, nrows = 0, seg_tiles = 0;
     int end_l = 0;        // lane r < nrows: bound of row row0 + r
     unsigned hist_m = 0;  // bit r: row r gets a histogram
+    // the next segment's weights (element lane + 32 i of its rows x H) and bounds, loaded ahead
+    constexpr int kPfRows = H > 32 ? 128 / H : kSegRows;
+    constexpr int kPfPerLane = kPfRows * H / 32;
+    int pf_row0 = -1, pf_end = 0;
+    float pf_w[kPfPerLane];
+#pragma unroll
+    for (int i = 0; i < kPfPerLane; ++i) pf_w[i] = 0.0f;
     bool aborted = false;
     for (int it = group;; it += kEpiGroups) {
         const int a = it % kAcc;
@@ -883,7 +953,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
             break;
         }
         tc_fence_after();
-        const int2 tag = ainfo[a];   // {tile in segment, segment}; segment -1 ends the sequence
+        const int4 tag = ainfo[a];   // {tile in segment, segment, first row, rows}; segment -1 ends the sequence
         if (tag.y < 0) break;
         if (tag.y != cur || seg_tiles == kHistFlushTiles) {
             if (cur >= 0 && hist_m) flush_group_hist(p, gh, group, row0, nrows, hist_m, e);
@@ -892,14 +962,31 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
         ++seg_tiles;
         if (tag.y != cur) {
             cur = tag.y;
-            const int4 si = p.segs[cur];
-            row0 = si.y;
-            nrows = si.z;
-            for (int i = lane; i < nrows * H; i += 32)
-                wsm[i] = __bfloat162float(p.w[static_cast<int64_t>(row0 + i / H) * p.w_stride + i % H]);
-            end_l = lane < nrows ? p.eff_end[row0 + lane] : 0;
+            row0 = tag.z;
+            nrows = tag.w;
+            if (pf_row0 == row0) {   // prefetched at the previous segment change
+#pragma unroll
+                for (int i = 0; i < kPfPerLane; ++i)
+                    if (lane + 32 * i < nrows * H) wsm[lane + 32 * i] = pf_w[i];
+                end_l = lane < nrows ? pf_end : 0;
+            } else {
+                for (int i = lane; i < nrows * H; i += 32)
+                    wsm[i] = __bfloat162float(p.w[static_cast<int64_t>(row0 + i / H) * p.w_stride + i % H]);
+                end_l = lane < nrows ? p.eff_end[row0 + lane] : 0;
+            }
             hist_m = __ballot_sync(0xFFFFFFFFu, lane < nrows && p.hist_k >= 0 && end_l > p.hist_k);
             __syncwarp();
+            // Segments lie in row order, so the next one most likely starts at row
+            // row0 + nrows: its weights and bounds are loaded now and used at the
+            // next change (the loads complete while the tiles in between are drained).
+            pf_row0 = row0 + nrows;
+#pragma unroll
+            for (int i = 0; i < kPfPerLane; ++i) {
+                const int r = pf_row0 + (lane + 32 * i) / H;
+                pf_w[i] = r < p.rows ? __bfloat162float(p.w[static_cast<int64_t>(r) * p.w_stride + (lane + 32 * i) % H])
+                                     : 0.0f;
+            }
+            pf_end = (lane < kPfRows && pf_row0 + lane < p.rows) ? p.eff_end[pf_row0 + lane] : 0;
         }
         const float ksm = f32scale ? reinterpret_cast<const float*>(smem + OFF_KS + a * 512)[m] : 1.0f;
         const int tpos = tag.x * kTileRows + m;
@@ -953,6 +1040,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     uint32_t* released = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 16);   // per accumulator
     uint32_t* published = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 32);
     uint32_t* consumed = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 48);   // per copy warp
+    uint32_t* armed = consumed + kCopyWarps;                                   // per copy warp
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
@@ -964,7 +1052,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         for (int b = 0; b < kAcc * kEpiGroups; ++b) mbar_init(tfull + b, 2);
         for (int b = 0; b < kAcc; ++b) released[b] = 0u;
         *published = 0u;
-        for (int c = 0; c < kCopyWarps; ++c) consumed[c] = 0u;
+        for (int c = 0; c < kCopyWarps; ++c) consumed[c] = armed[c] = 0u;
         mbar_init(done_bar, kMmaWarps);
         *abort = 0;
         mbar_fence_init();
@@ -1001,7 +1089,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     ring_stage_bytes(args.fmt),
                     reinterpret_cast<int4*>(smem + OFF_PRING),
                     published,
-                    consumed};
+                    consumed,
+                    armed};
         producer_role(pr, args, t0, t1, seg, S);
     } else if (warp < kFirstEpiWarp) {
         mma_role(args, smem, tmem, full, empty, qfull, tfull, released, done_bar, abort);
@@ -1010,7 +1099,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         else if (args.heads == 64) epilogue_role<64>(args, smem, tmem, tfull, released, abort);
         else epilogue_role<32>(args, smem, tmem, tfull, released, abort);
     } else {
-        copy_role(args, &kmap, &smap, smem, full, empty, published, consumed, abort, warp - kFirstCopyWarp);
+        copy_role(args, &kmap, &smap, smem, full, empty, published, consumed, armed, abort, warp - kFirstCopyWarp);
     }
     tc_fence_before();
     __syncthreads();
@@ -1207,6 +1296,7 @@ static int score_paged_impl(int fmt, const QueryOperands& qo, const void* cache,
     a.qs_stride = qo.qs_stride;
     a.qs_group_major = qo.qs_group_major ? 1 : 0;
     a.w_stride = qo.w_stride;
+    a.rows = static_cast<int>(rows);
     if (g_time_before && g_time_after)   // external: kept as a record node under stream capture
         cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_time_before), stream, cudaEventRecordExternal);
     if (launch_pdl(score_kernel, dim3(grid), dim3(kScoreThreads), kScoreSmem, stream, kmap, smap, qmap,
