@@ -138,16 +138,23 @@ constexpr uint32_t TM_SFA = kAcc * 128;              // kMaxStages x 4 columns
 constexpr uint32_t TM_SFB = TM_SFA + 4 * kMaxStages; // (2 buffers x kMmaWarps) x 4 columns
 constexpr uint32_t TM_COLS = 512;
 
-// Ring geometry of a format: packed MXFP4 tiles (either placement) take half
-// the shared memory of FP8 ones, so twice as many are in flight.
-// Stage counts are powers of two: position it uses stage it & (n - 1) in its
-// (it >> log2 n)-th round (no division on the per-tile paths).
-__host__ __device__ __forceinline__ int ring_stages_log2(int fmt) { return fmt_fp4(fmt) ? 4 : 3; }
-static_assert(kStages == 1 << 3 && kMaxStages == 1 << 4, "stage counts as their log2 above");
-__host__ __device__ __forceinline__ int ring_stage_bytes(int fmt) {
-    return fmt_fp4(fmt) ? kTileBytes / 2 : kTileBytes;
-}
+// Compile-time traits of a cache format: each (format, heads) pair is its own
+// kernel, so a kernel holds only its own format's code (a smaller instruction
+// footprint for its fifteen warps of five roles).  Ring geometry: packed MXFP4
+// tiles (either placement) take half the shared memory of FP8 ones, so twice
+// as many are in flight.  Stage counts are powers of two: position it uses
+// stage it & (n - 1) in its (it >> lg)-th round (no division on the per-tile paths).
+static_assert(kStages == 1 << 3 && kMaxStages == 1 << 4, "stage counts as their log2 below");
 static_assert(kMaxStages * (kTileBytes / 2) == kStages * kTileBytes, "both rings fill the tile area");
+template <int F>
+struct FmtT {
+    static constexpr bool fp4 = F == DSA_FMT_MXFP4 || F == DSA_FMT_MXFP4_RG;
+    static constexpr bool rg = F == DSA_FMT_MXFP4_RG;
+    static constexpr bool fp8mx = F == DSA_FMT_FP8_MX;
+    static constexpr bool key_scale = F == DSA_FMT_FP8;   // FP32 key scale applied in the epilogue
+    static constexpr int lg = fp4 ? 4 : 3;
+    static constexpr int stage_bytes = fp4 ? kTileBytes / 2 : kTileBytes;
+};
 
 struct ScoreArgs {
     int fmt;
@@ -441,7 +448,13 @@ __device__ __forceinline__ void issue_scales(const CUtensorMap* smap, uint8_t* s
 // of that position's use) or, once the stage has been taken again, by the
 // copy warp that owns the position kStages later having passed its wait for
 // it (armed counts; kStages is a multiple of the copy warps).
+template <int F, int H>
 struct Producer {
+    using T = FmtT<F>;
+    static constexpr bool fp4 = T::fp4;            // MXFP4 codes (either placement): transaction sizes
+    static constexpr bool rg = T::rg;              // row-group placement: packed boxes per column group
+    static constexpr int lg = T::lg;               // log2 of the ring's stage count
+    static constexpr int stage_bytes = T::stage_bytes;   // shared memory of a stage's codes
     const CUtensorMap* kmap;
     const CUtensorMap* smap;
     const CUtensorMap* qmap;
@@ -450,10 +463,6 @@ struct Producer {
     uint64_t* empty;
     uint64_t* qfull;
     volatile int* abort;
-    bool fp4;            // MXFP4 codes (either placement): transaction sizes
-    bool rg;             // row-group placement: packed boxes per column group
-    int lg;              // log2 of the ring's stage count
-    int stage_bytes;     // shared memory of a stage's codes
     int4* page_ring;     // per position: {first page, second page, tile in segment, segment}, {ordinal, first row, rows}
     uint32_t* published; // entries made visible (release)
     const uint32_t* consumed;   // [kCopyWarps]: entries each copy warp has taken (acquire)
@@ -534,7 +543,7 @@ struct Producer {
                 set_last_tile(qb, w, -1);
             }
             const uint32_t qsf = p.qs_group_major ? kQsfRowRg : kQsfRow;
-            const uint32_t qrow = fp4 ? 64u * p.heads : kFp8QRowTx;   // packed MXFP4: heads x 64 B
+            const uint32_t qrow = fp4 ? 64u * H : kFp8QRowTx;   // packed MXFP4: heads x 64 B
             const uint32_t bytes = si.y * (fp4 ? qrow + qsf : qrow);
             mbar_arrive_expect_tx(qfull + qb, bytes);
             uint8_t* qdst = smem + OFF_QBUF + qb * kQBufBytes;
@@ -543,7 +552,7 @@ struct Producer {
                     // packed: 16-byte column chunk c of every head at c * 2048 + (r * heads + h) * 16
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        tma_load_3d(qdst + c * kRgQChunk + r * 16 * p.heads, qmap, 16 * c, 0, si.x + r, qfull + qb);
+                        tma_load_3d(qdst + c * kRgQChunk + r * 16 * H, qmap, 16 * c, 0, si.x + r, qfull + qb);
                 } else {
                     // FP8 rows of 4096 bytes, packed MXFP4 rows of heads x 64 B
                     tma_load_3d(qdst + r * qrow, qmap, 0, 0, si.x + r, qfull + qb);
@@ -584,7 +593,9 @@ struct Producer {
 // Warp 0.  Its 32 lanes resolve the segments and block-table entries of 32
 // tiles at once (the next batch's loads are in flight while lane 0 issues the
 // current batch's tiles), so block-table latency is paid once per batch.
-__device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, int t0, int t1, int seg, int S) {
+template <int F, int H>
+__device__ __forceinline__ void producer_role(Producer<F, H>& pr, const ScoreArgs& p, int t0, int t1, int seg,
+                                              int S) {
     const int lane = threadIdx.x & 31;
     bool ok = true;
     if (t0 < t1) {
@@ -627,12 +638,13 @@ __device__ __forceinline__ void producer_role(Producer& pr, const ScoreArgs& p, 
 // barrier for those bytes.  Its stages are its own (the ring's stage count is
 // a multiple of the copy warps), so on the way out it drains the copies of its
 // last uses of them without ambiguity.
+template <int F>
 __device__ __forceinline__ void copy_role(const ScoreArgs& p, const CUtensorMap* kmap, const CUtensorMap* smap,
                                           uint8_t* smem, uint64_t* full, uint64_t* empty, const uint32_t* published,
                                           uint32_t* consumed, uint32_t* armed, volatile int* abort, int c) {
     if ((threadIdx.x & 31) != 0) return;
-    const bool fp4 = fmt_fp4(p.fmt), rg = (p.fmt == DSA_FMT_MXFP4_RG);
-    const int lg = ring_stages_log2(p.fmt), stage_bytes = ring_stage_bytes(p.fmt);
+    constexpr bool fp4 = FmtT<F>::fp4, rg = FmtT<F>::rg;
+    constexpr int lg = FmtT<F>::lg, stage_bytes = FmtT<F>::stage_bytes;
     const uint32_t page_tx = (fp4 ? kFp4PageTx : kFp8PageTx) + 256u;
     const uint64_t pol = l2_evict_first_policy();
     const int4* ring = reinterpret_cast<const int4*>(smem + OFF_PRING);
@@ -682,6 +694,7 @@ __device__ __forceinline__ void copy_role(const ScoreArgs& p, const CUtensorMap*
 // used by both issuers in turn, so its release is a count (four epilogue
 // warps per use) rather than an mbarrier phase, which an issuer running
 // ahead could mistake for a later one.
+template <int F, int H>
 __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* full,
                                          uint64_t* empty, uint64_t* qfull, uint64_t* tfull, const uint32_t* released,
                                          uint64_t* done_bar, volatile int* abort) {
@@ -692,13 +705,12 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
     // columns 32b..32b+31: the block-scaled FP8 MMA applies byte kk in its
     // instruction kk (K = 32), the query's scales being 1 (its scale is folded
     // into the head weights).  MXFP4 uses the block-scaled FP4 MMA.
-    const bool key_scale = (p.fmt == DSA_FMT_FP8);
-    const bool fp8mx = (p.fmt == DSA_FMT_FP8_MX);
-    const bool fp4 = fmt_fp4(p.fmt);
-    const bool block_scaled = !key_scale;
-    const bool rg = (p.fmt == DSA_FMT_MXFP4_RG);
-    const int lg = ring_stages_log2(p.fmt);
-    const int stage_bytes = ring_stage_bytes(p.fmt);
+    constexpr bool key_scale = FmtT<F>::key_scale;
+    constexpr bool fp8mx = FmtT<F>::fp8mx;
+    constexpr bool block_scaled = !key_scale;
+    constexpr bool rg = FmtT<F>::rg;
+    constexpr int lg = FmtT<F>::lg;
+    constexpr int stage_bytes = FmtT<F>::stage_bytes;
     const int4* sinfo = reinterpret_cast<const int4*>(smem + OFF_SINFO);
     int4* ainfo = reinterpret_cast<int4*>(smem + OFF_AINFO);
     int cur = -1, qb = 0, nrows = 0;
@@ -732,7 +744,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
                 // the word of MMA row n: head-major rows hold it as is; group-major
                 // rows hold block g's byte at g * 64 + head; FP8 queries are unscaled (2^0)
                 auto word = [&](int n) -> uint32_t {
-                    const int r = n / p.heads, h = n - r * p.heads;
+                    const int r = n / H, h = n - r * H;
                     if (r >= nrows || fp8mx) return 0x7F7F7F7Fu;
                     if (!p.qs_group_major) return reinterpret_cast<const uint32_t*>(raw + r * kQsfRow)[h];
                     const uint8_t* b = raw + r * kQsfRowRg + h;
@@ -790,7 +802,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& p, uint8_t* smem, uint
             const uint32_t d = tmem + TM_ACC + a * 128;
             const uint32_t ka = smem_u32(smem + OFF_TILES + s * stage_bytes);
             const uint32_t kb = smem_u32(smem + OFF_QBUF + qb * kQBufBytes);
-            const uint32_t n = static_cast<uint32_t>(p.heads * nrows);
+            const uint32_t n = static_cast<uint32_t>(H * nrows);
             if (key_scale) {
                 const uint64_t ad = desc_sw128(ka), bd = desc_sw128(kb);
                 const uint32_t id = idesc_f8f6f4(kMmaE4M3, kMmaE4M3, 128, n);
@@ -919,7 +931,7 @@ __device__ __forceinline__ void flush_group_hist(const ScoreArgs& p, uint32_t* g
 // sequence positions g, g + kEpiGroups, ...; every warp works on its own
 // (per-warp head weights, row bounds in registers, one release count per tile).
 // H query heads: row r of a segment owns accumulator columns r * H .. r * H + H - 1.
-template <int H>
+template <int F, int H>
 __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem, uint32_t tmem, uint64_t* tfull,
                                               uint32_t* released, volatile int* abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -928,7 +940,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
     const int m = quarter * 32 + lane;       // key of the tile this thread owns
     float* wsm = reinterpret_cast<float*>(smem + OFF_W) + (warp - kFirstEpiWarp) * 128;
     const int4* ainfo = reinterpret_cast<const int4*>(smem + OFF_AINFO);
-    const bool f32scale = (p.fmt == DSA_FMT_FP8);   // FP32 key scale (FP8-MX scales act inside the MMA)
+    constexpr bool f32scale = FmtT<F>::key_scale;   // FP32 key scale (FP8-MX scales act inside the MMA)
     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_ACC;
     uint32_t* gh = reinterpret_cast<uint32_t*>(smem + OFF_HIST) + group * kGroupHistWords;
     const int e = threadIdx.x - 32 * kFirstEpiWarp - group * 128;   // thread index within the group
@@ -1024,6 +1036,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& p, uint8_t* smem,
     if (cur >= 0 && !aborted && hist_m) flush_group_hist(p, gh, group, row0, nrows, hist_m, e);
 }
 
+template <int F, int H>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap smap,
                  const __grid_constant__ CUtensorMap qmap, const ScoreArgs args) {
@@ -1075,7 +1088,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int4 range = args.cta[blockIdx.x];   // {first tile, end tile, first segment, segments}
         const int t0 = range.x, t1 = range.y, S = range.w;
         const int seg = (t0 < t1 && range.z < 0) ? find_segment(args.seg_prefix, S, t0) : range.z;
-        Producer pr{&kmap,
+        Producer<F, H> pr{&kmap,
                     &smap,
                     &qmap,
                     smem,
@@ -1083,23 +1096,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     empty,
                     qfull,
                     abort,
-                    fmt_fp4(args.fmt),
-                    args.fmt == DSA_FMT_MXFP4_RG,
-                    ring_stages_log2(args.fmt),
-                    ring_stage_bytes(args.fmt),
                     reinterpret_cast<int4*>(smem + OFF_PRING),
                     published,
                     consumed,
                     armed};
         producer_role(pr, args, t0, t1, seg, S);
     } else if (warp < kFirstEpiWarp) {
-        mma_role(args, smem, tmem, full, empty, qfull, tfull, released, done_bar, abort);
+        mma_role<F, H>(args, smem, tmem, full, empty, qfull, tfull, released, done_bar, abort);
     } else if (warp < kFirstCopyWarp) {
-        if (args.heads == 16) epilogue_role<16>(args, smem, tmem, tfull, released, abort);
-        else if (args.heads == 64) epilogue_role<64>(args, smem, tmem, tfull, released, abort);
-        else epilogue_role<32>(args, smem, tmem, tfull, released, abort);
+        epilogue_role<F, H>(args, smem, tmem, tfull, released, abort);
     } else {
-        copy_role(args, &kmap, &smap, smem, full, empty, published, consumed, armed, abort, warp - kFirstCopyWarp);
+        copy_role<F>(args, &kmap, &smap, smem, full, empty, published, consumed, armed, abort, warp - kFirstCopyWarp);
     }
     tc_fence_before();
     __syncthreads();
@@ -1266,14 +1273,33 @@ static int score_paged_impl(int fmt, const QueryOperands& qo, const void* cache,
                    seg_rows, status) != cudaSuccess)
         return DSA_ERR_CUDA;
 
-    // The kernel's shared-memory limit is an attribute of each device's copy of it.
-    static bool attr_set[64] = {false};
+    // One kernel per (format, heads); its shared-memory limit is an attribute of
+    // each device's copy of it.
+    using ScoreFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const ScoreArgs);
+    ScoreFn fn = nullptr;
+    int variant = 0;
+    switch (fmt) {
+        case DSA_FMT_FP8: fn = score_kernel<DSA_FMT_FP8, 32>; variant = 0; break;
+        case DSA_FMT_FP8_MX: fn = score_kernel<DSA_FMT_FP8_MX, 32>; variant = 1; break;
+        case DSA_FMT_MXFP4:
+            fn = heads == 16 ? score_kernel<DSA_FMT_MXFP4, 16>
+                             : heads == 64 ? score_kernel<DSA_FMT_MXFP4, 64> : score_kernel<DSA_FMT_MXFP4, 32>;
+            variant = 2 + (heads == 16 ? 0 : heads == 64 ? 2 : 1);
+            break;
+        default:
+            fn = heads == 16 ? score_kernel<DSA_FMT_MXFP4_RG, 16>
+                             : heads == 64 ? score_kernel<DSA_FMT_MXFP4_RG, 64> : score_kernel<DSA_FMT_MXFP4_RG, 32>;
+            variant = 5 + (heads == 16 ? 0 : heads == 64 ? 2 : 1);
+            break;
+    }
+    if (!fp4 && heads != 32) return DSA_ERR_UNSUPPORTED;
+    static bool attr_set[64][8] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem) != cudaSuccess)
+    if (!attr_set[dev][variant]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem) != cudaSuccess)
             return DSA_ERR_CUDA;
-        attr_set[dev] = true;
+        attr_set[dev][variant] = true;
     }
     ScoreArgs a;
     a.fmt = fmt;
@@ -1299,8 +1325,7 @@ static int score_paged_impl(int fmt, const QueryOperands& qo, const void* cache,
     a.rows = static_cast<int>(rows);
     if (g_time_before && g_time_after)   // external: kept as a record node under stream capture
         cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_time_before), stream, cudaEventRecordExternal);
-    if (launch_pdl(score_kernel, dim3(grid), dim3(kScoreThreads), kScoreSmem, stream, kmap, smap, qmap,
-                   a) != cudaSuccess)
+    if (launch_pdl(fn, dim3(grid), dim3(kScoreThreads), kScoreSmem, stream, kmap, smap, qmap, a) != cudaSuccess)
         return DSA_ERR_CUDA;
     if (g_time_before && g_time_after)
         cudaEventRecordWithFlags(static_cast<cudaEvent_t>(g_time_after), stream, cudaEventRecordExternal);
