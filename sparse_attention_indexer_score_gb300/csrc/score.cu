@@ -194,7 +194,9 @@ __device__ __forceinline__ int find_segment(const int* prefix, int S, int t) {
 // One CTA: validates request starts and row bounds, splits requests into
 // segments of up to 4 rows and lays their 128-key tiles out in one index space.
 constexpr int kPlanThreads = 256;
-constexpr int kTileCostBase = 4;   // a tile's estimated cost: this + its segment's rows
+// A tile's estimated cost: kTileCostBase + kCostRow * its segment's rows.
+constexpr int kTileCostBase = 3;
+constexpr int kCostRow = 2;
 constexpr int kPlanSmemRows = 4096;   // row bounds the plan keeps on chip
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ starts,
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     if (bad && status) atomicOr(status, DSA_STATUS_BAD_GEOMETRY);
     const int S = min(carry, rows + 1);
     // Tile prefix and, when the segments fit on chip, the prefix of the tiles'
-    // estimated cost (kTileCostBase + the segment's rows per tile; `se` is free now).
+    // estimated cost (kTileCostBase + kCostRow x the segment's rows per tile; `se` is free now).
     const bool weighted = S <= kPlanSmemSegs && S <= kPlanSmemRows;
     carry = 0;
     int wcarry = 0;
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         int tiles = 0, cost = 0;
         if (i < S) {
             tiles = i < kPlanSmemSegs ? sp[i] : (segs[i].w + kTileRows - 1) / kTileRows;
-            if (weighted) cost = tiles * (kTileCostBase + segs[i].z);
+            if (weighted) cost = tiles * (kTileCostBase + kCostRow * segs[i].z);
         }
         const int inc = block_inclusive_scan(tiles, warp_tmp, &chunk_total);
         if (i < S) {
@@ -295,18 +297,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     __syncthreads();
     // Static tile range and first segment of every scoring CTA, so that a CTA
     // starts from one load instead of a search through global memory.  The
-    // ranges split the estimated cost evenly (a tile of a segment of n rows
-    // costs kTileCostBase + n: its copy and MMA, and n rows of epilogue), else
-    // the tiles.
+    // ranges split the estimated cost evenly, else the tiles.  A tile of a
+    // segment of n rows costs kTileCostBase + kCostRow n: its copy and MMA, then
+    // n rows of epilogue.  (3, 2) is the pair that timed best on GB300 over
+    // decode steps mixing segments of 1 to 4 rows; the ratio matters, and it
+    // leaves a 4-row tile at 11/5 of a 1-row one.
+    const bool wfit = static_cast<int64_t>(T) * (kTileCostBase + kCostRow * kSegRows) < 0x7FFFFFFF;   // int prefix holds
     auto tile_at = [&](int c) -> int {   // first tile of CTA c
-        if (!weighted || wcarry == 0) return static_cast<int>(static_cast<int64_t>(c) * T / G);
+        if (!weighted || !wfit || wcarry == 0) return static_cast<int>(static_cast<int64_t>(c) * T / G);
         const int64_t B = static_cast<int64_t>(c) * wcarry / G;
         int lo = 0, hi = S;   // the last segment with se[lo] <= B
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (se[mid] <= B) lo = mid; else hi = mid;
         }
-        const int per = kTileCostBase + segs[lo].z;
+        const int per = kTileCostBase + kCostRow * segs[lo].z;
         return min(sp[lo + 1], sp[lo] + static_cast<int>((B - se[lo]) / per));
     };
     for (int c = threadIdx.x; c < G; c += blockDim.x) {

@@ -525,3 +525,67 @@ def test_score_heads_parity(cuda_lib, fmt, heads, case):
     rows = range(wl.num_rows)
     check_logits(logits.cpu().numpy(), want, o["row_ends"], rows)
     check_topk(top.cpu().numpy(), want, o["row_ends"], wl.topk, rows)
+
+
+@pytest.mark.parametrize("seq", [(5000, 7000), (20000, 30000)])
+def test_topk_all_equal_logits(cuda_lib, seq):
+    """Zero queries make every logit +0: one histogram bin holds a whole row, so
+    the level-3 candidates exceed what a selecting team keeps on chip and, for
+    rows over 8192 keys, the level-1 candidate list overflows and the row is
+    re-read.  Any k distinct positions below the row's bound are correct."""
+    wl = make_workload("tiny_fp8", fmt="fp8", seed=41, R=3, seq=seq, qlen=(1, 2), pad_rows=1, topk=2048)
+    wl.q_bits[:] = 0
+    g = gpu_run(wl)
+    assert g["status"] == 0
+    k = wl.topk
+    for r in range(wl.num_rows):
+        n = int(g["row_ends"][r])
+        assert np.all(g["logits"][r, :n] == 0.0) and np.all(np.isneginf(g["logits"][r, n:]))
+        t = g["topk"][r]
+        if n <= k:
+            assert np.array_equal(t[:n], np.arange(n)) and np.all(t[n:] == -1)
+        else:
+            assert len(set(t.tolist())) == k and t.min() >= 0 and t.max() < n, r
+
+
+@pytest.mark.parametrize("topk", [64, 700])
+def test_topk_few_distinct_logits(cuda_lib, topk):
+    """One non-zero query element against MXFP4 keys: each logit is w * ReLU(q * k_d)
+    with k_d on the E2M1 grid times a power of two, about ten distinct values a
+    row, so 66..454 keys tie in the level-2 boundary bin and the level-3
+    histogram decides; the selected multiset of values is unique."""
+    wl = make_workload("tiny_fp8", fmt="mxfp4", seed=43, R=2, seq=(5000, 7000), qlen=(1, 2), pad_rows=0, topk=topk)
+    q = np.zeros_like(wl.q_bits)
+    q[:, 0, 0] = 0x3F80   # BF16 1.0
+    wl.q_bits[:] = q
+    g = gpu_run(wl)
+    o = oracle_run(wl)
+    assert g["status"] == 0
+    rows = range(wl.num_rows)
+    check_logits(g["logits"], o["scores"], o["row_ends"], rows)
+    check_topk(g["topk"], o["scores"], o["row_ends"], wl.topk, rows)
+
+
+def test_logits_buffer_with_odd_row_stride(cuda_lib):
+    """A caller logits buffer whose rows are not 16-byte aligned (row stride
+    width + 1): the top-k reads it with scalar loads.  Logits equal those of a
+    packed buffer, columns past the buffer's width stay untouched, and the top-k
+    sets agree with the logits."""
+    import torch
+    wl = make_workload("tiny_fp8", fmt="fp8_mx", seed=45, R=3, seq=(3000, 9000), qlen=(1, 3), pad_rows=1, topk=256)
+    g = gpu_run(wl)
+    dev = torch.device("cuda")
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    width = bt.shape[1] * 64
+    big = torch.full((wl.num_rows, width + 1), 7.0, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _, top = cuda_lib.score_paged(wl.fmt, torch.from_numpy(g["q_rows"]).to(dev),
+                                  torch.from_numpy(g["w"]).to(torch.bfloat16).to(dev), g["cache"], g["page_stride"],
+                                  wl.num_pages, bt, torch.from_numpy(g["starts"]).to(dev),
+                                  torch.from_numpy(g["row_ends"]).to(dev), int(wl.query_lens.max()), k=wl.topk,
+                                  status=status, logits=big[:, :width])
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = big.cpu().numpy()
+    assert np.array_equal(got[:, :width], g["logits"]) and np.all(got[:, width] == 7.0)
+    check_topk(top.cpu().numpy(), g["logits"].astype(np.float64), g["row_ends"], wl.topk, range(wl.num_rows))
