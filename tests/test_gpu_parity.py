@@ -589,3 +589,31 @@ def test_logits_buffer_with_odd_row_stride(cuda_lib):
     got = big.cpu().numpy()
     assert np.array_equal(got[:, :width], g["logits"]) and np.all(got[:, width] == 7.0)
     check_topk(top.cpu().numpy(), g["logits"].astype(np.float64), g["row_ends"], wl.topk, range(wl.num_rows))
+
+
+@pytest.mark.parametrize("kind", ["fp8", "mxf4"])
+def test_mma_probe_rate_is_plausible(cuda_lib, kind):
+    """The tensor-core rate probe behind roofline.tensor: its final wait ends
+    (status 0), a longer run takes longer, and the rate lies between a floor and
+    the nominal dense peak (FP8 4.5, FP4 13.5 PFLOP/s per GPU)."""
+    import torch
+    dev = torch.device("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    times = {}
+    for iters in (1 << 14, 1 << 16):
+        cuda_lib.probe_mma(kind, iters, status)   # warm-up
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        cuda_lib.probe_mma(kind, iters, status)
+        b.record()
+        torch.cuda.synchronize()
+        times[iters] = a.elapsed_time(b)
+    assert int(status.item()) == 0
+    assert times[1 << 16] > times[1 << 14]
+    flops = 2 * 128 * 128 * cuda_lib.MMA_K[kind] * (1 << 16) * sms
+    pflops = flops / (times[1 << 16] / 1e3) / 1e15
+    nominal = {"fp8": 4.5, "mxf4": 13.5}[kind]
+    assert 0.1 * nominal < pflops < 1.05 * nominal, pflops
+    with pytest.raises(RuntimeError):
+        cuda_lib.probe_mma(kind, 0, status)
