@@ -617,3 +617,46 @@ def test_mma_probe_rate_is_plausible(cuda_lib, kind):
     assert 0.1 * nominal < pflops < 1.05 * nominal, pflops
     with pytest.raises(RuntimeError):
         cuda_lib.probe_mma(kind, 0, status)
+
+
+@pytest.mark.parametrize("name", ["fp8_decode", "mxfp4_decode", "long_mxfp4", "spec_verify"])
+def test_full_size_topk_as_benched(cuda_lib, name):
+    """The decode step exactly as the bench times it (logits kept in the
+    workspace, no -inf fill), at full size, twice on one workspace: top-k sets
+    against the oracle (every row; spec_verify 40 sampled rows and the first and
+    last real rows), all row bounds exactly, the status word clean."""
+    import torch
+    from dsa_case import bf16_tensor
+    from sparse_attention_indexer_score_gb300.step import DecodeIndexer
+    wl = make_workload(name)
+    dev = torch.device("cuda")
+    ix = DecodeIndexer(wl.fmt, wl.num_pages, torch.from_numpy(wl.block_table), torch.from_numpy(wl.gamma),
+                       torch.from_numpy(wl.beta), wl.eps, wl.num_rows, wl.topk, dev)
+    for q in range(wl.R):
+        kb, sl = wl.prefill(q)
+        if kb.shape[0]:
+            ix.insert(bf16_tensor(kb, dev), torch.from_numpy(sl).to(dev))
+    args = (bf16_tensor(wl.q_bits, dev), bf16_tensor(wl.wv_bits, dev), bf16_tensor(wl.step_key_bits, dev),
+            torch.from_numpy(wl.step_slots).to(dev), torch.from_numpy(wl.seq_lens).to(dev),
+            torch.from_numpy(wl.query_lens).to(dev), int(wl.query_lens.max(initial=0)))
+    tops = []
+    for _ in range(2):   # the second call reuses the workspace the first left zero-filled
+        out = ix.step(*args, want_logits=False)
+        torch.cuda.synchronize()
+        assert out.logits is None
+        tops.append(out.topk.cpu().numpy())
+    assert ix.status_bits() == 0
+    real = [r for r in range(wl.num_rows) if wl.row_request[r] >= 0]
+    if name == "spec_verify":
+        rng = np.random.default_rng(5)
+        rows = sorted(set(rng.choice(real, 40, replace=False).tolist() + [real[0], real[-1]]))
+    else:
+        rows = real
+    scores, top, row_ends, starts, q_rows = oracle_rows(name, {}, rows)
+    assert np.array_equal(out.row_ends.cpu().numpy(), row_ends)
+    for r in rows:
+        for t in tops:
+            check_topk(t[r:r + 1], scores[r][None], row_ends[r:r + 1], wl.topk, [0])
+    pad = [r for r in range(wl.num_rows) if wl.row_request[r] < 0]
+    for t in tops:
+        assert np.all(t[pad] == -1)
