@@ -1,12 +1,12 @@
 """Benchmark of the DSA lightning-indexer decode step on GB300.
 
-One step = the whole hot path over one batch of seeded synthetic inputs:
-prepare_step (quantize_query + insert_key + decode_layout in one launch) ->
-score_paged (+ fused top-k).  The headline workload is ``spec_verify`` (128
-requests x 1..4 verify rows, 4096..65536 keys, FP8 keys with UE8M0 scales,
-top-2048), the largest one that the step runs on one GPU; ``fp8_decode``,
-``mxfp4_decode`` and ``long_mxfp4`` follow, each with an object of the same
-keys under ``configs``.
+One step = the whole hot path over one batch of seeded synthetic inputs, one
+decode_step call: quantize_query + insert_key + decode_layout in one launch ->
+the scoring plan -> the scoring kernel -> top-k selection.  The headline
+workload is ``spec_verify`` (128 requests x 1..4 verify rows, 4096..65536
+keys, FP8 keys with UE8M0 scales, top-2048), the largest one that the step
+runs on one GPU; ``fp8_decode``, ``mxfp4_decode`` and ``long_mxfp4`` follow,
+each with an object of the same keys under ``configs``.
 
 Prints one JSON line.  ``value`` is scored keys per second (sum of the row
 bounds of a step / device time of a step) with inputs resident in HBM.  The K
@@ -48,7 +48,7 @@ import numpy as np  # noqa: E402
 
 METRIC = "indexer scored keys/sec and cache GB/s (score+top-k) vs roofline, 1 GB300"
 UNIT = "keys/s"
-STEP_KERNELS = 4   # prepare_step (quantize + insert + layout), plan, score, select
+STEP_KERNELS = 4   # decode_step: prepare (quantize + insert + layout), plan, score, select
 FP4_FORMATS = ("mxfp4", "mxfp4_rg")
 
 

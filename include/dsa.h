@@ -312,6 +312,46 @@ int dsa_score_paged(int fmt, const void* q_rows, const void* w,
                     int32_t* status, void* stream);
 
 /*
+ * dsa_decode_step - one decode step in one call: dsa_prepare_step, then
+ * dsa_score_paged on what it produced.
+ *
+ * Page "cutedsl.dsa.overlap": the indexer path runs the preparation ahead of
+ * "scoring and top-k"; page "cutedsl.dsa.index" (DsaIndex) quantises the query
+ * and inserts the new key of a token together.  The call checks every
+ * argument of both parts before its first launch and then issues the same
+ * launches as the two calls (preparation, plan, scoring, selection), chained
+ * by programmatic dependent launch.  Results are those of
+ *   dsa_prepare_step(fmt, q, q_row_stride, wv, wv_row_stride, num_rows, q_out,
+ *                    w_out, k, k_row_stride, gamma, beta, eps, slots, n, cache,
+ *                    page_stride, num_pages, seq_lens, num_seq, query_lens,
+ *                    num_requests, num_rows, starts, row_ends, status)
+ * followed by
+ *   dsa_score_paged(fmt, q_out, w_out, cache, page_stride, num_pages,
+ *                   block_table, bt_stride, max_pages, starts, row_ends,
+ *                   num_requests, num_rows, max_query_len, logits, logits_ld,
+ *                   top_k, topk, workspace, workspace_bytes, status),
+ * every argument with the meaning, layout and checks it has there (q_out is
+ * uint8 [num_rows][4096], w_out BF16 [num_rows][32]).  Any argument error of
+ * either returns that error and launches nothing.  With num_rows = 0 only the
+ * keys are inserted.  Ownership: every buffer belongs to the caller; nothing is
+ * allocated; the workspace is dsa_score_paged's (dsa_workspace_size).
+ */
+int dsa_decode_step(int fmt, const void* q, int64_t q_row_stride,
+                    const void* wv, int64_t wv_row_stride,
+                    const void* k, int64_t k_row_stride,
+                    const float* gamma, const float* beta, float eps,
+                    const int64_t* slots, int64_t n,
+                    void* cache, int64_t page_stride, int64_t num_pages,
+                    const int32_t* seq_lens, int64_t num_seq,
+                    const int32_t* query_lens, int64_t num_requests, int64_t num_rows,
+                    const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                    int64_t max_query_len, void* q_out, void* w_out,
+                    int32_t* starts, int32_t* row_ends,
+                    float* logits, int64_t logits_ld, int64_t top_k, int32_t* topk,
+                    void* workspace, size_t workspace_bytes,
+                    int32_t* status, void* stream);
+
+/*
  * dsa_score_paged_heads - dsa_score_paged for MXFP4 queries of 16, 32 or 64
  * heads in the quantize_queries form.
  *

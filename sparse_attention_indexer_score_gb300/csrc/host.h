@@ -56,6 +56,21 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// dsa_prepare_step's argument checks alone (no launch).
+int check_prepare(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride, int64_t rows,
+                  const void* q_out, const void* w_out, const void* k, int64_t k_row_stride, const float* gamma,
+                  const float* beta, const int64_t* slots, int64_t n, const void* cache, int64_t page_stride,
+                  int64_t num_pages, const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens,
+                  int64_t num_requests, int64_t num_rows, const int32_t* starts, const int32_t* row_ends);
+
+// dsa_prepare_step's checks and launch.
+int launch_prepare(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride, int64_t rows,
+                   void* q_out, void* w_out, const void* k, int64_t k_row_stride, const float* gamma,
+                   const float* beta, float eps, const int64_t* slots, int64_t n, void* cache, int64_t page_stride,
+                   int64_t num_pages, const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens,
+                   int64_t num_requests, int64_t num_rows, int32_t* starts, int32_t* row_ends, int32_t* status,
+                   cudaStream_t stream);
+
 // Top-k selection launcher shared by dsa_score_paged and dsa_topk.
 int launch_select(const float* logits, float* logits_fill, int64_t ld, int64_t width, const int32_t* ends,
                   int64_t rows, int64_t k, int32_t* out, uint8_t* ws, const WsLayout& L, cudaStream_t stream,

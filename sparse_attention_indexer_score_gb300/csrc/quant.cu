@@ -411,12 +411,32 @@ extern "C" int dsa_insert_key(int fmt, const void* k, int64_t k_row_stride, cons
     return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
-extern "C" int dsa_prepare_step(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride,
-                                int64_t rows, void* q_out, void* w_out, const void* k, int64_t k_row_stride,
-                                const float* gamma, const float* beta, float eps, const int64_t* slots, int64_t n,
-                                void* cache, int64_t page_stride, int64_t num_pages, const int32_t* seq_lens,
-                                int64_t num_seq, const int32_t* query_lens, int64_t num_requests, int64_t num_rows,
-                                int32_t* starts, int32_t* row_ends, int32_t* status, void* stream) {
+namespace dsa {
+
+int check_prepare(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride, int64_t rows,
+                  const void* q_out, const void* w_out, const void* k, int64_t k_row_stride, const float* gamma,
+                  const float* beta, const int64_t* slots, int64_t n, const void* cache, int64_t page_stride,
+                  int64_t num_pages, const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens,
+                  int64_t num_requests, int64_t num_rows, const int32_t* starts, const int32_t* row_ends) {
+    int64_t qb = 0, kb = 0;
+    int rc = check_quantize(fmt, q, q_row_stride, wv, wv_row_stride, rows, const_cast<void*>(q_out),
+                            const_cast<void*>(w_out), &qb);
+    if (rc != DSA_OK) return rc;
+    rc = check_insert(fmt, k, k_row_stride, gamma, beta, slots, n, const_cast<void*>(cache), page_stride, num_pages,
+                      &kb);
+    if (rc != DSA_OK) return rc;
+    rc = check_layout(seq_lens, num_seq, query_lens, num_requests, num_rows, const_cast<int32_t*>(starts),
+                      const_cast<int32_t*>(row_ends));
+    if (rc != DSA_OK) return rc;
+    return (1 + kb + qb > 0x7FFFFFFF) ? DSA_ERR_UNSUPPORTED : DSA_OK;
+}
+
+int launch_prepare(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride, int64_t rows,
+                   void* q_out, void* w_out, const void* k, int64_t k_row_stride, const float* gamma,
+                   const float* beta, float eps, const int64_t* slots, int64_t n, void* cache, int64_t page_stride,
+                   int64_t num_pages, const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens,
+                   int64_t num_requests, int64_t num_rows, int32_t* starts, int32_t* row_ends, int32_t* status,
+                   cudaStream_t stream) {
     int64_t qb = 0, kb = 0;
     int rc = check_quantize(fmt, q, q_row_stride, wv, wv_row_stride, rows, q_out, w_out, &qb);
     if (rc != DSA_OK) return rc;
@@ -453,7 +473,20 @@ extern "C" int dsa_prepare_step(int fmt, const void* q, int64_t q_row_stride, co
     a.num_rows = num_rows;
     a.starts = starts;
     a.row_ends = row_ends;
-    const cudaError_t err = launch_pdl(prepare_step_kernel, dim3(static_cast<unsigned>(1 + kb + qb)), dim3(256), 0,
-                                       static_cast<cudaStream_t>(stream), a);
+    const dim3 grid(static_cast<unsigned>(1 + kb + qb));
+    const cudaError_t err = launch_pdl(prepare_step_kernel, grid, dim3(256), 0, stream, a);
     return err == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa
+
+extern "C" int dsa_prepare_step(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride,
+                                int64_t rows, void* q_out, void* w_out, const void* k, int64_t k_row_stride,
+                                const float* gamma, const float* beta, float eps, const int64_t* slots, int64_t n,
+                                void* cache, int64_t page_stride, int64_t num_pages, const int32_t* seq_lens,
+                                int64_t num_seq, const int32_t* query_lens, int64_t num_requests, int64_t num_rows,
+                                int32_t* starts, int32_t* row_ends, int32_t* status, void* stream) {
+    return launch_prepare(fmt, q, q_row_stride, wv, wv_row_stride, rows, q_out, w_out, k, k_row_stride, gamma, beta,
+                          eps, slots, n, cache, page_stride, num_pages, seq_lens, num_seq, query_lens, num_requests,
+                          num_rows, starts, row_ends, status, static_cast<cudaStream_t>(stream));
 }

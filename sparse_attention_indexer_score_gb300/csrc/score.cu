@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     __shared__ int chunk_total;
     __shared__ int sp[kPlanSmemSegs + 1];   // tiles per segment, then the tile prefix (when the segments fit)
     __shared__ int se[kPlanSmemRows];       // row bounds (when the rows fit)
+    __shared__ unsigned char sn[kPlanSmemSegs];   // rows per segment (when the segments fit)
     const bool rows_fit = rows <= kPlanSmemRows;
     // The first chunk's request starts and all row bounds are loaded together.
     int a0 = 0, b0 = 0;
@@ -253,7 +254,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                 maxend = max(maxend, e);
             }
             segs[sbase + i] = make_int4(q, row0, nr, maxend);
-            if (sbase + i < kPlanSmemSegs) sp[sbase + i] = (maxend + kTileRows - 1) / kTileRows;
+            if (sbase + i < kPlanSmemSegs) {
+                sp[sbase + i] = (maxend + kTileRows - 1) / kTileRows;
+                sn[sbase + i] = static_cast<unsigned char>(nr);
+            }
         }
         carry += chunk_total;
         __syncthreads();
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         int tiles = 0, cost = 0;
         if (i < S) {
             tiles = i < kPlanSmemSegs ? sp[i] : (segs[i].w + kTileRows - 1) / kTileRows;
-            if (weighted) cost = tiles * (kTileCostBase + kCostRow * segs[i].z);
+            if (weighted) cost = tiles * (kTileCostBase + kCostRow * sn[i]);
         }
         const int inc = block_inclusive_scan(tiles, warp_tmp, &chunk_total);
         if (i < S) {
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
             const int mid = (lo + hi) >> 1;
             if (se[mid] <= B) lo = mid; else hi = mid;
         }
-        const int per = kTileCostBase + kCostRow * segs[lo].z;
+        const int per = kTileCostBase + kCostRow * sn[lo];
         return min(sp[lo + 1], sp[lo] + static_cast<int>((B - se[lo]) / per));
     };
     for (int c = threadIdx.x; c < G; c += blockDim.x) {
@@ -1181,11 +1185,34 @@ struct QueryOperands {
     int64_t w_stride;
 };
 
+// The step's preparation (dsa_decode_step): its inputs, the rest being the
+// scoring call's own (cache, queries and weights out, row bounds out, status).
+struct PrepareCall {
+    const void* q;
+    int64_t q_row_stride;
+    const void* wv;
+    int64_t wv_row_stride;
+    const void* k;
+    int64_t k_row_stride;
+    const float* gamma;
+    const float* beta;
+    float eps;
+    const int64_t* slots;
+    int64_t n;
+    const int32_t* seq_lens;
+    int64_t num_seq;
+    const int32_t* query_lens;
+};
+
+// prep: when non-null, the preparation runs first, in one launch that also
+// lays out the plan (in place of plan_kernel); its outputs are q_rows, w,
+// starts and row_ends.
 static int score_paged_impl(int fmt, const QueryOperands& qo, const void* cache, int64_t page_stride,
                             int64_t num_pages, const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
                             const int32_t* starts, const int32_t* row_ends, int64_t num_requests, int64_t rows,
                             int64_t max_query_len, float* logits, int64_t logits_ld, int64_t k, int32_t* topk,
-                            void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t stream) {
+                            void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t stream,
+                            const PrepareCall* prep = nullptr) {
     if (fmt < DSA_FMT_FP8 || fmt > DSA_FMT_MXFP4_RG) return DSA_ERR_UNSUPPORTED;
     if (rows < 0 || num_requests < 0 || max_pages < 0 || num_pages < 0 || k < 0 || max_query_len < 0)
         return DSA_ERR_INVALID;
@@ -1273,9 +1300,18 @@ static int score_paged_impl(int fmt, const QueryOperands& qo, const void* cache,
     int* eff_end = reinterpret_cast<int*>(ws + L.eff_end);
     int4* cta = reinterpret_cast<int4*>(ws + L.cta);
     const int grid = device_sm_count() < kMaxScoreCtas ? device_sm_count() : kMaxScoreCtas;
+    if (prep) {
+        const int rc = launch_prepare(fmt, prep->q, prep->q_row_stride, prep->wv, prep->wv_row_stride, rows,
+                                      const_cast<void*>(q_rows), const_cast<void*>(w), prep->k, prep->k_row_stride,
+                                      prep->gamma, prep->beta, prep->eps, prep->slots, prep->n,
+                                      const_cast<void*>(cache), page_stride, num_pages, prep->seq_lens, prep->num_seq,
+                                      prep->query_lens, num_requests, rows, const_cast<int32_t*>(starts),
+                                      const_cast<int32_t*>(row_ends), status, stream);
+        if (rc != DSA_OK) return rc;
+    }
     if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, starts, row_ends, static_cast<int>(num_requests),
-                   static_cast<int>(rows), static_cast<int>(width), info, segs, seg_prefix, eff_end, cta, grid,
-                   seg_rows, status) != cudaSuccess)
+                   static_cast<int>(rows), static_cast<int>(width), info, segs, seg_prefix, eff_end, cta, grid, seg_rows,
+                   status) != cudaSuccess)
         return DSA_ERR_CUDA;
 
     // One kernel per (format, heads); its shared-memory limit is an attribute of
@@ -1370,4 +1406,32 @@ extern "C" int dsa_score_paged_heads(int fmt, int64_t heads, const void* payload
     return score_paged_impl(fmt, qo, cache, page_stride, num_pages, block_table, bt_stride, max_pages, starts,
                             row_ends, num_requests, rows, max_query_len, logits, logits_ld, k, topk, workspace,
                             workspace_bytes, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dsa_decode_step(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride,
+                               const void* k, int64_t k_row_stride, const float* gamma, const float* beta, float eps,
+                               const int64_t* slots, int64_t n, void* cache, int64_t page_stride, int64_t num_pages,
+                               const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens,
+                               int64_t num_requests, int64_t num_rows, const int32_t* block_table, int64_t bt_stride,
+                               int64_t max_pages, int64_t max_query_len, void* q_out, void* w_out, int32_t* starts,
+                               int32_t* row_ends, float* logits, int64_t logits_ld, int64_t top_k, int32_t* topk,
+                               void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+    // The preparation's 32-head query rows and weights, read by the scoring as dsa_score_paged reads them.
+    QueryOperands qo{kHeads, q_out, kQRowBytes,
+                     q_out ? static_cast<const uint8_t*>(q_out) + kFp4Scales : nullptr, kQRowBytes,
+                     fmt == DSA_FMT_MXFP4_RG, w_out, kHeads};
+    const PrepareCall prep{q, q_row_stride, wv, wv_row_stride, k, k_row_stride, gamma, beta, eps, slots, n,
+                           seq_lens, num_seq, query_lens};
+    // the preparation's argument errors first, before any work of the scoring's
+    const int rc = check_prepare(fmt, q, q_row_stride, wv, wv_row_stride, num_rows, q_out, w_out, k, k_row_stride,
+                                 gamma, beta, slots, n, cache, page_stride, num_pages, seq_lens, num_seq, query_lens,
+                                 num_requests, num_rows, starts, row_ends);
+    if (rc != DSA_OK) return rc;
+    if (num_rows == 0)   // nothing to score; the step's keys are still inserted
+        return launch_prepare(fmt, q, q_row_stride, wv, wv_row_stride, 0, q_out, w_out, k, k_row_stride, gamma, beta,
+                              eps, slots, n, cache, page_stride, num_pages, seq_lens, num_seq, query_lens,
+                              num_requests, 0, starts, row_ends, status, static_cast<cudaStream_t>(stream));
+    return score_paged_impl(fmt, qo, cache, page_stride, num_pages, block_table, bt_stride, max_pages, starts,
+                            row_ends, num_requests, num_rows, max_query_len, logits, logits_ld, top_k, topk,
+                            workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream), &prep);
 }

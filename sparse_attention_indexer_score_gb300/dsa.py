@@ -37,6 +37,9 @@ _SIGS = {
     "dsa_decode_layout": (_c.c_int, [_P, _I64, _P, _I64, _I64, _P, _P, _P]),
     "dsa_prepare_step": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _c.c_float, _P,
                                     _I64, _P, _I64, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P, _P]),
+    "dsa_decode_step": (_c.c_int, [_c.c_int, _P, _I64, _P, _I64, _P, _I64, _P, _P, _c.c_float, _P, _I64, _P, _I64,
+                                   _I64, _P, _I64, _P, _I64, _I64, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I64,
+                                   _I64, _P, _P, _c.c_size_t, _P, _P]),
     "dsa_decode_layout_dcp": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P]),
     "dsa_topk_merge": (_c.c_int, [_P, _I64, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _I64, _P, _P,
                                   _c.c_size_t, _P]),
@@ -262,6 +265,42 @@ def prepare_step(fmt: str, q: torch.Tensor, wv: torch.Tensor, k: torch.Tensor, g
                                 int(num_rows), _ptr(starts), _ptr(row_ends), _ptr(status), _stream(q.device))
     _check(rc, "dsa_prepare_step")
     return q_out, w_out, starts, row_ends
+
+
+def decode_step(fmt: str, q: torch.Tensor, wv: torch.Tensor, k: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor,
+                eps: float, slots: torch.Tensor, cache: torch.Tensor, page_stride: int, num_pages: int,
+                seq_lens: torch.Tensor, query_lens: torch.Tensor, block_table: torch.Tensor, max_query_len: int,
+                top_k: int = 0, want_logits: bool = False, workspace: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, q_out: Optional[torch.Tensor] = None,
+                w_out: Optional[torch.Tensor] = None, starts: Optional[torch.Tensor] = None,
+                row_ends: Optional[torch.Tensor] = None, topk_out: Optional[torch.Tensor] = None):
+    """prepare_step then score_paged on its outputs, in one call
+    (``dsa_decode_step``: every argument checked before the first launch).  Returns (q_rows, w, starts, row_ends, logits or
+    None, top-k or None)."""
+    num_rows = q.shape[0]
+    q_out, w_out = _query_args(q, wv, q_out, w_out)
+    _key_args(k, gamma, beta, slots)
+    starts, row_ends = _layout_args(seq_lens, query_lens, num_rows, starts, row_ends)
+    if block_table.dtype != torch.int32 or (block_table.dim() == 2 and block_table.numel() and block_table.stride(1) != 1):
+        raise ValueError("block_table must be int32 with contiguous rows")
+    R = query_lens.numel()
+    max_pages = block_table.shape[1] if block_table.dim() == 2 else 0
+    width = max_pages * 64
+    dev = q.device
+    logits = torch.empty((num_rows, width), dtype=torch.float32, device=dev) if want_logits else None
+    if top_k > 0 and topk_out is None:
+        topk_out = torch.empty((num_rows, top_k), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(workspace_size(fmt, num_rows, R, max_pages, top_k), dev)
+    rc = lib().dsa_decode_step(
+        _fmt(fmt), _ptr(q), q.stride(0), _ptr(wv), wv.stride(0), _ptr(k), k.stride(0), _ptr(gamma), _ptr(beta),
+        float(eps), _ptr(slots), k.shape[0], _ptr(cache), int(page_stride), int(num_pages), _ptr(seq_lens),
+        seq_lens.numel(), _ptr(query_lens), R, num_rows, _ptr(block_table),
+        block_table.stride(0) if block_table.dim() == 2 else 0, max_pages, int(max_query_len), _ptr(q_out),
+        _ptr(w_out), _ptr(starts), _ptr(row_ends), _ptr(logits), logits.stride(0) if logits is not None else 0,
+        int(top_k), _ptr(topk_out), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+    _check(rc, "dsa_decode_step")
+    return q_out, w_out, starts, row_ends, logits, topk_out
 
 
 def workspace_size(fmt: str, rows: int, num_requests: int, max_pages: int, k: int) -> int:

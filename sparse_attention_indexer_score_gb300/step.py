@@ -2,8 +2,8 @@
 
 ``DecodeIndexer`` owns the device state a serving loop keeps between steps
 (the paged key cache, the block table, a zero-filled workspace) and runs the
-step on the current stream: prepare_step (quantize_query + insert_key +
-decode_layout in one launch) -> score_paged (+ fused top-k).  ``GraphedStep``
+step on the current stream with one decode_step call: quantize_query +
+insert_key + decode_layout in one launch -> plan -> scoring -> top-k.  ``GraphedStep``
 captures a step with its host copies as one CUDA graph.
 """
 
@@ -54,14 +54,11 @@ class DecodeIndexer:
              seq_lens: torch.Tensor, query_lens: torch.Tensor, max_query_len: int,
              want_logits: bool = False, topk_out: Optional[torch.Tensor] = None,
              q_out: Optional[torch.Tensor] = None, w_out: Optional[torch.Tensor] = None) -> StepOutput:
-        rows = q.shape[0]
-        q_rows, w, starts, row_ends = dsa.prepare_step(
+        q_rows, w, starts, row_ends, logits, top = dsa.decode_step(
             self.fmt, q, wv, keys, self.gamma, self.beta, self.eps, slots, self.cache, self.page_stride,
-            self.num_pages, seq_lens, query_lens, rows, q_out=q_out, w_out=w_out, status=self.status)
-        logits, top = dsa.score_paged(self.fmt, q_rows, w, self.cache, self.page_stride, self.num_pages,
-                                      self.block_table, starts, row_ends, max_query_len, k=self.k,
-                                      want_logits=want_logits, workspace=self.workspace, status=self.status,
-                                      topk_out=topk_out)
+            self.num_pages, seq_lens, query_lens, self.block_table, max_query_len, top_k=self.k,
+            want_logits=want_logits, workspace=self.workspace, status=self.status, q_out=q_out, w_out=w_out,
+            topk_out=topk_out)
         return StepOutput(q_rows, w, starts, row_ends, top, logits)
 
     def status_bits(self) -> int:

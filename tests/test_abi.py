@@ -138,3 +138,37 @@ def test_the_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(dsa, "LIB_PATH", str(tmp_path / "libdsa.so"))
     with pytest.raises(RuntimeError, match="missing"):
         dsa.lib()
+
+
+def test_decode_step_returns_argument_errors_before_any_launch(lib):
+    """dsa_decode_step reports the argument error of the preparation or of the
+    scoring (no launch, so this runs without a GPU)."""
+    A = 1 << 20
+    prep_q = [0, A, 4096, A, 32]                              # fmt, q, stride, wv, stride
+    prep_k = [A, 128, A, A, 1e-6, A, 1, A, 8448, 1]           # k, stride, gamma, beta, eps, slots, n, cache, stride, pages
+    layout = [A, 1, A, 1, 1]                                  # seq_lens, num_seq, query_lens, R, num_rows
+    score = [A, 1, 1, 1, A, A, A, A, None, 0, 4, A, A, 1 << 30, None, None]
+    # block table, bt_stride, max_pages, max_query_len, q_out, w_out, starts, row_ends,
+    # logits, logits_ld, top_k, topk, workspace, workspace_bytes, status, stream
+
+    def call(q=prep_q, k=prep_k, l=layout, sc=score):
+        return lib.dsa_decode_step(*q, *k, *l, *sc)
+
+    bad = list(prep_q)
+    bad[0] = 9                                                # unknown format
+    assert call(q=bad) == -2
+    bad = list(prep_q)
+    bad[2] = 4000                                             # query row stride < 4096
+    assert call(q=bad) == -1
+    bad = list(prep_k)
+    bad[8] = 4352                                             # FP8 page stride < 8448
+    assert call(k=bad) == -1
+    bad = list(layout)
+    bad[1] = 0                                                # fewer seq_lens than requests
+    assert call(l=bad) == -1
+    bad = list(score)
+    bad[1] = 0                                                # block-table row stride < max_pages
+    assert call(sc=bad) == -1
+    bad = list(score)
+    bad[13] = 16                                              # workspace too small
+    assert call(sc=bad) == -1

@@ -660,3 +660,57 @@ def test_full_size_topk_as_benched(cuda_lib, name):
     pad = [r for r in range(wl.num_rows) if wl.row_request[r] < 0]
     for t in tops:
         assert np.all(t[pad] == -1)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_decode_step_equals_prepare_then_score(cuda_lib, fmt):
+    """dsa_decode_step gives the bytes of dsa_prepare_step followed by
+    dsa_score_paged: query rows, weights, cache,
+    row bounds, logits and top-k; with no rows it only inserts the keys."""
+    import torch
+    wl = make_workload("tiny_fp8", fmt=fmt, seed=31, R=9, seq=(60, 3000), qlen=(1, 5), pad_rows=2, topk=64)
+    dev = torch.device("cuda")
+    stride = O.page_bytes(fmt)
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    gamma, beta = torch.from_numpy(wl.gamma).to(dev), torch.from_numpy(wl.beta).to(dev)
+    base = torch.zeros(wl.num_pages * stride, dtype=torch.uint8, device=dev)
+    for q in range(wl.R):
+        kb, sl = wl.prefill(q)
+        if kb.shape[0]:
+            cuda_lib.insert_key(fmt, bf16_tensor(kb, dev), gamma, beta, wl.eps, torch.from_numpy(sl).to(dev), base,
+                                stride, wl.num_pages)
+    args = (bf16_tensor(wl.q_bits, dev), bf16_tensor(wl.wv_bits, dev), bf16_tensor(wl.step_key_bits, dev), gamma,
+            beta, wl.eps, torch.from_numpy(wl.step_slots).to(dev))
+    lens = (torch.from_numpy(wl.seq_lens).to(dev), torch.from_numpy(wl.query_lens).to(dev))
+    mq = int(wl.query_lens.max())
+
+    def run(fused, num_rows):
+        cache = base.clone()
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if fused:
+            q_rows, w, st, en, lg, top = cuda_lib.decode_step(fmt, args[0][:num_rows], args[1][:num_rows], *args[2:],
+                                                              cache, stride, wl.num_pages, *lens, bt, mq,
+                                                              top_k=wl.topk if num_rows else 0,
+                                                              want_logits=num_rows > 0, status=status)
+        else:
+            q_rows, w, st, en = cuda_lib.prepare_step(fmt, args[0][:num_rows], args[1][:num_rows], *args[2:], cache,
+                                                      stride, wl.num_pages, *lens, num_rows, status=status)
+            lg = top = None
+            if num_rows:
+                lg, top = cuda_lib.score_paged(fmt, q_rows, w, cache, stride, wl.num_pages, bt, st, en, mq,
+                                               k=wl.topk, want_logits=True, status=status)
+        torch.cuda.synchronize()
+        return q_rows.cpu(), w.float().cpu(), cache.cpu(), st.cpu(), en.cpu(), lg, top, int(status.item())
+
+    a, b = run(True, wl.num_rows), run(False, wl.num_rows)
+    for x, y in zip(a[:5], b[:5]):
+        assert torch.equal(x, y)
+    assert a[7] == b[7] == 0
+    ends = b[4].numpy()
+    la, lb = a[5].cpu().numpy(), b[5].cpu().numpy()
+    for r in range(wl.num_rows):
+        assert np.array_equal(la[r, :ends[r]], lb[r, :ends[r]]), r
+    check_topk(a[6].cpu().numpy(), lb.astype(np.float64), ends, wl.topk, range(wl.num_rows))
+    a0, b0 = run(True, 0), run(False, 0)
+    assert torch.equal(a0[2], b0[2]) and not torch.equal(a0[2], base.cpu())
+    assert a0[3].numel() == b0[3].numel() and torch.equal(a0[3], b0[3]) and a0[7] == b0[7] == 0
