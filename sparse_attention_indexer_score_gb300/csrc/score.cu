@@ -924,11 +924,14 @@ __device__ __forceinline__ void flush_group_hist(const ScoreArgs& p, uint32_t* g
         if (!((hist_m >> r) & 1u)) continue;
         uint32_t* hr = gh + r * (kHistBins / 2);
         unsigned* dst = p.hist + static_cast<int64_t>(row0 + r) * kHistBins;
+        // One 64-bit add per word updates both of its bins (2w in the low half,
+        // 2w + 1 in the high one): a row's count stays below 2^31, so the low
+        // bin never carries into its neighbour.
+        unsigned long long* dst2 = reinterpret_cast<unsigned long long*>(dst);
         for (int w = e; w < kHistBins / 2; w += 128) {
             const uint32_t c = hr[w];
             if (c) {
-                if (c & 0xFFFFu) atomicAdd(dst + 2 * w, c & 0xFFFFu);
-                if (c >> 16) atomicAdd(dst + 2 * w + 1, c >> 16);
+                atomicAdd(dst2 + w, (static_cast<unsigned long long>(c >> 16) << 32) | (c & 0xFFFFu));
                 hr[w] = 0u;
             }
         }

@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     __shared__ __align__(16) unsigned h2[kHistBins];   // level-2 histogram (read as uint4)
     __shared__ int tmp[32];
     __shared__ int s_b1, s_a1, s_b2, s_a2, s_b3, s_a3;
-    __shared__ unsigned long long s_wc;   // level-1 winners (bits 63..32) and candidates (31..0) placed
+    __shared__ int s_wc[2];   // level-1 winners and candidates placed
     __shared__ int s_w2, s_c3, s_w3, s_tie, s_last, s_wbase, s_cbase;
     extern __shared__ float4 sel_dyn[];
     float4* ring = sel_dyn;                                                    // kRing tiles of scores
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0;
     if (threadIdx.x == 0) {
         s_b1 = 0; s_a1 = 0; s_b2 = 0; s_a2 = 0; s_b3 = 0; s_a3 = 0;
-        s_wc = 0; s_w2 = 0; s_c3 = 0; s_w3 = 0; s_tie = 0;
+        s_wc[0] = 0; s_wc[1] = 0; s_w2 = 0; s_c3 = 0; s_w3 = 0; s_tie = 0;
     }
     __syncthreads();
     find_boundary4(hq1, k, &s_b1, &s_a1, tmp);
@@ -330,12 +330,14 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
             const int y = __shfl_up_sync(0xFFFFFFFFu, inc, d);
             if (lane >= d) inc += y;
         }
-        unsigned long long o = 0;   // one shared add reserves both runs
-        if (lane == 31 && inc)
-            o = atomicAdd(&s_wc, (static_cast<unsigned long long>(inc >> 16) << 32) | static_cast<unsigned>(inc & 0xFFFF));
-        o = __shfl_sync(0xFFFFFFFFu, o, 31);
-        int pw = static_cast<int>(o >> 32) + (inc >> 16) - cw;
-        int pc = static_cast<int>(o & 0xFFFFFFFFu) + (inc & 0xFFFF) - cc;
+        // Lanes 30 and 31 reserve the warp's runs of winners and candidates with
+        // one shared add each (one instruction, two counters).
+        const int tot = __shfl_sync(0xFFFFFFFFu, inc, 31);
+        const int want = lane == 30 ? tot >> 16 : (tot & 0xFFFF);
+        int o = 0;
+        if (lane >= 30 && want) o = atomicAdd(&s_wc[lane - 30], want);
+        int pw = __shfl_sync(0xFFFFFFFFu, o, 30) + (inc >> 16) - cw;
+        int pc = __shfl_sync(0xFFFFFFFFu, o, 31) + (inc & 0xFFFF) - cc;
         const int tb = base + 4 * threadIdx.x;   // position of value 0 of this thread
         while (wm) {
             const int u = __ffs(wm) - 1;
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     }
     cp_async_wait<0>();
     __syncthreads();
-    const int nwin = static_cast<int>(s_wc >> 32), mycand = static_cast<int>(s_wc & 0xFFFFFFFFu);
+    const int nwin = s_wc[0], mycand = s_wc[1];
     int ncand = mycand;
     const uint2* cand_src = ncand <= kRefineCap ? cbuf : nullptr;
     if (!split && wbuffered)
