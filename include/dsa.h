@@ -442,8 +442,8 @@ int dsa_topk_merge(const float* scores, int64_t scores_ld, const int32_t* idx,
  * cudaMalloc, or a plugin host that passes a kernel its inputs and outputs but
  * no allocator.  It computes what dsa_topk computes, with the same arguments
  * minus the workspace.  Its scratch is a file-scope device array of
- * DSA_TOPK_NOALLOC_SCRATCH_BYTES (about 5 MB: for each of the
- * DSA_TOPK_NOALLOC_MAX_ROWS rows two 8 KB histograms, 16 bytes of counters and
+ * DSA_TOPK_NOALLOC_SCRATCH_BYTES (about 4.5 MB: for each of the
+ * DSA_TOPK_NOALLOC_MAX_ROWS rows an 8 KB histogram, 16 bytes of counters and
  * 64 KB of candidates), held by every GPU that loads the library until the
  * process exits.
  *
@@ -459,7 +459,7 @@ int dsa_topk_merge(const float* scores, int64_t scores_ld, const int32_t* idx,
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
  */
 #define DSA_TOPK_NOALLOC_MAX_ROWS 64
-#define DSA_TOPK_NOALLOC_SCRATCH_BYTES 5243904
+#define DSA_TOPK_NOALLOC_SCRATCH_BYTES 4719616
 int dsa_topk_noalloc(const float* logits, int64_t ld, const int32_t* row_ends,
                      int64_t rows, int64_t width, int64_t k, int32_t* out, void* stream);
 

@@ -10,7 +10,7 @@
 namespace dsa {
 
 // Byte offsets of the regions of a dsa_score_paged / dsa_topk workspace.
-// Every region starts on a 256-byte boundary.  `hist`, `hist2` and `counters`
+// Every region starts on a 256-byte boundary.  `hist` and `counters`
 // must be zero on entry and are zero again when a call completes.
 constexpr int kMaxScoreCtas = 1024;   // largest scoring grid the plan table holds
 
@@ -21,7 +21,6 @@ struct WsLayout {
     size_t eff_end;     // int[rows]: row bounds after validation (0 outside every request)
     size_t cta;         // int4[kMaxScoreCtas]: per scoring CTA {first tile, end tile, first segment, segments}
     size_t hist;        // uint32[rows][2048]: histogram of the top 11 order-preserving score bits
-    size_t hist2;       // uint32[rows][2048]: level-2 histogram (bits 20..10) of rows split over CTAs
     size_t counters;    // int[rows][4]: winners published, candidates published, spans done, candidates dropped
     size_t cand;        // uint2[rows][kCandCap]: level-1 candidates of split rows (key, position)
     size_t logits;      // float[rows][width] when the caller keeps no logits

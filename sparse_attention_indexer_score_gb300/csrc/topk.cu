@@ -47,7 +47,6 @@ struct SelectArgs {
     int k;               // 0: fill only
     int32_t* out;
     unsigned* hist;      // level-1 histograms, [rows][2048]
-    unsigned* hist2;     // level-2 histograms of split rows, [rows][2048]
     int* counters;       // [rows][4]: winners published, candidates published, spans done, spare
     uint2* cand;         // [rows][kCandCap]: level-1 candidates of split rows (key, position)
     int span;            // positions per CTA, a multiple of kChunk
@@ -243,7 +242,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     if (static_cast<int>(blockIdx.y) >= nsp) return;
     const bool split = nsp > 1;
     unsigned* ghist = a.hist + static_cast<int64_t>(row) * kHistBins;
-    unsigned* ghist2 = a.hist2 + static_cast<int64_t>(row) * kHistBins;
     int* ctr = a.counters + static_cast<int64_t>(row) * 4;
     uint2* gcand = a.cand + static_cast<int64_t>(row) * kCandCap;
     const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
@@ -339,13 +337,22 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
         int pw = __shfl_sync(0xFFFFFFFFu, o, 30) + (inc >> 16) - cw;
         int pc = __shfl_sync(0xFFFFFFFFu, o, 31) + (inc & 0xFFFF) - cc;
         const int tb = base + 4 * threadIdx.x;   // position of value 0 of this thread
+        if (wbuffered) {
+            // predicated over the 8 values: no loop as long as the warp's busiest lane
+#pragma unroll
+            for (int u = 0; u < kPerThread; ++u) {
+                if ((wm >> u) & 1u) {
+                    if (pw < kWinCap) wbuf[pw] = tb + (u >> 2) * (kChunk / 2) + (u & 3);
+                    ++pw;
+                }
+            }
+            wm = 0;
+        }
         while (wm) {
             const int u = __ffs(wm) - 1;
             wm &= wm - 1u;
             const int t = tb + (u >> 2) * (kChunk / 2) + (u & 3);
-            if (wbuffered) {
-                if (pw < kWinCap) wbuf[pw] = t;
-            } else if (!split) {
+            if (!split) {
                 if (pw < k) out[pw] = t;
             } else {
                 const int g = atomicAdd(ctr + 0, 1);
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
             cm &= cm - 1u;
             const int off = (u >> 2) * (kChunk / 2) + (u & 3);
             const uint32_t key = order_key(ringf[slot + 4 * threadIdx.x + off]);
-            atomicAdd(&h2[(key >> 10) & 0x7FF], 1u);
+            if (!split) atomicAdd(&h2[(key >> 10) & 0x7FF], 1u);   // a split row's last span counts them all
             if (pc < kRefineCap) cbuf[pc] = make_uint2(key, static_cast<uint32_t>(tb + off));
             ++pc;
         }
@@ -386,8 +393,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
         if (ncand <= kRefineCap)
             for (int i = threadIdx.x; i < ncand; i += kSelThreads)
                 if (s_cbase + i < kCandCap) gcand[s_cbase + i] = cbuf[i];
-        for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
-            if (h2[i]) atomicAdd(ghist2 + i, h2[i]);
         if (threadIdx.x == 0 && ncand > kRefineCap) atomicAdd(ctr + 3, 1);   // candidates dropped
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -400,13 +405,21 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
         ncand = *reinterpret_cast<volatile int*>(ctr + 1);
         const bool dropped = *reinterpret_cast<volatile int*>(ctr + 3) != 0;
         cand_src = (!dropped && ncand <= kCandCap) ? gcand : nullptr;
+        // The row's level-2 counts, from every span's candidates (or from the
+        // row itself when a candidate buffer overflowed).
+        for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0;
+        __syncthreads();
+        const CandSource all{cand_src, ncand, src, n, B1};
+        all.for_each([&](bool valid, uint32_t kk, int) {
+            if (valid) atomicAdd(&h2[(kk >> 10) & 0x7FF], 1u);
+        });
     }
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h1[i] = 0;   // level 3 from here on
     __syncthreads();
 
     // ---- level 2: one pass over the candidates
     const int need = k - above1;
-    find_boundary4(hist_quad(split ? ghist2 : h2), need, &s_b2, &s_a2, tmp);
+    find_boundary4(hist_quad(h2), need, &s_b2, &s_a2, tmp);
     __syncthreads();
     const uint32_t B2 = static_cast<uint32_t>(s_b2);
     const int above2 = s_a2;
@@ -458,10 +471,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     }
     // Short only when the histogram disagreed with the scores (an aborted scoring pass).
     for (int e = placed + threadIdx.x; e < k; e += kSelThreads) out[e] = -1;
-    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) {
-        ghist[i] = 0;
-        if (split) ghist2[i] = 0;
-    }
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) ghist[i] = 0;
     if (split && threadIdx.x < 4) ctr[threadIdx.x] = 0;
 }
 
@@ -483,8 +493,6 @@ WsLayout workspace_layout(int64_t rows, int64_t width, bool with_plan, bool with
     L.cta = off;
     off = align256(off + (with_plan ? kMaxScoreCtas * sizeof(int4) : 0));
     L.hist = off;
-    off = align256(off + r * kHistBins * sizeof(unsigned));
-    L.hist2 = off;
     off = align256(off + r * kHistBins * sizeof(unsigned));
     L.counters = off;
     off = align256(off + r * 4 * sizeof(int));
@@ -542,7 +550,6 @@ int launch_select(const float* logits, float* logits_fill, int64_t ld, int64_t w
     a.k = static_cast<int>(k);
     a.out = out;
     a.hist = reinterpret_cast<unsigned*>(ws + L.hist);
-    a.hist2 = reinterpret_cast<unsigned*>(ws + L.hist2);
     a.counters = reinterpret_cast<int*>(ws + L.counters);
     a.cand = reinterpret_cast<uint2*>(ws + L.cand);
     if (rows == 0 || (k == 0 && (!logits_fill || width == 0))) return DSA_OK;
@@ -628,10 +635,9 @@ extern "C" const char* dsa_version(void) { return "dsa-gb300 0.1.0"; }
 namespace dsa {
 
 constexpr size_t noalloc_align(size_t x) { return (x + 255) & ~size_t(255); }
-// Two 2048-bin histograms per row (level 1 and level 2: 8 KB each), 16 bytes
-// of counters per row and 8192 candidates of 8 bytes per split row (64 KB):
-// with 64 rows 512 KB + 512 KB + 1 KB + 4 MB.
-constexpr size_t kNoAllocBytes = 2 * noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kHistBins * sizeof(unsigned)) +
+// A 2048-bin histogram per row (8 KB), 16 bytes of counters per row and 8192
+// candidates of 8 bytes per split row (64 KB): with 64 rows 512 KB + 1 KB + 4 MB.
+constexpr size_t kNoAllocBytes = noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kHistBins * sizeof(unsigned)) +
                                  noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * 4 * sizeof(int)) +
                                  noalloc_align(size_t(DSA_TOPK_NOALLOC_MAX_ROWS) * kCandCap * sizeof(uint2));
 static_assert(kNoAllocBytes == DSA_TOPK_NOALLOC_SCRATCH_BYTES, "the header states the array's size");
