@@ -37,4 +37,51 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* warp_tmp, int* t
     return result;
 }
 
+// Two inclusive scans (of a and of b) over the block with one set of
+// barriers; `warp_tmp` holds 64 ints, totals go to total_a / total_b (shared).
+__device__ __forceinline__ void block_inclusive_scan2(int& a, int& b, int* warp_tmp, int* total_a, int* total_b) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int oa = __shfl_up_sync(0xFFFFFFFFu, a, d);
+        const int ob = __shfl_up_sync(0xFFFFFFFFu, b, d);
+        if (lane >= d) {
+            a += oa;
+            b += ob;
+        }
+    }
+    if (lane == 31) {
+        warp_tmp[warp] = a;
+        warp_tmp[32 + warp] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int sa = (lane < nwarps) ? warp_tmp[lane] : 0;
+        int sb = (lane < nwarps) ? warp_tmp[32 + lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int oa = __shfl_up_sync(0xFFFFFFFFu, sa, d);
+            const int ob = __shfl_up_sync(0xFFFFFFFFu, sb, d);
+            if (lane >= d) {
+                sa += oa;
+                sb += ob;
+            }
+        }
+        warp_tmp[lane] = sa;
+        warp_tmp[32 + lane] = sb;
+        if (lane == 31) {
+            *total_a = sa;
+            *total_b = sb;
+        }
+    }
+    __syncthreads();
+    if (warp > 0) {
+        a += warp_tmp[warp - 1];
+        b += warp_tmp[32 + warp - 1];
+    }
+    __syncthreads();   // warp_tmp may be reused by the caller's next scan
+}
+
 }  // namespace dsa

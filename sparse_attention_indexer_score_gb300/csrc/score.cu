@@ -211,11 +211,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     // this kernel.
     pdl_wait();
     pdl_launch_dependents();
-    __shared__ int warp_tmp[32];
-    __shared__ int chunk_total;
+    __shared__ int warp_tmp[64];
+    __shared__ int chunk_total, chunk_wtotal;
     __shared__ int sp[kPlanSmemSegs + 1];   // tiles per segment, then the tile prefix (when the segments fit)
     __shared__ int se[kPlanSmemRows];       // row bounds (when the rows fit)
     __shared__ unsigned char sn[kPlanSmemSegs];   // rows per segment (when the segments fit)
+    __shared__ int bnd[kMaxScoreCtas + 1];        // first tile of every scoring CTA
     const bool rows_fit = rows <= kPlanSmemRows;
     // The first chunk's request starts and all row bounds are loaded together.
     int a0 = 0, b0 = 0;
@@ -276,19 +277,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
             tiles = i < kPlanSmemSegs ? sp[i] : (segs[i].w + kTileRows - 1) / kTileRows;
             if (weighted) cost = tiles * (kTileCostBase + kCostRow * sn[i]);
         }
-        const int inc = block_inclusive_scan(tiles, warp_tmp, &chunk_total);
+        int inc = tiles, winc = cost;   // both prefixes with one set of barriers
+        block_inclusive_scan2(inc, winc, warp_tmp, &chunk_total, &chunk_wtotal);
         if (i < S) {
             seg_prefix[i] = carry + inc - tiles;
             if (i < kPlanSmemSegs) sp[i] = carry + inc - tiles;   // this thread's own entry
+            if (weighted) se[i] = wcarry + winc - cost;
         }
         carry += chunk_total;
+        wcarry += chunk_wtotal;
         __syncthreads();
-        if (weighted) {
-            const int winc = block_inclusive_scan(cost, warp_tmp, &chunk_total);
-            if (i < S) se[i] = wcarry + winc - cost;
-            wcarry += chunk_total;
-            __syncthreads();
-        }
     }
     const int T = carry;
     if (threadIdx.x == 0) {
@@ -307,20 +305,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     // decode steps mixing segments of 1 to 4 rows; the ratio matters, and it
     // leaves a 4-row tile at 11/5 of a 1-row one.
     const bool wfit = static_cast<int64_t>(T) * (kTileCostBase + kCostRow * kSegRows) < 0x7FFFFFFF;   // int prefix holds
+    // floor(c * X / G) in 32 bits: c * (X / G) + c * (X % G) / G, exact for
+    // c <= G <= kMaxScoreCtas (c * (X % G) < 2^20) and X < 2^31.
+    auto share = [&](int c, int X) { return c * (X / G) + (c * (X % G)) / G; };
     auto tile_at = [&](int c) -> int {   // first tile of CTA c
-        if (!weighted || !wfit || wcarry == 0) return static_cast<int>(static_cast<int64_t>(c) * T / G);
-        const int64_t B = static_cast<int64_t>(c) * wcarry / G;
+        if (!weighted || !wfit || wcarry == 0) return share(c, T);
+        const int B = share(c, wcarry);
         int lo = 0, hi = S;   // the last segment with se[lo] <= B
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (se[mid] <= B) lo = mid; else hi = mid;
         }
         const int per = kTileCostBase + kCostRow * sn[lo];
-        return min(sp[lo + 1], sp[lo] + static_cast<int>((B - se[lo]) / per));
+        return min(sp[lo + 1], sp[lo] + (B - se[lo]) / per);
     };
+    // every boundary once (CTA c's range is [bnd[c], bnd[c + 1]))
+    for (int c = threadIdx.x; c <= G; c += blockDim.x) bnd[c] = c == 0 ? 0 : (c == G ? T : tile_at(c));
+    __syncthreads();
     for (int c = threadIdx.x; c < G; c += blockDim.x) {
-        const int t0 = c == 0 ? 0 : tile_at(c);
-        const int t1 = c + 1 == G ? T : tile_at(c + 1);
+        const int t0 = bnd[c];
+        const int t1 = bnd[c + 1];
         int seg = -1;
         if (S <= kPlanSmemSegs && S > 0) {
             int lo = 0, hi = S;

@@ -223,47 +223,26 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     if (pdl) pdl_wait();
     const int row = blockIdx.x;
     const int64_t lo = static_cast<int64_t>(blockIdx.y) * a.span;
-    const int n = clamp_end(a.ends, row, a.width);
-    if (a.fill) {
-        float* dst = a.fill + static_cast<int64_t>(row) * a.ld;
-        const int64_t hi = min(a.width, lo + a.span);
-        for (int64_t t = max(lo, static_cast<int64_t>(n)) + threadIdx.x; t < hi; t += kSelThreads)
-            dst[t] = -__int_as_float(0x7F800000);
-    }
     const int k = a.k;
-    if (k <= 0) return;
-    int32_t* out = a.out + static_cast<int64_t>(row) * k;
-    if (n <= k) {
-        const int64_t hi = min(static_cast<int64_t>(k), lo + a.span);
-        for (int64_t pos = lo + threadIdx.x; pos < hi; pos += kSelThreads) out[pos] = pos < n ? static_cast<int>(pos) : -1;
-        return;
-    }
-    const int nsp = static_cast<int>((n + a.span - 1) / a.span);
-    if (static_cast<int>(blockIdx.y) >= nsp) return;
-    const bool split = nsp > 1;
     unsigned* ghist = a.hist + static_cast<int64_t>(row) * kHistBins;
     int* ctr = a.counters + static_cast<int64_t>(row) * 4;
     uint2* gcand = a.cand + static_cast<int64_t>(row) * kCandCap;
     const float* src = a.logits + static_cast<int64_t>(row) * a.ld;
     const int lane = threadIdx.x & 31;
     const int lo32 = static_cast<int>(lo);
-    const int hi = static_cast<int>(min(static_cast<int64_t>(n), lo + a.span));
-    // Winners wait in shared memory (written out coalesced after the pass)
-    // when k allows; else they go straight to the output.
-    const bool wbuffered = k <= kWinCap;
 
     // ---- level 1: the row's histogram, then the span in tiles through a
     // ring of kRing tiles in shared memory.  Each thread copies, and later
     // reads, the same 8 scores of a tile: positions base + 4 * tid + j and
     // base + kChunk / 2 + 4 * tid + j (j < 4), so no barrier guards the ring.
     const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
-    auto issue_tile = [&](int i) {   // tile i of the span into ring slot i % kRing (none past the span)
+    auto issue_tile = [&](int i, int bound) {   // tile i of the span into ring slot i % kRing, up to `bound`
         const int base = lo32 + i * kChunk;
         float4* slot = ring + (i % kRing) * (kChunk / 4);
 #pragma unroll
-        for (int h = 0; h < 2 && base < hi; ++h) {
+        for (int h = 0; h < 2 && base < bound; ++h) {
             const int p = base + h * (kChunk / 2) + 4 * threadIdx.x;
-            const int avail = max(0, min(4, hi - p));
+            const int avail = max(0, min(4, bound - p));
             float4* d = slot + h * (kChunk / 8) + threadIdx.x;
             if (vec) {
                 cp_async16(d, avail ? src + p : src, 4u * avail);
@@ -275,9 +254,49 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
         }
         cp_async_commit();
     };
-    const uint4 hq1 = hist_quad(ghist);   // first in flight, then the tiles
+    // The row's histogram does not depend on the row's bound: it goes out
+    // together with the bound's load, and so do the first tiles of the row's
+    // first span (the one span that is needed whenever the row is longer than
+    // k), read up to the end of the span within the row's width; positions
+    // past the bound are never classified.  Later spans may lie past the
+    // bound and wait for it.
+    uint4 hq1 = make_uint4(0u, 0u, 0u, 0u);
+    const bool early = k > 0 && blockIdx.y == 0;
+    if (k > 0) hq1 = hist_quad(ghist);
+    if (early) {
+        const int wend = static_cast<int>(min(a.width, lo + a.span));
 #pragma unroll
-    for (int i = 0; i < kRing; ++i) issue_tile(i);
+        for (int i = 0; i < kRing; ++i) issue_tile(i, wend);
+    }
+    const int n = clamp_end(a.ends, row, a.width);
+    if (a.fill) {
+        float* dst = a.fill + static_cast<int64_t>(row) * a.ld;
+        const int64_t hi = min(a.width, lo + a.span);
+        for (int64_t t = max(lo, static_cast<int64_t>(n)) + threadIdx.x; t < hi; t += kSelThreads)
+            dst[t] = -__int_as_float(0x7F800000);
+    }
+    if (k <= 0) return;
+    int32_t* out = a.out + static_cast<int64_t>(row) * k;
+    if (n <= k) {
+        cp_async_wait<0>();   // no copy into this CTA's ring may outlive it
+        const int64_t hi = min(static_cast<int64_t>(k), lo + a.span);
+        for (int64_t pos = lo + threadIdx.x; pos < hi; pos += kSelThreads) out[pos] = pos < n ? static_cast<int>(pos) : -1;
+        return;
+    }
+    const int nsp = static_cast<int>((n + a.span - 1) / a.span);
+    if (static_cast<int>(blockIdx.y) >= nsp) {
+        cp_async_wait<0>();
+        return;
+    }
+    const bool split = nsp > 1;
+    const int hi = static_cast<int>(min(static_cast<int64_t>(n), lo + a.span));
+    if (!early) {
+#pragma unroll
+        for (int i = 0; i < kRing; ++i) issue_tile(i, hi);
+    }
+    // Winners wait in shared memory (written out coalesced after the pass)
+    // when k allows; else they go straight to the output.
+    const bool wbuffered = k <= kWinCap;
     for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0;
     if (threadIdx.x == 0) {
         s_b1 = 0; s_a1 = 0; s_b2 = 0; s_a2 = 0; s_b3 = 0; s_a3 = 0;
@@ -369,7 +388,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
             if (pc < kRefineCap) cbuf[pc] = make_uint2(key, static_cast<uint32_t>(tb + off));
             ++pc;
         }
-        issue_tile(i + kRing);   // this thread is done with the slot
+        issue_tile(i + kRing, hi);   // this thread is done with the slot
     }
     cp_async_wait<0>();
     __syncthreads();
