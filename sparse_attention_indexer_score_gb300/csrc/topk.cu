@@ -317,6 +317,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     // marked values are placed.
     const uint32_t kw = top_bin ? 0xFFFFFFFFu : kwin - 1u;
     const uint32_t crange = kw - kcand;
+    const bool pos_bounds = kcand >= 0x80000000u;   // the level-1 bin lies at or above +0
+    const int tw = static_cast<int>(kw & 0x7FFFFFFFu);   // winners: bits above, as a signed integer
+    const uint32_t tc = kcand & 0x7FFFFFFFu;            // candidates: bits in [tc, tc + crange]
     const int ntiles = (hi - lo32 + kChunk - 1) / kChunk;
     const float* ringf = reinterpret_cast<const float*>(ring);
     for (int i = 0; i < ntiles; ++i) {
@@ -326,11 +329,23 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
         const float4 va = ring[slot / 4 + threadIdx.x], vb = ring[slot / 4 + kChunk / 8 + threadIdx.x];
         const float x[kPerThread] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
         uint32_t wm = 0, cm = 0;
+        if (pos_bounds) {
+            // Both bounds among non-negative scores: the raw bits order those
+            // as the key does, and every score with the sign bit set lies
+            // below them (as a signed integer, or past kw unsigned).
 #pragma unroll
-        for (int u = 0; u < kPerThread; ++u) {
-            const uint32_t key = order_key(x[u]);
-            if (key > kw) wm |= 1u << u;
-            if (key - kcand <= crange) cm |= 1u << u;
+            for (int u = 0; u < kPerThread; ++u) {
+                const uint32_t b = __float_as_uint(x[u]);
+                if (static_cast<int>(b) > tw) wm |= 1u << u;
+                if (b - tc <= crange) cm |= 1u << u;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kPerThread; ++u) {
+                const uint32_t key = order_key(x[u]);
+                if (key > kw) wm |= 1u << u;
+                if (key - kcand <= crange) cm |= 1u << u;
+            }
         }
         if (base + kChunk > hi) {   // last, partial tile: drop positions past the end
             uint32_t inm = 0;
