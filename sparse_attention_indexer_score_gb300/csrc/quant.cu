@@ -413,11 +413,15 @@ extern "C" int dsa_insert_key(int fmt, const void* k, int64_t k_row_stride, cons
 
 namespace dsa {
 
-int check_prepare(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride, int64_t rows,
-                  const void* q_out, const void* w_out, const void* k, int64_t k_row_stride, const float* gamma,
-                  const float* beta, const int64_t* slots, int64_t n, const void* cache, int64_t page_stride,
-                  int64_t num_pages, const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens,
-                  int64_t num_requests, int64_t num_rows, const int32_t* starts, const int32_t* row_ends) {
+// The three parts' checks; *qb and *kb get the blocks of the quantise and
+// insert parts.
+static int check_prepare_blocks(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride,
+                                int64_t rows, const void* q_out, const void* w_out, const void* k,
+                                int64_t k_row_stride, const float* gamma, const float* beta, const int64_t* slots,
+                                int64_t n, const void* cache, int64_t page_stride, int64_t num_pages,
+                                const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens,
+                                int64_t num_requests, int64_t num_rows, const int32_t* starts,
+                                const int32_t* row_ends, int64_t* qb_out, int64_t* kb_out) {
     int64_t qb = 0, kb = 0;
     int rc = check_quantize(fmt, q, q_row_stride, wv, wv_row_stride, rows, const_cast<void*>(q_out),
                             const_cast<void*>(w_out), &qb);
@@ -428,7 +432,20 @@ int check_prepare(int fmt, const void* q, int64_t q_row_stride, const void* wv, 
     rc = check_layout(seq_lens, num_seq, query_lens, num_requests, num_rows, const_cast<int32_t*>(starts),
                       const_cast<int32_t*>(row_ends));
     if (rc != DSA_OK) return rc;
+    *qb_out = qb;
+    *kb_out = kb;
     return (1 + kb + qb > 0x7FFFFFFF) ? DSA_ERR_UNSUPPORTED : DSA_OK;
+}
+
+int check_prepare(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride, int64_t rows,
+                  const void* q_out, const void* w_out, const void* k, int64_t k_row_stride, const float* gamma,
+                  const float* beta, const int64_t* slots, int64_t n, const void* cache, int64_t page_stride,
+                  int64_t num_pages, const int32_t* seq_lens, int64_t num_seq, const int32_t* query_lens,
+                  int64_t num_requests, int64_t num_rows, const int32_t* starts, const int32_t* row_ends) {
+    int64_t qb = 0, kb = 0;
+    return check_prepare_blocks(fmt, q, q_row_stride, wv, wv_row_stride, rows, q_out, w_out, k, k_row_stride, gamma,
+                                beta, slots, n, cache, page_stride, num_pages, seq_lens, num_seq, query_lens,
+                                num_requests, num_rows, starts, row_ends, &qb, &kb);
 }
 
 int launch_prepare(int fmt, const void* q, int64_t q_row_stride, const void* wv, int64_t wv_row_stride, int64_t rows,
@@ -438,13 +455,10 @@ int launch_prepare(int fmt, const void* q, int64_t q_row_stride, const void* wv,
                    int64_t num_requests, int64_t num_rows, int32_t* starts, int32_t* row_ends, int32_t* status,
                    cudaStream_t stream) {
     int64_t qb = 0, kb = 0;
-    int rc = check_quantize(fmt, q, q_row_stride, wv, wv_row_stride, rows, q_out, w_out, &qb);
+    const int rc = check_prepare_blocks(fmt, q, q_row_stride, wv, wv_row_stride, rows, q_out, w_out, k, k_row_stride,
+                                        gamma, beta, slots, n, cache, page_stride, num_pages, seq_lens, num_seq,
+                                        query_lens, num_requests, num_rows, starts, row_ends, &qb, &kb);
     if (rc != DSA_OK) return rc;
-    rc = check_insert(fmt, k, k_row_stride, gamma, beta, slots, n, cache, page_stride, num_pages, &kb);
-    if (rc != DSA_OK) return rc;
-    rc = check_layout(seq_lens, num_seq, query_lens, num_requests, num_rows, starts, row_ends);
-    if (rc != DSA_OK) return rc;
-    if (1 + kb + qb > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
     PrepareArgs a;
     a.fmt = fmt;
     a.q = static_cast<const uint16_t*>(q);
