@@ -297,7 +297,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
     // Winners wait in shared memory (written out coalesced after the pass)
     // when k allows; else they go straight to the output.
     const bool wbuffered = k <= kWinCap;
-    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0;
+    if (!split)   // a split row's last span builds its level-2 histogram from scratch
+        for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0;
     if (threadIdx.x == 0) {
         s_b1 = 0; s_a1 = 0; s_b2 = 0; s_a2 = 0; s_b3 = 0; s_a3 = 0;
         s_wc[0] = 0; s_wc[1] = 0; s_w2 = 0; s_c3 = 0; s_w3 = 0; s_tie = 0;
@@ -372,12 +373,20 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const SelectArgs
         int pc = __shfl_sync(0xFFFFFFFFu, o, 31) + (inc & 0xFFFF) - cc;
         const int tb = base + 4 * threadIdx.x;   // position of value 0 of this thread
         if (wbuffered) {
-            // predicated over the 8 values: no loop as long as the warp's busiest lane
+            // predicated over the 8 values: no loop as long as the warp's busiest lane.
+            // A row has fewer than k <= kWinCap winners, so the bound is tested once
+            // (it only fails when the histogram disagreed with the scores).
+            if (pw + cw <= kWinCap) {
 #pragma unroll
-            for (int u = 0; u < kPerThread; ++u) {
-                if ((wm >> u) & 1u) {
-                    if (pw < kWinCap) wbuf[pw] = tb + (u >> 2) * (kChunk / 2) + (u & 3);
-                    ++pw;
+                for (int u = 0; u < kPerThread; ++u)
+                    if ((wm >> u) & 1u) wbuf[pw++] = tb + (u >> 2) * (kChunk / 2) + (u & 3);
+            } else {
+#pragma unroll
+                for (int u = 0; u < kPerThread; ++u) {
+                    if ((wm >> u) & 1u) {
+                        if (pw < kWinCap) wbuf[pw] = tb + (u >> 2) * (kChunk / 2) + (u & 3);
+                        ++pw;
+                    }
                 }
             }
             wm = 0;
