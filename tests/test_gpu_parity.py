@@ -326,6 +326,26 @@ def test_topk_standalone_exact(cuda_lib):
             assert np.array_equal(np.sort(g_vals), np.sort(logits[r, want[r]])), (k, r)
 
 
+def test_topk_split_rows_with_overflowing_candidates_exact(cuda_lib):
+    """Rows split over several CTAs whose scores all fall in one level-1 bin
+    (1 + 7i ulp, shuffled: distinct, below 1.25): every span's candidate
+    buffer overflows, so the row's last span builds the level-2 histogram by
+    re-reading the row.  The selection is unique and must equal the oracle's
+    exactly, as sets."""
+    import torch
+    rng = np.random.default_rng(9)
+    rows, width = 5, 20000
+    base = np.uint32(0x3F800000) + (np.arange(width, dtype=np.uint32) * np.uint32(7))
+    logits = np.stack([rng.permutation(base) for _ in range(rows)]).view(np.float32)
+    assert float(logits.max()) < 1.25
+    ends = np.array([width, width, 15000, 9000, 4097], np.int32)
+    for k in (64, 2048, 3000):
+        got = cuda_lib.topk(torch.from_numpy(logits).cuda(), torch.from_numpy(ends).cuda(), k).cpu().numpy()
+        want = O.topk(logits, ends, k)
+        for r in range(rows):
+            assert sorted(got[r].tolist()) == sorted(want[r].tolist()), (k, r)
+
+
 def test_workspace_reuse_and_status(cuda_lib):
     """A second call on the same workspace gives the same answer (the workspace
     is left zero-filled), and a bad block-table entry sets the status bit."""
