@@ -16,6 +16,11 @@
 
 namespace dsa {
 
+// Requests up to which the row-to-request search and the per-request offsets
+// stay in shared memory (12 KB, which keeps a 256-thread step-preparation
+// block at eight per SM); more requests read them from global memory.
+constexpr int kLayoutSmemReq = 1024;
+
 __device__ __forceinline__ void decode_layout_block(const int32_t* __restrict__ seq_lens,
                                                     const int32_t* __restrict__ query_lens, int num_req,
                                                     int64_t num_rows, int32_t* __restrict__ starts,
@@ -23,13 +28,23 @@ __device__ __forceinline__ void decode_layout_block(const int32_t* __restrict__ 
                                                     int64_t dcp_world = 1, int64_t interleave = 1) {
     __shared__ int warp_tmp[32];
     __shared__ int chunk_total;
+    __shared__ int s_starts[kLayoutSmemReq + 1];     // starts[1 .. R] when the requests fit
+    __shared__ long long s_off[kLayoutSmemReq];      // seq_len - query_len - start + 1 of each request
+    const bool fit = num_req <= kLayoutSmemReq;
     int carry = 0;
     if (threadIdx.x == 0) starts[0] = 0;
     for (int base = 0; base < num_req; base += blockDim.x) {
         const int i = base + threadIdx.x;
         const int v = (i < num_req) ? query_lens[i] : 0;
+        const int sl = (fit && i < num_req) ? seq_lens[i] : 0;
         const int inc = block_inclusive_scan(v, warp_tmp, &chunk_total);
-        if (i < num_req) starts[i + 1] = carry + inc;
+        if (i < num_req) {
+            starts[i + 1] = carry + inc;
+            if (fit) {
+                s_starts[i + 1] = carry + inc;
+                s_off[i] = static_cast<long long>(sl) - v - (carry + inc - v) + 1;
+            }
+        }
         carry += chunk_total;
         __syncthreads();
     }
@@ -40,12 +55,21 @@ __device__ __forceinline__ void decode_layout_block(const int32_t* __restrict__ 
         if (num_req > 0 && r < last) {
             // first q with starts[q + 1] > r  (searchsorted right on starts[1:])
             int lo = 0, hi = num_req;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (static_cast<int64_t>(starts[mid + 1]) > r) hi = mid; else lo = mid + 1;
+            int64_t e;
+            if (fit) {
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (static_cast<int64_t>(s_starts[mid + 1]) > r) hi = mid; else lo = mid + 1;
+                }
+                e = s_off[min(lo, num_req - 1)] + r;
+            } else {
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (static_cast<int64_t>(starts[mid + 1]) > r) hi = mid; else lo = mid + 1;
+                }
+                const int q = min(lo, num_req - 1);
+                e = static_cast<int64_t>(seq_lens[q]) - query_lens[q] + (r - starts[q]) + 1;
             }
-            const int q = min(lo, num_req - 1);
-            int64_t e = static_cast<int64_t>(seq_lens[q]) - query_lens[q] + (r - starts[q]) + 1;
             e = e > 0 ? e : 0;
             if (dcp_world > 1) {
                 const int64_t full = e / (dcp_world * interleave) * interleave;
